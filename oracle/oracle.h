@@ -1,0 +1,100 @@
+/* oracle.h -- plain, slow, single-threaded CPU sampler: TEST INFRASTRUCTURE ONLY.
+ *
+ * This is the definition the CUDA sampler is checked against.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it; the
+ * product library never links or calls it.  It shares no code, header or
+ * constant table with the CUDA path.
+ *
+ * What it computes, per row r (sources named by page and section):
+ *   counts       c_j = occurrences of j in the prompt ids plus the output ids
+ *                (TensorRT-LLM "Sampling", occurrence penalties: the history is
+ *                the prompt plus everything generated so far);
+ *   greedy route T == 0 or top_k == 1 or top_p == 0 or min_p == 1 (same page,
+ *                "LLM API sampling behavior": greedy whatever the rest);
+ *   penalties    repetition, then frequency, then presence, fp32, no FMA;
+ *   temperature  z_t = z * (1.0f / T), fp32; greedy rows use 1;
+ *   log-probs    log-softmax of z_t over the full row, in double (Tenstorrent
+ *                sampling README, LogProbsCalculator: global max then sum-exp);
+ *   filters      min-p first, then top-k, then top-p renormalised over the top-k
+ *                survivors (TensorRT-LLM "Sampling"), all on the total order
+ *                (z_t descending, index ascending);
+ *   draw         argmax over kept j of z_t - ln(-ln u_j), u_j from a SplitMix64
+ *                stream keyed by (seed, row, j); lowest index on equal scores
+ *                (vllm.cpp PR "the Gumbel draw that scanned 248,320 tokens on
+ *                one thread": GumbelScore, ExpNoise, ArgReduce).
+ */
+#ifndef VT_ORACLE_H
+#define VT_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORACLE_DTYPE_F32 0
+#define ORACLE_DTYPE_BF16 1
+#define ORACLE_MAX_ALT 8
+
+/* Row status codes. */
+#define ORACLE_ROW_OK 0
+#define ORACLE_ROW_NONFINITE 1 /* a NaN or +inf among the tempered logits */
+#define ORACLE_ROW_EMPTY 2     /* no finite tempered logit (all -inf)     */
+
+typedef struct oracle_row_result {
+  int32_t status;       /* ORACLE_ROW_* */
+  int32_t greedy;       /* 1 when the row takes the greedy route */
+  int32_t token;        /* drawn (or argmax) token; -1 when status != 0 */
+  int32_t kept_count;   /* length of the kept prefix of the total order */
+  float kth_value;      /* tempered logit of the last kept element */
+  int32_t kth_index;    /* index of the last kept element */
+  double max_logit;     /* m = max tempered logit */
+  double lse;           /* m + log(sum_j exp(z_t,j - m)) */
+  double logprob;       /* z_t[token] - lse */
+  double best_score;    /* Gumbel score of token (NaN on the greedy route) */
+  double second_score;  /* runner-up score over the same kept set, -inf if none */
+  int32_t second_token; /* runner-up token, -1 if none */
+  int32_t gumbel_near_tie; /* |best-second| <= 1e-6 * max(|best|,|second|,1) */
+  int32_t topp_near;       /* a top-p decision beside the boundary is within 1e-6 of p */
+  int32_t kept_lo;         /* smallest acceptable kept count */
+  int32_t kept_hi;         /* largest acceptable kept count */
+  int32_t n_alt;           /* acceptable tokens in alt_tokens (primary first) */
+  int32_t alt_tokens[ORACLE_MAX_ALT];
+} oracle_row_result;
+
+/* Sample every row of one step.
+ *   logits       host [B][ld] fp32 or bf16 bit patterns; columns >= V unread.
+ *   per-row      temperature, top_k, top_p, min_p, presence, frequency,
+ *                repetition, seed: host arrays of length B.
+ *   histories    CSR: row r owns prompt_ids[prompt_offsets[r] .. prompt_offsets[r+1]),
+ *                likewise output_ids; every id must lie in [0, V).
+ *   num_logprobs n >= 0 top log-probs per row into topn_ids / topn_logprobs
+ *                ([B][n], may be NULL when n == 0).
+ *   zt_out       optional [B][V] copy of the tempered logits z_t (NULL to skip).
+ *   first_row    batch index of the first row passed: row r of this call keys its
+ *                noise stream as row first_row + r (0 for a whole batch).
+ * Returns 0, or -1 on an argument error (nothing written). */
+int oracle_sample(int64_t first_row, int B, int V, int64_t ld, int dtype, const void* logits,
+                  const float* temperature, const int32_t* top_k, const float* top_p,
+                  const float* min_p, const float* presence, const float* frequency,
+                  const float* repetition, const uint64_t* seed,
+                  const int32_t* prompt_ids, const int64_t* prompt_offsets,
+                  const int32_t* output_ids, const int64_t* output_offsets,
+                  int num_logprobs, oracle_row_result* results, int32_t* topn_ids,
+                  double* topn_logprobs, float* zt_out);
+
+/* The SplitMix64 finaliser (Steele, Lea and Flood 2014; the public-domain
+ * splitmix64.c generator applies it to state += 0x9E3779B97F4A7C15). */
+uint64_t oracle_mix64(uint64_t z);
+
+/* u_j = (b_j + 0.5) * 2^-24 for (seed, row, j); exact in double. */
+double oracle_uniform(uint64_t seed, int64_t row, int64_t j);
+
+/* The seed a row carries into the next step: seed + 0x9E3779B97F4A7C15 mod 2^64. */
+uint64_t oracle_next_seed(uint64_t seed);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VT_ORACLE_H */
