@@ -1,0 +1,63 @@
+// vt_kernels.h -- internal interface between the C-ABI host code and the
+// CUDA kernels of the sampler (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vt {
+
+struct RowParams;
+
+// Everything one sampling launch needs.  Device pointers unless noted.
+struct SampleArgs {
+  const void* logits;        // [B][ld] elements
+  int64_t ld;                // row stride in elements
+  int32_t B, V;
+  int32_t n_logprobs;
+  int32_t update_counts;
+  int32_t slice;             // elements per CTA (multiple of 16)
+  int32_t use_bulk;          // rows 16-byte aligned: stage with bulk copies
+  const RowParams* params;   // [B]
+  uint64_t* seeds;           // [B], advanced by the kernel
+  int2* hist;                // [B][hist_cap] sorted (id, count)
+  int32_t* hist_len;         // [B]
+  int32_t hist_cap;
+  float* zside;              // [B][hist_cap] penalised logits of the table entries
+  int32_t* out_tokens;
+  float* out_logprobs;       // may be null
+  int32_t* out_topk_ids;     // [B][n], may be null when n == 0
+  float* out_topk_logprobs;
+  int32_t* row_status;       // [B]
+  float* dbg_kth_value;      // [B]
+  int32_t* dbg_kth_index;    // [B]
+  int32_t* dbg_kept;         // [B]
+  int32_t* err_word;         // one int, kErr* bits
+};
+
+struct LaunchPlan {
+  int cluster;       // CTAs per row
+  int slice;         // elements per CTA
+  size_t smem;       // dynamic shared memory per CTA
+};
+
+// Shared-memory plan for a (V, element size) pair; cluster in {1,2,4,8,16}.
+LaunchPlan plan_sample(int V, int elem_size);
+
+// Prepare kernel attributes (dynamic smem, non-portable clusters); checks that
+// at least one cluster of the plan can be resident.  Returns a cudaError_t.
+cudaError_t prepare_sample(const LaunchPlan& plan, int dtype, int* max_active_clusters);
+
+// Launch the fused sampling kernel: grid B * cluster CTAs.
+cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,
+                          cudaStream_t stream);
+
+// Build the per-row sorted (id, count) tables from raw ids.
+//   raw, offs  CSR: row r owns raw[offs[r] .. offs[r+1]) (prompt then output)
+//   max_len    the longest row (sizes the shared-memory sort)
+//   hist       [B][hist_cap] output, hist_len[B] output
+cudaError_t launch_build_counts(const int32_t* raw, const int64_t* offs, int max_len, int B,
+                                int2* hist, int32_t* hist_len, int32_t hist_cap,
+                                cudaStream_t stream);
+
+}  // namespace vt

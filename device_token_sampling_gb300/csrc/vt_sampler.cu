@@ -1,0 +1,547 @@
+// vt_sampler.cu -- the C ABI of include/vt_sampler.h over the CUDA kernels.
+//
+// Host side only: argument validation, the reset-then-sample state machine
+// (the Tenstorrent SamplingGenerator's reset_sampling_params / reset_seed /
+// reset_prompt_tokens / reset_output_state / sample shape, with its rule that
+// a sampler never reads state that was not reset), derived per-row values,
+// pinned staging uploads, launch planning and launches.  Every device buffer
+// and pinned buffer is allocated in vt_sampler_create; no other call allocates
+// (the anti-pattern the vllm.cpp pull request records: a per-step cudaMalloc
+// of the probabilities and a synchronising cudaFree).
+#include "vt_sampler.h"
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "vt_device.cuh"
+#include "vt_kernels.h"
+
+struct vt_sampler {
+  vt_sampler_config cfg{};
+  std::string err;
+  // device state and scratch
+  vt::RowParams* d_params = nullptr;
+  uint64_t* d_seeds = nullptr;
+  int2* d_hist = nullptr;
+  int32_t* d_hist_len = nullptr;
+  float* d_zside = nullptr;
+  int32_t* d_raw = nullptr;
+  int64_t* d_raw_offs = nullptr;
+  int32_t* d_status = nullptr;
+  float* d_kth_v = nullptr;
+  int32_t* d_kth_i = nullptr;
+  int32_t* d_kept = nullptr;
+  int32_t* d_err = nullptr;
+  // pinned host staging
+  vt::RowParams* h_params = nullptr;
+  uint64_t* h_seeds = nullptr;
+  int32_t* h_raw = nullptr;
+  int64_t* h_raw_offs = nullptr;
+  int32_t* h_err = nullptr;
+  cudaEvent_t ev_params = nullptr, ev_counts = nullptr;
+  bool params_pending = false, counts_pending = false;
+  // staging for vt_sample_host
+  void* d_io_logits = nullptr;
+  size_t io_bytes = 0;
+  int32_t* d_io_tokens = nullptr;
+  float* d_io_lp = nullptr;
+  int32_t* d_io_tid = nullptr;
+  float* d_io_tlp = nullptr;
+  // host mirror of the state machine
+  int params_B = 0;
+  std::vector<uint32_t> row_flags;
+  int counts_B = 0;
+  int last_B = 0;
+  cudaStream_t last_stream = nullptr;
+  std::map<std::pair<int, int>, vt::LaunchPlan> plans;
+};
+
+namespace {
+
+int set_err(vt_sampler* h, int code, const char* fmt, ...) {
+  if (h) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    h->err = buf;
+  }
+  return code;
+}
+
+// Make the handle's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+#define VT_CK(h, expr)                                                                      \
+  do {                                                                                      \
+    cudaError_t e_ = (expr);                                                                \
+    if (e_ != cudaSuccess)                                                                  \
+      return set_err((h), VT_ERR_CUDA, "%s failed: %s", #expr, cudaGetErrorString(e_));     \
+  } while (0)
+
+void free_all(vt_sampler* h) {
+  auto dfree = [](void* p) {
+    if (p) cudaFree(p);
+  };
+  auto hfree = [](void* p) {
+    if (p) cudaFreeHost(p);
+  };
+  dfree(h->d_params);
+  dfree(h->d_seeds);
+  dfree(h->d_hist);
+  dfree(h->d_hist_len);
+  dfree(h->d_zside);
+  dfree(h->d_raw);
+  dfree(h->d_raw_offs);
+  dfree(h->d_status);
+  dfree(h->d_kth_v);
+  dfree(h->d_kth_i);
+  dfree(h->d_kept);
+  dfree(h->d_err);
+  dfree(h->d_io_logits);
+  dfree(h->d_io_tokens);
+  dfree(h->d_io_lp);
+  dfree(h->d_io_tid);
+  dfree(h->d_io_tlp);
+  hfree(h->h_params);
+  hfree(h->h_seeds);
+  hfree(h->h_raw);
+  hfree(h->h_raw_offs);
+  hfree(h->h_err);
+  if (h->ev_params) cudaEventDestroy(h->ev_params);
+  if (h->ev_counts) cudaEventDestroy(h->ev_counts);
+}
+
+bool finite(float x) { return std::isfinite(x); }
+
+}  // namespace
+
+extern "C" {
+
+const char* vt_status_string(int code) {
+  switch (code) {
+    case VT_OK: return "VT_OK";
+    case VT_ERR_INVALID_ARG: return "VT_ERR_INVALID_ARG";
+    case VT_ERR_STATE: return "VT_ERR_STATE";
+    case VT_ERR_CAPACITY: return "VT_ERR_CAPACITY";
+    case VT_ERR_CUDA: return "VT_ERR_CUDA";
+    case VT_ERR_TIMEOUT: return "VT_ERR_TIMEOUT";
+    default: return "VT_ERR_UNKNOWN";
+  }
+}
+
+const char* vt_last_error(const vt_sampler* h) { return h ? h->err.c_str() : "null handle"; }
+
+int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
+  if (!cfg || !out) return VT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg->max_batch < 1 || cfg->max_batch > (1 << 20) || cfg->max_vocab < 1 ||
+      cfg->max_vocab > (1 << 26) || cfg->max_logprobs < 0 || cfg->max_logprobs > 32 ||
+      cfg->max_history < 0 || cfg->max_history > 32768 || cfg->device < 0)
+    return VT_ERR_INVALID_ARG;
+  vt_sampler* h = new (std::nothrow) vt_sampler();
+  if (!h) return VT_ERR_CUDA;
+  h->cfg = *cfg;
+  DeviceGuard guard(cfg->device);
+  auto bail = [&](int code) {
+    free_all(h);
+    delete h;
+    return code;
+  };
+  if (!guard.ok) return bail(VT_ERR_CUDA);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return bail(VT_ERR_CUDA);
+  if (!(prop.major == 10 && prop.minor == 3)) return bail(VT_ERR_CUDA);  // built for sm_103a only
+  // the largest row must fit the shared-memory plan
+  const vt::LaunchPlan worst = vt::plan_sample(cfg->max_vocab, 4);
+  if (worst.smem > (size_t)prop.sharedMemPerBlockOptin) return bail(VT_ERR_CAPACITY);
+
+  const size_t B = (size_t)cfg->max_batch;
+  const size_t H = (size_t)(cfg->max_history > 0 ? cfg->max_history : 1);
+  const size_t n = (size_t)cfg->max_logprobs;
+  bool ok = true;
+  auto dal = [&](void** p, size_t bytes) {
+    if (ok && cudaMalloc(p, bytes) != cudaSuccess) ok = false;
+  };
+  auto hal = [&](void** p, size_t bytes) {
+    if (ok && cudaMallocHost(p, bytes) != cudaSuccess) ok = false;
+  };
+  dal((void**)&h->d_params, B * sizeof(vt::RowParams));
+  dal((void**)&h->d_seeds, B * sizeof(uint64_t));
+  dal((void**)&h->d_hist, B * H * sizeof(int2));
+  dal((void**)&h->d_hist_len, B * sizeof(int32_t));
+  dal((void**)&h->d_zside, B * H * sizeof(float));
+  dal((void**)&h->d_raw, B * H * sizeof(int32_t));
+  dal((void**)&h->d_raw_offs, (B + 1) * sizeof(int64_t));
+  dal((void**)&h->d_status, B * sizeof(int32_t));
+  dal((void**)&h->d_kth_v, B * sizeof(float));
+  dal((void**)&h->d_kth_i, B * sizeof(int32_t));
+  dal((void**)&h->d_kept, B * sizeof(int32_t));
+  dal((void**)&h->d_err, sizeof(int32_t));
+  hal((void**)&h->h_params, B * sizeof(vt::RowParams));
+  hal((void**)&h->h_seeds, B * sizeof(uint64_t));
+  hal((void**)&h->h_raw, B * H * sizeof(int32_t));
+  hal((void**)&h->h_raw_offs, (B + 1) * sizeof(int64_t));
+  hal((void**)&h->h_err, sizeof(int32_t));
+  if (cfg->host_io) {
+    h->io_bytes = B * (size_t)cfg->max_vocab * 4;
+    dal(&h->d_io_logits, h->io_bytes);
+    dal((void**)&h->d_io_tokens, B * sizeof(int32_t));
+    dal((void**)&h->d_io_lp, B * sizeof(float));
+    dal((void**)&h->d_io_tid, B * (n ? n : 1) * sizeof(int32_t));
+    dal((void**)&h->d_io_tlp, B * (n ? n : 1) * sizeof(float));
+  }
+  if (!ok) return bail(VT_ERR_CUDA);
+  if (cudaEventCreateWithFlags(&h->ev_params, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_counts, cudaEventDisableTiming) != cudaSuccess)
+    return bail(VT_ERR_CUDA);
+  if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
+      cudaMemset(h->d_err, 0, sizeof(int32_t)) != cudaSuccess ||
+      cudaMemset(h->d_seeds, 0, B * sizeof(uint64_t)) != cudaSuccess ||
+      cudaMemset(h->d_status, 0, B * sizeof(int32_t)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess)
+    return bail(VT_ERR_CUDA);
+  *h->h_err = 0;
+  h->row_flags.assign(B, 0u);
+  *out = h;
+  return VT_OK;
+}
+
+void vt_sampler_destroy(vt_sampler* h) {
+  if (!h) return;
+  DeviceGuard guard(h->cfg.device);
+  if (h->last_stream) cudaStreamSynchronize(h->last_stream);
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+}
+
+int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const int32_t* top_k,
+                    const float* top_p, const float* min_p, const float* presence,
+                    const float* frequency, const float* repetition, const uint64_t* seed,
+                    void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  if (B < 1) return set_err(h, VT_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
+  if (B > h->cfg.max_batch)
+    return set_err(h, VT_ERR_CAPACITY, "B=%d exceeds max_batch=%d", B, h->cfg.max_batch);
+  if (!temperature || !top_k || !top_p || !min_p || !presence || !frequency || !repetition ||
+      !seed)
+    return set_err(h, VT_ERR_INVALID_ARG, "null parameter array");
+  for (int r = 0; r < B; ++r) {
+    const float T = temperature[r], p = top_p[r], mp = min_p[r], rep = repetition[r];
+    if (!(T >= 0.0f) || !finite(T) || (T > 0.0f && !finite(1.0f / T)))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: temperature %g out of range", r, T);
+    if (top_k[r] < 0) return set_err(h, VT_ERR_INVALID_ARG, "row %d: top_k < 0", r);
+    if (!(p >= 0.0f && p <= 1.0f))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: top_p %g not in [0,1]", r, p);
+    if (!(mp >= 0.0f && mp <= 1.0f))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: min_p %g not in [0,1]", r, mp);
+    if (!finite(presence[r]) || !finite(frequency[r]) || !finite(rep) || !(rep > 0.0f))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: penalties out of range", r);
+  }
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->params_pending) {
+    VT_CK(h, cudaEventSynchronize(h->ev_params));
+    h->params_pending = false;
+  }
+  for (int r = 0; r < B; ++r) {
+    const float T = temperature[r], p = top_p[r], mp = min_p[r];
+    const int k = top_k[r];
+    vt::RowParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    const bool greedy = T == 0.0f || k == 1 || p == 0.0f || mp == 1.0f;
+    rp.inv_t = greedy ? 1.0f : 1.0f / T;
+    rp.top_p = p;
+    rp.top_k = k;
+    rp.flags = 0;
+    if (greedy) rp.flags |= vt::kRowGreedy;
+    if (p > 0.0f && p < 1.0f) rp.flags |= vt::kRowTopP;
+    if (mp > 0.0f && mp < 1.0f) rp.flags |= vt::kRowMinP;
+    if (presence[r] != 0.0f || frequency[r] != 0.0f || repetition[r] != 1.0f)
+      rp.flags |= vt::kRowPenalty;
+    rp.presence = presence[r];
+    rp.frequency = frequency[r];
+    rp.repetition = repetition[r];
+    rp.min_p = mp;
+    rp.log_min_p = (mp > 0.0f && mp < 1.0f) ? std::log((double)mp) : 0.0;
+    h->h_params[r] = rp;
+    h->h_seeds[r] = seed[r];
+    h->row_flags[r] = rp.flags;
+  }
+  VT_CK(h, cudaMemcpyAsync(h->d_params, h->h_params, (size_t)B * sizeof(vt::RowParams),
+                           cudaMemcpyHostToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(h->d_seeds, h->h_seeds, (size_t)B * sizeof(uint64_t),
+                           cudaMemcpyHostToDevice, st));
+  VT_CK(h, cudaEventRecord(h->ev_params, st));
+  h->params_pending = true;
+  h->params_B = B;
+  h->last_stream = st;
+  h->err.clear();
+  return VT_OK;
+}
+
+int vt_reset_token_counts(vt_sampler* h, int32_t B, const int32_t* prompt_ids,
+                          const int64_t* prompt_offsets, const int32_t* output_ids,
+                          const int64_t* output_offsets, void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  if (B < 1) return set_err(h, VT_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
+  if (B > h->cfg.max_batch)
+    return set_err(h, VT_ERR_CAPACITY, "B=%d exceeds max_batch=%d", B, h->cfg.max_batch);
+  if (!prompt_offsets || !output_offsets)
+    return set_err(h, VT_ERR_INVALID_ARG, "null offsets");
+  if (prompt_offsets[0] != 0 || output_offsets[0] != 0)
+    return set_err(h, VT_ERR_INVALID_ARG, "offsets must start at 0");
+  int max_len = 0;
+  for (int r = 0; r < B; ++r) {
+    const int64_t np = prompt_offsets[r + 1] - prompt_offsets[r];
+    const int64_t no = output_offsets[r + 1] - output_offsets[r];
+    if (np < 0 || no < 0) return set_err(h, VT_ERR_INVALID_ARG, "row %d: decreasing offsets", r);
+    if (np + no > h->cfg.max_history)
+      return set_err(h, VT_ERR_CAPACITY, "row %d: %lld ids exceed max_history=%d", r,
+                     (long long)(np + no), h->cfg.max_history);
+    if ((np && !prompt_ids) || (no && !output_ids))
+      return set_err(h, VT_ERR_INVALID_ARG, "null id array");
+    max_len = (int)std::max<int64_t>(max_len, np + no);
+  }
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->counts_pending) {
+    VT_CK(h, cudaEventSynchronize(h->ev_counts));
+    h->counts_pending = false;
+  }
+  int64_t w = 0;
+  h->h_raw_offs[0] = 0;
+  for (int r = 0; r < B; ++r) {
+    for (int64_t i = prompt_offsets[r]; i < prompt_offsets[r + 1]; ++i) {
+      const int32_t id = prompt_ids[i];
+      if (id < 0 || id >= h->cfg.max_vocab)
+        return set_err(h, VT_ERR_INVALID_ARG, "row %d: prompt id %d out of range", r, id);
+      h->h_raw[w++] = id;
+    }
+    for (int64_t i = output_offsets[r]; i < output_offsets[r + 1]; ++i) {
+      const int32_t id = output_ids[i];
+      if (id < 0 || id >= h->cfg.max_vocab)
+        return set_err(h, VT_ERR_INVALID_ARG, "row %d: output id %d out of range", r, id);
+      h->h_raw[w++] = id;
+    }
+    h->h_raw_offs[r + 1] = w;
+  }
+  if (w > 0)
+    VT_CK(h, cudaMemcpyAsync(h->d_raw, h->h_raw, (size_t)w * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(h->d_raw_offs, h->h_raw_offs, (size_t)(B + 1) * sizeof(int64_t),
+                           cudaMemcpyHostToDevice, st));
+  VT_CK(h, vt::launch_build_counts(h->d_raw, h->d_raw_offs, max_len, B, h->d_hist,
+                                   h->d_hist_len, h->cfg.max_history > 0 ? h->cfg.max_history : 1,
+                                   st));
+  VT_CK(h, cudaEventRecord(h->ev_counts, st));
+  h->counts_pending = true;
+  h->counts_B = B;
+  h->last_stream = st;
+  h->err.clear();
+  return VT_OK;
+}
+
+static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t B, int32_t V,
+                       int64_t ld, int32_t n, int32_t update_counts, int32_t* out_tokens,
+                       float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
+                       cudaStream_t st) {
+  if (h->params_B == 0) return set_err(h, VT_ERR_STATE, "vt_sample before vt_reset_params");
+  if (B < 1 || B > h->params_B)
+    return set_err(h, B < 1 ? VT_ERR_INVALID_ARG : VT_ERR_STATE,
+                   "B=%d but parameters were reset for %d rows", B, h->params_B);
+  if (dtype != VT_DTYPE_F32 && dtype != VT_DTYPE_BF16)
+    return set_err(h, VT_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (V < 1 || ld < V) return set_err(h, VT_ERR_INVALID_ARG, "need 1 <= V <= ld");
+  if (V > h->cfg.max_vocab)
+    return set_err(h, VT_ERR_CAPACITY, "V=%d exceeds max_vocab=%d", V, h->cfg.max_vocab);
+  if (n < 0 || n > h->cfg.max_logprobs)
+    return set_err(h, n < 0 ? VT_ERR_INVALID_ARG : VT_ERR_CAPACITY,
+                   "num_logprobs=%d outside [0, %d]", n, h->cfg.max_logprobs);
+  if (!logits || !out_tokens) return set_err(h, VT_ERR_INVALID_ARG, "null logits or tokens");
+  if (n > 0 && (!out_topk_ids || !out_topk_logprobs))
+    return set_err(h, VT_ERR_INVALID_ARG, "top-k log-prob outputs are null");
+  if ((update_counts && h->cfg.max_history == 0))
+    return set_err(h, VT_ERR_CAPACITY, "update_counts needs max_history > 0");
+  for (int r = 0; r < B; ++r)
+    if ((h->row_flags[r] & vt::kRowPenalty) && r >= h->counts_B)
+      return set_err(h, VT_ERR_STATE, "row %d has penalties but its counts were never reset", r);
+  const int es = dtype == VT_DTYPE_F32 ? 4 : 2;
+  auto key = std::make_pair(V, dtype);
+  auto it = h->plans.find(key);
+  if (it == h->plans.end()) {
+    vt::LaunchPlan plan = vt::plan_sample(V, es);
+    int active = 0;
+    const cudaError_t e = vt::prepare_sample(plan, dtype, &active);
+    if (e != cudaSuccess)
+      return set_err(h, VT_ERR_CUDA, "cannot prepare a %d-CTA cluster plan: %s", plan.cluster,
+                     cudaGetErrorString(e));
+    it = h->plans.emplace(key, plan).first;
+  }
+  const vt::LaunchPlan& plan = it->second;
+  vt::SampleArgs a;
+  a.logits = logits;
+  a.ld = ld;
+  a.B = B;
+  a.V = V;
+  a.n_logprobs = n;
+  a.update_counts = update_counts ? 1 : 0;
+  a.slice = plan.slice;
+  a.use_bulk = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
+  a.params = h->d_params;
+  a.seeds = h->d_seeds;
+  a.hist = h->d_hist;
+  a.hist_len = h->d_hist_len;
+  a.hist_cap = h->cfg.max_history > 0 ? h->cfg.max_history : 1;
+  a.zside = h->d_zside;
+  a.out_tokens = out_tokens;
+  a.out_logprobs = out_logprobs;
+  a.out_topk_ids = out_topk_ids;
+  a.out_topk_logprobs = out_topk_logprobs;
+  a.row_status = h->d_status;
+  a.dbg_kth_value = h->d_kth_v;
+  a.dbg_kth_index = h->d_kth_i;
+  a.dbg_kept = h->d_kept;
+  a.err_word = h->d_err;
+  VT_CK(h, vt::launch_sample(a, plan, dtype, st));
+  h->last_B = B;
+  h->last_stream = st;
+  h->err.clear();
+  return VT_OK;
+}
+
+int vt_sample(vt_sampler* h, const void* logits, int32_t dtype, int32_t B, int32_t V, int64_t ld,
+              int32_t num_logprobs, int32_t update_counts, int32_t* out_tokens,
+              float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
+              void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
+  return sample_impl(h, logits, dtype, B, V, ld, num_logprobs, update_counts, out_tokens,
+                     out_logprobs, out_topk_ids, out_topk_logprobs, (cudaStream_t)stream);
+}
+
+int vt_check_device_errors(vt_sampler* h) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  VT_CK(h, cudaStreamSynchronize(h->last_stream));
+  VT_CK(h, cudaMemcpy(h->h_err, h->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  const int e = *h->h_err;
+  if (e != 0) {
+    VT_CK(h, cudaMemset(h->d_err, 0, sizeof(int32_t)));
+    if (e & vt::kErrTimeout) return set_err(h, VT_ERR_TIMEOUT, "a device wait ran out");
+    return set_err(h, VT_ERR_CUDA, "device error word 0x%x", e);
+  }
+  return VT_OK;
+}
+
+int vt_sample_host(vt_sampler* h, const void* host_logits, int32_t dtype, int32_t B, int32_t V,
+                   int64_t ld, int32_t n, int32_t update_counts, int32_t* host_tokens,
+                   float* host_logprobs, int32_t* host_topk_ids, float* host_topk_logprobs,
+                   void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  if (!h->d_io_logits) return set_err(h, VT_ERR_STATE, "handle created without host_io");
+  if (!host_logits || !host_tokens) return set_err(h, VT_ERR_INVALID_ARG, "null host buffer");
+  if (n > 0 && (!host_topk_ids || !host_topk_logprobs))
+    return set_err(h, VT_ERR_INVALID_ARG, "top-k log-prob outputs are null");
+  const int es = dtype == VT_DTYPE_F32 ? 4 : 2;
+  if (B < 1 || ld < 1) return set_err(h, VT_ERR_INVALID_ARG, "bad shape");
+  const size_t bytes = (size_t)B * (size_t)ld * es;
+  if (bytes > h->io_bytes) return set_err(h, VT_ERR_CAPACITY, "logits exceed host_io staging");
+  DeviceGuard guard(h->cfg.device);
+  cudaStream_t st = (cudaStream_t)stream;
+  VT_CK(h, cudaMemcpyAsync(h->d_io_logits, host_logits, bytes, cudaMemcpyHostToDevice, st));
+  const int rc = sample_impl(h, h->d_io_logits, dtype, B, V, ld, n, update_counts, h->d_io_tokens,
+                             h->d_io_lp, n ? h->d_io_tid : nullptr, n ? h->d_io_tlp : nullptr, st);
+  if (rc != VT_OK) return rc;
+  VT_CK(h, cudaMemcpyAsync(host_tokens, h->d_io_tokens, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
+  if (host_logprobs)
+    VT_CK(h, cudaMemcpyAsync(host_logprobs, h->d_io_lp, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
+  if (n > 0) {
+    VT_CK(h, cudaMemcpyAsync(host_topk_ids, h->d_io_tid, (size_t)B * n * 4,
+                             cudaMemcpyDeviceToHost, st));
+    VT_CK(h, cudaMemcpyAsync(host_topk_logprobs, h->d_io_tlp, (size_t)B * n * 4,
+                             cudaMemcpyDeviceToHost, st));
+  }
+  VT_CK(h, cudaStreamSynchronize(st));
+  return vt_check_device_errors(h);
+}
+
+int vt_get_row_status(vt_sampler* h, int32_t* dev_status, void* stream) {
+  if (!h || !dev_status) return VT_ERR_INVALID_ARG;
+  if (h->last_B == 0) return set_err(h, VT_ERR_STATE, "no vt_sample yet");
+  DeviceGuard guard(h->cfg.device);
+  VT_CK(h, cudaMemcpyAsync(dev_status, h->d_status, (size_t)h->last_B * 4,
+                           cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  return VT_OK;
+}
+
+int vt_debug_filter_boundary(vt_sampler* h, float* kth_value, int32_t* kth_index,
+                             int32_t* kept_count, void* stream) {
+  if (!h || !kth_value || !kth_index || !kept_count) return VT_ERR_INVALID_ARG;
+  if (h->last_B == 0) return set_err(h, VT_ERR_STATE, "no vt_sample yet");
+  DeviceGuard guard(h->cfg.device);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t b = (size_t)h->last_B * 4;
+  VT_CK(h, cudaMemcpyAsync(kth_value, h->d_kth_v, b, cudaMemcpyDeviceToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(kth_index, h->d_kth_i, b, cudaMemcpyDeviceToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(kept_count, h->d_kept, b, cudaMemcpyDeviceToDevice, st));
+  return VT_OK;
+}
+
+int vt_debug_get_counts(vt_sampler* h, int32_t row, int32_t* ids, int32_t* counts,
+                        int32_t capacity, int32_t* n_unique) {
+  if (!h || !n_unique || capacity < 0 || (capacity > 0 && (!ids || !counts)))
+    return VT_ERR_INVALID_ARG;
+  if (row < 0 || row >= h->cfg.max_batch) return set_err(h, VT_ERR_INVALID_ARG, "bad row");
+  DeviceGuard guard(h->cfg.device);
+  VT_CK(h, cudaStreamSynchronize(h->last_stream));
+  int32_t len = 0;
+  VT_CK(h, cudaMemcpy(&len, h->d_hist_len + row, 4, cudaMemcpyDeviceToHost));
+  *n_unique = len;
+  const int m = len < capacity ? len : capacity;
+  if (m > 0) {
+    const int cap = h->cfg.max_history > 0 ? h->cfg.max_history : 1;
+    std::vector<int2> tmp(m);
+    VT_CK(h, cudaMemcpy(tmp.data(), h->d_hist + (size_t)row * cap, (size_t)m * sizeof(int2),
+                        cudaMemcpyDeviceToHost));
+    for (int i = 0; i < m; ++i) {
+      ids[i] = tmp[i].x;
+      counts[i] = tmp[i].y;
+    }
+  }
+  return VT_OK;
+}
+
+int vt_debug_get_seeds(vt_sampler* h, uint64_t* host_seeds) {
+  if (!h || !host_seeds) return VT_ERR_INVALID_ARG;
+  if (h->params_B == 0) return set_err(h, VT_ERR_STATE, "no vt_reset_params yet");
+  DeviceGuard guard(h->cfg.device);
+  VT_CK(h, cudaStreamSynchronize(h->last_stream));
+  VT_CK(h, cudaMemcpy(host_seeds, h->d_seeds, (size_t)h->params_B * 8, cudaMemcpyDeviceToHost));
+  return VT_OK;
+}
+
+}  // extern "C"

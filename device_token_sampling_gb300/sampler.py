@@ -1,0 +1,290 @@
+"""Thin ctypes binding of the C ABI in ``include/vt_sampler.h``.
+
+Argument marshalling only: every step of the sampling path runs in the CUDA
+kernels of ``libvt_sampler.so``.  PyTorch supplies device memory (output
+tensors) and streams.  Importing this module loads the library and raises if it
+has not been built (``device_token_sampling_gb300.build()``); there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import _build
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+VT_OK = 0
+VT_ERR_INVALID_ARG = -1
+VT_ERR_STATE = -2
+VT_ERR_CAPACITY = -3
+VT_ERR_CUDA = -4
+VT_ERR_TIMEOUT = -5
+
+ROW_OK, ROW_NONFINITE, ROW_EMPTY, ROW_HISTORY_FULL = 0, 1, 2, 3
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+class VtError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_ERRNAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_ERRNAMES = {VT_ERR_INVALID_ARG: "VT_ERR_INVALID_ARG", VT_ERR_STATE: "VT_ERR_STATE",
+             VT_ERR_CAPACITY: "VT_ERR_CAPACITY", VT_ERR_CUDA: "VT_ERR_CUDA",
+             VT_ERR_TIMEOUT: "VT_ERR_TIMEOUT"}
+
+
+class Config(C.Structure):
+    _fields_ = [("max_batch", C.c_int32), ("max_vocab", C.c_int32),
+                ("max_logprobs", C.c_int32), ("max_history", C.c_int32),
+                ("device", C.c_int32), ("host_io", C.c_int32)]
+
+
+P = C.c_void_p
+I32, I64 = C.c_int32, C.c_int64
+
+# entry point -> (restype, argtypes); the single source of the binding's view
+# of include/vt_sampler.h
+SIGNATURES = {
+    "vt_sampler_create": (C.c_int, [C.POINTER(Config), C.POINTER(P)]),
+    "vt_sampler_destroy": (None, [P]),
+    "vt_reset_params": (C.c_int, [P, I32, P, P, P, P, P, P, P, P, P]),
+    "vt_reset_token_counts": (C.c_int, [P, I32, P, P, P, P, P]),
+    "vt_sample": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
+    "vt_sample_host": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
+    "vt_check_device_errors": (C.c_int, [P]),
+    "vt_get_row_status": (C.c_int, [P, P, P]),
+    "vt_debug_filter_boundary": (C.c_int, [P, P, P, P, P]),
+    "vt_debug_get_counts": (C.c_int, [P, I32, P, P, I32, P]),
+    "vt_debug_get_seeds": (C.c_int, [P, P]),
+    "vt_last_error": (C.c_char_p, [P]),
+    "vt_status_string": (C.c_char_p, [C.c_int]),
+}
+
+_lib = None
+
+
+def load_library() -> C.CDLL:
+    """Load libvt_sampler.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with device_token_sampling_gb300.build()")
+    lib = C.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data_as(P)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return P(stream.cuda_stream)
+
+
+class Sampler:
+    """One sampler handle (``vt_sampler_create``) on one CUDA device."""
+
+    def __init__(self, max_batch: int, max_vocab: int, max_logprobs: int = 0,
+                 max_history: int = 0, device: int | None = None, host_io: bool = False):
+        import torch
+        self._lib = load_library()
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = int(device)
+        cfg = Config(max_batch, max_vocab, max_logprobs, max_history, self.device,
+                     1 if host_io else 0)
+        h = P()
+        rc = self._lib.vt_sampler_create(C.byref(cfg), C.byref(h))
+        if rc != VT_OK:
+            raise VtError(rc, f"vt_sampler_create({max_batch}, {max_vocab}, {max_logprobs}, "
+                              f"{max_history}, device={self.device})")
+        self._h = h
+        self.cfg = cfg
+
+    # -- lifetime ------------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.vt_sampler_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def handle(self):
+        return self._h
+
+    def _check(self, rc: int, what: str):
+        if rc != VT_OK:
+            msg = self._lib.vt_last_error(self._h)
+            raise VtError(rc, f"{what}: {msg.decode() if msg else ''}")
+
+    # -- state ---------------------------------------------------------------
+    def reset_params(self, temperature, top_k, top_p, min_p, presence, frequency, repetition,
+                     seed, stream=None):
+        t = np.ascontiguousarray(temperature, np.float32)
+        B = t.shape[0]
+        arrs = [t, np.ascontiguousarray(top_k, np.int32), np.ascontiguousarray(top_p, np.float32),
+                np.ascontiguousarray(min_p, np.float32),
+                np.ascontiguousarray(presence, np.float32),
+                np.ascontiguousarray(frequency, np.float32),
+                np.ascontiguousarray(repetition, np.float32),
+                np.ascontiguousarray(seed, np.uint64)]
+        for a in arrs:
+            if a.shape != (B,):
+                raise ValueError("every parameter array must have shape (B,)")
+        rc = self._lib.vt_reset_params(self._h, B, *[_np_ptr(a) for a in arrs],
+                                       _stream_ptr(stream))
+        self._check(rc, "vt_reset_params")
+
+    def reset_token_counts(self, prompt_ids, prompt_offsets, output_ids, output_offsets,
+                           stream=None):
+        pi = np.ascontiguousarray(prompt_ids, np.int32)
+        po = np.ascontiguousarray(prompt_offsets, np.int64)
+        oi = np.ascontiguousarray(output_ids, np.int32)
+        oo = np.ascontiguousarray(output_offsets, np.int64)
+        B = po.shape[0] - 1
+        if oo.shape[0] != B + 1:
+            raise ValueError("prompt and output offsets disagree on B")
+        rc = self._lib.vt_reset_token_counts(self._h, B, _np_ptr(pi), _np_ptr(po), _np_ptr(oi),
+                                             _np_ptr(oo), _stream_ptr(stream))
+        self._check(rc, "vt_reset_token_counts")
+
+    def reset_workload(self, w, stream=None):
+        """Reset params, seeds and counts from a ``workloads.Workload``."""
+        self.reset_params(w.temperature, w.top_k, w.top_p, w.min_p, w.presence, w.frequency,
+                          w.repetition, w.seed, stream=stream)
+        if self.cfg.max_history > 0:
+            self.reset_token_counts(w.prompt_ids, w.prompt_offsets, w.output_ids,
+                                    w.output_offsets, stream=stream)
+
+    # -- sampling ------------------------------------------------------------
+    def sample(self, logits, V: int | None = None, num_logprobs: int = 0,
+               update_counts: bool = False, out=None, stream=None, dtype: int | None = None):
+        """Sample one token per row of a CUDA tensor ``logits`` [B, ld] (float32 or
+        bfloat16, or a uint16 tensor of bf16 bits with ``dtype=DTYPE_BF16``).
+
+        Returns ``(tokens, logprobs, topk_ids, topk_logprobs)`` CUDA tensors (the
+        last two have shape [B, num_logprobs]).  Stream-ordered; nothing waits."""
+        import torch
+        if logits.dim() != 2 or not logits.is_cuda:
+            raise ValueError("logits must be a 2-D CUDA tensor")
+        if logits.stride(1) != 1:
+            raise ValueError("logits rows must be contiguous")
+        if dtype is None:
+            if logits.dtype == torch.float32:
+                dtype = DTYPE_F32
+            elif logits.dtype in (torch.bfloat16, torch.uint16, torch.int16):
+                dtype = DTYPE_BF16
+            else:
+                raise ValueError(f"unsupported logits dtype {logits.dtype}")
+        B, ld = logits.shape[0], logits.stride(0)
+        V = logits.shape[1] if V is None else V
+        n = int(num_logprobs)
+        dev = logits.device
+        if out is None:
+            out = (torch.empty(B, dtype=torch.int32, device=dev),
+                   torch.empty(B, dtype=torch.float32, device=dev),
+                   torch.empty((B, n), dtype=torch.int32, device=dev),
+                   torch.empty((B, n), dtype=torch.float32, device=dev))
+        tok, lp, tid, tlp = out
+        rc = self._lib.vt_sample(self._h, P(logits.data_ptr()), dtype, B, V, ld, n,
+                                 1 if update_counts else 0, P(tok.data_ptr()),
+                                 P(lp.data_ptr()) if lp is not None else None,
+                                 P(tid.data_ptr()) if n else None,
+                                 P(tlp.data_ptr()) if n else None, _stream_ptr(stream))
+        self._check(rc, "vt_sample")
+        return out
+
+    def sample_ptr(self, logits_ptr: int, dtype: int, B: int, V: int, ld: int, num_logprobs: int,
+                   update_counts: bool, tokens_ptr: int, logprobs_ptr: int | None,
+                   topk_ids_ptr: int | None, topk_lp_ptr: int | None, stream_ptr: int):
+        """vt_sample on raw device pointers (no torch involvement)."""
+        rc = self._lib.vt_sample(self._h, P(logits_ptr), dtype, B, V, ld, num_logprobs,
+                                 1 if update_counts else 0, P(tokens_ptr),
+                                 P(logprobs_ptr) if logprobs_ptr else None,
+                                 P(topk_ids_ptr) if topk_ids_ptr else None,
+                                 P(topk_lp_ptr) if topk_lp_ptr else None, P(stream_ptr))
+        self._check(rc, "vt_sample")
+
+    def sample_host(self, logits: np.ndarray, V: int, dtype: int, num_logprobs: int = 0,
+                    update_counts: bool = False, stream=None, out=None):
+        """vt_sample_host: host logits [B, ld] in, host outputs back; synchronous."""
+        x = np.ascontiguousarray(logits)
+        B, ld = x.shape
+        n = int(num_logprobs)
+        if out is None:
+            out = (np.empty(B, np.int32), np.empty(B, np.float32), np.empty((B, n), np.int32),
+                   np.empty((B, n), np.float32))
+        tok, lp, tid, tlp = out
+        rc = self._lib.vt_sample_host(self._h, _np_ptr(x), dtype, B, V, ld, n,
+                                      1 if update_counts else 0, _np_ptr(tok), _np_ptr(lp),
+                                      _np_ptr(tid) if n else None, _np_ptr(tlp) if n else None,
+                                      _stream_ptr(stream))
+        self._check(rc, "vt_sample_host")
+        return out
+
+    # -- views -----------------------------------------------------------------
+    def check_device_errors(self):
+        self._check(self._lib.vt_check_device_errors(self._h), "vt_check_device_errors")
+
+    def row_status(self, B: int, stream=None):
+        import torch
+        st = torch.empty(B, dtype=torch.int32, device=f"cuda:{self.device}")
+        self._check(self._lib.vt_get_row_status(self._h, P(st.data_ptr()), _stream_ptr(stream)),
+                    "vt_get_row_status")
+        return st
+
+    def filter_boundary(self, B: int, stream=None):
+        import torch
+        d = f"cuda:{self.device}"
+        v = torch.empty(B, dtype=torch.float32, device=d)
+        i = torch.empty(B, dtype=torch.int32, device=d)
+        k = torch.empty(B, dtype=torch.int32, device=d)
+        self._check(self._lib.vt_debug_filter_boundary(self._h, P(v.data_ptr()), P(i.data_ptr()),
+                                                       P(k.data_ptr()), _stream_ptr(stream)),
+                    "vt_debug_filter_boundary")
+        return v, i, k
+
+    def counts(self, row: int):
+        cap = max(1, self.cfg.max_history)
+        ids = np.zeros(cap, np.int32)
+        cnt = np.zeros(cap, np.int32)
+        n = C.c_int32(0)
+        self._check(self._lib.vt_debug_get_counts(self._h, row, _np_ptr(ids), _np_ptr(cnt), cap,
+                                                  C.byref(n)), "vt_debug_get_counts")
+        return ids[:n.value].copy(), cnt[:n.value].copy()
+
+    def seeds(self, B: int):
+        s = np.zeros(self.cfg.max_batch, np.uint64)  # the call writes up to max_batch seeds
+        self._check(self._lib.vt_debug_get_seeds(self._h, _np_ptr(s)), "vt_debug_get_seeds")
+        return s[:B]

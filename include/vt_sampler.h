@@ -1,0 +1,206 @@
+/* vt_sampler.h -- C ABI of the GB300 batched decode sampler.
+ *
+ * One call of vt_sample turns a [B, V] logits tensor that lives in device
+ * memory into one next token per row.  The per-row pipeline, in this order:
+ *
+ *   1. occurrence penalties from the row's token counts over the prompt plus
+ *      everything generated so far: repetition (divide a non-negative logit by
+ *      the penalty, multiply a negative one), then frequency (subtract
+ *      frequency * count), then presence (subtract once when count > 0)
+ *      [TensorRT-LLM "Sampling" page, LLM API sampling behaviour, occurrence
+ *      penalties];
+ *   2. temperature: z_t = z * (1.0f / T) [same page: logits scaled by
+ *      1/temperature]; T = 0, top_k = 1, top_p = 0 or min_p = 1 make the row
+ *      greedy whatever its other settings [same page], and a greedy row uses
+ *      T = 1;
+ *   3. log-softmax log-probs of z_t over the whole row [Tenstorrent sampling
+ *      README, LogProbsCalculator: global max, then sum-exp] and the top-n
+ *      log-probs [TensorRT-LLM "Sampling", TopK LogProbs];
+ *   4. filters on the order (z_t descending, index ascending): min-p first,
+ *      then top-k, then top-p over the top-k survivors renormalised [TensorRT-
+ *      LLM "Sampling": min-p, top-k and top-p bullets];
+ *   5. the draw: token = argmax over kept j of z_t,j - ln(-ln u_j), where u_j
+ *      is a SplitMix64 stream keyed by (seed, row, j); equal scores go to the
+ *      lowest index; a greedy row takes the lowest-index argmax [vllm.cpp pull
+ *      request "the Gumbel draw that scanned 248,320 tokens on one thread":
+ *      GumbelScore, ExpNoise, ArgReduce comparing true global indices].
+ *
+ * The state carried between calls follows the reset-then-sample shape of the
+ * Tenstorrent SamplingGenerator (reset_sampling_params, reset_seed,
+ * reset_prompt_tokens / reset_output_state, sample): per-row parameters and
+ * seeds (vt_reset_params) and per-row token counts (vt_reset_token_counts).
+ * Each vt_sample call advances every sampled row's seed once and, on request,
+ * adds the drawn token to the row's counts.
+ *
+ * Conventions for every entry point:
+ *   - The return value is VT_OK (0) or a negative VT_ERR_* code; nothing is
+ *     thrown across the ABI.  vt_last_error() gives a message for the last
+ *     failure on a handle.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it in stream order; unless stated, calls do
+ *     not wait for the GPU, and the caller synchronises the stream before
+ *     reading device outputs.
+ *   - "host" pointers are ordinary CPU memory, read before the call returns;
+ *     the caller keeps ownership.  "device" pointers are CUDA device memory
+ *     on the handle's device, owned by the caller.
+ *   - A handle is not thread-safe: one host thread at a time.
+ */
+#ifndef VT_SAMPLER_H
+#define VT_SAMPLER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define VT_OK 0
+#define VT_ERR_INVALID_ARG (-1) /* a bad pointer, size or parameter value      */
+#define VT_ERR_STATE (-2)       /* a call out of order (sample before reset)   */
+#define VT_ERR_CAPACITY (-3)    /* a size beyond the capacities given at create */
+#define VT_ERR_CUDA (-4)        /* a CUDA runtime call failed                   */
+#define VT_ERR_TIMEOUT (-5)     /* a bounded device wait ran out                */
+
+/* ---- logits element types ----------------------------------------------- */
+#define VT_DTYPE_F32 0  /* IEEE binary32                                        */
+#define VT_DTYPE_BF16 1 /* bfloat16 (the top 16 bits of a binary32), widened exactly */
+
+/* ---- per-row status written by vt_sample (see vt_get_row_status) ------- */
+#define VT_ROW_OK 0           /* token drawn                                    */
+#define VT_ROW_NONFINITE 1    /* a NaN or +inf among the tempered logits; token -1 */
+#define VT_ROW_EMPTY 2        /* no finite tempered logit (all -inf); token -1   */
+#define VT_ROW_HISTORY_FULL 3 /* token drawn, but the row's count table was full,
+                                 so update_counts could not record it            */
+
+typedef struct vt_sampler vt_sampler; /* opaque handle */
+
+typedef struct vt_sampler_config {
+  int32_t max_batch;    /* largest B of any call, >= 1                          */
+  int32_t max_vocab;    /* largest V of any call, >= 1                          */
+  int32_t max_logprobs; /* largest num_logprobs, 0..32                          */
+  int32_t max_history;  /* per-row capacity of the count table in distinct ids,
+                           and the largest prompt + output length per row at a
+                           counts reset; 0..32768                               */
+  int32_t device;       /* CUDA device ordinal                                  */
+  int32_t host_io;      /* 1: also allocate device staging for vt_sample_host   */
+} vt_sampler_config;
+
+/* Create a sampler: validates the capacities, makes `device` current, and
+ * allocates every piece of device scratch and pinned host staging the handle
+ * will ever use (no later call allocates).  On success *out owns all of it.
+ * Errors: VT_ERR_INVALID_ARG (null pointer, capacity out of range),
+ * VT_ERR_CUDA (no such device, out of memory, not an sm_103 GPU). */
+int vt_sampler_create(const vt_sampler_config* config, vt_sampler** out);
+
+/* Free everything the handle owns.  Waits for the handle's pending work.
+ * NULL is ignored. */
+void vt_sampler_destroy(vt_sampler* handle);
+
+/* Upload per-row sampling parameters and seeds for rows 0..B-1 (host arrays
+ * of length B).  Row r's seed is the seed its next vt_sample call keys its
+ * noise stream with; each vt_sample advances it by 0x9E3779B97F4A7C15.
+ *   temperature  >= 0 and finite; 0 means greedy; 1.0f/T must be finite.
+ *   top_k        >= 0; 0 or >= V disables; 1 means greedy.
+ *   top_p        in [0, 1]; 1 disables; 0 means greedy.
+ *   min_p        in [0, 1]; 0 disables; 1 means greedy.
+ *   presence, frequency  finite (0 disables).
+ *   repetition   finite and > 0 (1 disables).
+ * Errors: VT_ERR_INVALID_ARG (any value out of range; nothing uploaded),
+ * VT_ERR_CAPACITY (B > max_batch), VT_ERR_CUDA. */
+int vt_reset_params(vt_sampler* handle, int32_t B, const float* temperature,
+                    const int32_t* top_k, const float* top_p, const float* min_p,
+                    const float* presence, const float* frequency,
+                    const float* repetition, const uint64_t* seed, void* stream);
+
+/* Rebuild the token counts of rows 0..B-1 from host CSR arrays: row r's prompt
+ * ids are prompt_ids[prompt_offsets[r] .. prompt_offsets[r+1]), likewise its
+ * output ids (offsets: B+1 entries, non-decreasing, starting at 0).  The counts
+ * of a row are the multiset counts over both.  Ids must lie in
+ * [0, max_vocab); a vt_sample call with a smaller V ignores ids >= V.
+ * Errors: VT_ERR_INVALID_ARG (bad offsets or ids), VT_ERR_CAPACITY (B >
+ * max_batch, or a row with more than max_history ids), VT_ERR_CUDA. */
+int vt_reset_token_counts(vt_sampler* handle, int32_t B, const int32_t* prompt_ids,
+                          const int64_t* prompt_offsets, const int32_t* output_ids,
+                          const int64_t* output_offsets, void* stream);
+
+/* Sample one token for each of rows 0..B-1.
+ *   logits            device [B][ld] elements of `dtype`; row r starts at
+ *                     logits + r*ld; only columns [0, V) are read.  Rows whose
+ *                     start is 16-byte aligned (base pointer and ld * element
+ *                     size multiples of 16) are staged with bulk copies; other
+ *                     layouts are read with plain loads (slower, same result).
+ *   V, ld             1 <= V <= max_vocab, ld >= V.
+ *   num_logprobs      0..max_logprobs top log-probs per row.
+ *   update_counts     nonzero: add each row's drawn token to its counts.
+ *   out_tokens        device int32[B]: token id, or -1 for a row with status
+ *                     NONFINITE or EMPTY.
+ *   out_logprobs      device float[B]: log-softmax of z_t at the token (NaN for
+ *                     a row without a token); may be NULL.
+ *   out_topk_ids      device int32[B][num_logprobs] and
+ *   out_topk_logprobs device float[B][num_logprobs]: the num_logprobs first
+ *                     tokens of the order (z_t descending, index ascending)
+ *                     and their log-probs; -1 / NaN for a row without a token;
+ *                     may be NULL only when num_logprobs == 0.
+ * The call enqueues device work only: it allocates nothing, does not
+ * synchronise, and may be captured into a CUDA graph.
+ * Errors: VT_ERR_STATE (no vt_reset_params yet, B larger than the rows given
+ * there, or a row with penalties whose counts were never reset),
+ * VT_ERR_INVALID_ARG, VT_ERR_CAPACITY, VT_ERR_CUDA (launch failure).  Device-
+ * side faults of the call (a bounded wait that ran out) are reported by
+ * vt_check_device_errors. */
+int vt_sample(vt_sampler* handle, const void* logits, int32_t dtype, int32_t B, int32_t V,
+              int64_t ld, int32_t num_logprobs, int32_t update_counts, int32_t* out_tokens,
+              float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
+              void* stream);
+
+/* vt_sample from host memory: copies host logits [B][ld] into the handle's
+ * device staging (created with host_io = 1), samples, copies the outputs back
+ * into the host arrays (same shapes as vt_sample's), and synchronises
+ * `stream` before returning.  Errors as vt_sample, plus VT_ERR_STATE when the
+ * handle has no host staging. */
+int vt_sample_host(vt_sampler* handle, const void* host_logits, int32_t dtype, int32_t B,
+                   int32_t V, int64_t ld, int32_t num_logprobs, int32_t update_counts,
+                   int32_t* host_tokens, float* host_logprobs, int32_t* host_topk_ids,
+                   float* host_topk_logprobs, void* stream);
+
+/* Synchronise the handle's last stream and report device-side faults raised
+ * since the previous check: VT_ERR_TIMEOUT when a bounded wait inside a kernel
+ * ran out (the kernel then returned early and its outputs are not valid),
+ * VT_OK otherwise.  Clears the device error word.  vt_sample_host calls it. */
+int vt_check_device_errors(vt_sampler* handle);
+
+/* Copy the row status of the last vt_sample (VT_ROW_*) into device int32[B]
+ * (B of that call). */
+int vt_get_row_status(vt_sampler* handle, int32_t* dev_status, void* stream);
+
+/* Test and debug view of the last vt_sample, per row, into device arrays of
+ * that call's B: the tempered logit and index of the last kept element of the
+ * order after min-p, top-k and top-p, and the number of kept elements (1 for a
+ * greedy row; 0 for a row without a token). */
+int vt_debug_filter_boundary(vt_sampler* handle, float* kth_value, int32_t* kth_index,
+                             int32_t* kept_count, void* stream);
+
+/* Read row `row`'s count table into host arrays of `capacity` entries: the
+ * distinct ids in increasing order and their counts; *n_unique is set to the
+ * table length (entries beyond capacity are not written).  Synchronises the
+ * handle's last stream. */
+int vt_debug_get_counts(vt_sampler* handle, int32_t row, int32_t* ids, int32_t* counts,
+                        int32_t capacity, int32_t* n_unique);
+
+/* Read the current per-row seeds of rows 0..B-1 into a host array (B of the
+ * last vt_reset_params).  Synchronises the handle's last stream. */
+int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
+
+/* Message for the last failing call on `handle` ("" if none); static storage
+ * owned by the handle, valid until the next call on it. */
+const char* vt_last_error(const vt_sampler* handle);
+
+/* Name of a VT_OK / VT_ERR_* code. */
+const char* vt_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VT_SAMPLER_H */
