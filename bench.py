@@ -1,0 +1,399 @@
+"""Benchmark of the batched decode sampler (one JSON line on rank 0).
+
+A step is one vt_sample call over one batch of synthetic logits: penalties,
+temperature, min-p / top-k / top-p, the seeded Gumbel-max draw, log-probs and
+top-n log-probs for every row.  The default workload is B=256 rows of
+V=151,936 bf16 logits with mixed per-row strategies (25% greedy, 25% top-k
+only, 25% top-p only, 25% top_k=50 + top_p=0.95 + min_p=0.05; T ~ U[0.3, 1.5];
+20 top log-probs), the configuration the 70%-of-HBM-peak target is stated on.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload b256|b32|b64|large|tiny]
+                  [--impl reference]
+For N > 1 launch with torchrun; each rank samples its own batch (weak scaling,
+no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import glob
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from device_token_sampling_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sampled rows/s, full sampling pipeline"
+UNIT = "rows/s"
+PEAK_FALLBACK_GBS = 6800.0
+N_ROTATE = 4  # input buffers rotated between steps (b256: 4 x 77.8 MB > 129 MB L2)
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def make_workload(name: str, rank: int) -> W.Workload:
+    if name == "b256":
+        return W.b256(seed=3 + 1000 * rank)
+    if name == "b32":
+        return W.b32(seed=1 + 1000 * rank)
+    if name == "b64":
+        return W.b64(seed=2 + 1000 * rank)
+    if name == "tiny":
+        return W.tiny(seed=1000 * rank)
+    if name == "large":
+        return W.large(seed=4 + 1000 * rank)
+    raise ValueError(name)
+
+
+def algorithmic_bytes_per_row(w: W.Workload) -> np.ndarray:
+    """Bytes one row must move at minimum: its logits once, its distinct
+    (id, count) history pairs, its parameters and seed (read + write), and its
+    outputs (token, log-prob, status, kept boundary, top-n ids and log-probs)."""
+    uniq = np.zeros(w.B, np.int64)
+    for r in range(w.B):
+        ids = np.concatenate([w.prompt_ids[w.prompt_offsets[r]:w.prompt_offsets[r + 1]],
+                              w.output_ids[w.output_offsets[r]:w.output_offsets[r + 1]]])
+        pen = (w.presence[r] != 0) or (w.frequency[r] != 0) or (w.repetition[r] != 1)
+        uniq[r] = len(np.unique(ids)) if pen else 0
+    params = 48 + 16
+    outputs = 4 + 4 + 4 + 12 + 8 * w.num_logprobs
+    return w.V * w.elem_size + 8 * uniq + params + outputs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return PEAK_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "device_token_sampling_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"vt_sample_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_h = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_h or not m_t or m_h.group(1) != kernel_source_hash():
+        return None
+    return int(m_t.group(1))
+
+
+class ClockSampler:
+    """Samples the SM clock and clock-event reasons through NVML (read only)."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.ok = False
+        self.max_mhz = None
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value & ~0x1
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+
+    def stop(self):
+        if self._t:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "unavailable"}
+        names = [n for b, n in self.REASONS.items() if self.reasons & b]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples), "source": "nvml"}
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample of the workload
+# --------------------------------------------------------------------------
+
+def time_oracle_rows(w: W.Workload, rows: np.ndarray):
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.sample_workload(w, rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: W.Workload, budget_rows: int | None = None):
+    rows = np.arange(w.B) if budget_rows is None else np.arange(min(w.B, budget_rows))
+    dt = time_oracle_rows(w, rows)
+    return {"value": len(rows) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(rows)} rows of one {w.name} step (every strategy class), "
+                      f"single-threaded C++ oracle, {dt:.2f} s"}
+
+
+# --------------------------------------------------------------------------
+# reference arm
+# --------------------------------------------------------------------------
+
+def run_reference(args, w: W.Workload):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    # a step of the reference arm is one row of the workload (the oracle is
+    # timed as it stands, single-threaded); rows cycle through every class
+    import oracle
+    oracle.build()
+    order = np.arange(w.B)
+    for i in range(args.warmup):
+        oracle.sample_workload(w, rows=[int(order[i % w.B])])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.sample_workload(w, rows=[int(order[(args.warmup + i) % w.B])])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"one {w.name} row per step, rows cycling through "
+                                       "every strategy class, single thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: W.Workload):
+    return {"workload": w.name, "B": w.B, "V": w.V, "ld": w.ld,
+            "logits_dtype": "f32" if w.dtype == W.DTYPE_F32 else "bf16",
+            "num_logprobs": w.num_logprobs,
+            "l2": f"{N_ROTATE} rotating input buffers"
+                  f" ({N_ROTATE * w.logits_bytes() / 1e6:.0f} MB > 129 MB L2)",
+            "parallelism": "row batches per GPU (replicas)"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args, w: W.Workload):
+    import torch
+    import torch.distributed as dist
+
+    from device_token_sampling_gb300 import sampler as S
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    B, V, n = w.B, w.V, w.num_logprobs
+    penalised = bool(((w.presence != 0) | (w.frequency != 0) | (w.repetition != 1)).any())
+    hist = int(np.max(np.diff(w.prompt_offsets) + np.diff(w.output_offsets))) if B else 0
+    max_hist = hist + args.steps + args.warmup + 512 if penalised else 0
+    s = S.Sampler(max_batch=B, max_vocab=V, max_logprobs=n, max_history=max_hist, device=local,
+                  host_io=True)
+    s.reset_workload(w)
+    update = penalised
+    # device inputs: N_ROTATE distinct batches (inputs larger than L2)
+    base = torch.from_numpy(np.ascontiguousarray(w.logits))
+    if w.dtype == W.DTYPE_BF16:
+        base = base.view(torch.int16)
+    bufs = []
+    gen = torch.Generator(device=dev)
+    for i in range(N_ROTATE):
+        x = base.to(dev)
+        if i > 0:  # a different batch of the same distribution: permute rows
+            gen.manual_seed(1000 * rank + i)
+            x = x[torch.randperm(B, device=dev, generator=gen)].contiguous()
+        bufs.append(x)
+    dt = W.DTYPE_BF16 if w.dtype == W.DTYPE_BF16 else W.DTYPE_F32
+    stream = torch.cuda.Stream(device=dev)
+    outs = [(torch.empty(B, dtype=torch.int32, device=dev),
+             torch.empty(B, dtype=torch.float32, device=dev),
+             torch.empty((B, n), dtype=torch.int32, device=dev),
+             torch.empty((B, n), dtype=torch.float32, device=dev)) for _ in range(N_ROTATE)]
+
+    def step(i):
+        s.sample(bufs[i % N_ROTATE], V=V, num_logprobs=n, update_counts=update,
+                 out=outs[i % N_ROTATE], stream=stream, dtype=dt)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    stream.synchronize()
+    s.check_device_errors()
+    # capture N_ROTATE steps into one graph (launch overhead out of the timed region)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(N_ROTATE):
+            step(i)
+    for _ in range(2):
+        graph.replay()
+    stream.synchronize()
+    reps, rem = divmod(args.steps, N_ROTATE)
+    clocks = ClockSampler(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        for i in range(rem):
+            step(i)
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    clocks.stop()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    s.check_device_errors()
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    ms_per_step = max_ms / args.steps
+    rows_total = B * args.steps * world
+    value = rows_total / (max_ms / 1e3)
+
+    # end to end through the C ABI with host buffers: H2D of the step's logits
+    # from pinned memory, sampling, D2H of the step's outputs, every step
+    e2e_steps = max(3, min(args.steps, 200))
+    host = torch.from_numpy(np.ascontiguousarray(w.logits)).pin_memory().numpy()
+    ho = (np.empty(B, np.int32), np.empty(B, np.float32), np.empty((B, n), np.int32),
+          np.empty((B, n), np.float32))
+    for i in range(3):
+        s.sample_host(host, V, dt, n, update, stream=stream, out=ho)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        s.sample_host(host, V, dt, n, update, stream=stream, out=ho)
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = B * e2e_steps * world / float(te.item())
+    h2d = int(host.nbytes)
+    d2h = int(sum(a.nbytes for a in ho))
+
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        alg = int(algorithmic_bytes_per_row(w).sum())
+        kernel_ms = max_ms / args.steps  # one kernel per step in the timed region
+        achieved = alg / (kernel_ms * 1e-3) / 1e9
+        traffic = profiled_traffic(w.name)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(w),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} (hbm_gbs)",
+                         "algorithmic_bytes_per_launch": alg, "kernel": "sample_kernel",
+                         "kernel_ms": kernel_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "api": "vt_sample_host (pinned host logits in, host outputs back)"},
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+            "ns_per_row": 1e6 * ms_per_step / B,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, budget_rows=args.cpu_rows)
+        print(json.dumps(line), flush=True)
+    s.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="b256", choices=W.NAMES)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, _ = dist_env()
+    w = make_workload(args.workload, rank)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        from device_token_sampling_gb300 import _build
+        _build.build()
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

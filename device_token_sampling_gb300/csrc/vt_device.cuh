@@ -163,7 +163,7 @@ __device__ __forceinline__ float log_exp_noise(uint32_t b) {
 
 // Gumbel score z_t - ln(-ln u).
 __device__ __forceinline__ float gumbel_score(float zt, uint32_t b) {
-  return zt - log_exp_noise(b);
+  return __fsub_rn(zt, log_exp_noise(b));
 }
 
 // A cheap certificate that an element cannot beat the score `s_cur`:
@@ -172,7 +172,7 @@ __device__ __forceinline__ float gumbel_score(float zt, uint32_t b) {
 // score has to be computed.
 __device__ __forceinline__ bool may_beat(float zt, float s_cur, uint32_t b) {
   const float one_minus_u = (float)(2u * (0xFFFFFFu - b) + 1u) * 0x1p-25f;
-  const float t = ex2_approx((zt - s_cur) * kLog2e);
+  const float t = ex2_approx(__fmul_rn(__fsub_rn(zt, s_cur), kLog2e));
   return one_minus_u < t * 1.00390625f;
 }
 
@@ -195,9 +195,10 @@ __device__ __forceinline__ float key_z(uint64_t k) { return key_value((uint32_t)
 __device__ __forceinline__ uint32_t key_idx(uint64_t k) { return ~(uint32_t)k; }
 
 // Mass of an element relative to the row max, in 2^-40 fixed point (exact,
-// order-independent sums).
+// order-independent sums).  Explicitly rounded operations: the same element
+// must get the same mass in every pass, whatever the compiler fuses.
 __device__ __forceinline__ unsigned long long mass_fixed(float zt, float m_t) {
-  const float w = ex2_approx((zt - m_t) * kLog2e);
+  const float w = ex2_approx(__fmul_rn(__fsub_rn(zt, m_t), kLog2e));
   return __float2ull_rz(w * 0x1p40f);
 }
 

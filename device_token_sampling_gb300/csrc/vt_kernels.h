@@ -16,8 +16,13 @@ struct SampleArgs {
   int32_t B, V;
   int32_t n_logprobs;
   int32_t update_counts;
-  int32_t slice;             // elements per CTA (multiple of 16)
-  int32_t use_bulk;          // rows 16-byte aligned: stage with bulk copies
+  int32_t slice;             // elements per CTA (multiple of 32)
+  int32_t aligned;           // rows 16-byte aligned: 16-byte vector loads
+  int32_t pen_smem;          // dynamic smem holds the penalty bitmap and prefix
+  uint32_t off_gmax;         // dynamic smem offsets (bytes)
+  uint32_t off_mrg;
+  uint32_t off_bitmap;
+  uint32_t off_prefix;
   const RowParams* params;   // [B]
   uint64_t* seeds;           // [B], advanced by the kernel
   int2* hist;                // [B][hist_cap] sorted (id, count)
@@ -33,20 +38,31 @@ struct SampleArgs {
   int32_t* dbg_kth_index;    // [B]
   int32_t* dbg_kept;         // [B]
   int32_t* err_word;         // one int, kErr* bits
+  unsigned long long* trace; // optional [grid][kTraceSlots] phase timestamps (ns)
 };
+
+constexpr int kTraceSlots = 16;
 
 struct LaunchPlan {
-  int cluster;       // CTAs per row
-  int slice;         // elements per CTA
-  size_t smem;       // dynamic shared memory per CTA
+  int cluster;        // CTAs per row
+  int slice;          // elements per CTA
+  int pen_smem;       // penalty bitmap in shared memory
+  uint32_t off_gmax, off_mrg, off_bitmap, off_prefix;
+  size_t smem;        // dynamic shared memory per CTA
+  int active_clusters;  // clusters resident at once (filled by prepare_sample)
 };
 
-// Shared-memory plan for a (V, element size) pair; cluster in {1,2,4,8,16}.
-LaunchPlan plan_sample(int V, int elem_size);
+// Shared-memory layout for V elements of elem_size bytes split over `cluster`
+// CTAs (1, 2, 4, 8 or 16).
+LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties);
 
-// Prepare kernel attributes (dynamic smem, non-portable clusters); checks that
-// at least one cluster of the plan can be resident.  Returns a cudaError_t.
-cudaError_t prepare_sample(const LaunchPlan& plan, int dtype, int* max_active_clusters);
+// Choose the cluster size for a call: as many CTAs per row as still lets all
+// B rows be resident in one wave, within the slice-size limits.
+LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, int num_sms);
+
+// Prepare kernel attributes (dynamic smem, non-portable clusters); fills
+// plan.active_clusters.  Returns a cudaError_t.
+cudaError_t prepare_sample(LaunchPlan& plan, int dtype);
 
 // Launch the fused sampling kernel: grid B * cluster CTAs.
 cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,

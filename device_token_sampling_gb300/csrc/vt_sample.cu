@@ -1,33 +1,35 @@
 // vt_sample.cu -- the fused batched decode sampling kernel for sm_103a.
 //
-// One thread-block cluster per logits row.  Each CTA of the cluster owns one
-// contiguous slice of the row, stages it ONCE in shared memory with bulk
-// asynchronous copies (cp.async.bulk, completion on an mbarrier), and runs
-// every pass of the pipeline over shared memory; HBM sees each logit once.
-// Cross-CTA results move through distributed shared memory (DSMEM) between
-// hardware cluster barriers, so no CTA ever spins on another.
+// One thread-block cluster per logits row; each CTA owns a contiguous slice
+// of the row.  The cluster size is chosen per call so that every row of the
+// batch is resident at once (one wave): a row's latency then overlaps every
+// other row's HBM stream, and HBM sees each logit once.
 //
 // Pipeline per row (pages: TensorRT-LLM "Sampling" for the penalty, temperature
 // and filter formulas; vllm.cpp's Gumbel-draw pull request for the seeded
 // draw and the lowest-index ArgReduce; the Tenstorrent sampling README for the
 // log-softmax and the reset-then-sample state):
-//   1. penalties: the row's (id, count) table entries that fall in the slice
-//      are rewritten (repetition, frequency, presence) into a side list and
-//      masked out of the dense slice;
-//   2. pass A: row max, online sum of exp, lowest-index argmax, per-group and
-//      per-thread maxima (temperature folded into one FFMA per element);
-//   3. candidates: a threshold that provably admits at least K elements
-//      (the K/C-th largest per-thread maximum of each CTA, minimum over the
-//      cluster) collects a prefix of the order (value desc, index asc) into
-//      the leader CTA, which sorts it and applies min-p, top-k and top-p
-//      without touching the rest of the row;
-//   4. when the kept set is not inside the candidates (a wide top-p nucleus,
-//      a large top-k, an unfiltered draw), a cluster-wide radix select on
-//      64-bit (value, index) keys with count/mass histograms finds the exact
-//      boundary, and a draw pass scores only elements that can still win
-//      (a 1 - u >= exp(z - s) certificate skips the logarithms);
-//   5. outputs: token, its log-prob, top-n log-probs, row status, the kept
-//      boundary, the seed advance and the optional count append.
+//   setup    the row's (id, count) entries inside the slice are penalised
+//            (repetition, frequency, presence) into a side list, and a bitmap
+//            marks their positions; every load of the slice patches them in
+//            registers, so all passes see the penalised values;
+//   pass A   16-byte vector loads stream the slice once: row max, sum of
+//            exp (temperature folded into one FFMA), lowest-index argmax, a
+//            conservative max per 32-byte group, and per-thread maxima, from
+//            which each CTA derives a candidate threshold that admits at
+//            least K/C of its elements (published with the pass-A partials);
+//   pass B   only groups whose max clears the cluster-wide threshold are
+//            re-read (from L2) and their candidates kept in shared memory;
+//   leader   the candidates (a prefix of the order value desc, index asc) are
+//            gathered into one CTA, sorted in registers, and min-p, top-k,
+//            top-p and the Gumbel-max draw run on them;
+//   slow     when the kept set reaches past the candidates (a wide top-p
+//            nucleus, a large top-k, an unfiltered draw), a cluster-wide radix
+//            select on 64-bit (value, index) keys with count/mass histograms
+//            finds the exact boundary and a draw pass scores only elements
+//            that can still win.
+// Cross-CTA results move through distributed shared memory between hardware
+// cluster barriers; no CTA spins on another.
 #include "vt_device.cuh"
 #include "vt_kernels.h"
 
@@ -38,13 +40,20 @@ namespace cg = cooperative_groups;
 namespace vt {
 namespace {
 
-constexpr int kGatherCap = 2048;    // keys the leader CTA can hold and sort
+constexpr int kBufCap = 2048;       // candidate keys a CTA (and the leader) can hold
 constexpr int kBinBits = 10;
 constexpr int kBins = 1 << kBinBits;
 constexpr int kDefaultCand = 512;   // candidates tried for top-p / min-p rows
 constexpr int kGroupBytes = 32;     // one thread step: two 16-byte vectors
-constexpr uint32_t kBulkChunk = 32768;
 constexpr int kMaxCluster = 16;
+constexpr int kStageBytes = kThreads * kGroupBytes;  // 8 KB: one group per thread
+constexpr int kStages = 4;                           // bulk-copy ring depth of pass A
+constexpr int kRingBytes = kStageBytes * kStages;    // aliases the candidate buffer
+constexpr int kSmallK = 32;  // up to this many per CTA, thresholds come from thread maxima
+// the ring region also holds the candidate buffer (kBufCap keys) followed by
+// the level-0 per-bin bests; the histograms alias the buffer
+static_assert(kBufCap * 8 + (1 << 10) * 8 <= kRingBytes, "ring region too small");
+static_assert((1 << 10) * 12 <= kBufCap * 8, "histograms exceed the candidate buffer");
 
 // Row status codes (match VT_ROW_* in the public header).
 constexpr int kRowOk = 0, kRowNonfinite = 1, kRowEmpty = 2, kRowHistoryFull = 3;
@@ -54,30 +63,31 @@ struct Elt;
 
 template <>
 struct Elt<float> {
-  static constexpr int kPerGroup = kGroupBytes / 4;
-  __device__ static void load(const float* d, int g, float* x) {
-    const uint4* p = reinterpret_cast<const uint4*>(d + g * kPerGroup);
-    const uint4 a = p[0], b = p[1];
+  static constexpr int E = kGroupBytes / 4;
+  __device__ static void load_vec(const float* p, float* x) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    const uint4 a = __ldg(q), b = __ldg(q + 1);
     x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
     x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
     x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
     x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
   }
-  __device__ static float at(const float* d, int e) { return d[e]; }
-  __device__ static void mask(float* d, int e) { d[e] = -INFINITY; }
-  __device__ static void copy_global(float* d, int e, const float* row, int64_t j) {
-    d[e] = __ldg(row + j);
+  __device__ static float load1(const float* p) { return __ldg(p); }
+  __device__ static void unpack(const uint4& a, const uint4& b, float* x) {
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
   }
-  __device__ static void fill_neg_inf(float* d, int e) { d[e] = -INFINITY; }
 };
 
 // bfloat16 stored as its 16 bits; widening to fp32 is exact (a 16-bit shift).
 template <>
 struct Elt<uint16_t> {
-  static constexpr int kPerGroup = kGroupBytes / 2;
-  __device__ static void load(const uint16_t* d, int g, float* x) {
-    const uint4* p = reinterpret_cast<const uint4*>(d + g * kPerGroup);
-    const uint4 a = p[0], b = p[1];
+  static constexpr int E = kGroupBytes / 2;
+  __device__ static void load_vec(const uint16_t* p, float* x) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    const uint4 a = __ldg(q), b = __ldg(q + 1);
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -85,22 +95,50 @@ struct Elt<uint16_t> {
       x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
   }
-  __device__ static float at(const uint16_t* d, int e) {
-    return __uint_as_float((uint32_t)d[e] << 16);
+  __device__ static float load1(const uint16_t* p) {
+    return __uint_as_float((uint32_t)__ldg(p) << 16);
   }
-  __device__ static void mask(uint16_t* d, int e) { d[e] = 0xFF80u; }
-  __device__ static void copy_global(uint16_t* d, int e, const uint16_t* row, int64_t j) {
-    d[e] = __ldg(row + j);
+  __device__ static void unpack(const uint4& a, const uint4& b, float* x) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
   }
-  __device__ static void fill_neg_inf(uint16_t* d, int e) { d[e] = 0xFF80u; }
 };
+
+// Group maxima are kept as the largest bf16 value <= the true maximum: a lower
+// bound for the candidate threshold, and (one bf16 step up) an upper bound for
+// the group filters, so both stay exact.
+__device__ __forceinline__ uint16_t bf16_down(float f) {
+  const uint32_t u = __float_as_uint(f);
+  if (f != f) return 0x7FC0u;
+  if (u & 0x80000000u) return (uint16_t)((u >> 16) + ((u & 0xFFFFu) ? 1u : 0u));
+  return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ float bf16_val(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// The next bf16 value above b (an upper bound of the group's true maximum).
+__device__ __forceinline__ float bf16_next_up(uint16_t b) {
+  uint32_t n;
+  if (b == 0xFF80u) return -INFINITY;  // a group of -inf stays -inf
+  if (b & 0x8000u)
+    n = (b & 0x7FFFu) ? (uint32_t)(b - 1u) : 0x0001u;
+  else
+    n = (b >= 0x7F80u) ? b : (uint32_t)(b + 1u);
+  return __uint_as_float(n << 16);
+}
+// Order-preserving 16-bit key of a bf16 bit pattern (no NaNs).
+__device__ __forceinline__ uint32_t ord16(uint16_t b) {
+  return (b & 0x8000u) ? (uint32_t)(~b & 0xFFFFu) : (uint32_t)(b | 0x8000u);
+}
 
 // Per-CTA partial results; other CTAs of the cluster read them over DSMEM.
 struct Part {
   float m, s, bv;
   int bi;
   int nonfinite;
-  float tau;
+  float tau, tau_n;  // candidate thresholds: for the kept set, for top-n only
   int ncand, ncand_minp;
   unsigned long long cand_mass;
   unsigned long long rng_cnt, rng_mass;
@@ -112,24 +150,23 @@ struct Part {
   int err;
 };
 
-// Row-level values every CTA derives identically from the partials.
 struct RowStats {
   float M, S, m_t, lnS, bv;
   int bi;
   int nonfinite;
-  float tau;
-  int nc, nc_minp;
+  float tau, tau_n;
+  int nc, nc_minp, push_off, overflow;
   unsigned long long cand_mass;
   int err;
 };
 
-// Selection result, written by the leader and read by every CTA.
 struct SelOut {
   unsigned long long kb, cnt_incl, mass_incl, total_cnt, total_mass;
+  unsigned long long win;  // best (score, index) key over the kept set when draw_ok
   int all;
+  int draw_ok;
 };
 
-// Digit walk of one selection level (identical in every CTA).
 struct Walk {
   int d;
   int found;
@@ -137,17 +174,18 @@ struct Walk {
 };
 
 struct __align__(16) Smem {
-  uint64_t mbar;
+  uint64_t full[kStages];  // bulk-copy completion, one mbarrier per ring slot
+  unsigned int hist256[256];
   Part part;
   RowStats rs;
   SelOut sel;
   Walk walk;
-  int gcount;
-  int e_lo, e_hi;
+  int nloc;    // candidates in this CTA's buffer
+  int gcount;  // band keys gathered in the leader (selection)
   int bcast_i[4];
   float bcast_f[4];
   unsigned long long bcast_u[4];
-  float tmax[kThreads];
+  __align__(16) float tmax[kThreads];
   float rf[kWarps * 4];
   int ri[kWarps * 4];
   unsigned long long ru[kWarps * 4];
@@ -156,23 +194,135 @@ struct __align__(16) Smem {
 struct Ctx {
   int tid, lane, warp;
   int C, rank, row, V, lo, hi, slice, ngroups;
-  float inv_t, ax;     // 1/T and log2(e)/T
-  float m_t, lnS;      // row max of z_t, ln(sum exp(z_t - m_t))
+  bool aligned, pen;
+  float inv_t, ax;  // 1/T and log2(e)/T
+  float m_t, lnS;   // row max of z_t, ln(sum exp(z_t - m_t))
   bool greedy, topk, topp, minp;
   int top_k;
   float top_p;
-  double lmp;          // ln(min_p)
-  float* gmax;         // per group max of the pre-temperature values
-  uint64_t* gather;    // leader key buffer (this CTA's copy)
-  unsigned int* hcnt;  // selection histograms (alias the gather buffer)
+  double lmp;       // ln(min_p)
+  const void* rowp;
+  uint16_t* gmax;   // conservative bf16 max of each group (pre-temperature)
+  uint64_t* buf;    // candidate keys / gathered keys / histograms
+  unsigned int* hcnt;
   unsigned long long* hmass;
   unsigned int* mcnt;  // merged bins of this CTA's digit range
   unsigned long long* mmass;
-  const int2* tab;     // this row's count table
-  const float* zs;     // penalised values of the table entries
-  int e_lo, e_hi;      // table entries inside the slice
-  uint64_t rkey;       // noise stream key
+  unsigned long long* hbest;  // level-0 best Gumbel key per bin (score, index)
+  unsigned long long* mbest;
+  const uint32_t* bitmap;  // penalised positions of the slice
+  const uint16_t* prefix;  // side-list index of each bitmap word's first bit
+  const float* side_z;     // penalised values, in id order, of this slice
+  uint64_t rkey;           // noise stream key
+  unsigned long long* trace;  // optional phase trace of this CTA (kTraceSlots stamps)
 };
+
+// Phase stamp from inside helpers (slot k of this CTA's trace).
+#define VT_CTRACE(c, k)                                                   \
+  do {                                                                    \
+    if ((c).trace && threadIdx.x == 0) (c).trace[(k)] = global_timer_ns(); \
+  } while (0)
+
+// Optional phase trace: thread 0 stamps the global timer into slot k.
+#define VT_TRACE(k)                                                        \
+  do {                                                                     \
+    if (a.trace && threadIdx.x == 0)                                       \
+      a.trace[(size_t)blockIdx.x * kTraceSlots + (k)] = global_timer_ns(); \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// loading one 32-byte group of the slice into registers
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void patch_group(const Ctx& c, int g, float* x);
+
+template <typename T>
+__device__ __forceinline__ void load_group(const Ctx& c, int g, float* x) {
+  constexpr int E = Elt<T>::E;
+  const T* row = reinterpret_cast<const T*>(c.rowp);
+  const int j0 = c.lo + g * E;
+  if (c.aligned && j0 + E <= c.hi) {
+    Elt<T>::load_vec(row + j0, x);
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = (j0 + i < c.hi) ? Elt<T>::load1(row + j0 + i) : -INFINITY;
+  }
+  patch_group<T>(c, g, x);
+}
+
+// Replace the penalised positions of group g by their side-list values.
+template <typename T>
+__device__ __forceinline__ void patch_group(const Ctx& c, int g, float* x) {
+  constexpr int E = Elt<T>::E;
+  if (c.pen) {
+    const int bit0 = g * E;
+    const uint32_t word = c.bitmap[bit0 >> 5];
+    const uint32_t m = (word >> (bit0 & 31)) & ((E == 32) ? 0xFFFFFFFFu : ((1u << E) - 1u));
+    if (m != 0u) {
+      int idx = (int)c.prefix[bit0 >> 5] + __popc(word & ((1u << (bit0 & 31)) - 1u));
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        if (m & (1u << i)) {
+          x[i] = c.side_z[idx];
+          ++idx;
+        }
+      }
+    }
+  }
+}
+
+// Visit the elements of every group whose conservative max passes
+// group_ok(max * inv_t); elem(zt, j) gets the tempered value and global index.
+template <typename T, typename GF, typename FN>
+__device__ __forceinline__ void for_each_group(const Ctx& c, GF group_ok, FN fn) {
+  // Groups whose conservative max passes group_ok(max * inv_t), in the order
+  // g = tid, tid + kThreads, ...; the next such group's 32 bytes are loaded
+  // while the current one is processed.  fn(x, g, j0) gets the (penalised)
+  // pre-temperature values of elements j0 .. j0 + E - 1 (-inf past the row).
+  constexpr int E = Elt<T>::E;
+  auto next_ok = [&](int g) {
+    while (g < c.ngroups && !group_ok(__fmul_rn(bf16_next_up(c.gmax[g]), c.inv_t))) g += kThreads;
+    return g;
+  };
+  auto vec_ok = [&](int g) { return c.aligned && c.lo + (g + 1) * E <= c.hi; };
+  auto fetch = [&](int g, uint4& u0, uint4& u1) {
+    const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(c.rowp) + c.lo +
+                                                    g * E);
+    u0 = __ldg(q);
+    u1 = __ldg(q + 1);
+  };
+  int g = next_ok(c.tid);
+  uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
+  if (g < c.ngroups && vec_ok(g)) fetch(g, a0, a1);
+  while (g < c.ngroups) {
+    const int gn = next_ok(g + kThreads);
+    uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
+    if (gn < c.ngroups && vec_ok(gn)) fetch(gn, b0, b1);
+    float x[E];
+    if (vec_ok(g)) {
+      Elt<T>::unpack(a0, a1, x);
+      patch_group<T>(c, g, x);
+    } else {
+      load_group<T>(c, g, x);
+    }
+    fn(x, g, c.lo + g * E);
+    a0 = b0;
+    a1 = b1;
+    g = gn;
+  }
+}
+
+// Elementwise view of for_each_group: elem(zt, j) gets the tempered value
+// fl(x * (1/T)) and the global index of every element of the row.
+template <typename T, typename GF, typename EF>
+__device__ __forceinline__ void for_each_elem(const Ctx& c, GF group_ok, EF elem) {
+  constexpr int E = Elt<T>::E;
+  for_each_group<T>(c, group_ok, [&](float* x, int, int j0) {
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+      if (j0 + i < c.hi) elem(__fmul_rn(x[i], c.inv_t), j0 + i);
+  });
+}
 
 // ---------------------------------------------------------------------------
 // block-level helpers (all threads of the CTA must call them)
@@ -259,7 +409,7 @@ __device__ unsigned long long block_exclusive_u64(unsigned long long v, Smem& s,
   if (lane == 31) s.ru[warp] = inc;
   __syncthreads();
   if (threadIdx.x < 32) {
-    unsigned long long t = threadIdx.x < kWarps ? s.ru[threadIdx.x] : 0ull;
+    const unsigned long long t = threadIdx.x < kWarps ? s.ru[threadIdx.x] : 0ull;
     unsigned long long ti = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -324,55 +474,83 @@ __device__ void block_argmax(float& v, int& i, float& z, Smem& s) {
   __syncthreads();
 }
 
-// Bitonic sort, descending, of n (a power of two) keys in shared memory.
-__device__ void bitonic_desc_u64(uint64_t* keys, int n) {
-  for (int k = 2; k <= n; k <<= 1) {
+// Descending bitonic sort of KPT * kThreads keys held KPT per thread
+// (consecutive), exchanging through registers, warp shuffles, and shared
+// memory only for partners in other warps.
+template <int KPT>
+__device__ void block_sort_desc_impl(uint64_t* keys) {
+  constexpr int N = KPT * kThreads;
+  uint64_t v[KPT];
+  const int base = threadIdx.x * KPT;
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) v[q] = keys[base + q];
+  for (int k = 2; k <= N; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t a = keys[i], b = keys[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            keys[i] = b;
-            keys[ixj] = a;
+      if (j < KPT) {
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {
+          const int p = q ^ j;
+          if (p > q) {
+            const bool up = ((base + q) & k) == 0;
+            const uint64_t a = v[q], b = v[p];
+            if (up ? (a < b) : (a > b)) {
+              v[q] = b;
+              v[p] = a;
+            }
           }
         }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-__device__ void bitonic_desc_f32(float* v, int n) {
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const float a = v[i], b = v[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            v[i] = b;
-            v[ixj] = a;
-          }
+      } else if (j < 32 * KPT) {
+        const int lm = j / KPT;
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, v[q], lm);
+          const int i = base + q;
+          const bool lower = (i & j) == 0;
+          const bool up = (i & k) == 0;
+          v[q] = (lower == up) ? (v[q] > o ? v[q] : o) : (v[q] < o ? v[q] : o);
         }
+      } else {
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) keys[base + q] = v[q];
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {
+          const int i = base + q;
+          const uint64_t o = keys[i ^ j];
+          const bool lower = (i & j) == 0;
+          const bool up = (i & k) == 0;
+          v[q] = (lower == up) ? (v[q] > o ? v[q] : o) : (v[q] < o ? v[q] : o);
+        }
+        __syncthreads();
       }
-      __syncthreads();
     }
   }
+#pragma unroll
+  for (int q = 0; q < KPT; ++q) keys[base + q] = v[q];
+  __syncthreads();
 }
 
-__device__ __forceinline__ int pow2_ceil(int n) {
-  int p = 1;
-  while (p < n) p <<= 1;
-  return p;
+// Sort keys[0, n) descending (n <= kBufCap); pads with zeros up to a power of
+// two of at least kThreads.
+__device__ void block_sort_desc(uint64_t* keys, int n) {
+  int P2 = kThreads;
+  while (P2 < n) P2 <<= 1;
+  for (int i = n + threadIdx.x; i < P2; i += kThreads) keys[i] = 0ull;
+  __syncthreads();
+  if (P2 <= kThreads)
+    block_sort_desc_impl<1>(keys);
+  else if (P2 <= 2 * kThreads)
+    block_sort_desc_impl<2>(keys);
+  else if (P2 <= 4 * kThreads)
+    block_sort_desc_impl<4>(keys);
+  else
+    block_sort_desc_impl<8>(keys);
 }
 
 // min-p test z_t - m >= ln(min_p), decided exactly in double; fp32 decides
 // whenever it is far from the threshold.
 __device__ __forceinline__ bool minp_pass(float zt, float m_t, double lmp) {
-  const float d = zt - m_t;
+  const float d = __fsub_rn(zt, m_t);
   const float l = (float)lmp;
   const float margin = 1e-4f * (1.0f + fabsf(l));
   if (d > l + margin) return true;
@@ -391,38 +569,6 @@ __device__ __forceinline__ float penalize(float x, int count, const RowParams& P
   return z;
 }
 
-// Does this dense slot hold a penalised token (whose value lives in the side
-// list instead)?  Binary search of the slice's table entries.
-__device__ bool is_side_slot(const Ctx& c, int j) {
-  int a = c.e_lo, b = c.e_hi;
-  while (a < b) {
-    const int mid = (a + b) >> 1;
-    const int id = c.tab[mid].x;
-    if (id == j) return true;
-    if (id < j) a = mid + 1; else b = mid;
-  }
-  return false;
-}
-
-// Visit every element of the slice: dense groups whose max passes
-// `group_ok(fl(gmax * inv_t))`, then the side list.  elem(zt, j) gets the
-// tempered value and the global index.
-template <typename T, typename GF, typename EF>
-__device__ __forceinline__ void for_each_elem(const Ctx& c, const T* data, GF group_ok,
-                                              EF elem) {
-  constexpr int E = Elt<T>::kPerGroup;
-  for (int g = c.tid; g < c.ngroups; g += kThreads) {
-    if (!group_ok(c.gmax[g] * c.inv_t)) continue;
-    float x[E];
-    Elt<T>::load(data, g, x);
-    const int j0 = c.lo + g * E;
-#pragma unroll
-    for (int i = 0; i < E; ++i) elem(x[i] * c.inv_t, j0 + i, false);
-  }
-  for (int e = c.e_lo + c.tid; e < c.e_hi; e += kThreads)
-    elem(c.zs[e] * c.inv_t, c.tab[e].x, true);
-}
-
 // ---------------------------------------------------------------------------
 // cluster-wide radix selection on (value, index) keys
 // ---------------------------------------------------------------------------
@@ -433,62 +579,132 @@ enum Pred { kPredAll = 0, kPredSurv = 1 };
 // (by_mass = false) or whose inclusive mass exceeds p * (mass of the set)
 // (by_mass = true).  Every CTA of the cluster calls it with identical
 // arguments and receives the same result.
+//
+// Level 0 bins by distance below the row max (1/64 per bin, the last bin
+// catches everything from 16 down), which spreads any row's mass over many
+// bins; deeper levels split the surviving bin's 64-bit key range 1024 ways.
+// A band of at most kBufCap keys is then gathered, sorted and walked.
+//
+// With with_draw, level 0 also keeps the best Gumbel key (score, index) of
+// every bin.  The kept set is then every bin above the boundary bin plus the
+// band's prefix up to the boundary, so the draw's winner is the best of the
+// bins above and of the kept band elements: no separate draw pass (draw_ok).
+constexpr float kDScale = 64.0f;
+constexpr unsigned long long kNegInfKey = 0x007FFFFF00000000ull;  // elem_key(-inf, ~0)
+
 template <typename T>
-__device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_group& cluster,
-                                 int pred, unsigned long long kbound, bool by_mass,
-                                 unsigned long long count_target, float p) {
+__device__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group& cluster, int pred,
+                                 unsigned long long kbound, bool by_mass,
+                                 unsigned long long count_target, float p, bool with_draw) {
+  constexpr int E = Elt<T>::E;
   unsigned long long Klo = kbound, Khi = ~0ull;
   unsigned long long acc_c = 0, acc_m = 0;
   unsigned long long target = count_target;
   unsigned long long total_c = 0, total_m = 0;
-  bool first = true;
+  int dsel = -1;  // the level-0 bin every later level stays inside
+  bool band_at_level0 = false;
   SelOut out;
   out.all = 0;
-  const int b0 = c.rank * (kBins / c.C), nb = kBins / c.C;
+  out.draw_ok = 0;
+  out.win = kNegInfKey;
+  const int nb = kBins / c.C, b0 = c.rank * nb;
 
-  auto in_pred = [&](float zt, int j, bool side) -> bool {
-    if (pred == kPredAll) {
-      if (j >= c.V) return false;
-      if (zt == -INFINITY && !side && is_side_slot(c, j)) return false;
-      return true;
-    }
+  auto in_pred = [&](float zt) -> bool {
+    if (pred == kPredAll) return true;
     if (!(zt > -INFINITY)) return false;
     return !c.minp || minp_pass(zt, c.m_t, c.lmp);
   };
+  auto dbin = [&](float zt) -> int {
+    const float d = __fsub_rn(c.m_t, zt) * kDScale;  // exact scaling of a rounded difference
+    return d < (float)(kBins - 1) ? (int)d : kBins - 1;
+  };
 
   for (int level = 0; level < 8; ++level) {
+    const bool dlevel = level == 0;
     const unsigned long long range = Khi - Klo;
     const int bits = range == 0 ? 0 : 64 - __clzll((long long)range);
     const int shift = bits > kBinBits ? bits - kBinBits : 0;
     for (int b = c.tid; b < kBins; b += kThreads) {
       c.hcnt[b] = 0u;
       c.hmass[b] = 0ull;
+      c.hbest[b] = kNegInfKey;
     }
     __syncthreads();
     const uint32_t klo_hi = (uint32_t)(Klo >> 32);
-    for_each_elem<T>(
-        c, data, [&](float gz) { return ord_key(gz) >= klo_hi; },
-        [&](float zt, int j, bool side) {
-          if (!in_pred(zt, j, side)) return;
-          const unsigned long long K = elem_key(zt, (uint32_t)j);
-          if (K < Klo || K > Khi) return;
-          const int d = (int)((Khi - K) >> shift);
+    if (dlevel) {
+      // the catch-all bin is summed per thread (no contention on one word)
+      unsigned int cc = 0u;
+      unsigned long long cm = 0ull, cb = kNegInfKey;
+      auto count0 = [&](float zt, int j, uint32_t nbits, bool draw) {
+        const int d = dbin(zt);
+        const unsigned long long q = by_mass ? mass_fixed(zt, c.m_t) : 0ull;
+        if (d == kBins - 1) {
+          ++cc;
+          cm += q;
+        } else {
           atomicAdd(&c.hcnt[d], 1u);
-          if (by_mass) atomicAdd(&c.hmass[d], mass_fixed(zt, c.m_t));
-        });
+          if (by_mass) atomicAdd(&c.hmass[d], q);
+        }
+        if (draw) {
+          const unsigned long long cur = (d == kBins - 1) ? cb : c.hbest[d];
+          if (may_beat(zt, key_z(cur), nbits)) {
+            const unsigned long long key = elem_key(gumbel_score(zt, nbits), (uint32_t)j);
+            if (d == kBins - 1)
+              cb = key > cb ? key : cb;
+            else
+              atomicMax(&c.hbest[d], key);
+          }
+        }
+      };
+      auto member = [&](float zt, int j) {
+        return j < c.hi && in_pred(zt) && (kbound == 0ull || elem_key(zt, (uint32_t)j) >= kbound);
+      };
+      for_each_group<T>(
+          c, [&](float gz) { return ord_key(gz) >= klo_hi; },
+          [&](float* x, int, int j0) {
+#pragma unroll
+            for (int i = 0; i < E; i += 2) {
+              const float z0 = __fmul_rn(x[i], c.inv_t), z1 = __fmul_rn(x[i + 1], c.inv_t);
+              const bool m0 = member(z0, j0 + i), m1 = member(z1, j0 + i + 1);
+              if (!(m0 || m1)) continue;
+              uint64_t h = 0ull;
+              if (with_draw) h = pair_hash(c.rkey, j0 + i);  // one output per column pair
+              if (m0) count0(z0, j0 + i, bits_even(h), with_draw);
+              if (m1) count0(z1, j0 + i + 1, bits_odd(h), with_draw);
+            }
+          });
+      if (cc) atomicAdd(&c.hcnt[kBins - 1], cc);
+      if (cm) atomicAdd(&c.hmass[kBins - 1], cm);
+      if (cb != kNegInfKey) atomicMax(&c.hbest[kBins - 1], cb);
+      VT_CTRACE(c, 12);
+    } else {
+      for_each_elem<T>(
+          c, [&](float gz) { return ord_key(gz) >= klo_hi; },
+          [&](float zt, int j) {
+            if (!in_pred(zt)) return;
+            const unsigned long long K = elem_key(zt, (uint32_t)j);
+            if (K < Klo || K > Khi || dbin(zt) != dsel) return;
+            const int d = (int)((Khi - K) >> shift);
+            atomicAdd(&c.hcnt[d], 1u);
+            if (by_mass) atomicAdd(&c.hmass[d], mass_fixed(zt, c.m_t));
+          });
+    }
     cluster.sync();
     // distributed merge: this CTA sums its digit range over the cluster
     unsigned long long my_c = 0, my_m = 0;
     for (int b = c.tid; b < nb; b += kThreads) {
-      unsigned long long sc = 0, sm = 0;
+      unsigned long long sc = 0, sm = 0, sb = kNegInfKey;
       for (int r = 0; r < c.C; ++r) {
-        const unsigned int* rc = cluster.map_shared_rank(c.hcnt, r);
-        const unsigned long long* rm = cluster.map_shared_rank(c.hmass, r);
-        sc += rc[b0 + b];
-        sm += rm[b0 + b];
+        sc += cluster.map_shared_rank(c.hcnt, r)[b0 + b];
+        sm += cluster.map_shared_rank(c.hmass, r)[b0 + b];
+        if (dlevel && with_draw) {
+          const unsigned long long v = cluster.map_shared_rank(c.hbest, r)[b0 + b];
+          sb = v > sb ? v : sb;
+        }
       }
       c.mcnt[b] = (unsigned int)sc;
       c.mmass[b] = sm;
+      if (dlevel && with_draw) c.mbest[b] = sb;
       my_c += sc;
       my_m += sm;
     }
@@ -524,11 +740,10 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
         s.walk.total_m = tm;
       }
       unsigned long long tgt = target;
-      if (first && by_mass) tgt = (unsigned long long)((double)tm * (double)p);
-      // first range whose inclusive cumulative value exceeds the target
+      if (dlevel && by_mass) tgt = (unsigned long long)((double)tm * (double)p);
       const unsigned long long base_c = acc_c, base_m = acc_m;
-      const bool cross = c.lane < c.C &&
-                         (by_mass ? (base_m + im > tgt) : (base_c + ic > tgt));
+      const bool cross =
+          c.lane < c.C && (by_mass ? (base_m + im > tgt) : (base_c + ic > tgt));
       const unsigned int mask = __ballot_sync(0xffffffffu, cross);
       if (c.lane == 0) {
         s.walk.found = mask != 0;
@@ -538,13 +753,12 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
         const int r = __ffs(mask) - 1;
         const unsigned long long before_c = base_c + __shfl_sync(0xffffffffu, ic - rc, r);
         const unsigned long long before_m = base_m + __shfl_sync(0xffffffffu, im - rm, r);
-        // digits of range r live in CTA r's merged arrays
         const unsigned int* mc = cluster.map_shared_rank(c.mcnt, r);
         const unsigned long long* mm = cluster.map_shared_rank(c.mmass, r);
         unsigned long long run_c = before_c, run_m = before_m;
-        int dsel = -1;
+        int dpick = -1;
         unsigned long long sel_c = 0, sel_m = 0, band = 0;
-        for (int base = 0; base < nb && dsel < 0; base += 32) {
+        for (int base = 0; base < nb && dpick < 0; base += 32) {
           const int b = base + c.lane;
           const unsigned long long vc = b < nb ? mc[b] : 0ull;
           const unsigned long long vm = b < nb ? mm[b] : 0ull;
@@ -562,7 +776,7 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
           const unsigned int hm = __ballot_sync(0xffffffffu, hit);
           if (hm != 0) {
             const int l = __ffs(hm) - 1;
-            dsel = r * nb + base + l;
+            dpick = r * nb + base + l;
             sel_c = run_c + __shfl_sync(0xffffffffu, xc - vc, l);
             sel_m = run_m + __shfl_sync(0xffffffffu, xm - vm, l);
             band = __shfl_sync(0xffffffffu, vc, l);
@@ -572,7 +786,7 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
           }
         }
         if (c.lane == 0) {
-          s.walk.d = dsel;
+          s.walk.d = dpick;
           s.walk.acc_c = sel_c;
           s.walk.acc_m = sel_m;
           s.walk.band_cnt = band;
@@ -580,11 +794,10 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
       }
     }
     __syncthreads();
-    if (first) {
+    if (dlevel) {
       total_c = s.walk.total_c;
       total_m = s.walk.total_m;
       target = s.bcast_u[0];
-      first = false;
     }
     const bool found = s.walk.found;
     const int d = s.walk.d;
@@ -592,8 +805,8 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
     acc_c = s.walk.acc_c;
     acc_m = s.walk.acc_m;
     if (c.rank == 0 && c.tid == 0) s.gcount = 0;
-    cluster.sync();  // merged arrays and parts are free again
     if (!found) {
+      cluster.sync();  // merged arrays and parts are free again
       out.all = 1;
       out.kb = kbound;
       out.cnt_incl = total_c;
@@ -602,42 +815,53 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
       out.total_mass = total_m;
       return out;
     }
-    // narrow the key range to digit d
-    const unsigned long long hi_new = Khi - ((unsigned long long)d << shift);
-    const unsigned long long width = shift >= 64 ? ~0ull : ((1ull << shift) - 1ull);
-    const unsigned long long lo_new = (hi_new - Klo > width) ? hi_new - width : Klo;
-    Khi = hi_new;
-    Klo = lo_new;
-    if (band <= (unsigned long long)kGatherCap || Klo == Khi) break;
+    if (dlevel) {
+      // the key range of bin d, widened so that rounding cannot leave it
+      dsel = d;
+      const float margin = 1e-3f * (1.0f + fabsf(c.m_t));
+      const float z_hi = c.m_t - (float)d / kDScale + margin;
+      const float z_lo = (d == kBins - 1) ? -INFINITY : c.m_t - (float)(d + 1) / kDScale - margin;
+      Khi = elem_key(z_hi, 0u);
+      const unsigned long long klo = (d == kBins - 1) ? 0ull : elem_key(z_lo, 0xFFFFFFFFu);
+      Klo = klo > kbound ? klo : kbound;
+    } else {
+      const unsigned long long hi_new = Khi - ((unsigned long long)d << shift);
+      const unsigned long long width = (1ull << shift) - 1ull;
+      const unsigned long long lo_new = (hi_new - Klo > width) ? hi_new - width : Klo;
+      Khi = hi_new;
+      Klo = lo_new;
+    }
+    const bool stop = band <= (unsigned long long)kBufCap || Klo == Khi;
+    band_at_level0 = dlevel && stop;
+    cluster.sync();  // merged arrays, parts and the leader's buffer are free again
+    if (dlevel) VT_CTRACE(c, 13);
+    if (stop) break;
   }
   // collect the band into the leader, sort it, and walk it
   {
-    uint64_t* lg = cluster.map_shared_rank(c.gather, 0);
+    uint64_t* lg = cluster.map_shared_rank(c.buf, 0);
     int* lcount = cluster.map_shared_rank(&s.gcount, 0);
     const uint32_t klo_hi = (uint32_t)(Klo >> 32);
     for_each_elem<T>(
-        c, data, [&](float gz) { return ord_key(gz) >= klo_hi; },
-        [&](float zt, int j, bool side) {
-          if (!in_pred(zt, j, side)) return;
+        c, [&](float gz) { return ord_key(gz) >= klo_hi; },
+        [&](float zt, int j) {
+          if (!in_pred(zt)) return;
           const unsigned long long K = elem_key(zt, (uint32_t)j);
-          if (K < Klo || K > Khi) return;
+          if (K < Klo || K > Khi || dbin(zt) != dsel) return;
           const int pos = atomicAdd(lcount, 1);
-          if (pos < kGatherCap) lg[pos] = K;
+          if (pos < kBufCap) lg[pos] = K;
         });
+    VT_CTRACE(c, 14);
     cluster.sync();
     if (c.rank == 0) {
-      const int n = min(s.gcount, kGatherCap);
-      const int P2 = pow2_ceil(max(n, 1));
-      for (int i = n + c.tid; i < P2; i += kThreads) c.gather[i] = 0ull;
-      __syncthreads();
-      bitonic_desc_u64(c.gather, P2);
-      // chunked inclusive scan of the band, first crossing position
+      const int n = min(s.gcount, kBufCap);
+      block_sort_desc(c.buf, n);
       const int per = (n + kThreads - 1) / kThreads;
-      const int i0 = c.tid * per, i1 = min(n, i0 + per);
+      const int i0 = min(n, c.tid * per), i1 = min(n, i0 + per);
       unsigned long long lc = 0, lm = 0;
       for (int i = i0; i < i1; ++i) {
         lc += 1;
-        if (by_mass) lm += mass_fixed(key_z(c.gather[i]), c.m_t);
+        if (by_mass) lm += mass_fixed(key_z(c.buf[i]), c.m_t);
       }
       unsigned long long tot;
       const unsigned long long ex_c = block_exclusive_u64(lc, s, &tot);
@@ -647,7 +871,7 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
       unsigned long long rc = acc_c + ex_c, rm = acc_m + ex_m;
       for (int i = i0; i < i1; ++i) {
         rc += 1;
-        if (by_mass) rm += mass_fixed(key_z(c.gather[i]), c.m_t);
+        if (by_mass) rm += mass_fixed(key_z(c.buf[i]), c.m_t);
         if (by_mass ? (rm > target) : (rc > target)) {
           hit = i;
           hit_c = rc;
@@ -655,7 +879,6 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
           break;
         }
       }
-      // lowest crossing position over the CTA
       int hmin = hit;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) hmin = min(hmin, __shfl_xor_sync(0xffffffffu, hmin, o));
@@ -669,13 +892,20 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
       __syncthreads();
       const int h = s.bcast_i[0];
       if (h != INT_MAX && hit == h) {
-        s.sel.kb = c.gather[h];
+        s.sel.kb = c.buf[h];
         s.sel.cnt_incl = hit_c;
         s.sel.mass_incl = hit_m;
         s.sel.all = 0;
       }
+#ifdef VT_DEBUG_SELECT
+      if (h == INT_MAX && c.tid == 0)
+        printf("select miss row %d rank %d by_mass %d n %d acc_c %llu acc_m %llu target %llu "
+               "total_c %llu total_m %llu tot %llu Klo %llx Khi %llx dsel %d m_t %g\n",
+               c.row, c.rank, (int)by_mass, n, acc_c, acc_m, target, total_c, total_m, tot, Klo,
+               Khi, dsel, c.m_t);
+#endif
       if (h == INT_MAX && c.tid == 0) {  // cannot happen: the band holds the crossing
-        s.sel.kb = n > 0 ? c.gather[n - 1] : kbound;
+        s.sel.kb = n > 0 ? c.buf[n - 1] : kbound;
         s.sel.cnt_incl = acc_c + n;
         s.sel.mass_incl = acc_m;
         s.sel.all = 0;
@@ -684,11 +914,39 @@ __device__ SelOut cluster_select(Ctx& c, const T* data, Smem& s, cg::cluster_gro
       if (c.tid == 0) {
         s.sel.total_cnt = total_c;
         s.sel.total_mass = total_m;
+        s.sel.draw_ok = 0;
+      }
+      if (band_at_level0 && with_draw && h != INT_MAX) {
+        // winner: the kept band prefix [0, h] and every bin above the band
+        unsigned long long best = kNegInfKey;
+        for (int i = c.tid; i <= h; i += kThreads) {
+          const uint64_t k = c.buf[i];
+          const int j = (int)key_idx(k);
+          const unsigned long long key =
+              elem_key(gumbel_score(key_z(k), noise_bits(c.rkey, j)), (uint32_t)j);
+          best = key > best ? key : best;
+        }
+        for (int b = c.tid; b < dsel; b += kThreads) {
+          const unsigned long long v = cluster.map_shared_rank(c.mbest, b / nb)[b % nb];
+          best = v > best ? v : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long w = __shfl_xor_sync(0xffffffffu, best, o);
+          best = w > best ? w : best;
+        }
+        if (c.lane == 0) s.ru[c.warp] = best;
+        __syncthreads();
+        if (c.tid == 0) {
+          unsigned long long t = kNegInfKey;
+          for (int w = 0; w < kWarps; ++w) t = s.ru[w] > t ? s.ru[w] : t;
+          s.sel.win = t;
+          s.sel.draw_ok = 1;
+        }
       }
     }
     cluster.sync();
-    const SelOut* ls = cluster.map_shared_rank(&s.sel, 0);
-    out = *ls;
+    out = *cluster.map_shared_rank(&s.sel, 0);
     __syncthreads();
     cluster.sync();  // the leader's buffers may be reused after this
   }
@@ -713,11 +971,10 @@ __device__ void append_token(int2* tab, int32_t* len_p, int cap, int tok, Smem& 
     if (threadIdx.x == 0) *status_p = kRowHistoryFull;
     return;
   }
-  // shift [pos, len) up by one, highest chunk first
   for (int top = len; top > pos; top -= kThreads) {
     const int e = top - 1 - threadIdx.x;
     int2 v = make_int2(0, 0);
-    const bool mine = e >= pos && e >= top - kThreads;
+    const bool mine = e >= pos;
     if (mine) v = tab[e];
     __syncthreads();
     if (mine) tab[e + 1] = v;
@@ -729,14 +986,61 @@ __device__ void append_token(int2* tab, int32_t* len_p, int cap, int tok, Smem& 
   }
 }
 
+// Kept-set processing on the sorted candidates in the leader's buffer.
+// Returns L3 (kept count); writes the drawn token and its tempered logit.
+__device__ int leader_draw(Ctx& c, Smem& s, int N, bool L2_inside, double S_fixed, int* tok,
+                           float* ztok) {
+  int pass = 0;
+  if (c.minp)
+    for (int i = c.tid; i < N; i += kThreads) pass += minp_pass(key_z(c.buf[i]), c.m_t, c.lmp);
+  const int L1 = c.minp ? block_sum_int(pass, s) : N;
+  const int L2 = c.topk ? min(c.top_k, L1) : L1;
+  int L3 = L2;
+  if (c.topp) {
+    const int per = (L2 + kThreads - 1) / kThreads;
+    const int i0 = min(L2, c.tid * per), i1 = min(L2, i0 + per);
+    unsigned long long lm = 0;
+    for (int i = i0; i < i1; ++i) lm += mass_fixed(key_z(c.buf[i]), c.m_t);
+    unsigned long long tot;
+    const unsigned long long ex = block_exclusive_u64(lm, s, &tot);
+    const unsigned long long W2 = L2_inside ? tot : (unsigned long long)S_fixed;
+    const unsigned long long Tm = (unsigned long long)((double)W2 * (double)c.top_p);
+    int kept = 0;
+    unsigned long long run = ex;
+    for (int i = i0; i < i1; ++i) {
+      if (run <= Tm) ++kept;
+      run += mass_fixed(key_z(c.buf[i]), c.m_t);
+    }
+    L3 = max(1, block_sum_int(kept, s));
+  }
+  float bs = -INFINITY, bz = 0.f;
+  int bidx = INT_MAX;
+  for (int i = c.tid; i < L3; i += kThreads) {
+    const uint64_t k = c.buf[i];
+    const int j = (int)key_idx(k);
+    const float zt = key_z(k);
+    const float sc = gumbel_score(zt, noise_bits(c.rkey, j));
+    if (pair_better(sc, j, bs, bidx)) {
+      bs = sc;
+      bidx = j;
+      bz = zt;
+    }
+  }
+  block_argmax(bs, bidx, bz, s);
+  *tok = bidx;
+  *ztok = bz;
+  return L3;
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ Smem s;
   cg::cluster_group cluster = cg::this_cluster();
+  constexpr int E = Elt<T>::E;
 
   Ctx c;
   c.tid = threadIdx.x;
@@ -749,18 +1053,24 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
   c.slice = a.slice;
   c.lo = c.rank * a.slice;
   c.hi = min(c.lo + a.slice, a.V);
-  constexpr int E = Elt<T>::kPerGroup;
   c.ngroups = a.slice / E;
-
-  T* data = reinterpret_cast<T*>(dsm);
-  const size_t data_bytes = (size_t)a.slice * sizeof(T);
-  c.gmax = reinterpret_cast<float*>(dsm + data_bytes);
-  uint8_t* uni = dsm + data_bytes + (((size_t)c.ngroups * 4 + 15) & ~(size_t)15);
-  c.gather = reinterpret_cast<uint64_t*>(uni);
-  c.hmass = reinterpret_cast<unsigned long long*>(uni);
-  c.hcnt = reinterpret_cast<unsigned int*>(uni + kBins * 8);
-  c.mmass = reinterpret_cast<unsigned long long*>(uni + kBins * 12);
-  c.mcnt = reinterpret_cast<unsigned int*>(uni + kBins * 12 + (size_t)(kBins / c.C) * 8);
+  c.aligned = a.aligned != 0;
+  c.rowp = reinterpret_cast<const T*>(a.logits) + (int64_t)c.row * a.ld;
+  c.buf = reinterpret_cast<uint64_t*>(dsm);
+  c.hmass = reinterpret_cast<unsigned long long*>(dsm);
+  c.hcnt = reinterpret_cast<unsigned int*>(dsm + kBins * 8);
+  // per-bin bests live past the gather buffer, so they survive the band collect
+  c.hbest = reinterpret_cast<unsigned long long*>(dsm + (size_t)kBufCap * 8);
+  c.gmax = reinterpret_cast<uint16_t*>(dsm + a.off_gmax);
+  if (c.C > 1) {
+    c.mmass = reinterpret_cast<unsigned long long*>(dsm + a.off_mrg);
+    c.mbest = reinterpret_cast<unsigned long long*>(dsm + a.off_mrg + (kBins / c.C) * 8);
+    c.mcnt = reinterpret_cast<unsigned int*>(dsm + a.off_mrg + (kBins / c.C) * 16);
+  } else {
+    c.mmass = c.hmass;
+    c.mcnt = c.hcnt;
+    c.mbest = c.hbest;
+  }
 
   const RowParams P = a.params[c.row];
   c.greedy = (P.flags & kRowGreedy) != 0;
@@ -773,107 +1083,83 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
   c.minp = !c.greedy && (P.flags & kRowMinP) != 0;
   c.lmp = P.log_min_p;
   c.rkey = row_key(a.seeds[c.row], c.row);
+  c.trace = a.trace ? a.trace + (size_t)blockIdx.x * kTraceSlots : nullptr;
   const int n = a.n_logprobs;
   const int hist_len = a.hist_len[c.row];
-  const bool pen = (P.flags & kRowPenalty) != 0 && hist_len > 0;
-  c.tab = a.hist + (int64_t)c.row * a.hist_cap;
-  c.zs = a.zside + (int64_t)c.row * a.hist_cap;
-  c.e_lo = c.e_hi = 0;
+  c.pen = a.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0;
+  c.bitmap = nullptr;
+  c.prefix = nullptr;
+  c.side_z = nullptr;
+  VT_TRACE(0);
 
-  // ---- phase 0: stage the slice in shared memory ---------------------------
-  const T* rowp = reinterpret_cast<const T*>(a.logits) + (int64_t)c.row * a.ld;
-  const int nloc = max(0, c.hi - c.lo);
   if (c.tid == 0) {
     s.part.err = 0;
+    s.nloc = 0;
     s.gcount = 0;
-    if (a.use_bulk) {
-      mbar_init(&s.mbar, 1);
-      fence_mbar_init();
-    }
   }
-  __syncthreads();
-  int bulk_elems = 0;
-  if (a.use_bulk) {
-    const uint32_t bulk_bytes = ((uint32_t)nloc * (uint32_t)sizeof(T)) & ~15u;
-    bulk_elems = (int)(bulk_bytes / sizeof(T));
-    if (c.tid == 0) {
-      mbar_arrive_expect_tx(&s.mbar, bulk_bytes);
-      const char* src = reinterpret_cast<const char*>(rowp + c.lo);
-      char* dst = reinterpret_cast<char*>(data);
-      for (uint32_t off = 0; off < bulk_bytes; off += kBulkChunk)
-        bulk_copy_g2s(dst + off, src + off, min(kBulkChunk, bulk_bytes - off), &s.mbar);
-    }
-  }
-  for (int e = bulk_elems + c.tid; e < a.slice; e += kThreads) {
-    if (e < nloc)
-      Elt<T>::copy_global(data, e, rowp, (int64_t)c.lo + e);
-    else
-      Elt<T>::fill_neg_inf(data, e);
-  }
-  bool timed_out = false;
-  if (a.use_bulk) timed_out = !mbar_wait_bounded(&s.mbar, 0);
-  if (timed_out) {
-    atomicOr(&s.part.err, kErrTimeout);
-    mbar_wait_bounded(&s.mbar, 0);  // second bounded wait for the copy in flight
-  }
-  __syncthreads();
 
-  // ---- phase 1: occurrence penalties into the side list ----------------------
-  if (pen) {
+  // ---- setup: penalties of the slice's seen tokens ----------------------------
+  if (c.pen) {
+    const int2* tab = a.hist + (int64_t)c.row * a.hist_cap;
+    float* zs = a.zside + (int64_t)c.row * a.hist_cap;
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(dsm + a.off_bitmap);
+    uint16_t* prefix = reinterpret_cast<uint16_t*>(dsm + a.off_prefix);
+    const int nwords = a.slice / 32;
+    for (int w = c.tid; w < nwords; w += kThreads) bitmap[w] = 0u;
     int below_lo = 0, below_hi = 0;
     for (int e = c.tid; e < hist_len; e += kThreads) {
-      const int id = c.tab[e].x;
+      const int id = tab[e].x;
       below_lo += id < c.lo;
       below_hi += id < c.hi;
     }
-    c.e_lo = block_sum_int(below_lo, s);
-    c.e_hi = block_sum_int(below_hi, s);
-    float* zs = a.zside + (int64_t)c.row * a.hist_cap;
-    for (int e = c.e_lo + c.tid; e < c.e_hi; e += kThreads) {
-      const int2 t = c.tab[e];
+    const int e_lo = block_sum_int(below_lo, s);
+    const int e_hi = block_sum_int(below_hi, s);
+    const T* row = reinterpret_cast<const T*>(c.rowp);
+    for (int e = e_lo + c.tid; e < e_hi; e += kThreads) {
+      const int2 t = tab[e];
       const int local = t.x - c.lo;
-      if (local < 0 || local >= nloc) {  // unsorted table: never write outside the slice
+      if (local < 0 || local >= c.hi - c.lo) {  // an unsorted table never writes outside
         atomicOr(&s.part.err, kErrInternal);
         continue;
       }
-      zs[e] = penalize(Elt<T>::at(data, local), t.y, P);
-      Elt<T>::mask(data, local);
+      zs[e] = penalize(Elt<T>::load1(row + t.x), t.y, P);
+      atomicOr(&bitmap[local >> 5], 1u << (local & 31));
     }
+    __syncthreads();
+    // side-list index of each word's first position: exclusive scan of popcounts
+    const int per = (nwords + kThreads - 1) / kThreads;
+    const int w0 = min(nwords, c.tid * per), w1 = min(nwords, w0 + per);
+    unsigned long long cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
+    unsigned long long tot;
+    unsigned long long run = block_exclusive_u64(cnt, s, &tot);
+    for (int w = w0; w < w1; ++w) {
+      prefix[w] = (uint16_t)run;
+      run += __popc(bitmap[w]);
+    }
+    c.bitmap = bitmap;
+    c.prefix = prefix;
+    c.side_z = zs + e_lo;
     __syncthreads();
   }
 
-  // ---- phase 2: pass A (max, sum exp, argmax, group and thread maxima) -----
+  // ---- pass A: stream the slice ----------------------------------------------
+  // Candidates the kept set may need (K_main) and the top-n alone (n).
+  int K_main = c.greedy ? n : max(n, c.topk ? c.top_k : ((c.topp || c.minp) ? kDefaultCand : 0));
+  bool topk_beyond = false;
+  if (K_main > kBufCap) {
+    K_main = n;
+    topk_beyond = true;
+  }
   {
     float rm = -INFINITY, rsum = 0.f, bv = -INFINITY;
     int bi = INT_MAX;
-    bool nonfin = false;
-    for (int g = c.tid; g < c.ngroups; g += kThreads) {
-      float x[E];
-      Elt<T>::load(data, g, x);
+    bool nanf = false;
+    auto consume = [&](float* x, int g) {
       float gm = x[0];
-      bool nan = x[0] != x[0];
 #pragma unroll
-      for (int i = 1; i < E; ++i) {
-        gm = fmaxf(gm, x[i]);
-        nan |= x[i] != x[i];
-      }
-      nonfin |= nan;
-      c.gmax[g] = gm;
-      if (gm > rm) {
-        rsum = (rm == -INFINITY) ? 0.f : rsum * ex2_approx((rm - gm) * c.ax);
-        rm = gm;
-      }
-      if (rm > -INFINITY) {
-        const float nb = -rm * c.ax;
-        float e[E];
-#pragma unroll
-        for (int i = 0; i < E; ++i) e[i] = ex2_approx(fmaf(x[i], c.ax, nb));
-#pragma unroll
-        for (int w = 1; w < E; w <<= 1)
-#pragma unroll
-          for (int i = 0; i + w < E; i += 2 * w) e[i] += e[i + w];
-        rsum += e[0];
-      }
+      for (int i = 1; i < E; ++i) gm = fmaxf(gm, x[i]);
+      c.gmax[g] = bf16_down(gm);
       if (gm > bv) {
         int first = 0;
 #pragma unroll
@@ -882,24 +1168,100 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         bv = gm;
         bi = c.lo + g * E + first;
       }
-    }
-    for (int e = c.e_lo + c.tid; e < c.e_hi; e += kThreads) {
-      const float z = c.zs[e];
-      const int id = c.tab[e].x;
-      nonfin |= z != z;
-      if (z > rm) {
-        rsum = (rm == -INFINITY) ? 0.f : rsum * ex2_approx((rm - z) * c.ax);
-        rm = z;
+      if (gm > rm) {
+        rsum = (rm == -INFINITY) ? 0.f : rsum * ex2_approx((rm - gm) * c.ax);
+        rm = gm;
       }
-      if (rm > -INFINITY) rsum += ex2_approx(fmaf(z, c.ax, -rm * c.ax));
-      if (pair_better(z, id, bv, bi)) {
-        bv = z;
-        bi = id;
+      if (rm > -INFINITY) {
+        // exponentials in place, then a pairwise sum of the group
+        const float nb = -rm * c.ax;
+#pragma unroll
+        for (int i = 0; i < E; ++i) x[i] = ex2_approx(fmaf(x[i], c.ax, nb));
+#pragma unroll
+        for (int w = 1; w < E; w <<= 1)
+#pragma unroll
+          for (int i = 0; i + w < E; i += 2 * w) x[i] += x[i + w];
+        rsum += x[0];
+      } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) nanf |= x[i] != x[i];
+      }
+    };
+    if (c.aligned) {
+      // bulk copies through a ring of kStages 8 KB slots: one group per thread
+      // per stage, kStages - 1 stages in flight while one is consumed
+      const uint32_t bulk = ((uint32_t)(c.hi > c.lo ? c.hi - c.lo : 0) * (uint32_t)sizeof(T)) & ~15u;
+      const int nstage = (c.ngroups + kThreads - 1) / kThreads;
+      const char* src = reinterpret_cast<const char*>(reinterpret_cast<const T*>(c.rowp) + c.lo);
+      uint8_t* ring = reinterpret_cast<uint8_t*>(c.buf);
+      auto stage_bytes = [&](int k) -> uint32_t {
+        const int64_t b = (int64_t)bulk - (int64_t)k * kStageBytes;
+        return b <= 0 ? 0u : (b > kStageBytes ? (uint32_t)kStageBytes : (uint32_t)b);
+      };
+      if (c.tid == 0) {
+        for (int st = 0; st < kStages; ++st) mbar_init(&s.full[st], 1);
+        fence_mbar_init();
+      }
+      __syncthreads();
+      if (c.tid == 0) {
+        for (int k = 0; k < min(kStages, nstage); ++k) {
+          const uint32_t by = stage_bytes(k);
+          if (by) {
+            mbar_arrive_expect_tx(&s.full[k], by);
+            bulk_copy_g2s(ring + k * kStageBytes, src + (size_t)k * kStageBytes, by, &s.full[k]);
+          }
+        }
+      }
+      for (int k = 0; k < nstage; ++k) {
+        const int slot = k % kStages;
+        const uint32_t by = stage_bytes(k);
+        if (by && !mbar_wait_bounded(&s.full[slot], (uint32_t)((k / kStages) & 1)))
+          atomicOr(&s.part.err, kErrTimeout);
+        const int g = k * kThreads + c.tid;
+        if (g < c.ngroups) {
+          float x[E];
+          if ((uint32_t)(c.tid + 1) * kGroupBytes <= by) {
+            const uint4* q = reinterpret_cast<const uint4*>(ring + slot * kStageBytes) + 2 * c.tid;
+            if constexpr (E == 8) {
+              const uint4 u0 = q[0], u1 = q[1];
+              x[0] = __uint_as_float(u0.x); x[1] = __uint_as_float(u0.y);
+              x[2] = __uint_as_float(u0.z); x[3] = __uint_as_float(u0.w);
+              x[4] = __uint_as_float(u1.x); x[5] = __uint_as_float(u1.y);
+              x[6] = __uint_as_float(u1.z); x[7] = __uint_as_float(u1.w);
+            } else {
+              const uint4 u0 = q[0], u1 = q[1];
+              const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                x[2 * i] = __uint_as_float(w[i] << 16);
+                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+              }
+            }
+            patch_group<T>(c, g, x);
+          } else {
+            load_group<T>(c, g, x);  // the ragged tail, from global memory
+          }
+          consume(x, g);
+        }
+        __syncthreads();  // slot free
+        if (c.tid == 0 && k + kStages < nstage) {
+          const uint32_t nb = stage_bytes(k + kStages);
+          if (nb) {
+            mbar_arrive_expect_tx(&s.full[slot], nb);
+            bulk_copy_g2s(ring + slot * kStageBytes, src + (size_t)(k + kStages) * kStageBytes,
+                          nb, &s.full[slot]);
+          }
+        }
+      }
+    } else {
+      for (int g = c.tid; g < c.ngroups; g += kThreads) {
+        float x[E];
+        load_group<T>(c, g, x);
+        consume(x, g);
       }
     }
-    nonfin |= rm == INFINITY;
+    const bool nonfin = nanf || (rsum != rsum) || rm == INFINITY;
     s.tmax[c.tid] = rm;
-    // CTA reduction
     float m = rm, sm = rsum;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -908,8 +1270,90 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       lse_combine(m, sm, m2, s2, c.ax);
     }
     float dz = 0.f;
-    block_argmax(bv, bi, dz, s);
+    block_argmax(bv, bi, dz, s);  // also a barrier: s.tmax is complete after it
     const int nf = __syncthreads_or(nonfin);
+    // This CTA's candidate thresholds: at least Kc of its elements are >= them.
+    // Up to kThreads, the Kc-th largest thread maximum; beyond, a two-round
+    // radix select over the bf16 lower bounds of the group maxima.
+    const int Kc = (K_main + c.C - 1) / c.C, Kn = (n + c.C - 1) / c.C;
+    if (c.tid == 0) {
+      s.part.tau = INFINITY;
+      s.part.tau_n = INFINITY;
+    }
+    __syncthreads();
+    if ((Kc > 0 && Kc <= kSmallK) || Kn > 0) {
+      const float v = s.tmax[c.tid];
+      int rank = 0;
+      const float4* t4 = reinterpret_cast<const float4*>(s.tmax);
+#pragma unroll 4
+      for (int u = 0; u < kThreads / 4; ++u) {
+        const float4 w = t4[u];
+        const int b = 4 * u;
+        rank += (w.x > v) || (w.x == v && b < c.tid);
+        rank += (w.y > v) || (w.y == v && b + 1 < c.tid);
+        rank += (w.z > v) || (w.z == v && b + 2 < c.tid);
+        rank += (w.w > v) || (w.w == v && b + 3 < c.tid);
+      }
+      if (Kc > 0 && Kc <= kSmallK && rank == Kc - 1) s.part.tau = v;
+      if (Kn > 0 && rank == Kn - 1) s.part.tau_n = v;
+    }
+    if (Kc > kSmallK) {
+      if (Kc > c.ngroups || bv == -INFINITY) {
+        if (c.tid == 0) s.part.tau = -INFINITY;
+      } else {
+        // bins of 1/16 (tempered units) below this CTA's max: the first bin
+        // where the count of group maxima reaches Kc, then the smallest group
+        // maximum inside it and above (an exact lower bound)
+        const float scale = 16.0f * c.inv_t;
+        auto gbin = [&](int g) {
+          const float d = __fmul_rn(__fsub_rn(bv, bf16_val(c.gmax[g])), scale);
+          return d < 255.0f ? (int)d : 255;
+        };
+        s.hist256[c.tid] = 0u;
+        __syncthreads();
+        for (int g = c.tid; g < c.ngroups; g += kThreads) atomicAdd(&s.hist256[gbin(g)], 1u);
+        __syncthreads();
+        if (c.warp == 0) {
+          uint32_t cnt[8], tot = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            cnt[q] = s.hist256[8 * c.lane + q];
+            tot += cnt[q];
+          }
+          uint32_t inc = tot;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t w = __shfl_up_sync(0xffffffffu, inc, o);
+            if (c.lane >= o) inc += w;
+          }
+          const uint32_t before = inc - tot;
+          if (before < (uint32_t)Kc && inc >= (uint32_t)Kc) {
+            uint32_t run = before;
+            for (int q = 0; q < 8; ++q) {
+              run += cnt[q];
+              if (run >= (uint32_t)Kc) {
+                s.bcast_i[2] = 8 * c.lane + q;
+                break;
+              }
+            }
+          }
+        }
+        __syncthreads();
+        const int bsel = s.bcast_i[2];
+        float mn = INFINITY;
+        for (int g = c.tid; g < c.ngroups; g += kThreads)
+          if (gbin(g) <= bsel) mn = fminf(mn, bf16_val(c.gmax[g]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        if (c.lane == 0) s.rf[2 * kWarps + 2 + c.warp] = mn;
+        __syncthreads();
+        if (c.tid == 0) {
+          float t = INFINITY;
+          for (int w = 0; w < kWarps; ++w) t = fminf(t, s.rf[2 * kWarps + 2 + w]);
+          s.part.tau = t;
+        }
+      }
+    }
     if (c.lane == 0) {
       s.rf[c.warp] = m;
       s.rf[kWarps + c.warp] = sm;
@@ -925,9 +1369,11 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       s.part.nonfinite = nf;
     }
   }
-  cluster.sync();  // (1) pass-A partials visible
+  VT_TRACE(2);
+  cluster.sync();  // (1) pass-A partials and thresholds visible
+  VT_TRACE(3);
   if (c.warp == 0) {
-    float m = -INFINITY, sm = 0.f, bv = -INFINITY;
+    float m = -INFINITY, sm = 0.f, bv = -INFINITY, tau = INFINITY, tau_n = INFINITY;
     int bi = INT_MAX, nf = 0, er = 0;
     if (c.lane < c.C) {
       const Part* p = cluster.map_shared_rank(&s.part, c.lane);
@@ -937,6 +1383,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       bi = p->bi;
       nf = p->nonfinite;
       er = p->err;
+      tau = p->tau;
+      tau_n = p->tau_n;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -951,48 +1399,32 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       }
       nf |= __shfl_xor_sync(0xffffffffu, nf, o);
       er |= __shfl_xor_sync(0xffffffffu, er, o);
+      tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, o));
+      tau_n = fminf(tau_n, __shfl_xor_sync(0xffffffffu, tau_n, o));
     }
     if (c.lane == 0) {
       s.rs.M = m;
       s.rs.S = sm;
-      s.rs.m_t = m * c.inv_t;
+      s.rs.m_t = __fmul_rn(m, c.inv_t);
       s.rs.lnS = logf(sm);
       s.rs.bv = bv;
       s.rs.bi = bi;
-      s.rs.nonfinite = nf || m == INFINITY || (m * c.inv_t) == INFINITY;
+      s.rs.nonfinite = nf || m == INFINITY || __fmul_rn(m, c.inv_t) == INFINITY;
       s.rs.err = er;
+      s.rs.tau = tau;
+      s.rs.tau_n = tau_n;
     }
   }
   __syncthreads();
   c.m_t = s.rs.m_t;
   c.lnS = s.rs.lnS;
   const int status0 = s.rs.nonfinite ? kRowNonfinite : (s.rs.M == -INFINITY ? kRowEmpty : kRowOk);
-  // Pass A sums 2^(x*log2e/T - max*log2e/T) with one FFMA per element; the
-  // rounding of max*log2e/T makes that inexact once |max| is large.  Such rows
-  // re-sum exp(z_t - m_t) from the tempered values themselves.
-  if (status0 == kRowOk && fabsf(c.m_t) > 32.0f) {
-    float acc = 0.f;
-    for_each_elem<T>(
-        c, data, [](float) { return true; },
-        [&](float zt, int, bool) { acc += ex2_approx((zt - c.m_t) * kLog2e); });
-    acc = block_sum_f(acc, s);
-    if (c.tid == 0) s.part.s_exact = acc;
-    cluster.sync();
-    if (c.tid == 0) {
-      float t = 0.f;
-      for (int r = 0; r < c.C; ++r) t += cluster.map_shared_rank(&s.part, r)->s_exact;
-      s.rs.S = t;
-      s.rs.lnS = logf(t);
-    }
-    __syncthreads();
-    c.lnS = s.rs.lnS;
-  }
   const bool leader = c.rank == 0;
   int32_t* out_ids = n > 0 ? a.out_topk_ids + (int64_t)c.row * n : nullptr;
   float* out_lps = n > 0 ? a.out_topk_logprobs + (int64_t)c.row * n : nullptr;
 
   if (status0 != kRowOk) {
-    cluster.sync();  // (2) nobody reads another CTA's shared memory after this
+    cluster.sync();  // nobody reads another CTA's shared memory after this
     if (leader) {
       if (c.tid < n) {
         out_ids[c.tid] = -1;
@@ -1012,91 +1444,130 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     return;
   }
 
-  // ---- phase 3: candidate threshold --------------------------------------
-  int K_need = c.greedy ? n : max(n, c.topk ? c.top_k : ((c.topp || c.minp) ? kDefaultCand : 0));
-  if (!c.greedy && !c.topk && (c.topp || c.minp)) K_need = min(K_need, max(n, c.C * kThreads));
-  bool topk_beyond = false;
-  if (K_need > c.C * kThreads) {
-    K_need = n;
-    topk_beyond = true;
-  }
-  float tau = INFINITY;
-  if (K_need > 0) {
-    const int Kc = (K_need + c.C - 1) / c.C;
-    __syncthreads();
-    bitonic_desc_f32(s.tmax, kThreads);
-    if (c.tid == 0) s.part.tau = s.tmax[Kc - 1];
-  }
-  cluster.sync();  // (2) taus visible; pass-A partials no longer read
-  if (K_need > 0) {
-    if (c.warp == 0) {
-      float t = INFINITY;
-      if (c.lane < c.C) t = cluster.map_shared_rank(&s.part, c.lane)->tau;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t = fminf(t, __shfl_xor_sync(0xffffffffu, t, o));
-      if (c.lane == 0) s.rs.tau = t;
+  // Pass A sums 2^(x*log2e/T - max*log2e/T) with one FFMA per element; the
+  // rounding of max*log2e/T makes that inexact once |max| is large.  Such rows
+  // re-sum exp(z_t - m_t) from the tempered values themselves.
+  if (fabsf(c.m_t) > 32.0f) {
+    float acc = 0.f;
+    for_each_elem<T>(
+        c, [](float) { return true; },
+        [&](float zt, int) { acc += ex2_approx(__fmul_rn(__fsub_rn(zt, c.m_t), kLog2e)); });
+    acc = block_sum_f(acc, s);
+    if (c.tid == 0) s.part.s_exact = acc;
+    cluster.sync();
+    if (c.tid == 0) {
+      float t = 0.f;
+      for (int r = 0; r < c.C; ++r) t += cluster.map_shared_rank(&s.part, r)->s_exact;
+      s.rs.S = t;
+      s.rs.lnS = logf(t);
     }
     __syncthreads();
-    tau = s.rs.tau;
+    c.lnS = s.rs.lnS;
   }
-  const bool complete = tau == -INFINITY;
 
-  // ---- phase 4: pass B, candidates into the leader ---------------------------
+  // ---- pass B: candidates at or above the cluster threshold ----------------
+  // A top-p row without top-k keeps at least p * S elements (none weighs more
+  // than the maximum): past the buffer it cannot stay on the candidates, so
+  // only the top-n ones are collected.
+  bool likely_slow = topk_beyond;
+  if (!c.greedy && !c.topk && c.topp && (double)c.top_p * (double)s.rs.S > (double)kBufCap)
+    likely_slow = true;
+  if (!c.greedy && !c.topk && !c.topp && !c.minp) likely_slow = true;  // unfiltered draw
+  const int K_need = likely_slow ? n : K_main;
+  const float tau = likely_slow ? s.rs.tau_n : s.rs.tau;
+  const bool complete = K_need > 0 && tau == -INFINITY;
   {
     int my_n = 0, my_minp = 0;
     unsigned long long my_mass = 0;
     if (K_need > 0) {
-      const float tau_t = tau * c.inv_t;
-      uint64_t* lg = cluster.map_shared_rank(c.gather, 0);
-      int* lcount = cluster.map_shared_rank(&s.gcount, 0);
-      for_each_elem<T>(
-          c, data, [&](float gz) { return gz >= tau_t; },
-          [&](float zt, int j, bool) {
-            if (zt >= tau_t && zt > -INFINITY) {
-              const int pos = atomicAdd(lcount, 1);
-              if (pos < kGatherCap) lg[pos] = elem_key(zt, (uint32_t)j);
-              ++my_n;
-              my_mass += mass_fixed(zt, c.m_t);
-              if (c.minp && minp_pass(zt, c.m_t, c.lmp)) ++my_minp;
+      const float tau_t = __fmul_rn(tau, c.inv_t);
+      for_each_group<T>(
+          c, [&](float gz) { return gz >= tau_t; },
+          [&](float* x, int, int j0) {
+            uint32_t take = 0u;
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+              const float zt = __fmul_rn(x[i], c.inv_t);
+              x[i] = zt;
+              if (j0 + i < c.hi && zt >= tau_t && zt > -INFINITY) take |= 1u << i;
+            }
+            if (take == 0u) return;
+            int pos = atomicAdd(&s.nloc, __popc(take));  // one atomic per group
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+              if (take & (1u << i)) {
+                if (pos < kBufCap) c.buf[pos] = elem_key(x[i], (uint32_t)(j0 + i));
+                ++pos;
+                ++my_n;
+                my_mass += mass_fixed(x[i], c.m_t);
+                if (c.minp && minp_pass(x[i], c.m_t, c.lmp)) ++my_minp;
+              }
             }
           });
     }
-    my_n = block_sum_int(my_n, s);
-    my_minp = block_sum_int(my_minp, s);
-    my_mass = block_sum_u64(my_mass, s);
+    // one combined CTA reduction of (count, min-p count, mass)
+    my_n = warp_sum_i(my_n);
+    my_minp = warp_sum_i(my_minp);
+    my_mass = warp_sum_u64(my_mass);
+    if (c.lane == 0) {
+      s.ri[c.warp] = my_n;
+      s.ri[kWarps + c.warp] = my_minp;
+      s.ru[c.warp] = my_mass;
+    }
+    __syncthreads();
     if (c.tid == 0) {
-      s.part.ncand = my_n;
-      s.part.ncand_minp = my_minp;
-      s.part.cand_mass = my_mass;
+      int tn = 0, tm = 0;
+      unsigned long long tmass = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        tn += s.ri[w];
+        tm += s.ri[kWarps + w];
+        tmass += s.ru[w];
+      }
+      s.part.ncand = tn;
+      s.part.ncand_minp = tm;
+      s.part.cand_mass = tmass;
     }
   }
-  cluster.sync();  // (3) candidates and their counts visible
+  VT_TRACE(6);
+  cluster.sync();  // (2) candidate counts visible
+  VT_TRACE(7);
   if (c.warp == 0) {
-    int nc = 0, nm = 0;
+    int nc = 0, nm = 0, ov = 0;
     unsigned long long mass = 0;
     if (c.lane < c.C) {
       const Part* p = cluster.map_shared_rank(&s.part, c.lane);
       nc = p->ncand;
       nm = p->ncand_minp;
       mass = p->cand_mass;
+      ov = nc > kBufCap;
     }
-    nc = warp_sum_i(nc);
+    int inc = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int w = __shfl_up_sync(0xffffffffu, inc, o);
+      if (c.lane >= o) inc += w;
+    }
+    const int off = __shfl_sync(0xffffffffu, inc - nc, c.rank);
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
     nm = warp_sum_i(nm);
     mass = warp_sum_u64(mass);
+    ov = warp_sum_i(ov);
     if (c.lane == 0) {
-      s.rs.nc = nc;
+      s.rs.nc = tot;
       s.rs.nc_minp = nm;
       s.rs.cand_mass = mass;
+      s.rs.push_off = off;
+      s.rs.overflow = ov;
     }
   }
   __syncthreads();
   const int nc = s.rs.nc;
-  const bool cand_ok = K_need > 0 ? nc <= kGatherCap : true;
+  const bool cand_ok = K_need > 0 ? (nc <= kBufCap && !s.rs.overflow) : true;
   const bool topn_ok = n == 0 || (cand_ok && nc >= n);
   const double S_fixed = (double)s.rs.S * 1099511627776.0;  // 2^40
   // The kept prefix is known from the candidates when every min-p survivor is
   // a candidate, or when top-k ends inside them; a top-p-only row also stays
-  // fast when the candidates already hold more than p of the row's mass.
+  // on the candidates when they already hold more than p of the row's mass.
   const bool surv_inside = complete || (c.minp && s.rs.nc_minp < nc);
   const bool L2_inside = surv_inside || (c.topk && !topk_beyond && c.top_k <= nc);
   bool fast;
@@ -1113,17 +1584,25 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       fast = cand_ok && L2_inside;
     fast = fast && topn_ok && K_need > 0;
   }
-  cluster.sync();  // (4) partials read; after this the fast path needs only the leader
+  // every CTA pushes its candidates into the leader's buffer when they fit
+  if (cand_ok && nc > 0 && (fast || topn_ok) && c.rank > 0) {
+    uint64_t* lb = cluster.map_shared_rank(c.buf, 0);
+    const int mine = min(s.nloc, kBufCap);
+    const int off = s.rs.push_off;
+    for (int i = c.tid; i < mine; i += kThreads) lb[off + i] = c.buf[i];
+  }
+  cluster.sync();  // (3) gathered; partials read
+  VT_TRACE(8);
 
   if (fast) {
-    if (!leader) return;
+    if (!leader) {
+      VT_TRACE(15);
+      return;
+    }
     const int N = nc;
-    const int P2 = pow2_ceil(max(N, 1));
-    for (int i = N + c.tid; i < P2; i += kThreads) c.gather[i] = 0ull;
-    __syncthreads();
-    bitonic_desc_u64(c.gather, P2);
+    block_sort_desc(c.buf, N);
     for (int t = c.tid; t < n; t += kThreads) {
-      const uint64_t k = c.gather[t];
+      const uint64_t k = c.buf[t];
       out_ids[t] = (int)key_idx(k);
       out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
     }
@@ -1135,50 +1614,10 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       ztok = c.m_t;
       L3 = 1;
     } else {
-      // min-p prefix length among the candidates
-      int pass = 0;
-      if (c.minp)
-        for (int i = c.tid; i < N; i += kThreads) pass += minp_pass(key_z(c.gather[i]), c.m_t, c.lmp);
-      const int L1 = c.minp ? block_sum_int(pass, s) : N;
-      const int L2 = c.topk ? min(c.top_k, L1) : L1;
-      L3 = L2;
-      if (c.topp) {
-        const int per = (L2 + kThreads - 1) / kThreads;
-        const int i0 = c.tid * per, i1 = min(L2, i0 + per);
-        unsigned long long lm = 0;
-        for (int i = i0; i < i1; ++i) lm += mass_fixed(key_z(c.gather[i]), c.m_t);
-        unsigned long long tot;
-        const unsigned long long ex = block_exclusive_u64(lm, s, &tot);
-        const unsigned long long W2 = L2_inside ? tot : (unsigned long long)S_fixed;
-        const unsigned long long Tm = (unsigned long long)((double)W2 * (double)c.top_p);
-        int kept = 0;
-        unsigned long long run = ex;
-        for (int i = i0; i < i1; ++i) {
-          if (run <= Tm) ++kept;
-          run += mass_fixed(key_z(c.gather[i]), c.m_t);
-        }
-        L3 = max(1, block_sum_int(kept, s));
-      }
-      // Gumbel-max draw over the kept prefix
-      float bs = -INFINITY, bz = 0.f;
-      int bidx = INT_MAX;
-      for (int i = c.tid; i < L3; i += kThreads) {
-        const uint64_t k = c.gather[i];
-        const int j = (int)key_idx(k);
-        const float zt = key_z(k);
-        const float sc = gumbel_score(zt, noise_bits(c.rkey, j));
-        if (pair_better(sc, j, bs, bidx)) {
-          bs = sc;
-          bidx = j;
-          bz = zt;
-        }
-      }
-      block_argmax(bs, bidx, bz, s);
-      tok = bidx;
-      ztok = bz;
+      L3 = leader_draw(c, s, N, L2_inside, S_fixed, &tok, &ztok);
     }
     if (c.tid == 0) {
-      const uint64_t kk = c.gather[L3 - 1];
+      const uint64_t kk = c.buf[L3 - 1];
       a.out_tokens[c.row] = tok;
       if (a.out_logprobs) a.out_logprobs[c.row] = (ztok - c.m_t) - c.lnS;
       a.row_status[c.row] = kRowOk;
@@ -1188,60 +1627,53 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       a.seeds[c.row] += kSeedStep;
       if (s.rs.err) atomicOr(a.err_word, s.rs.err);
     }
+    VT_TRACE(9);
     if (a.update_counts) {
       __syncthreads();
       append_token(a.hist + (int64_t)c.row * a.hist_cap, a.hist_len + c.row, a.hist_cap, tok, s,
                    a.row_status + c.row);
     }
+    VT_TRACE(15);
     return;
   }
+  VT_TRACE(10);
 
   // ---- slow path: every CTA stays ------------------------------------------
-  // top-n log-probs first (the gather buffer is reused below)
   if (n > 0) {
     if (topn_ok) {
       if (leader) {
-        const int N = nc;
-        const int P2 = pow2_ceil(max(N, 1));
-        for (int i = N + c.tid; i < P2; i += kThreads) c.gather[i] = 0ull;
-        __syncthreads();
-        bitonic_desc_u64(c.gather, P2);
+        block_sort_desc(c.buf, nc);
         for (int t = c.tid; t < n; t += kThreads) {
-          const uint64_t k = c.gather[t];
+          const uint64_t k = c.buf[t];
           out_ids[t] = (int)key_idx(k);
           out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
         }
       }
     } else {
-      // rank n-1 of every non-NaN element (the -inf ones included, by index)
-      SelOut so = cluster_select<T>(c, data, s, cluster, kPredAll, 0ull, false,
-                                    (unsigned long long)(n - 1), 0.f);
+      // rank n-1 of every element (the -inf ones included, by index)
+      SelOut so = cluster_select<T>(c, s, cluster, kPredAll, 0ull, false,
+                                    (unsigned long long)(n - 1), 0.f, false);
       const unsigned long long kb = so.all ? 0ull : so.kb;
       if (leader && c.tid == 0) s.gcount = 0;
       cluster.sync();
-      uint64_t* lg = cluster.map_shared_rank(c.gather, 0);
+      uint64_t* lg = cluster.map_shared_rank(c.buf, 0);
       int* lcount = cluster.map_shared_rank(&s.gcount, 0);
       const uint32_t kb_hi = (uint32_t)(kb >> 32);
       for_each_elem<T>(
-          c, data, [&](float gz) { return ord_key(gz) >= kb_hi; },
-          [&](float zt, int j, bool side) {
-            if (j >= c.V) return;
-            if (zt == -INFINITY && !side && is_side_slot(c, j)) return;
+          c, [&](float gz) { return ord_key(gz) >= kb_hi; },
+          [&](float zt, int j) {
             const unsigned long long K = elem_key(zt, (uint32_t)j);
             if (K < kb) return;
             const int pos = atomicAdd(lcount, 1);
-            if (pos < kGatherCap) lg[pos] = K;
+            if (pos < kBufCap) lg[pos] = K;
           });
       cluster.sync();
       if (leader) {
-        const int N = min(s.gcount, kGatherCap);
-        const int P2 = pow2_ceil(max(N, 1));
-        for (int i = N + c.tid; i < P2; i += kThreads) c.gather[i] = 0ull;
-        __syncthreads();
-        bitonic_desc_u64(c.gather, P2);
+        const int N = min(s.gcount, kBufCap);
+        block_sort_desc(c.buf, N);
         for (int t = c.tid; t < n; t += kThreads) {
           if (t < N) {
-            const uint64_t k = c.gather[t];
+            const uint64_t k = c.buf[t];
             out_ids[t] = (int)key_idx(k);
             out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
           } else {
@@ -1262,35 +1694,68 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
   if (c.greedy) {
     tok = s.rs.bi;
     ztok = c.m_t;
+    cluster.sync();
+    if (!leader) return;
   } else {
-    // kept set: threshold rows (no top-k, no top-p) or a selected boundary
-    bool bounded = false;
-    unsigned long long kb = 0ull;
+    bool bounded = false, draw_known = false;
+    unsigned long long kb = 0ull, win = kNegInfKey;
     if (c.topk || c.topp) {
       unsigned long long kbk = 0ull;
       if (c.topk) {
-        SelOut so = cluster_select<T>(c, data, s, cluster, kPredSurv, 0ull, false,
-                                      (unsigned long long)(c.top_k - 1), 0.f);
+        SelOut so = cluster_select<T>(c, s, cluster, kPredSurv, 0ull, false,
+                                      (unsigned long long)(c.top_k - 1), 0.f, !c.topp);
         if (!so.all) {
           kbk = so.kb;
           bounded = true;
           kb = so.kb;
           kept = (int)so.cnt_incl;
+          if (!c.topp && so.draw_ok) {
+            draw_known = true;
+            win = so.win;
+          }
         } else {
           kept = (int)so.total_cnt;
         }
       }
       if (c.topp) {
-        SelOut so = cluster_select<T>(c, data, s, cluster, kPredSurv, kbk, true, 0ull, c.top_p);
+        SelOut so = cluster_select<T>(c, s, cluster, kPredSurv, kbk, true, 0ull, c.top_p, true);
         if (!so.all) {
           bounded = true;
           kb = so.kb;
           kept = (int)so.cnt_incl;
+          if (so.draw_ok) {
+            draw_known = true;
+            win = so.win;
+          }
         } else {
           kept = (int)so.total_cnt;
         }
       }
     }
+    if (draw_known) {
+      // the winner's tempered logit comes from the CTA that owns its index
+      const int wi = (int)key_idx(win);
+      if (c.tid == 0 && wi >= c.lo && wi < c.hi) {
+        const int g = (wi - c.lo) / E;
+        float x[E];
+        load_group<T>(c, g, x);
+        float xv = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+          if (c.lo + g * E + i == wi) xv = x[i];
+        cluster.map_shared_rank(&s.bcast_f[0], 0)[0] = __fmul_rn(xv, c.inv_t);
+      }
+      VT_TRACE(11);
+      cluster.sync();  // final: no DSMEM access after this
+      if (!leader) {
+        VT_TRACE(15);
+        return;
+      }
+      tok = wi;
+      ztok = s.bcast_f[0];
+      kth_v = key_z(kb);
+      kth_i = (int)key_idx(kb);
+    } else {
     // draw pass over the kept elements
     float s_cur = -INFINITY, bz = 0.f;
     int bidx = INT_MAX;
@@ -1298,25 +1763,37 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     unsigned long long kmin = ~0ull;
     const uint32_t kb_hi = (uint32_t)(kb >> 32);
     const bool threshold_row = !bounded;  // kept = every survivor: count it here
-    for_each_elem<T>(
-        c, data,
-        [&](float gz) { return gz > -INFINITY && (!bounded || ord_key(gz) >= kb_hi); },
-        [&](float zt, int j, bool) {
-          if (!(zt > -INFINITY)) return;
-          if (c.minp && !minp_pass(zt, c.m_t, c.lmp)) return;
-          const unsigned long long K = elem_key(zt, (uint32_t)j);
-          if (bounded && K < kb) return;
-          if (threshold_row) {
-            ++cnt;
-            kmin = K < kmin ? K : kmin;
-          }
-          const uint32_t b = noise_bits(c.rkey, j);
-          if (!may_beat(zt, s_cur, b)) return;
-          const float sc = gumbel_score(zt, b);
-          if (pair_better(sc, j, s_cur, bidx)) {
-            s_cur = sc;
-            bidx = j;
-            bz = zt;
+    auto kept_elem = [&](float zt, int j) -> bool {
+      if (!(zt > -INFINITY) || j >= c.hi) return false;
+      if (c.minp && !minp_pass(zt, c.m_t, c.lmp)) return false;
+      return !bounded || elem_key(zt, (uint32_t)j) >= kb;
+    };
+    auto score_elem = [&](float zt, int j, uint32_t b) {
+      if (threshold_row) {
+        ++cnt;
+        const unsigned long long K = elem_key(zt, (uint32_t)j);
+        kmin = K < kmin ? K : kmin;
+      }
+      if (!may_beat(zt, s_cur, b)) return;
+      const float sc = gumbel_score(zt, b);
+      if (pair_better(sc, j, s_cur, bidx)) {
+        s_cur = sc;
+        bidx = j;
+        bz = zt;
+      }
+    };
+    for_each_group<T>(
+        c, [&](float gz) { return gz > -INFINITY && (!bounded || ord_key(gz) >= kb_hi); },
+        [&](float* x, int, int j0) {
+#pragma unroll
+          for (int i = 0; i < E; i += 2) {
+            // one SplitMix64 output serves the column pair (j0 + i, j0 + i + 1)
+            const float z0 = __fmul_rn(x[i], c.inv_t), z1 = __fmul_rn(x[i + 1], c.inv_t);
+            const bool k0 = kept_elem(z0, j0 + i), k1 = kept_elem(z1, j0 + i + 1);
+            if (!(k0 || k1)) continue;
+            const uint64_t h = pair_hash(c.rkey, j0 + i);
+            if (k0) score_elem(z0, j0 + i, bits_even(h));
+            if (k1) score_elem(z1, j0 + i + 1, bits_odd(h));
           }
         });
     block_argmax(s_cur, bidx, bz, s);
@@ -1363,8 +1840,12 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
         s.bcast_u[1] = km;
       }
     }
+    VT_TRACE(11);
     cluster.sync();  // final: no DSMEM access after this
-    if (!leader) return;
+    if (!leader) {
+      VT_TRACE(15);
+      return;
+    }
     __syncthreads();
     tok = s.bcast_i[0];
     ztok = s.bcast_f[0];
@@ -1376,10 +1857,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
       kth_v = key_z(kb);
       kth_i = (int)key_idx(kb);
     }
-  }
-  if (c.greedy) {
-    cluster.sync();
-    if (!leader) return;
+    }
   }
   if (c.tid == 0) {
     a.out_tokens[c.row] = tok;
@@ -1397,6 +1875,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
     append_token(a.hist + (int64_t)c.row * a.hist_cap, a.hist_len + c.row, a.hist_cap, tok, s,
                  a.row_status + c.row);
   }
+  VT_TRACE(15);
 }
 
 }  // namespace
@@ -1404,39 +1883,50 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs a) {
 // ---------------------------------------------------------------------------
 // host side: plans and launches
 // ---------------------------------------------------------------------------
-static size_t union_bytes(int C) {
-  const size_t hist = (size_t)kBins * 12 + (size_t)(kBins / C) * 12;
-  const size_t gath = (size_t)kGatherCap * 8;
-  return hist > gath ? hist : gath;
-}
-
-LaunchPlan plan_sample(int V, int elem_size) {
-  // Smallest power-of-two cluster whose slices fit a ~48 KB staging budget
-  // (several CTAs per SM), capped at 16 CTAs per row.
-  const size_t target = 48 * 1024;
-  int C = 1;
-  while (C < kMaxCluster && (size_t)((V + C - 1) / C) * elem_size > target) C <<= 1;
-  int slice = (V + C - 1) / C;
-  slice = (slice + 15) & ~15;
+LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties) {
   LaunchPlan p;
-  p.cluster = C;
+  p.cluster = cluster;
+  int slice = (V + cluster - 1) / cluster;
+  slice = (slice + 31) & ~31;
   p.slice = slice;
+  p.pen_smem = penalties ? 1 : 0;
   const int E = kGroupBytes / elem_size;
   const size_t ngroups = (size_t)slice / E;
-  p.smem = (size_t)slice * elem_size + ((ngroups * 4 + 15) & ~(size_t)15) + union_bytes(C);
+  // [0, 32 KB): the pass-A bulk-copy ring, later the candidate buffer (16 KB)
+  // and the selection histograms (12 KB)
+  size_t off = (size_t)kRingBytes;
+  p.off_gmax = (uint32_t)off;
+  off += (ngroups * 2 + 15) & ~(size_t)15;
+  p.off_mrg = (uint32_t)off;
+  if (cluster > 1) off += (size_t)(kBins / cluster) * 20;
+  off = (off + 15) & ~(size_t)15;
+  p.off_bitmap = (uint32_t)off;
+  p.off_prefix = (uint32_t)off;
+  if (penalties) {
+    off += (size_t)(slice / 32) * 4;
+    p.off_prefix = (uint32_t)off;
+    off += (size_t)(slice / 32) * 2;
+    off = (off + 15) & ~(size_t)15;
+  }
+  p.smem = off;
+  p.active_clusters = 0;
   return p;
 }
 
 template <typename T>
-static cudaError_t prepare_one(const LaunchPlan& plan, int* max_active) {
-  cudaError_t e = cudaFuncSetAttribute(sample_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)plan.smem);
-  if (e != cudaSuccess) return e;
-  if (plan.cluster > 8) {
-    e = cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+static cudaError_t prepare_one(LaunchPlan& plan) {
+  // The dynamic shared-memory limit only ever grows, so that every cached
+  // plan stays launchable; clusters above 8 CTAs are always allowed.
+  static size_t smem_set = 0;
+  cudaError_t e = cudaSuccess;
+  if (plan.smem > smem_set) {
+    e = cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)plan.smem);
     if (e != cudaSuccess) return e;
+    smem_set = plan.smem;
   }
+  e = cudaFuncSetAttribute(sample_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.cluster, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1448,16 +1938,36 @@ static cudaError_t prepare_one(const LaunchPlan& plan, int* max_active) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, sample_kernel<T>, &cfg);
+  int nclusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&nclusters, sample_kernel<T>, &cfg);
   if (e != cudaSuccess) return e;
-  if (max_active) *max_active = n;
-  return n > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+  plan.active_clusters = nclusters;
+  return nclusters > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
-cudaError_t prepare_sample(const LaunchPlan& plan, int dtype, int* max_active_clusters) {
-  return dtype == 0 ? prepare_one<float>(plan, max_active_clusters)
-                    : prepare_one<uint16_t>(plan, max_active_clusters);
+cudaError_t prepare_sample(LaunchPlan& plan, int dtype) {
+  return dtype == 0 ? prepare_one<float>(plan) : prepare_one<uint16_t>(plan);
+}
+
+LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, int num_sms) {
+  // Slices of at most 256 KB (so the per-group structures stay small) and at
+  // least 8 KB of logits; among those, the largest cluster that still lets
+  // all B rows be resident at once, else the smallest one.
+  (void)num_sms;
+  const size_t max_slice = 256 * 1024, min_slice = 8 * 1024;
+  int cmin = 1;
+  while (cmin < kMaxCluster && (size_t)((V + cmin - 1) / cmin) * elem_size > max_slice) cmin <<= 1;
+  LaunchPlan best = plan_layout(V, elem_size, cmin, penalties);
+  if (prepare_sample(best, dtype) != cudaSuccess) return best;
+  if ((int64_t)B > best.active_clusters) return best;  // several waves even so
+  for (int C = cmin * 2; C <= kMaxCluster; C <<= 1) {
+    if ((size_t)((V + C - 1) / C) * elem_size < min_slice) break;
+    LaunchPlan p = plan_layout(V, elem_size, C, penalties);
+    if (prepare_sample(p, dtype) != cudaSuccess) break;
+    if ((int64_t)B > p.active_clusters) break;  // would no longer fit in one wave
+    best = p;
+  }
+  return best;
 }
 
 template <typename T>

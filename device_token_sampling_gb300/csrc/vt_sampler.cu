@@ -60,7 +60,10 @@ struct vt_sampler {
   int counts_B = 0;
   int last_B = 0;
   cudaStream_t last_stream = nullptr;
-  std::map<std::pair<int, int>, vt::LaunchPlan> plans;
+  std::map<std::pair<std::pair<int, int>, std::pair<int, int>>, vt::LaunchPlan> plans;
+  int num_sms = 0;
+  unsigned long long* trace = nullptr;  // debug phase trace (caller-owned)
+  int64_t trace_ctas = 0;
 };
 
 namespace {
@@ -171,9 +174,10 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return bail(VT_ERR_CUDA);
   if (!(prop.major == 10 && prop.minor == 3)) return bail(VT_ERR_CUDA);  // built for sm_103a only
-  // the largest row must fit the shared-memory plan
-  const vt::LaunchPlan worst = vt::plan_sample(cfg->max_vocab, 4);
+  // the largest row must fit the shared-memory plan (16 CTAs per row at most)
+  const vt::LaunchPlan worst = vt::plan_layout(cfg->max_vocab, 4, 16, true);
   if (worst.smem > (size_t)prop.sharedMemPerBlockOptin) return bail(VT_ERR_CAPACITY);
+  h->num_sms = prop.multiProcessorCount;
 
   const size_t B = (size_t)cfg->max_batch;
   const size_t H = (size_t)(cfg->max_history > 0 ? cfg->max_history : 1);
@@ -389,12 +393,13 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     if ((h->row_flags[r] & vt::kRowPenalty) && r >= h->counts_B)
       return set_err(h, VT_ERR_STATE, "row %d has penalties but its counts were never reset", r);
   const int es = dtype == VT_DTYPE_F32 ? 4 : 2;
-  auto key = std::make_pair(V, dtype);
+  bool any_pen = false;
+  for (int r = 0; r < B && !any_pen; ++r) any_pen = (h->row_flags[r] & vt::kRowPenalty) != 0;
+  auto key = std::make_pair(std::make_pair(B, V), std::make_pair(dtype, any_pen ? 1 : 0));
   auto it = h->plans.find(key);
   if (it == h->plans.end()) {
-    vt::LaunchPlan plan = vt::plan_sample(V, es);
-    int active = 0;
-    const cudaError_t e = vt::prepare_sample(plan, dtype, &active);
+    vt::LaunchPlan plan = vt::plan_sample(B, V, es, any_pen, dtype, h->num_sms);
+    const cudaError_t e = vt::prepare_sample(plan, dtype);
     if (e != cudaSuccess)
       return set_err(h, VT_ERR_CUDA, "cannot prepare a %d-CTA cluster plan: %s", plan.cluster,
                      cudaGetErrorString(e));
@@ -409,7 +414,12 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
   a.n_logprobs = n;
   a.update_counts = update_counts ? 1 : 0;
   a.slice = plan.slice;
-  a.use_bulk = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
+  a.aligned = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
+  a.pen_smem = plan.pen_smem;
+  a.off_gmax = plan.off_gmax;
+  a.off_mrg = plan.off_mrg;
+  a.off_bitmap = plan.off_bitmap;
+  a.off_prefix = plan.off_prefix;
   a.params = h->d_params;
   a.seeds = h->d_seeds;
   a.hist = h->d_hist;
@@ -425,6 +435,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
   a.dbg_kth_index = h->d_kth_i;
   a.dbg_kept = h->d_kept;
   a.err_word = h->d_err;
+  a.trace = (h->trace && (int64_t)B * plan.cluster <= h->trace_ctas) ? h->trace : nullptr;
   VT_CK(h, vt::launch_sample(a, plan, dtype, st));
   h->last_B = B;
   h->last_stream = st;
@@ -532,6 +543,29 @@ int vt_debug_get_counts(vt_sampler* h, int32_t row, int32_t* ids, int32_t* count
       counts[i] = tmp[i].y;
     }
   }
+  return VT_OK;
+}
+
+int vt_debug_set_trace(vt_sampler* h, uint64_t* dev_trace, int64_t capacity_ctas,
+                       int32_t* slots_per_cta) {
+  if (!h || capacity_ctas < 0 || (capacity_ctas > 0 && !dev_trace)) return VT_ERR_INVALID_ARG;
+  h->trace = reinterpret_cast<unsigned long long*>(dev_trace);
+  h->trace_ctas = dev_trace ? capacity_ctas : 0;
+  if (slots_per_cta) *slots_per_cta = vt::kTraceSlots;
+  return VT_OK;
+}
+
+int vt_debug_launch_shape(vt_sampler* h, int32_t dtype, int32_t V, int32_t* ctas_per_row,
+                          int32_t* slice_elems, int64_t* smem_bytes) {
+  if (!h || !ctas_per_row || (dtype != VT_DTYPE_F32 && dtype != VT_DTYPE_BF16) || V < 1)
+    return VT_ERR_INVALID_ARG;
+  const int B = h->params_B > 0 ? h->params_B : h->cfg.max_batch;
+  DeviceGuard guard(h->cfg.device);
+  const vt::LaunchPlan p =
+      vt::plan_sample(B, V, dtype == VT_DTYPE_F32 ? 4 : 2, false, dtype, h->num_sms);
+  *ctas_per_row = p.cluster;
+  if (slice_elems) *slice_elems = p.slice;
+  if (smem_bytes) *smem_bytes = (int64_t)p.smem;
   return VT_OK;
 }
 

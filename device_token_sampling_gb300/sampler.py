@@ -66,6 +66,8 @@ SIGNATURES = {
     "vt_debug_filter_boundary": (C.c_int, [P, P, P, P, P]),
     "vt_debug_get_counts": (C.c_int, [P, I32, P, P, I32, P]),
     "vt_debug_get_seeds": (C.c_int, [P, P]),
+    "vt_debug_set_trace": (C.c_int, [P, P, I64, P]),
+    "vt_debug_launch_shape": (C.c_int, [P, I32, I32, P, P, P]),
     "vt_last_error": (C.c_char_p, [P]),
     "vt_status_string": (C.c_char_p, [C.c_int]),
 }
@@ -283,6 +285,24 @@ class Sampler:
         self._check(self._lib.vt_debug_get_counts(self._h, row, _np_ptr(ids), _np_ptr(cnt), cap,
                                                   C.byref(n)), "vt_debug_get_counts")
         return ids[:n.value].copy(), cnt[:n.value].copy()
+
+    def launch_shape(self, dtype: int, V: int):
+        c, sl, sm = C.c_int32(), C.c_int32(), C.c_int64()
+        self._check(self._lib.vt_debug_launch_shape(self._h, dtype, V, C.byref(c), C.byref(sl),
+                                                    C.byref(sm)), "vt_debug_launch_shape")
+        return c.value, sl.value, sm.value
+
+    def set_trace(self, buf=None):
+        """Enable the per-CTA phase trace into a CUDA int64 tensor [ctas, slots]
+        (None disables it).  Returns the slot count."""
+        slots = C.c_int32()
+        if buf is None:
+            self._check(self._lib.vt_debug_set_trace(self._h, None, 0, C.byref(slots)),
+                        "vt_debug_set_trace")
+        else:
+            self._check(self._lib.vt_debug_set_trace(self._h, P(buf.data_ptr()), buf.shape[0],
+                                                     C.byref(slots)), "vt_debug_set_trace")
+        return slots.value
 
     def seeds(self, B: int):
         s = np.zeros(self.cfg.max_batch, np.uint64)  # the call writes up to max_batch seeds

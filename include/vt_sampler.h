@@ -188,6 +188,20 @@ int vt_debug_filter_boundary(vt_sampler* handle, float* kth_value, int32_t* kth_
 int vt_debug_get_counts(vt_sampler* handle, int32_t row, int32_t* ids, int32_t* counts,
                         int32_t capacity, int32_t* n_unique);
 
+/* Debug: the launch shape vt_sample would use for (dtype, V), the B of the last
+ * vt_reset_params (max_batch before any) and rows without penalties: CTAs per
+ * row, logits elements per CTA and dynamic shared memory per CTA. */
+int vt_debug_launch_shape(vt_sampler* handle, int32_t dtype, int32_t V, int32_t* ctas_per_row,
+                          int32_t* slice_elems, int64_t* smem_bytes);
+
+/* Debug: phase trace.  With a device buffer of capacity_ctas * slots_per_cta
+ * uint64 entries set, each later vt_sample whose grid fits writes, per CTA,
+ * the GPU global timer (ns) at each phase boundary (slots not reached keep
+ * their old value).  *slots_per_cta receives the slot count.  NULL turns it
+ * off.  The buffer stays owned by the caller and must outlive its use. */
+int vt_debug_set_trace(vt_sampler* handle, uint64_t* dev_trace, int64_t capacity_ctas,
+                       int32_t* slots_per_cta);
+
 /* Read the current per-row seeds of rows 0..B-1 into a host array (B of the
  * last vt_reset_params).  Synchronises the handle's last stream. */
 int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
