@@ -68,6 +68,8 @@ SIGNATURES = {
     "vt_debug_get_seeds": (C.c_int, [P, P]),
     "vt_debug_set_trace": (C.c_int, [P, P, I64, P]),
     "vt_debug_launch_shape": (C.c_int, [P, I32, I32, P, P, P]),
+    "vt_sample_noalloc": (C.c_int, [I32, P, I32, I32, I32, I64, P, P, P, P, P, I32, P, P, P, P,
+                                    P, I32, P, C.c_char_p, I32]),
     "vt_last_error": (C.c_char_p, [P]),
     "vt_status_string": (C.c_char_p, [C.c_int]),
 }
@@ -308,3 +310,42 @@ class Sampler:
         s = np.zeros(self.cfg.max_batch, np.uint64)  # the call writes up to max_batch seeds
         self._check(self._lib.vt_debug_get_seeds(self._h, _np_ptr(s)), "vt_debug_get_seeds")
         return s[:B]
+
+
+NOALLOC_MAX_BATCH = 1024
+
+
+def sample_noalloc(logits, temperature, top_k, top_p, min_p, seed, out_tokens,
+                   V: int | None = None, dtype: int | None = None, num_logprobs: int = 0,
+                   out_logprobs=None, out_topk_ids=None, out_topk_logprobs=None,
+                   row_status=None, synchronize: bool = True, stream=None):
+    """``vt_sample_noalloc``: one sampling step without a handle, in the
+    library's fixed device scratch.  All outputs are caller-owned CUDA tensors;
+    the parameters are host sequences of length B.  Raises VtError on failure."""
+    import torch
+    lib = load_library()
+    if logits.dim() != 2 or not logits.is_cuda or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D CUDA tensor with contiguous rows")
+    if dtype is None:
+        if logits.dtype == torch.float32:
+            dtype = DTYPE_F32
+        elif logits.dtype in (torch.bfloat16, torch.uint16, torch.int16):
+            dtype = DTYPE_BF16
+        else:
+            raise ValueError(f"unsupported logits dtype {logits.dtype}")
+    B, ld = logits.shape[0], logits.stride(0)
+    V = logits.shape[1] if V is None else V
+    arr = lambda x, t: np.ascontiguousarray(np.asarray(x, dtype=t))  # noqa: E731
+    T, K, Pp, MP = arr(temperature, np.float32), arr(top_k, np.int32), arr(top_p, np.float32), \
+        arr(min_p, np.float32)
+    S = arr(seed, np.uint64)
+    tp = lambda t: None if t is None else P(t.data_ptr())  # noqa: E731
+    err = C.create_string_buffer(256)
+    rc = lib.vt_sample_noalloc(logits.device.index,
+                               P(logits.data_ptr()), dtype, B, V, ld, _np_ptr(T), _np_ptr(K),
+                               _np_ptr(Pp), _np_ptr(MP), _np_ptr(S), num_logprobs,
+                               tp(out_tokens), tp(out_logprobs), tp(out_topk_ids),
+                               tp(out_topk_logprobs), tp(row_status), 1 if synchronize else 0,
+                               _stream_ptr(stream), err, len(err))
+    if rc != VT_OK:
+        raise VtError(rc, err.value.decode(errors="replace"))

@@ -206,6 +206,50 @@ int vt_debug_set_trace(vt_sampler* handle, uint64_t* dev_trace, int64_t capacity
  * last vt_reset_params).  Synchronises the handle's last stream. */
 int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
 
+/* ---- sampling without any allocation -------------------------------------
+ * The paper has no counterpart of this entry point.  It serves callers that
+ * may not allocate device memory: an engine that reserves nearly all of it
+ * for its KV cache at start-up, a host whose device memory belongs to a
+ * framework's caching allocator, a decode loop that keeps cudaMalloc and
+ * cudaFree (which waits for the whole device) out of its step.  Such callers
+ * cannot create a handle, because vt_sampler_create allocates its buffers.
+ *
+ * vt_sample_noalloc runs the same sampling kernel as vt_sample, for rows
+ * without penalties, and allocates nothing: it calls no cudaMalloc, cudaFree
+ * or allocating library routine.  Its per-row state lives in one fixed
+ * device array of VT_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * call on a device shares.  Calls whose GPU work overlaps (other streams,
+ * other host threads) race on that array and give undefined results; calls on
+ * one stream, one after another, are safe.
+ *
+ *   device        CUDA device ordinal; it is made current during the call
+ *   logits        device [B][ld] of dtype, as in vt_sample
+ *   temperature, top_k, top_p, min_p, seed
+ *                 host arrays [B], the values vt_reset_params takes (no
+ *                 penalties).  seed[r] keys row r's noise exactly as a handle
+ *                 whose seed for row r is seed[r]; the caller advances its own
+ *                 seeds (a handle adds 0x9E3779B97F4A7C15 per call).
+ *   num_logprobs, out_tokens, out_logprobs, out_topk_ids, out_topk_logprobs
+ *                 as in vt_sample (device memory owned by the caller)
+ *   row_status    device int32[B] receiving VT_ROW_* per row, or NULL
+ *   synchronize   nonzero: wait for the stream and report a device-side
+ *                 timeout as VT_ERR_TIMEOUT; zero: return after enqueueing
+ *                 (device-side faults then go unreported)
+ *   errbuf        host buffer of errbuf_len bytes for a message, or NULL
+ * The parameters are uploaded from pageable host memory, so the call waits
+ * for work already queued on `stream` before it enqueues its own.
+ * Errors: VT_ERR_CAPACITY when B > VT_NOALLOC_MAX_BATCH (checked before any
+ * CUDA call) or V needs more shared memory than a CTA has; VT_ERR_INVALID_ARG;
+ * VT_ERR_CUDA (wrong architecture, failed set-up or launch). */
+#define VT_NOALLOC_MAX_BATCH 1024          /* rows per vt_sample_noalloc call  */
+#define VT_NOALLOC_SCRATCH_BYTES (80 * 1024) /* the fixed device scratch array */
+int vt_sample_noalloc(int32_t device, const void* logits, int32_t dtype, int32_t B, int32_t V,
+                      int64_t ld, const float* temperature, const int32_t* top_k,
+                      const float* top_p, const float* min_p, const uint64_t* seed,
+                      int32_t num_logprobs, int32_t* out_tokens, float* out_logprobs,
+                      int32_t* out_topk_ids, float* out_topk_logprobs, int32_t* row_status,
+                      int32_t synchronize, void* stream, char* errbuf, int32_t errbuf_len);
+
 /* Message for the last failing call on `handle` ("" if none); static storage
  * owned by the handle, valid until the next call on it. */
 const char* vt_last_error(const vt_sampler* handle);
