@@ -147,8 +147,10 @@ __device__ __forceinline__ uint32_t noise_bits(uint64_t key, int64_t j) {
 }
 
 // ln(e) with e = -ln(u), u = (b + 1/2) 2^-24, evaluated through inputs that are
-// exact in fp32: u itself below 1/2, 1 - u from 1/2 up.
-__device__ __forceinline__ float log_exp_noise(uint32_t b) {
+// exact in fp32: u itself below 1/2, 1 - u from 1/2 up.  Kept out of line: the
+// scans call it rarely (behind may_beat) from unrolled loops, where inlined
+// copies of the logarithms would crowd the instruction cache.
+static __device__ __noinline__ float log_exp_noise(uint32_t b) {
   float e;
   if (b < (1u << 23)) {
     const float u = (float)(2u * b + 1u) * 0x1p-25f;

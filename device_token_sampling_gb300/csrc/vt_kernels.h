@@ -9,6 +9,14 @@ namespace vt {
 
 struct RowParams;
 
+// A row the streaming kernel hands to the selection kernel.
+struct __align__(16) SlowRow {
+  float m_t;      // tempered row maximum
+  float lnS;      // ln(sum exp(z_t - m_t))
+  int32_t bi;     // lowest index of the maximum
+  int32_t topn_done;  // the top-n outputs are already written
+};
+
 // Everything one sampling launch needs.  Device pointers unless noted.
 struct SampleArgs {
   const void* logits;        // [B][ld] elements
@@ -38,7 +46,23 @@ struct SampleArgs {
   int32_t* dbg_kth_index;    // [B]
   int32_t* dbg_kept;         // [B]
   int32_t* err_word;         // one int, kErr* bits
+  SlowRow* slow;             // [B] hand-over records
+  int32_t* slow_list;        // [B] rows handed over, in arrival order
+  uint32_t* slow_ctl;        // [2] rows handed over, selection CTAs done; zero between calls
   unsigned long long* trace; // optional [grid][kTraceSlots] phase timestamps (ns)
+  int64_t trace_ctas;        // CTAs the trace buffer holds
+};
+
+// Launch shape of the selection kernel (kernel 2).
+struct SelectPlan {
+  int cluster;          // CTAs per row
+  int slice;            // elements per CTA
+  int pen_smem;
+  int staged;           // the slice is copied into shared memory
+  uint32_t off_gmax, off_mrg, off_bitmap, off_prefix, off_stage;
+  size_t smem;
+  int clusters;         // persistent clusters launched
+  int kernel1_cluster;  // CTAs per row of the streaming kernel (trace layout)
 };
 
 constexpr int kTraceSlots = 16;
@@ -50,6 +74,7 @@ struct LaunchPlan {
   uint32_t off_gmax, off_mrg, off_bitmap, off_prefix;
   size_t smem;        // dynamic shared memory per CTA
   int active_clusters;  // clusters resident at once (filled by prepare_sample)
+  SelectPlan sel;       // the selection kernel that finishes handed-over rows
 };
 
 // Shared-memory layout for V elements of elem_size bytes split over `cluster`
@@ -64,7 +89,8 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
 // plan.active_clusters.  Returns a cudaError_t.
 cudaError_t prepare_sample(LaunchPlan& plan, int dtype);
 
-// Launch the fused sampling kernel: grid B * cluster CTAs.
+// Launch the sampling kernels: the streaming kernel (grid B * cluster CTAs),
+// then the selection kernel for the rows it handed over.
 cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,
                           cudaStream_t stream);
 

@@ -38,10 +38,14 @@ constexpr size_t kOffStatus = kOffHistLen + kMaxRows * sizeof(int32_t);   // int
 constexpr size_t kOffKthV = kOffStatus + kMaxRows * sizeof(int32_t);      // float[rows]
 constexpr size_t kOffKthI = kOffKthV + kMaxRows * sizeof(float);          // int32[rows]
 constexpr size_t kOffKept = kOffKthI + kMaxRows * sizeof(int32_t);        // int32[rows]
-constexpr size_t kOffErr = kOffKept + kMaxRows * sizeof(int32_t);         // int32, zero
+constexpr size_t kOffSlow = kOffKept + kMaxRows * sizeof(int32_t);        // SlowRow[rows]
+constexpr size_t kOffSlowList = kOffSlow + kMaxRows * sizeof(vt::SlowRow);  // int32[rows]
+constexpr size_t kOffSlowCtl = kOffSlowList + kMaxRows * sizeof(int32_t);   // uint32[2], zero
+constexpr size_t kOffErr = kOffSlowCtl + 16;                               // int32, zero
 constexpr size_t kUsedBytes = kOffErr + 256;
 static_assert(kUsedBytes <= VT_NOALLOC_SCRATCH_BYTES, "scratch layout exceeds its array");
-static_assert(kOffSeeds % 16 == 0 && kOffErr % 16 == 0, "scratch fields stay aligned");
+static_assert(kOffSeeds % 16 == 0 && kOffSlow % 16 == 0 && kOffErr % 16 == 0,
+              "scratch fields stay aligned");
 
 }  // namespace
 
@@ -220,9 +224,11 @@ extern "C" int vt_sample_noalloc(int32_t device, const void* logits, int32_t dty
   }
   e = cudaMemcpyAsync(d_seeds, seed, (size_t)B * sizeof(uint64_t), cudaMemcpyHostToDevice, st);
   // What must start at zero: the rows' count-table lengths (no penalties, so
-  // no table) and the device error word.
+  // no table), the hand-over counters between the two kernels and the device
+  // error word (the last three are contiguous).
+  auto* d_slow_ctl = reinterpret_cast<uint32_t*>(scr + kOffSlowCtl);
   if (e == cudaSuccess) e = cudaMemsetAsync(d_hist_len, 0, (size_t)B * sizeof(int32_t), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(d_err, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d_slow_ctl, 0, kOffErr + sizeof(int32_t) - kOffSlowCtl, st);
   if (e != cudaSuccess)
     return fail(errbuf, errbuf_len, VT_ERR_CUDA, "scratch set-up: %s", cudaGetErrorString(e));
 
@@ -256,7 +262,11 @@ extern "C" int vt_sample_noalloc(int32_t device, const void* logits, int32_t dty
   a.dbg_kth_index = reinterpret_cast<int32_t*>(scr + kOffKthI);
   a.dbg_kept = reinterpret_cast<int32_t*>(scr + kOffKept);
   a.err_word = d_err;
+  a.slow = reinterpret_cast<vt::SlowRow*>(scr + kOffSlow);
+  a.slow_list = reinterpret_cast<int32_t*>(scr + kOffSlowList);
+  a.slow_ctl = d_slow_ctl;
   a.trace = nullptr;
+  a.trace_ctas = 0;
   e = vt::launch_sample(a, plan, dtype, st);
   if (e != cudaSuccess)
     return fail(errbuf, errbuf_len, VT_ERR_CUDA, "launch: %s", cudaGetErrorString(e));

@@ -128,11 +128,6 @@ __device__ __forceinline__ float bf16_next_up(uint16_t b) {
     n = (b >= 0x7F80u) ? b : (uint32_t)(b + 1u);
   return __uint_as_float(n << 16);
 }
-// Order-preserving 16-bit key of a bf16 bit pattern (no NaNs).
-__device__ __forceinline__ uint32_t ord16(uint16_t b) {
-  return (b & 0x8000u) ? (uint32_t)(~b & 0xFFFFu) : (uint32_t)(b | 0x8000u);
-}
-
 // Per-CTA partial results; other CTAs of the cluster read them over DSMEM.
 struct Part {
   float m, s, bv;
@@ -146,12 +141,11 @@ struct Part {
   int didx;
   int kept;
   unsigned long long kmin;
-  float s_exact;
   int err;
 };
 
 struct RowStats {
-  float M, S, m_t, lnS, bv;
+  float S, m_t, lnS, bv;
   int bi;
   int nonfinite;
   float tau, tau_n;
@@ -213,6 +207,7 @@ struct Ctx {
   const uint32_t* bitmap;  // penalised positions of the slice
   const uint16_t* prefix;  // side-list index of each bitmap word's first bit
   const float* side_z;     // penalised values, in id order, of this slice
+  const uint4* stage;      // the slice copied to shared memory (selection kernel), or null
   uint64_t rkey;           // noise stream key
   unsigned long long* trace;  // optional phase trace of this CTA (kTraceSlots stamps)
 };
@@ -239,6 +234,11 @@ __device__ __forceinline__ void patch_group(const Ctx& c, int g, float* x);
 template <typename T>
 __device__ __forceinline__ void load_group(const Ctx& c, int g, float* x) {
   constexpr int E = Elt<T>::E;
+  if (c.stage) {  // staged slices are padded with -inf to whole groups
+    Elt<T>::unpack(c.stage[2 * g], c.stage[2 * g + 1], x);
+    patch_group<T>(c, g, x);
+    return;
+  }
   const T* row = reinterpret_cast<const T*>(c.rowp);
   const int j0 = c.lo + g * E;
   if (c.aligned && j0 + E <= c.hi) {
@@ -284,8 +284,15 @@ __device__ __forceinline__ void for_each_group(const Ctx& c, GF group_ok, FN fn)
     while (g < c.ngroups && !group_ok(__fmul_rn(bf16_next_up(c.gmax[g]), c.inv_t))) g += kThreads;
     return g;
   };
-  auto vec_ok = [&](int g) { return c.aligned && c.lo + (g + 1) * E <= c.hi; };
+  auto vec_ok = [&](int g) {
+    return c.stage != nullptr || (c.aligned && c.lo + (g + 1) * E <= c.hi);
+  };
   auto fetch = [&](int g, uint4& u0, uint4& u1) {
+    if (c.stage) {
+      u0 = c.stage[2 * g];
+      u1 = c.stage[2 * g + 1];
+      return;
+    }
     const uint4* q = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(c.rowp) + c.lo +
                                                     g * E);
     u0 = __ldg(q);
@@ -338,22 +345,6 @@ __device__ int block_sum_int(int v, Smem& s) {
   }
   __syncthreads();
   const int r = s.ri[kWarps];
-  __syncthreads();
-  return r;
-}
-
-__device__ float block_sum_f(float v, Smem& s) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) s.rf[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kWarps; ++w) t += s.rf[w];
-    s.rf[kWarps] = t;
-  }
-  __syncthreads();
-  const float r = s.rf[kWarps];
   __syncthreads();
   return r;
 }
@@ -593,7 +584,7 @@ constexpr float kDScale = 64.0f;
 constexpr unsigned long long kNegInfKey = 0x007FFFFF00000000ull;  // elem_key(-inf, ~0)
 
 template <typename T>
-__device__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group& cluster, int pred,
+__device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group& cluster, int pred,
                                  unsigned long long kbound, bool by_mass,
                                  unsigned long long count_target, float p, bool with_draw) {
   constexpr int E = Elt<T>::E;
@@ -630,6 +621,7 @@ __device__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group& cluster, in
       c.hbest[b] = kNegInfKey;
     }
     __syncthreads();
+    if (dlevel) VT_CTRACE(c, 4);
     const uint32_t klo_hi = (uint32_t)(Klo >> 32);
     if (dlevel) {
       // the catch-all bin is summed per thread (no contention on one word)
@@ -1033,46 +1025,42 @@ __device__ int leader_draw(Ctx& c, Smem& s, int N, bool L2_inside, double S_fixe
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// per-row set-up shared by both kernels
 // ---------------------------------------------------------------------------
+// Geometry, shared-memory views and parameters of row `row` for CTA `rank` of
+// a C-CTA cluster whose CTAs own `slice` elements each.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ Smem s;
-  cg::cluster_group cluster = cg::this_cluster();
-  constexpr int E = Elt<T>::E;
-
-  Ctx c;
+__device__ RowParams init_row(Ctx& c, const SampleArgs& a, uint8_t* dsm, int row, int C,
+                              int rank, int slice, uint32_t off_gmax, uint32_t off_mrg) {
   c.tid = threadIdx.x;
   c.lane = c.tid & 31;
   c.warp = c.tid >> 5;
-  c.C = (int)cluster_nctarank();
-  c.rank = (int)cluster_ctarank();
-  c.row = blockIdx.x / c.C;
+  c.C = C;
+  c.rank = rank;
+  c.row = row;
   c.V = a.V;
-  c.slice = a.slice;
-  c.lo = c.rank * a.slice;
-  c.hi = min(c.lo + a.slice, a.V);
-  c.ngroups = a.slice / E;
+  c.slice = slice;
+  c.lo = rank * slice;
+  c.hi = min(c.lo + slice, a.V);
+  c.ngroups = slice / Elt<T>::E;
   c.aligned = a.aligned != 0;
-  c.rowp = reinterpret_cast<const T*>(a.logits) + (int64_t)c.row * a.ld;
+  c.rowp = reinterpret_cast<const T*>(a.logits) + (int64_t)row * a.ld;
   c.buf = reinterpret_cast<uint64_t*>(dsm);
   c.hmass = reinterpret_cast<unsigned long long*>(dsm);
   c.hcnt = reinterpret_cast<unsigned int*>(dsm + kBins * 8);
   // per-bin bests live past the gather buffer, so they survive the band collect
   c.hbest = reinterpret_cast<unsigned long long*>(dsm + (size_t)kBufCap * 8);
-  c.gmax = reinterpret_cast<uint16_t*>(dsm + a.off_gmax);
-  if (c.C > 1) {
-    c.mmass = reinterpret_cast<unsigned long long*>(dsm + a.off_mrg);
-    c.mbest = reinterpret_cast<unsigned long long*>(dsm + a.off_mrg + (kBins / c.C) * 8);
-    c.mcnt = reinterpret_cast<unsigned int*>(dsm + a.off_mrg + (kBins / c.C) * 16);
+  c.gmax = reinterpret_cast<uint16_t*>(dsm + off_gmax);
+  if (C > 1) {
+    c.mmass = reinterpret_cast<unsigned long long*>(dsm + off_mrg);
+    c.mbest = reinterpret_cast<unsigned long long*>(dsm + off_mrg + (kBins / C) * 8);
+    c.mcnt = reinterpret_cast<unsigned int*>(dsm + off_mrg + (kBins / C) * 16);
   } else {
     c.mmass = c.hmass;
     c.mcnt = c.hcnt;
     c.mbest = c.hbest;
   }
-
-  const RowParams P = a.params[c.row];
+  const RowParams P = a.params[row];
   c.greedy = (P.flags & kRowGreedy) != 0;
   c.inv_t = P.inv_t;
   c.ax = P.inv_t * kLog2e;
@@ -1082,14 +1070,84 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   c.topp = !c.greedy && (P.flags & kRowTopP) != 0;
   c.minp = !c.greedy && (P.flags & kRowMinP) != 0;
   c.lmp = P.log_min_p;
-  c.rkey = row_key(a.seeds[c.row], c.row);
-  c.trace = a.trace ? a.trace + (size_t)blockIdx.x * kTraceSlots : nullptr;
-  const int n = a.n_logprobs;
-  const int hist_len = a.hist_len[c.row];
-  c.pen = a.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0;
+  c.rkey = row_key(a.seeds[row], row);
+  c.trace = nullptr;
+  c.pen = false;
   c.bitmap = nullptr;
   c.prefix = nullptr;
   c.side_z = nullptr;
+  c.stage = nullptr;
+  return P;
+}
+
+// Penalties of the slice's seen tokens: a bitmap of their positions and the
+// side-list index of each bitmap word in shared memory; their penalised values
+// go to the row's side list in global memory (id order).
+template <typename T>
+__device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowParams& P,
+                                uint8_t* dsm, uint32_t off_bitmap, uint32_t off_prefix,
+                                int hist_len) {
+  const int2* tab = a.hist + (int64_t)c.row * a.hist_cap;
+  float* zs = a.zside + (int64_t)c.row * a.hist_cap;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(dsm + off_bitmap);
+  uint16_t* prefix = reinterpret_cast<uint16_t*>(dsm + off_prefix);
+  const int nwords = c.slice / 32;
+  for (int w = c.tid; w < nwords; w += kThreads) bitmap[w] = 0u;
+  int below_lo = 0, below_hi = 0;
+  for (int e = c.tid; e < hist_len; e += kThreads) {
+    const int id = tab[e].x;
+    below_lo += id < c.lo;
+    below_hi += id < c.hi;
+  }
+  const int e_lo = block_sum_int(below_lo, s);
+  const int e_hi = block_sum_int(below_hi, s);
+  const T* row = reinterpret_cast<const T*>(c.rowp);
+  for (int e = e_lo + c.tid; e < e_hi; e += kThreads) {
+    const int2 t = tab[e];
+    const int local = t.x - c.lo;
+    if (local < 0 || local >= c.hi - c.lo) {  // an unsorted table never writes outside
+      atomicOr(&s.part.err, kErrInternal);
+      continue;
+    }
+    zs[e] = penalize(Elt<T>::load1(row + t.x), t.y, P);
+    atomicOr(&bitmap[local >> 5], 1u << (local & 31));
+  }
+  __syncthreads();
+  // side-list index of each word's first position: exclusive scan of popcounts
+  const int per = (nwords + kThreads - 1) / kThreads;
+  const int w0 = min(nwords, c.tid * per), w1 = min(nwords, w0 + per);
+  unsigned long long cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
+  unsigned long long tot;
+  unsigned long long run = block_exclusive_u64(cnt, s, &tot);
+  for (int w = w0; w < w1; ++w) {
+    prefix[w] = (uint16_t)run;
+    run += __popc(bitmap[w]);
+  }
+  c.bitmap = bitmap;
+  c.prefix = prefix;
+  c.side_z = zs + e_lo;
+  c.pen = true;
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// kernel 1: stream every row once; finish the rows its candidates can finish
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ Smem s;
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int E = Elt<T>::E;
+
+  Ctx c;
+  const int C = (int)cluster_nctarank();
+  const RowParams P = init_row<T>(c, a, dsm, blockIdx.x / C, C, (int)cluster_ctarank(), a.slice,
+                                  a.off_gmax, a.off_mrg);
+  c.trace = a.trace ? a.trace + (size_t)blockIdx.x * kTraceSlots : nullptr;
+  const int n = a.n_logprobs;
+  const int hist_len = a.hist_len[c.row];
   VT_TRACE(0);
 
   if (c.tid == 0) {
@@ -1098,50 +1156,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     s.gcount = 0;
   }
 
-  // ---- setup: penalties of the slice's seen tokens ----------------------------
-  if (c.pen) {
-    const int2* tab = a.hist + (int64_t)c.row * a.hist_cap;
-    float* zs = a.zside + (int64_t)c.row * a.hist_cap;
-    uint32_t* bitmap = reinterpret_cast<uint32_t*>(dsm + a.off_bitmap);
-    uint16_t* prefix = reinterpret_cast<uint16_t*>(dsm + a.off_prefix);
-    const int nwords = a.slice / 32;
-    for (int w = c.tid; w < nwords; w += kThreads) bitmap[w] = 0u;
-    int below_lo = 0, below_hi = 0;
-    for (int e = c.tid; e < hist_len; e += kThreads) {
-      const int id = tab[e].x;
-      below_lo += id < c.lo;
-      below_hi += id < c.hi;
-    }
-    const int e_lo = block_sum_int(below_lo, s);
-    const int e_hi = block_sum_int(below_hi, s);
-    const T* row = reinterpret_cast<const T*>(c.rowp);
-    for (int e = e_lo + c.tid; e < e_hi; e += kThreads) {
-      const int2 t = tab[e];
-      const int local = t.x - c.lo;
-      if (local < 0 || local >= c.hi - c.lo) {  // an unsorted table never writes outside
-        atomicOr(&s.part.err, kErrInternal);
-        continue;
-      }
-      zs[e] = penalize(Elt<T>::load1(row + t.x), t.y, P);
-      atomicOr(&bitmap[local >> 5], 1u << (local & 31));
-    }
-    __syncthreads();
-    // side-list index of each word's first position: exclusive scan of popcounts
-    const int per = (nwords + kThreads - 1) / kThreads;
-    const int w0 = min(nwords, c.tid * per), w1 = min(nwords, w0 + per);
-    unsigned long long cnt = 0;
-    for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
-    unsigned long long tot;
-    unsigned long long run = block_exclusive_u64(cnt, s, &tot);
-    for (int w = w0; w < w1; ++w) {
-      prefix[w] = (uint16_t)run;
-      run += __popc(bitmap[w]);
-    }
-    c.bitmap = bitmap;
-    c.prefix = prefix;
-    c.side_z = zs + e_lo;
-    __syncthreads();
-  }
+  if (a.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0)
+    setup_penalties<T>(c, s, a, P, dsm, a.off_bitmap, a.off_prefix, hist_len);
 
   // ---- pass A: stream the slice ----------------------------------------------
   // Candidates the kept set may need (K_main) and the top-n alone (n).
@@ -1152,7 +1168,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     topk_beyond = true;
   }
   {
-    float rm = -INFINITY, rsum = 0.f, bv = -INFINITY;
+    // rm: this thread's running maximum (pre-temperature); rmt = fl(rm / T),
+    // the tempered reference of rsum = sum of exp(z_t - rmt).
+    float rm = -INFINITY, rmt = -INFINITY, rsum = 0.f, bv = -INFINITY;
     int bi = INT_MAX;
     bool nanf = false;
     auto consume = [&](float* x, int g) {
@@ -1169,14 +1187,27 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
         bi = c.lo + g * E + first;
       }
       if (gm > rm) {
-        rsum = (rm == -INFINITY) ? 0.f : rsum * ex2_approx((rm - gm) * c.ax);
+        const float gmt = __fmul_rn(gm, c.inv_t);
+        rsum = (rm == -INFINITY) ? 0.f
+                                 : rsum * ex2_approx(__fmul_rn(__fsub_rn(rmt, gmt), kLog2e));
         rm = gm;
+        rmt = gmt;
       }
       if (rm > -INFINITY) {
-        // exponentials in place, then a pairwise sum of the group
-        const float nb = -rm * c.ax;
+        // exponentials in place, then a pairwise sum of the group.  Near zero
+        // one FFMA per element, 2^(x a - rm a) with a = log2(e) / T; once the
+        // reference is large, the rounding of rm a would show, and the
+        // tempered difference fl(fl(x / T) - rmt) is formed instead (exact
+        // where it matters, by Sterbenz).
+        if (fabsf(rmt) <= 16.0f) {
+          const float nb = -rm * c.ax;
 #pragma unroll
-        for (int i = 0; i < E; ++i) x[i] = ex2_approx(fmaf(x[i], c.ax, nb));
+          for (int i = 0; i < E; ++i) x[i] = ex2_approx(fmaf(x[i], c.ax, nb));
+        } else {
+#pragma unroll
+          for (int i = 0; i < E; ++i)
+            x[i] = ex2_approx(__fmul_rn(__fsub_rn(__fmul_rn(x[i], c.inv_t), rmt), kLog2e));
+        }
 #pragma unroll
         for (int w = 1; w < E; w <<= 1)
 #pragma unroll
@@ -1262,12 +1293,12 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     }
     const bool nonfin = nanf || (rsum != rsum) || rm == INFINITY;
     s.tmax[c.tid] = rm;
-    float m = rm, sm = rsum;
+    float m = rmt, sm = rsum;  // partials combine in tempered units
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
       const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-      lse_combine(m, sm, m2, s2, c.ax);
+      lse_combine(m, sm, m2, s2, kLog2e);
     }
     float dz = 0.f;
     block_argmax(bv, bi, dz, s);  // also a barrier: s.tmax is complete after it
@@ -1361,7 +1392,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     __syncthreads();
     if (c.tid == 0) {
       float mm = -INFINITY, ss = 0.f;
-      for (int w = 0; w < kWarps; ++w) lse_combine(mm, ss, s.rf[w], s.rf[kWarps + w], c.ax);
+      for (int w = 0; w < kWarps; ++w) lse_combine(mm, ss, s.rf[w], s.rf[kWarps + w], kLog2e);
       s.part.m = mm;
       s.part.s = ss;
       s.part.bv = bv;
@@ -1390,7 +1421,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
       const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-      lse_combine(m, sm, m2, s2, c.ax);
+      lse_combine(m, sm, m2, s2, kLog2e);
       const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
       const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
       if (pair_better(v2, i2, bv, bi)) {
@@ -1403,13 +1434,13 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
       tau_n = fminf(tau_n, __shfl_xor_sync(0xffffffffu, tau_n, o));
     }
     if (c.lane == 0) {
-      s.rs.M = m;
+      // m is the tempered row maximum fl(max / T) (rounding is monotone)
+      s.rs.m_t = m;
       s.rs.S = sm;
-      s.rs.m_t = __fmul_rn(m, c.inv_t);
       s.rs.lnS = logf(sm);
       s.rs.bv = bv;
       s.rs.bi = bi;
-      s.rs.nonfinite = nf || m == INFINITY || __fmul_rn(m, c.inv_t) == INFINITY;
+      s.rs.nonfinite = nf || m == INFINITY;
       s.rs.err = er;
       s.rs.tau = tau;
       s.rs.tau_n = tau_n;
@@ -1418,7 +1449,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   __syncthreads();
   c.m_t = s.rs.m_t;
   c.lnS = s.rs.lnS;
-  const int status0 = s.rs.nonfinite ? kRowNonfinite : (s.rs.M == -INFINITY ? kRowEmpty : kRowOk);
+  const int status0 = s.rs.nonfinite ? kRowNonfinite : (s.rs.m_t == -INFINITY ? kRowEmpty : kRowOk);
   const bool leader = c.rank == 0;
   int32_t* out_ids = n > 0 ? a.out_topk_ids + (int64_t)c.row * n : nullptr;
   float* out_lps = n > 0 ? a.out_topk_logprobs + (int64_t)c.row * n : nullptr;
@@ -1442,27 +1473,6 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
       }
     }
     return;
-  }
-
-  // Pass A sums 2^(x*log2e/T - max*log2e/T) with one FFMA per element; the
-  // rounding of max*log2e/T makes that inexact once |max| is large.  Such rows
-  // re-sum exp(z_t - m_t) from the tempered values themselves.
-  if (fabsf(c.m_t) > 32.0f) {
-    float acc = 0.f;
-    for_each_elem<T>(
-        c, [](float) { return true; },
-        [&](float zt, int) { acc += ex2_approx(__fmul_rn(__fsub_rn(zt, c.m_t), kLog2e)); });
-    acc = block_sum_f(acc, s);
-    if (c.tid == 0) s.part.s_exact = acc;
-    cluster.sync();
-    if (c.tid == 0) {
-      float t = 0.f;
-      for (int r = 0; r < c.C; ++r) t += cluster.map_shared_rank(&s.part, r)->s_exact;
-      s.rs.S = t;
-      s.rs.lnS = logf(t);
-    }
-    __syncthreads();
-    c.lnS = s.rs.lnS;
   }
 
   // ---- pass B: candidates at or above the cluster threshold ----------------
@@ -1636,20 +1646,46 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     VT_TRACE(15);
     return;
   }
-  VT_TRACE(10);
-
-  // ---- slow path: every CTA stays ------------------------------------------
-  if (n > 0) {
-    if (topn_ok) {
-      if (leader) {
-        block_sort_desc(c.buf, nc);
-        for (int t = c.tid; t < n; t += kThreads) {
-          const uint64_t k = c.buf[t];
-          out_ids[t] = (int)key_idx(k);
-          out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
-        }
+  // ---- rows the candidates cannot finish go to the selection kernel ---------
+  if (leader) {
+    if (n > 0 && topn_ok) {
+      block_sort_desc(c.buf, nc);
+      for (int t = c.tid; t < n; t += kThreads) {
+        const uint64_t k = c.buf[t];
+        out_ids[t] = (int)key_idx(k);
+        out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
       }
-    } else {
+    }
+    if (c.tid == 0) {
+      SlowRow r;
+      r.m_t = c.m_t;
+      r.lnS = c.lnS;
+      r.bi = s.rs.bi;
+      r.topn_done = (n == 0 || topn_ok) ? 1 : 0;
+      a.slow[c.row] = r;
+      a.slow_list[atomicAdd(a.slow_ctl, 1u)] = c.row;
+      if (s.rs.err) atomicOr(a.err_word, s.rs.err);
+    }
+  }
+  VT_TRACE(15);
+}
+
+// ---------------------------------------------------------------------------
+// the selection path of one row (every CTA of the cluster calls it)
+// ---------------------------------------------------------------------------
+// Top-n by selection when the candidates did not hold it, then the kept set by
+// radix selection (top-k by count, top-p by mass) and the draw; the leader
+// writes the row's outputs.  c.m_t, c.lnS, s.rs.bi are set by the caller.
+template <typename T>
+__device__ __noinline__ void slow_row(Ctx& c, Smem& s, const SampleArgs& a, cg::cluster_group& cluster,
+                         bool topn_done) {
+  constexpr int E = Elt<T>::E;
+  const int n = a.n_logprobs;
+  const bool leader = c.rank == 0;
+  int32_t* out_ids = n > 0 ? a.out_topk_ids + (int64_t)c.row * n : nullptr;
+  float* out_lps = n > 0 ? a.out_topk_logprobs + (int64_t)c.row * n : nullptr;
+  if (n > 0 && !topn_done) {
+    {
       // rank n-1 of every element (the -inf ones included, by index)
       SelOut so = cluster_select<T>(c, s, cluster, kPredAll, 0ull, false,
                                     (unsigned long long)(n - 1), 0.f, false);
@@ -1745,10 +1781,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
           if (c.lo + g * E + i == wi) xv = x[i];
         cluster.map_shared_rank(&s.bcast_f[0], 0)[0] = __fmul_rn(xv, c.inv_t);
       }
-      VT_TRACE(11);
+      VT_CTRACE(c, 11);
       cluster.sync();  // final: no DSMEM access after this
       if (!leader) {
-        VT_TRACE(15);
+        VT_CTRACE(c, 15);
         return;
       }
       tok = wi;
@@ -1840,10 +1876,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
         s.bcast_u[1] = km;
       }
     }
-    VT_TRACE(11);
+    VT_CTRACE(c, 11);
     cluster.sync();  // final: no DSMEM access after this
     if (!leader) {
-      VT_TRACE(15);
+      VT_CTRACE(c, 15);
       return;
     }
     __syncthreads();
@@ -1875,7 +1911,116 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     append_token(a.hist + (int64_t)c.row * a.hist_cap, a.hist_len + c.row, a.hist_cap, tok, s,
                  a.row_status + c.row);
   }
-  VT_TRACE(15);
+  VT_CTRACE(c, 15);
+}
+
+// ---------------------------------------------------------------------------
+// kernel 2: the rows kernel 1 handed over, one cluster per row at a time
+// ---------------------------------------------------------------------------
+// Copy this CTA's slice into shared memory, padded with -inf to whole groups,
+// and rebuild its group maxima for the selection kernel's slice size.
+template <typename T>
+__device__ __noinline__ void stage_slice(Ctx& c, uint8_t* stage_mem) {
+  constexpr int E = Elt<T>::E;
+  T* st = reinterpret_cast<T*>(stage_mem);
+  const T neg_inf = sizeof(T) == 4 ? (T)0 : (T)0xFF80u;  // bf16 -inf; f32 below
+  const int nvalid = c.hi > c.lo ? c.hi - c.lo : 0;
+  const T* src = reinterpret_cast<const T*>(c.rowp) + c.lo;
+  constexpr int per_vec = 16 / (int)sizeof(T);
+  const int nfull = c.aligned ? nvalid / per_vec : 0;  // whole 16-byte vectors of the row
+  const uint4* src4 = reinterpret_cast<const uint4*>(src);
+  uint4* st4 = reinterpret_cast<uint4*>(st);
+  for (int v0 = c.tid; v0 < nfull; v0 += 4 * kThreads) {
+    uint4 r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * kThreads;
+      if (v < nfull) r[u] = __ldg(src4 + v);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v0 + u * kThreads;
+      if (v < nfull) st4[v] = r[u];
+    }
+  }
+  for (int i = nfull * per_vec + c.tid; i < c.slice; i += kThreads) {
+    if constexpr (sizeof(T) == 4) {
+      st[i] = i < nvalid ? __ldg(src + i) : -INFINITY;
+    } else {
+      st[i] = i < nvalid ? __ldg(src + i) : neg_inf;
+    }
+  }
+  __syncthreads();
+  c.stage = reinterpret_cast<const uint4*>(stage_mem);
+  for (int g = c.tid; g < c.ngroups; g += kThreads) {
+    float x[E];
+    load_group<T>(c, g, x);
+    float gm = x[0];
+#pragma unroll
+    for (int i = 1; i < E; ++i) gm = fmaxf(gm, x[i]);
+    c.gmax[g] = bf16_down(gm);
+  }
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
+                                                             const SelectPlan p) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ Smem s;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+  const int cid = (int)blockIdx.x / C, G = (int)gridDim.x / C;
+  const int count = (int)a.slow_ctl[0];
+  for (int i = cid; i < count; i += G) {
+    const int row = a.slow_list[i];
+    const SlowRow rec = a.slow[row];
+    cluster.sync();  // every CTA of the cluster is done with the previous row
+    Ctx c;
+    const RowParams P = init_row<T>(c, a, dsm, row, C, rank, p.slice, p.off_gmax, p.off_mrg);
+    if (a.trace && rank == 0 && (int64_t)row * p.kernel1_cluster < a.trace_ctas)
+      c.trace = a.trace + (size_t)row * p.kernel1_cluster * kTraceSlots;
+    VT_CTRACE(c, 10);
+    if (c.tid == 0) {
+      s.part.err = 0;
+      s.nloc = 0;
+      s.gcount = 0;
+      s.rs.bi = rec.bi;
+      s.rs.err = 0;
+    }
+    c.m_t = rec.m_t;
+    c.lnS = rec.lnS;
+    const int hist_len = a.hist_len[row];
+    if (p.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0)
+      setup_penalties<T>(c, s, a, P, dsm, p.off_bitmap, p.off_prefix, hist_len);
+    VT_CTRACE(c, 5);
+    if (p.staged) {
+      stage_slice<T>(c, dsm + p.off_stage);
+    } else {
+      for (int g = c.tid; g < c.ngroups; g += kThreads) {
+        float x[Elt<T>::E];
+        load_group<T>(c, g, x);
+        float gm = x[0];
+#pragma unroll
+        for (int q = 1; q < Elt<T>::E; ++q) gm = fmaxf(gm, x[q]);
+        c.gmax[g] = bf16_down(gm);
+      }
+      __syncthreads();
+    }
+    VT_CTRACE(c, 1);
+    slow_row<T>(c, s, a, cluster, rec.topn_done != 0);
+  }
+  // The last CTA to finish clears the hand-over counters for the next call.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int done = atomicAdd(&a.slow_ctl[1], 1u);
+    if (done == gridDim.x - 1) {
+      a.slow_ctl[0] = 0u;
+      a.slow_ctl[1] = 0u;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace
@@ -1910,6 +2055,28 @@ LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties) {
   }
   p.smem = off;
   p.active_clusters = 0;
+  p.sel = SelectPlan{};
+  return p;
+}
+
+// The selection kernel's layout: kernel 1's regions for its own slice size,
+// then (when staged) the slice itself.
+static SelectPlan plan_select_layout(int V, int elem_size, int cluster, bool penalties,
+                                     bool staged) {
+  const LaunchPlan q = plan_layout(V, elem_size, cluster, penalties);
+  SelectPlan p{};
+  p.cluster = cluster;
+  p.slice = q.slice;
+  p.pen_smem = q.pen_smem;
+  p.off_gmax = q.off_gmax;
+  p.off_mrg = q.off_mrg;
+  p.off_bitmap = q.off_bitmap;
+  p.off_prefix = q.off_prefix;
+  size_t off = (q.smem + 127) & ~(size_t)127;
+  p.off_stage = (uint32_t)off;
+  p.staged = staged ? 1 : 0;
+  if (staged) off += (size_t)q.slice * elem_size;
+  p.smem = off;
   return p;
 }
 
@@ -1945,8 +2112,72 @@ static cudaError_t prepare_one(LaunchPlan& plan) {
   return nclusters > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
+template <typename T>
+static cudaLaunchConfig_t select_config(const SelectPlan& plan, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.cluster, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Kernel attributes of the selection kernel; plan.clusters = how many of its
+// clusters are resident at once.
+template <typename T>
+static cudaError_t prepare_select_one(SelectPlan& plan) {
+  static size_t smem_set = 0;
+  cudaError_t e = cudaSuccess;
+  if (plan.smem > smem_set) {
+    e = cudaFuncSetAttribute(select_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)plan.smem);
+    if (e != cudaSuccess) return e;
+    smem_set = plan.smem;
+  }
+  e = cudaFuncSetAttribute(select_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = select_config<T>(plan, attr);
+  int nclusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&nclusters, select_kernel<T>, &cfg);
+  if (e != cudaSuccess) return e;
+  plan.clusters = nclusters;
+  return nclusters > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 cudaError_t prepare_sample(LaunchPlan& plan, int dtype) {
-  return dtype == 0 ? prepare_one<float>(plan) : prepare_one<uint16_t>(plan);
+  cudaError_t e = dtype == 0 ? prepare_one<float>(plan) : prepare_one<uint16_t>(plan);
+  if (e != cudaSuccess || plan.sel.cluster == 0) return e;
+  const int want = plan.sel.clusters;
+  e = dtype == 0 ? prepare_select_one<float>(plan.sel) : prepare_select_one<uint16_t>(plan.sel);
+  if (want > 0 && want < plan.sel.clusters) plan.sel.clusters = want;
+  return e;
+}
+
+// The selection kernel: CTAs per row such that a slice holds at least 16K
+// elements (fewer, fuller CTAs keep the cluster barriers cheap), more while
+// a slice is over 96 KB; staged in shared memory when it fits in 96 KB; as
+// many persistent clusters as are resident at once, at most one per row.
+static SelectPlan plan_select(int B, int V, int elem_size, bool penalties, int dtype,
+                              int kernel1_cluster) {
+  int C = kMaxCluster;
+  while (C > 1 && (V + C - 1) / C < 16384) C >>= 1;
+  while (C < kMaxCluster && (size_t)((V + C - 1) / C) * elem_size > 96 * 1024) C <<= 1;
+  const bool staged = (size_t)((V + C - 1) / C + 31) * elem_size <= 96 * 1024;
+  SelectPlan p = plan_select_layout(V, elem_size, C, penalties, staged);
+  p.kernel1_cluster = kernel1_cluster;
+  const cudaError_t e = dtype == 0 ? prepare_select_one<float>(p) : prepare_select_one<uint16_t>(p);
+  if (e != cudaSuccess) {
+    p.clusters = 0;
+    return p;
+  }
+  if (p.clusters > B) p.clusters = B;
+  return p;
 }
 
 LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, int num_sms) {
@@ -1959,7 +2190,10 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
   while (cmin < kMaxCluster && (size_t)((V + cmin - 1) / cmin) * elem_size > max_slice) cmin <<= 1;
   LaunchPlan best = plan_layout(V, elem_size, cmin, penalties);
   if (prepare_sample(best, dtype) != cudaSuccess) return best;
-  if ((int64_t)B > best.active_clusters) return best;  // several waves even so
+  if ((int64_t)B > best.active_clusters) {  // several waves even so
+    best.sel = plan_select(B, V, elem_size, penalties, dtype, best.cluster);
+    return best;
+  }
   for (int C = cmin * 2; C <= kMaxCluster; C <<= 1) {
     if ((size_t)((V + C - 1) / C) * elem_size < min_slice) break;
     LaunchPlan p = plan_layout(V, elem_size, C, penalties);
@@ -1967,6 +2201,7 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
     if ((int64_t)B > p.active_clusters) break;  // would no longer fit in one wave
     best = p;
   }
+  best.sel = plan_select(B, V, elem_size, penalties, dtype, best.cluster);
   return best;
 }
 
@@ -1985,7 +2220,14 @@ static cudaError_t launch_one(const SampleArgs& args, const LaunchPlan& plan,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel<T>, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel<T>, args);
+  if (e != cudaSuccess) return e;
+  if (plan.sel.clusters < 1) return cudaErrorInvalidConfiguration;
+  cudaLaunchAttribute attr2[1];
+  cudaLaunchConfig_t cfg2 = select_config<T>(plan.sel, attr2);
+  cfg2.gridDim = dim3((unsigned)(plan.sel.clusters * plan.sel.cluster), 1, 1);
+  cfg2.stream = stream;
+  return cudaLaunchKernelEx(&cfg2, select_kernel<T>, args, plan.sel);
 }
 
 cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,

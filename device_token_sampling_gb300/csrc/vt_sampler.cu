@@ -39,6 +39,9 @@ struct vt_sampler {
   int32_t* d_kth_i = nullptr;
   int32_t* d_kept = nullptr;
   int32_t* d_err = nullptr;
+  vt::SlowRow* d_slow = nullptr;  // rows handed from the streaming to the selection kernel
+  int32_t* d_slow_list = nullptr;
+  uint32_t* d_slow_ctl = nullptr;
   // pinned host staging
   vt::RowParams* h_params = nullptr;
   uint64_t* h_seeds = nullptr;
@@ -120,6 +123,9 @@ void free_all(vt_sampler* h) {
   dfree(h->d_kth_i);
   dfree(h->d_kept);
   dfree(h->d_err);
+  dfree(h->d_slow);
+  dfree(h->d_slow_list);
+  dfree(h->d_slow_ctl);
   dfree(h->d_io_logits);
   dfree(h->d_io_tokens);
   dfree(h->d_io_lp);
@@ -201,6 +207,9 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_kth_i, B * sizeof(int32_t));
   dal((void**)&h->d_kept, B * sizeof(int32_t));
   dal((void**)&h->d_err, sizeof(int32_t));
+  dal((void**)&h->d_slow, B * sizeof(vt::SlowRow));
+  dal((void**)&h->d_slow_list, B * sizeof(int32_t));
+  dal((void**)&h->d_slow_ctl, 2 * sizeof(uint32_t));
   hal((void**)&h->h_params, B * sizeof(vt::RowParams));
   hal((void**)&h->h_seeds, B * sizeof(uint64_t));
   hal((void**)&h->h_raw, B * H * sizeof(int32_t));
@@ -220,6 +229,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
     return bail(VT_ERR_CUDA);
   if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(int32_t)) != cudaSuccess ||
+      cudaMemset(h->d_slow_ctl, 0, 2 * sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_seeds, 0, B * sizeof(uint64_t)) != cudaSuccess ||
       cudaMemset(h->d_status, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
@@ -435,7 +445,11 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
   a.dbg_kth_index = h->d_kth_i;
   a.dbg_kept = h->d_kept;
   a.err_word = h->d_err;
+  a.slow = h->d_slow;
+  a.slow_list = h->d_slow_list;
+  a.slow_ctl = h->d_slow_ctl;
   a.trace = (h->trace && (int64_t)B * plan.cluster <= h->trace_ctas) ? h->trace : nullptr;
+  a.trace_ctas = a.trace ? h->trace_ctas : 0;
   VT_CK(h, vt::launch_sample(a, plan, dtype, st));
   h->last_B = B;
   h->last_stream = st;

@@ -242,7 +242,7 @@ int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
  * CUDA call) or V needs more shared memory than a CTA has; VT_ERR_INVALID_ARG;
  * VT_ERR_CUDA (wrong architecture, failed set-up or launch). */
 #define VT_NOALLOC_MAX_BATCH 1024          /* rows per vt_sample_noalloc call  */
-#define VT_NOALLOC_SCRATCH_BYTES (80 * 1024) /* the fixed device scratch array */
+#define VT_NOALLOC_SCRATCH_BYTES (112 * 1024) /* the fixed device scratch array */
 int vt_sample_noalloc(int32_t device, const void* logits, int32_t dtype, int32_t B, int32_t V,
                       int64_t ld, const float* temperature, const int32_t* top_k,
                       const float* top_p, const float* min_p, const uint64_t* seed,
