@@ -48,7 +48,8 @@ struct SampleArgs {
   int32_t* err_word;         // one int, kErr* bits
   SlowRow* slow;             // [B] hand-over records
   int32_t* slow_list;        // [B] rows handed over, in arrival order
-  uint32_t* slow_ctl;        // [2] rows handed over, selection CTAs done; zero between calls
+  uint32_t* slow_ctl;        // [3] rows handed over, selection CTAs done (both zero between
+                             // calls), rows handed over by the last call
   unsigned long long* trace; // optional [grid][kTraceSlots] phase timestamps (ns)
   int64_t trace_ctas;        // CTAs the trace buffer holds
 };
@@ -92,7 +93,7 @@ cudaError_t prepare_sample(LaunchPlan& plan, int dtype);
 // Launch the sampling kernels: the streaming kernel (grid B * cluster CTAs),
 // then the selection kernel for the rows it handed over.
 cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,
-                          cudaStream_t stream);
+                          cudaStream_t stream, cudaEvent_t between = nullptr);
 
 // Build the per-row sorted (id, count) tables from raw ids.
 //   raw, offs  CSR: row r owns raw[offs[r] .. offs[r+1]) (prompt then output)

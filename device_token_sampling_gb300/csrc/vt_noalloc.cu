@@ -42,6 +42,7 @@ constexpr size_t kOffSlow = kOffKept + kMaxRows * sizeof(int32_t);        // Slo
 constexpr size_t kOffSlowList = kOffSlow + kMaxRows * sizeof(vt::SlowRow);  // int32[rows]
 constexpr size_t kOffSlowCtl = kOffSlowList + kMaxRows * sizeof(int32_t);   // uint32[2], zero
 constexpr size_t kOffErr = kOffSlowCtl + 16;                               // int32, zero
+static_assert(kOffErr - kOffSlowCtl >= 3 * sizeof(uint32_t), "three hand-over words");
 constexpr size_t kUsedBytes = kOffErr + 256;
 static_assert(kUsedBytes <= VT_NOALLOC_SCRATCH_BYTES, "scratch layout exceeds its array");
 static_assert(kOffSeeds % 16 == 0 && kOffSlow % 16 == 0 && kOffErr % 16 == 0,

@@ -2016,6 +2016,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
     __threadfence();
     const unsigned int done = atomicAdd(&a.slow_ctl[1], 1u);
     if (done == gridDim.x - 1) {
+      a.slow_ctl[2] = a.slow_ctl[0];  // kept for vt_debug_last_handover
       a.slow_ctl[0] = 0u;
       a.slow_ctl[1] = 0u;
       __threadfence();
@@ -2207,7 +2208,7 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
 
 template <typename T>
 static cudaError_t launch_one(const SampleArgs& args, const LaunchPlan& plan,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, cudaEvent_t between) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)args.B * plan.cluster, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -2222,6 +2223,10 @@ static cudaError_t launch_one(const SampleArgs& args, const LaunchPlan& plan,
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, sample_kernel<T>, args);
   if (e != cudaSuccess) return e;
+  if (between) {
+    e = cudaEventRecord(between, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (plan.sel.clusters < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t cfg2 = select_config<T>(plan.sel, attr2);
@@ -2231,9 +2236,9 @@ static cudaError_t launch_one(const SampleArgs& args, const LaunchPlan& plan,
 }
 
 cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,
-                          cudaStream_t stream) {
-  return dtype == 0 ? launch_one<float>(args, plan, stream)
-                    : launch_one<uint16_t>(args, plan, stream);
+                          cudaStream_t stream, cudaEvent_t between) {
+  return dtype == 0 ? launch_one<float>(args, plan, stream, between)
+                    : launch_one<uint16_t>(args, plan, stream, between);
 }
 
 }  // namespace vt

@@ -65,6 +65,7 @@ struct vt_sampler {
   cudaStream_t last_stream = nullptr;
   std::map<std::pair<std::pair<int, int>, std::pair<int, int>>, vt::LaunchPlan> plans;
   int num_sms = 0;
+  cudaEvent_t phase_event = nullptr;    // debug: recorded between the two launches
   unsigned long long* trace = nullptr;  // debug phase trace (caller-owned)
   int64_t trace_ctas = 0;
 };
@@ -209,7 +210,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_err, sizeof(int32_t));
   dal((void**)&h->d_slow, B * sizeof(vt::SlowRow));
   dal((void**)&h->d_slow_list, B * sizeof(int32_t));
-  dal((void**)&h->d_slow_ctl, 2 * sizeof(uint32_t));
+  dal((void**)&h->d_slow_ctl, 4 * sizeof(uint32_t));
   hal((void**)&h->h_params, B * sizeof(vt::RowParams));
   hal((void**)&h->h_seeds, B * sizeof(uint64_t));
   hal((void**)&h->h_raw, B * H * sizeof(int32_t));
@@ -229,7 +230,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
     return bail(VT_ERR_CUDA);
   if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(int32_t)) != cudaSuccess ||
-      cudaMemset(h->d_slow_ctl, 0, 2 * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_slow_ctl, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_seeds, 0, B * sizeof(uint64_t)) != cudaSuccess ||
       cudaMemset(h->d_status, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
@@ -450,7 +451,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
   a.slow_ctl = h->d_slow_ctl;
   a.trace = (h->trace && (int64_t)B * plan.cluster <= h->trace_ctas) ? h->trace : nullptr;
   a.trace_ctas = a.trace ? h->trace_ctas : 0;
-  VT_CK(h, vt::launch_sample(a, plan, dtype, st));
+  VT_CK(h, vt::launch_sample(a, plan, dtype, st, h->phase_event));
   h->last_B = B;
   h->last_stream = st;
   h->err.clear();
@@ -566,6 +567,22 @@ int vt_debug_set_trace(vt_sampler* h, uint64_t* dev_trace, int64_t capacity_ctas
   h->trace = reinterpret_cast<unsigned long long*>(dev_trace);
   h->trace_ctas = dev_trace ? capacity_ctas : 0;
   if (slots_per_cta) *slots_per_cta = vt::kTraceSlots;
+  return VT_OK;
+}
+
+int vt_debug_last_handover(vt_sampler* h, int32_t* rows) {
+  if (!h || !rows) return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  VT_CK(h, cudaStreamSynchronize(h->last_stream));
+  uint32_t v = 0;
+  VT_CK(h, cudaMemcpy(&v, h->d_slow_ctl + 2, sizeof v, cudaMemcpyDeviceToHost));
+  *rows = (int32_t)v;
+  return VT_OK;
+}
+
+int vt_debug_set_phase_event(vt_sampler* h, void* event) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  h->phase_event = static_cast<cudaEvent_t>(event);
   return VT_OK;
 }
 

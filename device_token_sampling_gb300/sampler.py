@@ -68,6 +68,8 @@ SIGNATURES = {
     "vt_debug_get_seeds": (C.c_int, [P, P]),
     "vt_debug_set_trace": (C.c_int, [P, P, I64, P]),
     "vt_debug_launch_shape": (C.c_int, [P, I32, I32, P, P, P]),
+    "vt_debug_set_phase_event": (C.c_int, [P, P]),
+    "vt_debug_last_handover": (C.c_int, [P, P]),
     "vt_sample_noalloc": (C.c_int, [I32, P, I32, I32, I32, I64, P, P, P, P, P, I32, P, P, P, P,
                                     P, I32, P, C.c_char_p, I32]),
     "vt_last_error": (C.c_char_p, [P]),
@@ -305,6 +307,18 @@ class Sampler:
             self._check(self._lib.vt_debug_set_trace(self._h, P(buf.data_ptr()), buf.shape[0],
                                                      C.byref(slots)), "vt_debug_set_trace")
         return slots.value
+
+    def set_phase_event(self, event=None):
+        """Record a ``torch.cuda.Event`` between the two launches of every later
+        ``sample`` (None turns it off); the caller keeps the event alive."""
+        ptr = None if event is None else P(event.cuda_event)
+        self._check(self._lib.vt_debug_set_phase_event(self._h, ptr), "vt_debug_set_phase_event")
+
+    def last_handover(self) -> int:
+        """Rows the last ``sample`` handed to the selection kernel."""
+        v = C.c_int32()
+        self._check(self._lib.vt_debug_last_handover(self._h, C.byref(v)), "vt_debug_last_handover")
+        return int(v.value)
 
     def seeds(self, B: int):
         s = np.zeros(self.cfg.max_batch, np.uint64)  # the call writes up to max_batch seeds

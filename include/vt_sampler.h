@@ -202,6 +202,17 @@ int vt_debug_launch_shape(vt_sampler* handle, int32_t dtype, int32_t V, int32_t*
 int vt_debug_set_trace(vt_sampler* handle, uint64_t* dev_trace, int64_t capacity_ctas,
                        int32_t* slots_per_cta);
 
+/* Debug: record `event` (a cudaEvent_t passed as void*) on the stream of each
+ * later vt_sample between its two launches (the streaming kernel, then the
+ * selection kernel for the rows handed over), so that a caller can time the
+ * two apart.  NULL turns it off.  The event stays owned by the caller. */
+int vt_debug_set_phase_event(vt_sampler* handle, void* event);
+
+/* Debug: how many rows the last vt_sample handed from the streaming kernel to
+ * the selection kernel (rows whose kept set or top-n the candidates gathered
+ * in one pass could not settle).  Synchronises the handle's last stream. */
+int vt_debug_last_handover(vt_sampler* handle, int32_t* rows);
+
 /* Read the current per-row seeds of rows 0..B-1 into a host array (B of the
  * last vt_reset_params).  Synchronises the handle's last stream. */
 int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
