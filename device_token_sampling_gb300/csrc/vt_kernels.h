@@ -13,8 +13,8 @@ struct RowParams;
 struct __align__(16) SlowRow {
   float m_t;      // tempered row maximum
   float lnS;      // ln(sum exp(z_t - m_t))
-  int32_t bi;     // lowest index of the maximum
-  int32_t topn_done;  // the top-n outputs are already written
+  float xmax;     // row maximum before temperature
+  uint32_t bi_topn;  // lowest index of the maximum; bit 31: top-n outputs already written
 };
 
 // Everything one sampling launch needs.  Device pointers unless noted.
@@ -61,6 +61,7 @@ struct SelectPlan {
   int pen_smem;
   int staged;           // the slice is copied into shared memory
   uint32_t off_gmax, off_mrg, off_bitmap, off_prefix, off_stage;
+  uint32_t off_code;     // bf16 code-slot histograms (0: none)
   size_t smem;
   int clusters;         // persistent clusters launched
   int kernel1_cluster;  // CTAs per row of the streaming kernel (trace layout)
@@ -79,8 +80,9 @@ struct LaunchPlan {
 };
 
 // Shared-memory layout for V elements of elem_size bytes split over `cluster`
-// CTAs (1, 2, 4, 8 or 16).
-LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties);
+// CTAs (1, 2, 4, 8 or 16), for the streaming kernel (select = false) or the
+// selection kernel (select = true, without its staged slice).
+LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties, bool select);
 
 // Choose the cluster size for a call: as many CTAs per row as still lets all
 // B rows be resident in one wave, within the slice-size limits.

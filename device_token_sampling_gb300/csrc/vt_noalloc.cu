@@ -145,6 +145,8 @@ extern "C" int vt_sample_noalloc(int32_t device, const void* logits, int32_t dty
     return fail(errbuf, errbuf_len, VT_ERR_INVALID_ARG, "device %d out of range", device);
   if (dtype != VT_DTYPE_F32 && dtype != VT_DTYPE_BF16)
     return fail(errbuf, errbuf_len, VT_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (V > (1 << 20))
+    return fail(errbuf, errbuf_len, VT_ERR_CAPACITY, "V=%d exceeds 1048576", V);
   if (V < 1 || ld < V)
     return fail(errbuf, errbuf_len, VT_ERR_INVALID_ARG, "need 1 <= V <= ld (V=%d, ld=%lld)", V,
                 (long long)ld);

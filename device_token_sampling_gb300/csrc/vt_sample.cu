@@ -52,8 +52,8 @@ constexpr int kRingBytes = kStageBytes * kStages;    // aliases the candidate bu
 constexpr int kSmallK = 32;  // up to this many per CTA, thresholds come from thread maxima
 // the ring region also holds the candidate buffer (kBufCap keys) followed by
 // the level-0 per-bin bests; the histograms alias the buffer
-static_assert(kBufCap * 8 + (1 << 10) * 8 <= kRingBytes, "ring region too small");
-static_assert((1 << 10) * 12 <= kBufCap * 8, "histograms exceed the candidate buffer");
+static_assert(kBufCap * 8 <= kRingBytes, "the candidate buffer lives in the ring region");
+static_assert((1 << 10) * 16 <= kBufCap * 8, "selection histograms exceed the gather buffer");
 
 // Row status codes (match VT_ROW_* in the public header).
 constexpr int kRowOk = 0, kRowNonfinite = 1, kRowEmpty = 2, kRowHistoryFull = 3;
@@ -137,11 +137,42 @@ struct Part {
   int ncand, ncand_minp;
   unsigned long long cand_mass;
   unsigned long long rng_cnt, rng_mass;
+  unsigned long long rng_all, rng_tmass;  // code walk: range totals
+  int rng_last;
+  float best_score;      // code walk: best wholly kept slot of the range
+  int best_slot, best_tie;
+  unsigned int best_bits;
   float dscore, dz;
   int didx;
   int kept;
   unsigned long long kmin;
+  unsigned long long tiny_mass, catch_mass;  // code bins: masses summed per element
+  // selection on bf16 codes: the two several-valued slots (tiny, catch-all)
+  unsigned long long sp_all[2], sp_cnt[2], sp_mass[2];
+  unsigned long long sp_key[2];  // best (Gumbel score, index) key of each
+  unsigned long long cb_key;     // best ((bits + 1), ~index) in the boundary slot's kept prefix
+  int cb_last;           // the last kept index of the boundary slot
+  int cw_j;              // lowest index of the winning slot's best element
+  int last_j;            // last index of the last survivor slot (no boundary)
   int err;
+};
+
+// Outcome of the leader's walk over the bf16 code slots.
+struct CodeWalk {
+  int fallback;       // the row needs the generic selection
+  int slot, kp;       // boundary slot and its kept elements (slot -1: all survivors kept)
+  unsigned long long above;  // survivors before the boundary slot
+  unsigned long long total;  // survivors
+  int last_slot;      // last occupied survivor slot
+  int nwin;           // 1 when a wholly kept regular slot holds the best score
+  int wslot;          // that slot
+  unsigned int wb;    // its best noise bits + 1
+  float wscore;
+  int sp_kept[2];     // the tiny / catch-all slot is wholly kept
+  unsigned long long sp_all[2], sp_cnt[2], sp_mass[2], sp_key[2];  // their totals
+  int slot_n, kn;     // top-n boundary slot and its elements in the top-n (-1: none)
+  int k_slot, k_kept; // top-k boundary slot and its kept elements
+  unsigned long long k_mass;  // mass of the top-k set
 };
 
 struct RowStats {
@@ -174,6 +205,7 @@ struct __align__(16) Smem {
   RowStats rs;
   SelOut sel;
   Walk walk;
+  CodeWalk cw;
   int nloc;    // candidates in this CTA's buffer
   int gcount;  // band keys gathered in the leader (selection)
   int bcast_i[4];
@@ -191,6 +223,7 @@ struct Ctx {
   bool aligned, pen;
   float inv_t, ax;  // 1/T and log2(e)/T
   float m_t, lnS;   // row max of z_t, ln(sum exp(z_t - m_t))
+  float xmax;       // the row maximum before temperature (selection kernel)
   bool greedy, topk, topp, minp;
   int top_k;
   float top_p;
@@ -198,12 +231,9 @@ struct Ctx {
   const void* rowp;
   uint16_t* gmax;   // conservative bf16 max of each group (pre-temperature)
   uint64_t* buf;    // candidate keys / gathered keys / histograms
-  unsigned int* hcnt;
-  unsigned long long* hmass;
+  unsigned int* hcnt;  // selection histogram: counts, then three partial mass sums
   unsigned int* mcnt;  // merged bins of this CTA's digit range
   unsigned long long* mmass;
-  unsigned long long* hbest;  // level-0 best Gumbel key per bin (score, index)
-  unsigned long long* mbest;
   const uint32_t* bitmap;  // penalised positions of the slice
   const uint16_t* prefix;  // side-list index of each bitmap word's first bit
   const float* side_z;     // penalised values, in id order, of this slice
@@ -574,129 +604,225 @@ enum Pred { kPredAll = 0, kPredSurv = 1 };
 // Level 0 bins by distance below the row max (1/64 per bin, the last bin
 // catches everything from 16 down), which spreads any row's mass over many
 // bins; deeper levels split the surviving bin's 64-bit key range 1024 ways.
-// A band of at most kBufCap keys is then gathered, sorted and walked.
+// A band of at most kBufCap keys is then gathered, sorted and walked.  Bin
+// masses are exact sums of the elements' 2^-40 fixed-point masses, kept as
+// three 32-bit partial sums per bin so that every update is a 32-bit shared
+// atomic (slices of at most 65536 elements cannot overflow them).
 //
-// With with_draw, level 0 also keeps the best Gumbel key (score, index) of
-// every bin.  The kept set is then every bin above the boundary bin plus the
-// band's prefix up to the boundary, so the draw's winner is the best of the
-// bins above and of the kept band elements: no separate draw pass (draw_ok).
+// With with_draw, the pass that gathers the band also draws over the
+// elements above it (all kept): each thread keeps its best Gumbel score, and
+// the leader combines those with the kept prefix of the sorted band.  The
+// winner's key comes back in `win` (draw_ok).
 constexpr float kDScale = 64.0f;
 constexpr unsigned long long kNegInfKey = 0x007FFFFF00000000ull;  // elem_key(-inf, ~0)
 
+// bf16 code bins.  Every element whose bf16 pattern is the same has the same
+// tempered value and mass, so a bin per bf16 value below the row maximum
+// gives exact masses as count x mass.  code16 is a signed code, monotone in the
+// value, that merges the magnitudes below 2^-12 (and both zeros) into code 0;
+// slot = code(max) - code(x), slots from kCodeSlots - 1 on are one catch-all.
+// The code-0 slot and the catch-all hold several values: their masses are
+// summed per element.
+constexpr int kCodeSlots = 4096;
+constexpr int kCodeEmin = 115;  // bf16 exponent field of 2^-12
+__device__ __forceinline__ int code16(uint32_t u) {
+  const int m = (int)(u & 0x7FFFu) - (kCodeEmin << 7) + 1;
+  const int v = m > 0 ? m : 0;
+  return (u & 0x8000u) ? -v : v;
+}
+__device__ __forceinline__ float code_value(int code) {  // code != 0
+  const uint32_t mag = (uint32_t)((code < 0 ? -code : code) - 1 + (kCodeEmin << 7));
+  return __uint_as_float(((code < 0 ? 0x8000u : 0u) | mag) << 16);
+}
+// tempered value of regular slot sl below the maximum code cmax
+__device__ __forceinline__ float zq_value(int cmax, int sl, float inv_t) {
+  return __fmul_rn(code_value(cmax - sl), inv_t);
+}
+
+// Histogram words: count, then the three partial mass sums, kBins each.
+__device__ __forceinline__ void hist_add(unsigned int* h, int d, unsigned long long q,
+                                         bool by_mass) {
+  atomicAdd(&h[d], 1u);
+  if (by_mass) {
+    atomicAdd(&h[kBins + d], (unsigned int)(q & 0xFFFFull));
+    atomicAdd(&h[2 * kBins + d], (unsigned int)((q >> 16) & 0xFFFFull));
+    atomicAdd(&h[3 * kBins + d], (unsigned int)(q >> 32));
+  }
+}
+__device__ __forceinline__ unsigned long long hist_mass(const unsigned int* h, int d) {
+  return (unsigned long long)h[kBins + d] + ((unsigned long long)h[2 * kBins + d] << 16) +
+         ((unsigned long long)h[3 * kBins + d] << 32);
+}
+
 template <typename T>
-__device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group& cluster, int pred,
-                                 unsigned long long kbound, bool by_mass,
-                                 unsigned long long count_target, float p, bool with_draw) {
+__device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group& cluster,
+                                              int pred, unsigned long long kbound, bool by_mass,
+                                              unsigned long long count_target, float p,
+                                              bool with_draw, bool codes) {
   constexpr int E = Elt<T>::E;
+  // values the scans use, in registers
+  const float m_t = c.m_t, inv_t = c.inv_t;
+  const int hi = c.hi;
+  const bool minp = c.minp;
+  const double lmp = c.lmp;
+  const uint64_t rkey = c.rkey;
+  unsigned int* const h = c.hcnt;
   unsigned long long Klo = kbound, Khi = ~0ull;
   unsigned long long acc_c = 0, acc_m = 0;
   unsigned long long target = count_target;
   unsigned long long total_c = 0, total_m = 0;
   int dsel = -1;  // the level-0 bin every later level stays inside
-  bool band_at_level0 = false;
   SelOut out;
   out.all = 0;
   out.draw_ok = 0;
   out.win = kNegInfKey;
-  const int nb = kBins / c.C, b0 = c.rank * nb;
+  const int nslots0 = codes ? kCodeSlots : kBins;  // level-0 bins
+  const int cmax = codes ? code16(__float_as_uint(c.xmax) >> 16) : 0;
+  const int tiny_slot = (cmax >= 0 && cmax < kCodeSlots - 1) ? cmax : -1;
 
   auto in_pred = [&](float zt) -> bool {
     if (pred == kPredAll) return true;
     if (!(zt > -INFINITY)) return false;
-    return !c.minp || minp_pass(zt, c.m_t, c.lmp);
+    return !minp || minp_pass(zt, m_t, lmp);
   };
   auto dbin = [&](float zt) -> int {
-    const float d = __fsub_rn(c.m_t, zt) * kDScale;  // exact scaling of a rounded difference
+    const float d = __fsub_rn(m_t, zt) * kDScale;  // exact scaling of a rounded difference
     return d < (float)(kBins - 1) ? (int)d : kBins - 1;
+  };
+  // level-0 bin of an element (x before temperature, zt after)
+  auto slot = [&](float x, float zt) -> int {
+    if (!codes) return dbin(zt);
+    const int d = cmax - code16(__float_as_uint(x) >> 16);
+    return d < kCodeSlots - 1 ? d : kCodeSlots - 1;
+  };
+  // mass of the level-0 bin b holding n elements (code bins only)
+  auto code_mass = [&](int b, unsigned long long n, unsigned long long tiny,
+                       unsigned long long catchall) -> unsigned long long {
+    if (b == tiny_slot) return tiny;
+    if (b == kCodeSlots - 1) return catchall;
+    if (n == 0) return 0ull;
+    return n * mass_fixed(__fmul_rn(code_value(cmax - b), inv_t), m_t);
   };
 
   for (int level = 0; level < 8; ++level) {
     const bool dlevel = level == 0;
+    const bool cl = dlevel && codes;  // this level bins by bf16 code
+    const int nb = (dlevel ? nslots0 : kBins) / c.C, b0 = c.rank * nb;
     const unsigned long long range = Khi - Klo;
     const int bits = range == 0 ? 0 : 64 - __clzll((long long)range);
     const int shift = bits > kBinBits ? bits - kBinBits : 0;
-    for (int b = c.tid; b < kBins; b += kThreads) {
-      c.hcnt[b] = 0u;
-      c.hmass[b] = 0ull;
-      c.hbest[b] = kNegInfKey;
-    }
+    for (int b = c.tid; b < 4 * kBins; b += kThreads) h[b] = 0u;
     __syncthreads();
     if (dlevel) VT_CTRACE(c, 4);
     const uint32_t klo_hi = (uint32_t)(Klo >> 32);
-    if (dlevel) {
-      // the catch-all bin is summed per thread (no contention on one word)
-      unsigned int cc = 0u;
-      unsigned long long cm = 0ull, cb = kNegInfKey;
-      auto count0 = [&](float zt, int j, uint32_t nbits, bool draw) {
-        const int d = dbin(zt);
-        const unsigned long long q = by_mass ? mass_fixed(zt, c.m_t) : 0ull;
-        if (d == kBins - 1) {
-          ++cc;
-          cm += q;
-        } else {
-          atomicAdd(&c.hcnt[d], 1u);
-          if (by_mass) atomicAdd(&c.hmass[d], q);
-        }
-        if (draw) {
-          const unsigned long long cur = (d == kBins - 1) ? cb : c.hbest[d];
-          if (may_beat(zt, key_z(cur), nbits)) {
-            const unsigned long long key = elem_key(gumbel_score(zt, nbits), (uint32_t)j);
-            if (d == kBins - 1)
-              cb = key > cb ? key : cb;
-            else
-              atomicMax(&c.hbest[d], key);
-          }
-        }
-      };
-      auto member = [&](float zt, int j) {
-        return j < c.hi && in_pred(zt) && (kbound == 0ull || elem_key(zt, (uint32_t)j) >= kbound);
-      };
+    if (cl) {
+      // one count per element; the masses of the two several-valued bins are
+      // summed per element
+      unsigned long long tm = 0ull, cm = 0ull;
       for_each_group<T>(
           c, [&](float gz) { return ord_key(gz) >= klo_hi; },
           [&](float* x, int, int j0) {
 #pragma unroll
-            for (int i = 0; i < E; i += 2) {
-              const float z0 = __fmul_rn(x[i], c.inv_t), z1 = __fmul_rn(x[i + 1], c.inv_t);
-              const bool m0 = member(z0, j0 + i), m1 = member(z1, j0 + i + 1);
-              if (!(m0 || m1)) continue;
-              uint64_t h = 0ull;
-              if (with_draw) h = pair_hash(c.rkey, j0 + i);  // one output per column pair
-              if (m0) count0(z0, j0 + i, bits_even(h), with_draw);
-              if (m1) count0(z1, j0 + i + 1, bits_odd(h), with_draw);
+            for (int i = 0; i < E; ++i) {
+              const float zt = __fmul_rn(x[i], inv_t);
+              const int j = j0 + i;
+              if (j >= hi || !in_pred(zt)) continue;
+              if (kbound != 0ull && elem_key(zt, (uint32_t)j) < kbound) continue;
+              const int d = slot(x[i], zt);
+              atomicAdd(&h[d], 1u);
+              if (by_mass) {
+                if (d == tiny_slot) tm += mass_fixed(zt, m_t);
+                if (d == kCodeSlots - 1) cm += mass_fixed(zt, m_t);
+              }
             }
           });
-      if (cc) atomicAdd(&c.hcnt[kBins - 1], cc);
-      if (cm) atomicAdd(&c.hmass[kBins - 1], cm);
-      if (cb != kNegInfKey) atomicMax(&c.hbest[kBins - 1], cb);
+      tm = block_sum_u64(tm, s);
+      cm = block_sum_u64(cm, s);
+      if (c.tid == 0) {
+        s.part.tiny_mass = tm;
+        s.part.catch_mass = cm;
+      }
+      VT_CTRACE(c, 12);
+    } else if (dlevel) {
+      // the catch-all bin is summed per thread (no contention on one word)
+      unsigned int cc = 0u;
+      unsigned long long cm = 0ull;
+      for_each_group<T>(
+          c, [&](float gz) { return ord_key(gz) >= klo_hi; },
+          [&](float* x, int, int j0) {
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+              const float zt = __fmul_rn(x[i], inv_t);
+              const int j = j0 + i;
+              if (j >= hi || !in_pred(zt)) continue;
+              if (kbound != 0ull && elem_key(zt, (uint32_t)j) < kbound) continue;
+              const int d = dbin(zt);
+              const unsigned long long q = by_mass ? mass_fixed(zt, m_t) : 0ull;
+              if (d == kBins - 1) {
+                ++cc;
+                cm += q;
+              } else {
+                hist_add(h, d, q, by_mass);
+              }
+            }
+          });
+      if (cc) {
+        atomicAdd(&h[kBins - 1], cc);
+        if (by_mass) {
+          atomicAdd(&h[2 * kBins - 1], (unsigned int)(cm & 0xFFFFull));
+          atomicAdd(&h[3 * kBins - 1], (unsigned int)((cm >> 16) & 0xFFFFull));
+          atomicAdd(&h[4 * kBins - 1], (unsigned int)(cm >> 32));
+        }
+      }
       VT_CTRACE(c, 12);
     } else {
-      for_each_elem<T>(
+      const unsigned long long lo = Klo, hk = Khi;
+      const int ds = dsel;
+      for_each_group<T>(
           c, [&](float gz) { return ord_key(gz) >= klo_hi; },
-          [&](float zt, int j) {
-            if (!in_pred(zt)) return;
-            const unsigned long long K = elem_key(zt, (uint32_t)j);
-            if (K < Klo || K > Khi || dbin(zt) != dsel) return;
-            const int d = (int)((Khi - K) >> shift);
-            atomicAdd(&c.hcnt[d], 1u);
-            if (by_mass) atomicAdd(&c.hmass[d], mass_fixed(zt, c.m_t));
+          [&](float* x, int, int j0) {
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+              const float zt = __fmul_rn(x[i], inv_t);
+              const int j = j0 + i;
+              if (j >= hi || !in_pred(zt)) continue;
+              const unsigned long long K = elem_key(zt, (uint32_t)j);
+              if (K < lo || K > hk || slot(x[i], zt) != ds) continue;
+              hist_add(h, (int)((hk - K) >> shift), by_mass ? mass_fixed(zt, m_t) : 0ull,
+                       by_mass);
+            }
           });
     }
     cluster.sync();
     // distributed merge: this CTA sums its digit range over the cluster
     unsigned long long my_c = 0, my_m = 0;
-    for (int b = c.tid; b < nb; b += kThreads) {
-      unsigned long long sc = 0, sm = 0, sb = kNegInfKey;
-      for (int r = 0; r < c.C; ++r) {
-        sc += cluster.map_shared_rank(c.hcnt, r)[b0 + b];
-        sm += cluster.map_shared_rank(c.hmass, r)[b0 + b];
-        if (dlevel && with_draw) {
-          const unsigned long long v = cluster.map_shared_rank(c.hbest, r)[b0 + b];
-          sb = v > sb ? v : sb;
-        }
+    unsigned long long tiny_all = 0, catch_all = 0;
+    if (cl && by_mass && c.tid < c.C) {
+      const Part* pr = cluster.map_shared_rank(&s.part, c.tid);
+      tiny_all = pr->tiny_mass;
+      catch_all = pr->catch_mass;
+    }
+    if (cl && by_mass) {
+      tiny_all = warp_sum_u64(c.lane < c.C ? tiny_all : 0ull);
+      catch_all = warp_sum_u64(c.lane < c.C ? catch_all : 0ull);
+      if (c.lane == 0 && c.warp == 0) {
+        s.bcast_u[2] = tiny_all;
+        s.bcast_u[3] = catch_all;
       }
+      __syncthreads();
+      tiny_all = s.bcast_u[2];
+      catch_all = s.bcast_u[3];
+    }
+    for (int b = c.tid; b < nb; b += kThreads) {
+      unsigned long long sc = 0, sm = 0;
+      for (int r = 0; r < c.C; ++r) {
+        const unsigned int* hr = cluster.map_shared_rank(h, r);
+        sc += hr[b0 + b];
+        if (by_mass && !cl) sm += hist_mass(hr, b0 + b);
+      }
+      if (by_mass && cl) sm = code_mass(b0 + b, sc, tiny_all, catch_all);
       c.mcnt[b] = (unsigned int)sc;
       c.mmass[b] = sm;
-      if (dlevel && with_draw) c.mbest[b] = sb;
       my_c += sc;
       my_m += sm;
     }
@@ -807,12 +933,30 @@ __device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group
       out.total_mass = total_m;
       return out;
     }
-    if (dlevel) {
+    if (cl) {
+      // the key range of code bin d: one value, or (code 0, catch-all) the
+      // range of its values, widened so that rounding cannot leave it
+      dsel = d;
+      if (d != tiny_slot && d != kCodeSlots - 1) {
+        const float zv = __fmul_rn(code_value(cmax - d), inv_t);
+        Khi = elem_key(zv, 0u);
+        const unsigned long long klo = elem_key(zv, 0xFFFFFFFFu);
+        Klo = klo > kbound ? klo : kbound;
+      } else {
+        const float zh = (d == tiny_slot) ? __fmul_rn(0x1p-12f, inv_t)
+                                          : __fmul_rn(code_value(cmax - (kCodeSlots - 2)), inv_t);
+        const float margin = 1e-3f * (1.0f + fabsf(zh));
+        Khi = elem_key(zh + margin, 0u);
+        const unsigned long long klo =
+            (d == tiny_slot) ? elem_key(-zh - margin, 0xFFFFFFFFu) : 0ull;
+        Klo = klo > kbound ? klo : kbound;
+      }
+    } else if (dlevel) {
       // the key range of bin d, widened so that rounding cannot leave it
       dsel = d;
-      const float margin = 1e-3f * (1.0f + fabsf(c.m_t));
-      const float z_hi = c.m_t - (float)d / kDScale + margin;
-      const float z_lo = (d == kBins - 1) ? -INFINITY : c.m_t - (float)(d + 1) / kDScale - margin;
+      const float margin = 1e-3f * (1.0f + fabsf(m_t));
+      const float z_hi = m_t - (float)d / kDScale + margin;
+      const float z_lo = (d == kBins - 1) ? -INFINITY : m_t - (float)(d + 1) / kDScale - margin;
       Khi = elem_key(z_hi, 0u);
       const unsigned long long klo = (d == kBins - 1) ? 0ull : elem_key(z_lo, 0xFFFFFFFFu);
       Klo = klo > kbound ? klo : kbound;
@@ -824,25 +968,64 @@ __device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group
       Klo = lo_new;
     }
     const bool stop = band <= (unsigned long long)kBufCap || Klo == Khi;
-    band_at_level0 = dlevel && stop;
     cluster.sync();  // merged arrays, parts and the leader's buffer are free again
     if (dlevel) VT_CTRACE(c, 13);
     if (stop) break;
   }
-  // collect the band into the leader, sort it, and walk it
+  // Gather the band into the leader; with_draw, draw over the elements above
+  // it: bin below dsel, or bin dsel with a key above the band.
   {
     uint64_t* lg = cluster.map_shared_rank(c.buf, 0);
     int* lcount = cluster.map_shared_rank(&s.gcount, 0);
     const uint32_t klo_hi = (uint32_t)(Klo >> 32);
-    for_each_elem<T>(
+    const unsigned long long lo = Klo, hk = Khi;
+    const int ds = dsel;
+    float s_cur = -INFINITY, bz = 0.f;
+    int bidx = INT_MAX;
+    // 0: not in the set or below the band, 1: above the band, 2: in the band
+    auto classify = [&](float x, float zt, int j) -> int {
+      if (j >= hi || !in_pred(zt)) return 0;
+      const unsigned long long K = elem_key(zt, (uint32_t)j);
+      if (K < kbound) return 0;
+      const int dd = slot(x, zt);
+      if (dd < ds || (dd == ds && K > hk)) return 1;
+      return (dd == ds && K >= lo) ? 2 : 0;
+    };
+    auto visit = [&](float zt, int j, int cls, uint32_t nbits) {
+      if (cls == 2) {
+        const int pos = atomicAdd(lcount, 1);
+        if (pos < kBufCap) lg[pos] = elem_key(zt, (uint32_t)j);
+      } else if (cls == 1 && with_draw && may_beat(zt, s_cur, nbits)) {
+        const float sc = gumbel_score(zt, nbits);
+        if (pair_better(sc, j, s_cur, bidx)) {
+          s_cur = sc;
+          bidx = j;
+          bz = zt;
+        }
+      }
+    };
+    for_each_group<T>(
         c, [&](float gz) { return ord_key(gz) >= klo_hi; },
-        [&](float zt, int j) {
-          if (!in_pred(zt)) return;
-          const unsigned long long K = elem_key(zt, (uint32_t)j);
-          if (K < Klo || K > Khi || dbin(zt) != dsel) return;
-          const int pos = atomicAdd(lcount, 1);
-          if (pos < kBufCap) lg[pos] = K;
+        [&](float* x, int, int j0) {
+#pragma unroll
+          for (int i = 0; i < E; i += 2) {
+            const float z0 = __fmul_rn(x[i], inv_t), z1 = __fmul_rn(x[i + 1], inv_t);
+            const int c0 = classify(x[i], z0, j0 + i), c1 = classify(x[i + 1], z1, j0 + i + 1);
+            if ((c0 | c1) == 0) continue;
+            // one SplitMix64 output serves the column pair (j0 + i, j0 + i + 1)
+            const uint64_t hh = (with_draw && ((c0 | c1) & 1)) ? pair_hash(rkey, j0 + i) : 0ull;
+            if (c0) visit(z0, j0 + i, c0, bits_even(hh));
+            if (c1) visit(z1, j0 + i + 1, c1, bits_odd(hh));
+          }
         });
+    if (with_draw) {
+      block_argmax(s_cur, bidx, bz, s);
+      if (c.tid == 0) {
+        s.part.dscore = s_cur;
+        s.part.didx = bidx;
+        s.part.dz = bz;
+      }
+    }
     VT_CTRACE(c, 14);
     cluster.sync();
     if (c.rank == 0) {
@@ -853,7 +1036,7 @@ __device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group
       unsigned long long lc = 0, lm = 0;
       for (int i = i0; i < i1; ++i) {
         lc += 1;
-        if (by_mass) lm += mass_fixed(key_z(c.buf[i]), c.m_t);
+        if (by_mass) lm += mass_fixed(key_z(c.buf[i]), m_t);
       }
       unsigned long long tot;
       const unsigned long long ex_c = block_exclusive_u64(lc, s, &tot);
@@ -863,7 +1046,7 @@ __device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group
       unsigned long long rc = acc_c + ex_c, rm = acc_m + ex_m;
       for (int i = i0; i < i1; ++i) {
         rc += 1;
-        if (by_mass) rm += mass_fixed(key_z(c.buf[i]), c.m_t);
+        if (by_mass) rm += mass_fixed(key_z(c.buf[i]), m_t);
         if (by_mass ? (rm > target) : (rc > target)) {
           hit = i;
           hit_c = rc;
@@ -877,26 +1060,19 @@ __device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group
       if (c.lane == 0) s.ri[c.warp] = hmin;
       __syncthreads();
       if (c.tid == 0) {
-        int h = INT_MAX;
-        for (int w = 0; w < kWarps; ++w) h = min(h, s.ri[w]);
-        s.bcast_i[0] = h;
+        int hh = INT_MAX;
+        for (int w = 0; w < kWarps; ++w) hh = min(hh, s.ri[w]);
+        s.bcast_i[0] = hh;
       }
       __syncthreads();
-      const int h = s.bcast_i[0];
-      if (h != INT_MAX && hit == h) {
-        s.sel.kb = c.buf[h];
+      const int hb = s.bcast_i[0];
+      if (hb != INT_MAX && hit == hb) {
+        s.sel.kb = c.buf[hb];
         s.sel.cnt_incl = hit_c;
         s.sel.mass_incl = hit_m;
         s.sel.all = 0;
       }
-#ifdef VT_DEBUG_SELECT
-      if (h == INT_MAX && c.tid == 0)
-        printf("select miss row %d rank %d by_mass %d n %d acc_c %llu acc_m %llu target %llu "
-               "total_c %llu total_m %llu tot %llu Klo %llx Khi %llx dsel %d m_t %g\n",
-               c.row, c.rank, (int)by_mass, n, acc_c, acc_m, target, total_c, total_m, tot, Klo,
-               Khi, dsel, c.m_t);
-#endif
-      if (h == INT_MAX && c.tid == 0) {  // cannot happen: the band holds the crossing
+      if (hb == INT_MAX && c.tid == 0) {  // cannot happen: the band holds the crossing
         s.sel.kb = n > 0 ? c.buf[n - 1] : kbound;
         s.sel.cnt_incl = acc_c + n;
         s.sel.mass_incl = acc_m;
@@ -908,19 +1084,22 @@ __device__ __noinline__ SelOut cluster_select(Ctx& c, Smem& s, cg::cluster_group
         s.sel.total_mass = total_m;
         s.sel.draw_ok = 0;
       }
-      if (band_at_level0 && with_draw && h != INT_MAX) {
-        // winner: the kept band prefix [0, h] and every bin above the band
+      if (with_draw && hb != INT_MAX) {
+        // winner: the kept band prefix [0, hb] and every CTA's best above the band
         unsigned long long best = kNegInfKey;
-        for (int i = c.tid; i <= h; i += kThreads) {
+        for (int i = c.tid; i <= hb; i += kThreads) {
           const uint64_t k = c.buf[i];
           const int j = (int)key_idx(k);
           const unsigned long long key =
-              elem_key(gumbel_score(key_z(k), noise_bits(c.rkey, j)), (uint32_t)j);
+              elem_key(gumbel_score(key_z(k), noise_bits(rkey, j)), (uint32_t)j);
           best = key > best ? key : best;
         }
-        for (int b = c.tid; b < dsel; b += kThreads) {
-          const unsigned long long v = cluster.map_shared_rank(c.mbest, b / nb)[b % nb];
-          best = v > best ? v : best;
+        if (c.tid < c.C) {
+          const Part* pr = cluster.map_shared_rank(&s.part, c.tid);
+          if (pr->didx != INT_MAX) {
+            const unsigned long long key = elem_key(pr->dscore, (uint32_t)pr->didx);
+            best = key > best ? key : best;
+          }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -1046,20 +1225,10 @@ __device__ RowParams init_row(Ctx& c, const SampleArgs& a, uint8_t* dsm, int row
   c.aligned = a.aligned != 0;
   c.rowp = reinterpret_cast<const T*>(a.logits) + (int64_t)row * a.ld;
   c.buf = reinterpret_cast<uint64_t*>(dsm);
-  c.hmass = reinterpret_cast<unsigned long long*>(dsm);
-  c.hcnt = reinterpret_cast<unsigned int*>(dsm + kBins * 8);
-  // per-bin bests live past the gather buffer, so they survive the band collect
-  c.hbest = reinterpret_cast<unsigned long long*>(dsm + (size_t)kBufCap * 8);
+  c.hcnt = reinterpret_cast<unsigned int*>(dsm);  // aliases the gather buffer
   c.gmax = reinterpret_cast<uint16_t*>(dsm + off_gmax);
-  if (C > 1) {
-    c.mmass = reinterpret_cast<unsigned long long*>(dsm + off_mrg);
-    c.mbest = reinterpret_cast<unsigned long long*>(dsm + off_mrg + (kBins / C) * 8);
-    c.mcnt = reinterpret_cast<unsigned int*>(dsm + off_mrg + (kBins / C) * 16);
-  } else {
-    c.mmass = c.hmass;
-    c.mcnt = c.hcnt;
-    c.mbest = c.hbest;
-  }
+  c.mmass = reinterpret_cast<unsigned long long*>(dsm + off_mrg);
+  c.mcnt = reinterpret_cast<unsigned int*>(dsm + off_mrg + (kCodeSlots / C) * 8);
   const RowParams P = a.params[row];
   c.greedy = (P.flags & kRowGreedy) != 0;
   c.inv_t = P.inv_t;
@@ -1077,6 +1246,7 @@ __device__ RowParams init_row(Ctx& c, const SampleArgs& a, uint8_t* dsm, int row
   c.prefix = nullptr;
   c.side_z = nullptr;
   c.stage = nullptr;
+  c.xmax = 0.f;
   return P;
 }
 
@@ -1660,14 +1830,682 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
       SlowRow r;
       r.m_t = c.m_t;
       r.lnS = c.lnS;
-      r.bi = s.rs.bi;
-      r.topn_done = (n == 0 || topn_ok) ? 1 : 0;
+      r.xmax = s.rs.bv;
+      r.bi_topn = (uint32_t)s.rs.bi | ((n == 0 || topn_ok) ? 0x80000000u : 0u);
       a.slow[c.row] = r;
       a.slow_list[atomicAdd(a.slow_ctl, 1u)] = c.row;
       if (s.rs.err) atomicOr(a.err_word, s.rs.err);
     }
   }
   VT_TRACE(15);
+}
+
+// ---------------------------------------------------------------------------
+// selection on bf16 codes (selection kernel, bf16 rows without penalties)
+// ---------------------------------------------------------------------------
+// Every element of one bf16 code has the same tempered value and mass, so the
+// survivors counted per code slot (slot = code(max) - code(x)) settle the kept
+// set exactly: the kept count of the boundary slot follows from its count and
+// its one per-element mass, and inside a slot the order is by index.  The
+// draw's best element of a slot is the one with the largest noise bits
+// (lowest index on ties), so the main pass keeps, per slot, only a count and
+// the largest noise bits.  The leader then walks the 4096 slots (top-n, top-k,
+// top-p over the top-k survivors, min-p per slot) and finds the best wholly
+// kept slot; one index-ordered pass settles the kept prefix of the boundary
+// slot, the index of the winning element and the top-n.  The tiny slot
+// (|x| < 2^-12 and both zeros) and the catch-all hold several values: their
+// elements are counted, summed and drawn one by one (shared atomics; they are
+// rare).  A boundary inside one of them, a top-n that reaches -inf, or two
+// slots with the same best score leave the row to the generic selection
+// (returns false before any output; every CTA of the cluster returns the same).
+
+// One element of the tiny (w = 0) or catch-all (w = 1) slot.
+__device__ __noinline__ void code_special(Part& pt, int w, uint32_t u, int j, uint32_t bits,
+                                          float inv_t, float m_t, bool minp, double lmp,
+                                          bool draw) {
+  const float zt = __fmul_rn(__uint_as_float(u << 16), inv_t);
+  atomicAdd(&pt.sp_all[w], 1ull);
+  if (minp && !minp_pass(zt, m_t, lmp)) return;
+  atomicAdd(&pt.sp_cnt[w], 1ull);
+  atomicAdd(&pt.sp_mass[w], mass_fixed(zt, m_t));
+  if (draw) atomicMax(&pt.sp_key[w], elem_key(gumbel_score(zt, bits), (uint32_t)j));
+}
+
+// A fast approximation of the Gumbel score (for choosing where to compute
+// the exact one): z - ln(-ln u), u = (b + 1/2) 2^-24.
+__device__ __forceinline__ float approx_score(float z, uint32_t b) {
+  const float u = (float)(2u * b + 1u) * 0x1p-25f;
+  return z - __logf(-__logf(u));
+}
+
+template <typename T>
+__device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
+                                      cg::cluster_group& cluster, bool topn_done,
+                                      uint8_t* code_mem) {
+  if constexpr (sizeof(T) != 2) {
+    return false;
+  } else {
+    const int n = a.n_logprobs;
+    const bool want_topn = n > 0 && !topn_done;
+    const bool draw = !c.greedy;
+    const bool leader = c.rank == 0;
+    const int tid = c.tid, lane = c.lane, warp = c.warp, C = c.C, rank = c.rank;
+    unsigned int* hc = reinterpret_cast<unsigned int*>(code_mem);  // counts per slot
+    unsigned int* hb = hc + kCodeSlots;                            // best noise bits + 1
+    unsigned int* mc = c.mcnt;                                     // merged, this CTA's range
+    unsigned int* mb = reinterpret_cast<unsigned int*>(c.mmass);
+    const int nb = kCodeSlots / C, b0 = rank * nb;
+    const int cmax = code16(__float_as_uint(c.xmax) >> 16);
+    const int tiny = (cmax >= 0 && cmax < kCodeSlots - 1) ? cmax : -1;
+    constexpr int kCatch = kCodeSlots - 1;
+    const float m_t = c.m_t, inv_t = c.inv_t, lnS = c.lnS, top_p = c.top_p;
+    const bool minp = c.minp, topk = c.topk, topp = c.topp;
+    const int top_k = c.top_k;
+    const double lmp = c.lmp;
+    const int hi = c.hi, lo = c.lo, ngroups = c.ngroups, row = c.row;
+    const uint64_t rkey = c.rkey;
+    const uint4* stage = c.stage;
+
+    for (int b = tid; b < 2 * kCodeSlots; b += kThreads) hc[b] = 0u;
+    if (tid < 2) {
+      s.part.sp_all[tid] = 0ull;
+      s.part.sp_cnt[tid] = 0ull;
+      s.part.sp_mass[tid] = 0ull;
+      s.part.sp_key[tid] = 0ull;
+    }
+    if (leader && tid == 0) s.gcount = 0;
+    __syncthreads();
+    VT_CTRACE(c, 4);
+
+    // ---- pass 1: counts and best noise bits per slot --------------------------
+    for (int g = tid; g < ngroups; g += kThreads) {
+      const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const int j0 = lo + g * 16;
+      // SplitMix64 counter of the column pair (j0 + 2q, j0 + 2q + 1)
+      const uint64_t base = rkey + kSeedStep * ((uint64_t)(j0 >> 1) + 1ull);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint64_t h = draw ? sm64_mix(base + kSeedStep * (uint64_t)q) : 0ull;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t u = e ? (w[q] >> 16) : (w[q] & 0xFFFFu);
+          const uint32_t bits = e ? bits_odd(h) : bits_even(h);
+          const int j = j0 + 2 * q + e;
+          if (u == 0xFF80u || j >= hi) continue;  // -inf is never a survivor
+          int sl = cmax - code16(u);
+          sl = sl < kCatch ? sl : kCatch;
+          if (sl == tiny || sl == kCatch) {
+            code_special(s.part, sl == tiny ? 0 : 1, u, j, bits, inv_t, m_t, minp, lmp, draw);
+          } else {
+            atomicAdd(&hc[sl], 1u);
+            if (draw) atomicMax(&hb[sl], bits + 1u);
+          }
+        }
+      }
+    }
+    VT_CTRACE(c, 12);
+    cluster.sync();  // (a) slot counts and special parts complete
+
+    // ---- special totals, then merge this CTA's slot range --------------------
+    unsigned long long sp_all0, sp_all1, sp_cnt0, sp_cnt1, sp_m0, sp_m1, sp_k0, sp_k1;
+    {
+      unsigned long long v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (lane < C) {
+        const Part* pr = cluster.map_shared_rank(&s.part, lane);
+        v[0] = pr->sp_all[0];
+        v[1] = pr->sp_all[1];
+        v[2] = pr->sp_cnt[0];
+        v[3] = pr->sp_cnt[1];
+        v[4] = pr->sp_mass[0];
+        v[5] = pr->sp_mass[1];
+        v[6] = pr->sp_key[0];
+        v[7] = pr->sp_key[1];
+      }
+#pragma unroll
+      for (int q = 0; q < 6; ++q) v[q] = warp_sum_u64(v[q]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long x6 = __shfl_xor_sync(0xffffffffu, v[6], o);
+        const unsigned long long x7 = __shfl_xor_sync(0xffffffffu, v[7], o);
+        v[6] = x6 > v[6] ? x6 : v[6];
+        v[7] = x7 > v[7] ? x7 : v[7];
+      }
+      sp_all0 = v[0];
+      sp_all1 = v[1];
+      sp_cnt0 = v[2];
+      sp_cnt1 = v[3];
+      sp_m0 = v[4];
+      sp_m1 = v[5];
+      sp_k0 = v[6];
+      sp_k1 = v[7];
+    }
+    for (int b = tid; b < nb; b += kThreads) {
+      unsigned int cnt[kMaxCluster], bst[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < C) {
+          const unsigned int* hr = cluster.map_shared_rank(hc, r);
+          cnt[r] = hr[b0 + b];
+          bst[r] = hr[kCodeSlots + b0 + b];
+        }
+      }
+      unsigned int sc = 0u, sbm = 0u;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < C) {
+          sc += cnt[r];
+          sbm = bst[r] > sbm ? bst[r] : sbm;
+        }
+      }
+      mc[b] = sc;
+      mb[b] = sbm;
+    }
+    __syncthreads();
+    VT_CTRACE(c, 11);
+
+    // ---- the walk, distributed: each CTA walks its own slot range ------------
+    // slot sl: count of finite elements, of survivors, and the survivors' mass
+    auto zq = [&](int sl) { return __fmul_rn(code_value(cmax - sl), inv_t); };
+    auto vals = [&](int sl, unsigned int& na, unsigned int& ns, unsigned long long& ms) {
+      if (sl == tiny) {
+        na = (unsigned int)sp_all0;
+        ns = (unsigned int)sp_cnt0;
+        ms = sp_m0;
+        return;
+      }
+      if (sl == kCatch) {
+        na = (unsigned int)sp_all1;
+        ns = (unsigned int)sp_cnt1;
+        ms = sp_m1;
+        return;
+      }
+      na = mc[sl - b0];
+      ns = 0u;
+      ms = 0ull;
+      if (na != 0u) {
+        const float z = zq(sl);
+        if (!minp || minp_pass(z, m_t, lmp)) {
+          ns = na;
+          ms = (unsigned long long)na * mass_fixed(z, m_t);
+        }
+      }
+    };
+    // mass of the first k survivors of slot sl (regular: k equal masses)
+    auto part_mass = [&](int sl, unsigned int k, unsigned int ns, unsigned long long ms) {
+      if (k == ns) return ms;
+      return (unsigned long long)k * mass_fixed(zq(sl), m_t);
+    };
+    const int per_t = (nb + kThreads - 1) / kThreads;  // contiguous slots per thread
+    const int t0 = min(b0 + nb, b0 + tid * per_t), t1 = min(b0 + nb, t0 + per_t);
+    unsigned long long t_all = 0, t_cnt = 0, t_mass = 0;
+    int t_last = -1;
+    for (int sl = t0; sl < t1; ++sl) {
+      unsigned int na, ns;
+      unsigned long long ms;
+      vals(sl, na, ns, ms);
+      t_all += na;
+      t_cnt += ns;
+      t_mass += ms;
+      if (ns != 0u) t_last = sl;
+    }
+    unsigned long long r_all, r_cnt, r_mass;
+    const unsigned long long x_all = block_exclusive_u64(t_all, s, &r_all);
+    const unsigned long long x_cnt = block_exclusive_u64(t_cnt, s, &r_cnt);
+    const unsigned long long x_mass = block_exclusive_u64(t_mass, s, &r_mass);
+    int lastw = t_last;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lastw = max(lastw, __shfl_xor_sync(0xffffffffu, lastw, o));
+    if (lane == 0) s.ri[warp] = lastw;
+    __syncthreads();
+    if (tid == 0) {
+      int lm = -1;
+      for (int w = 0; w < kWarps; ++w) lm = max(lm, s.ri[w]);
+      s.part.rng_all = r_all;
+      s.part.rng_cnt = r_cnt;
+      s.part.rng_mass = r_mass;
+      s.part.rng_last = lm;
+      if (leader) {  // the leader's walk record starts clean
+        s.cw.fallback = 0;
+        s.cw.slot = -1;
+        s.cw.kp = 0;
+        s.cw.above = 0ull;
+        s.cw.slot_n = -1;
+        s.cw.kn = 0;
+        s.cw.k_slot = -1;
+        s.cw.k_kept = 0;
+        s.cw.k_mass = 0ull;
+      }
+    }
+    cluster.sync();  // (w1) range totals visible
+    // prefix of the ranges before mine, and the row totals
+    unsigned long long p_all = 0, p_cnt = 0, p_mass = 0, tot_all = 0, tot_cnt = 0, tot_mass = 0;
+    int last_slot = -1;
+    for (int r = 0; r < C; ++r) {
+      const Part* pr = cluster.map_shared_rank(&s.part, r);
+      if (r < rank) {
+        p_all += pr->rng_all;
+        p_cnt += pr->rng_cnt;
+        p_mass += pr->rng_mass;
+      }
+      tot_all += pr->rng_all;
+      tot_cnt += pr->rng_cnt;
+      tot_mass += pr->rng_mass;
+      last_slot = max(last_slot, pr->rng_last);
+    }
+    CodeWalk* lw = cluster.map_shared_rank(&s.cw, 0);
+    const unsigned long long e_all = p_all + x_all, e_cnt = p_cnt + x_cnt, e_mass = p_mass + x_mass;
+    // top-n over every finite element
+    if (want_topn) {
+      const unsigned long long tg = (unsigned long long)(n - 1);
+      unsigned long long run = e_all;
+      for (int sl = t0; sl < t1; ++sl) {
+        unsigned int na, ns;
+        unsigned long long ms;
+        vals(sl, na, ns, ms);
+        if (run <= tg && run + na > tg) {
+          lw->slot_n = sl;
+          lw->kn = (int)(tg + 1 - run);
+          if (sl == tiny || sl == kCatch) lw->fallback = 1;
+        }
+        run += na;
+      }
+    }
+    // top-k by count over the survivors; without top-p it is the boundary
+    const bool k_active = draw && topk && tot_cnt > (unsigned long long)(top_k - 1);
+    if (k_active) {
+      const unsigned long long tg = (unsigned long long)(top_k - 1);
+      unsigned long long run = e_cnt, runm = e_mass;
+      for (int sl = t0; sl < t1; ++sl) {
+        unsigned int na, ns;
+        unsigned long long ms;
+        vals(sl, na, ns, ms);
+        if (run <= tg && run + ns > tg) {
+          const unsigned int kk = (unsigned int)(tg + 1 - run);
+          if (sl == tiny || sl == kCatch) {
+            lw->fallback = 1;
+          } else {
+            lw->k_slot = sl;
+            lw->k_kept = (int)kk;
+            lw->k_mass = runm + part_mass(sl, kk, ns, ms);
+            if (!topp) {
+              lw->slot = sl;
+              lw->kp = (int)kk;
+              lw->above = run;
+            }
+          }
+        }
+        run += ns;
+        runm += ms;
+      }
+    }
+    if (draw && topp) {
+      int slot_k = -1;
+      unsigned int kk = 0u;
+      unsigned long long W = tot_mass, e_tm = e_mass;
+      if (k_active) {
+        cluster.sync();  // (w1b) the top-k boundary is known
+        slot_k = lw->k_slot;
+        kk = (unsigned int)lw->k_kept;
+        W = lw->k_mass;
+        // survivors' masses truncated to the top-k set
+        unsigned long long tm = 0ull;
+        for (int sl = t0; sl < t1 && sl <= slot_k; ++sl) {
+          unsigned int na, ns;
+          unsigned long long ms;
+          vals(sl, na, ns, ms);
+          tm += sl < slot_k ? ms : part_mass(sl, kk, ns, ms);
+        }
+        unsigned long long r_tm;
+        const unsigned long long x_tm = block_exclusive_u64(tm, s, &r_tm);
+        if (tid == 0) s.part.rng_tmass = r_tm;
+        cluster.sync();  // (w1c) truncated range totals visible
+        unsigned long long p_tm = 0ull;
+        for (int r = 0; r < rank; ++r) p_tm += cluster.map_shared_rank(&s.part, r)->rng_tmass;
+        e_tm = p_tm + x_tm;
+      }
+      const unsigned long long tgt_m = (unsigned long long)((double)W * (double)top_p);
+      // the boundary element is the first whose inclusive mass exceeds the
+      // target; its slot is the first whose inclusive mass does
+      unsigned long long A = e_tm, run = e_cnt;
+      for (int sl = t0; sl < t1; ++sl) {
+        if (slot_k >= 0 && sl > slot_k) break;
+        unsigned int na, ns;
+        unsigned long long ms;
+        vals(sl, na, ns, ms);
+        const unsigned int nc = (slot_k >= 0 && sl == slot_k) ? kk : ns;
+        if (nc == 0u) continue;
+        const unsigned long long mc2 = part_mass(sl, nc, ns, ms);
+        if (A <= tgt_m && A + mc2 > tgt_m) {
+          if (sl == tiny || sl == kCatch) {
+            lw->fallback = 1;
+          } else {
+            const unsigned long long kq = (tgt_m - A) / mass_fixed(zq(sl), m_t) + 1ull;
+            lw->slot = sl;
+            lw->kp = kq < (unsigned long long)nc ? (int)kq : (int)nc;
+            lw->above = run;
+          }
+        }
+        A += mc2;
+        run += ns;
+      }
+    }
+    cluster.sync();  // (w2) the boundary is known
+    int bslot = lw->slot, bkp = lw->kp;
+    if (draw && topp && k_active && bslot < 0) {
+      // every top-k survivor is kept: top-k's boundary stands
+      bslot = lw->k_slot;
+      bkp = lw->k_kept;
+    }
+    // the best wholly kept regular slot of my range: approximate scores first,
+    // then the exact score where it can matter
+    float emax = -INFINITY;
+    int eslot = -1, etie = 0;
+    if (draw) {
+      float amax = -INFINITY;
+      for (int sl = t0; sl < t1; ++sl) {
+        if (sl == tiny || sl == kCatch || (bslot >= 0 && sl >= bslot)) continue;
+        const unsigned int na = mc[sl - b0], bbits = mb[sl - b0];
+        if (na == 0u || bbits == 0u) continue;
+        const float z = zq(sl);
+        if (minp && !minp_pass(z, m_t, lmp)) continue;
+        amax = fmaxf(amax, approx_score(z, bbits - 1u));
+      }
+      amax = warp_max(amax);
+      if (lane == 0) s.rf[warp] = amax;
+      __syncthreads();
+      float cmax_a = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) cmax_a = fmaxf(cmax_a, s.rf[w]);
+      __syncthreads();
+      if (cmax_a > -INFINITY) {
+        const float margin = 1e-3f * (1.0f + fabsf(cmax_a));
+        for (int sl = t0; sl < t1; ++sl) {
+          if (sl == tiny || sl == kCatch || (bslot >= 0 && sl >= bslot)) continue;
+          const unsigned int na = mc[sl - b0], bbits = mb[sl - b0];
+          if (na == 0u || bbits == 0u) continue;
+          const float z = zq(sl);
+          if (minp && !minp_pass(z, m_t, lmp)) continue;
+          if (approx_score(z, bbits - 1u) < cmax_a - margin) continue;
+          const float sc = gumbel_score(z, bbits - 1u);
+          if (sc > emax) {
+            emax = sc;
+            eslot = sl;
+            etie = 0;
+          } else if (sc == emax) {
+            etie = 1;
+          }
+        }
+      }
+      // CTA best; equal scores of different slots mark a tie
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float e2 = __shfl_xor_sync(0xffffffffu, emax, o);
+        const int s2 = __shfl_xor_sync(0xffffffffu, eslot, o);
+        const int t2 = __shfl_xor_sync(0xffffffffu, etie, o);
+        if (e2 > emax) {
+          emax = e2;
+          eslot = s2;
+          etie = t2;
+        } else if (e2 == emax && e2 > -INFINITY && s2 != eslot) {
+          etie = 1;
+        } else if (e2 == emax) {
+          etie |= t2;
+        }
+      }
+      if (lane == 0) {
+        s.rf[warp] = emax;
+        s.ri[warp] = eslot;
+        s.ri[kWarps + warp] = etie;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float e = -INFINITY;
+        int es = -1, et = 0;
+        for (int w = 0; w < kWarps; ++w) {
+          if (s.rf[w] > e) {
+            e = s.rf[w];
+            es = s.ri[w];
+            et = s.ri[kWarps + w];
+          } else if (s.rf[w] == e && e > -INFINITY && (s.ri[w] != es || s.ri[kWarps + w])) {
+            et = 1;
+          }
+        }
+        s.part.best_score = e;
+        s.part.best_slot = es;
+        s.part.best_tie = et;
+        s.part.best_bits = es >= 0 ? mb[es - b0] : 0u;
+      }
+    }
+    cluster.sync();  // (w3) range bests visible
+    VT_CTRACE(c, 13);
+    const int fallback = lw->fallback;
+    const int nslot = lw->slot_n, nkn = lw->kn;
+    const unsigned long long above = lw->above;
+    float wscore = -INFINITY;
+    int wslot = -1;
+    unsigned int wbits = 0u;
+    int wtie = 0;
+    if (draw) {
+      for (int r = 0; r < C; ++r) {
+        const Part* pr = cluster.map_shared_rank(&s.part, r);
+        if (pr->best_score > wscore) {
+          wscore = pr->best_score;
+          wslot = pr->best_slot;
+          wbits = pr->best_bits;
+          wtie = pr->best_tie;
+        } else if (pr->best_score == wscore && wscore > -INFINITY) {
+          wtie = 1;
+        }
+      }
+    }
+    const int sp_kept0 = tiny >= 0 && (bslot < 0 || tiny < bslot);
+    const int sp_kept1 = bslot < 0;
+    const int lslot = last_slot;
+    const bool give_up = fallback || wtie ||
+                         (draw && bslot < 0 && (lslot == tiny || lslot == kCatch)) ||
+                         (want_topn && tot_all < (unsigned long long)n);
+    __syncthreads();
+    if (give_up) {
+      cluster.sync();  // nobody reads another CTA's walk data after this
+      return false;
+    }
+
+    // ---- pass 2: index-ordered over contiguous group ranges -------------------
+    const int per = (ngroups + kThreads - 1) / kThreads;
+    const int g0 = min(ngroups, tid * per), g1 = min(ngroups, g0 + per);
+    int pre_b = 0, pre_n = 0;
+    for (int r = 0; r < rank; ++r) {
+      const unsigned int* hr = cluster.map_shared_rank(hc, r);
+      if (bslot >= 0) pre_b += (int)hr[bslot];
+      if (nslot >= 0) pre_n += (int)hr[nslot];
+    }
+    const int kb_r = bslot >= 0 ? max(0, min(bkp - pre_b, (int)hc[bslot])) : 0;
+    const int kn_r = nslot >= 0 ? max(0, min(nkn - pre_n, (int)hc[nslot])) : 0;
+    int cnt_b = 0, cnt_n = 0;
+    if (bslot >= 0 || nslot >= 0) {
+      for (int g = g0; g < g1; ++g) {
+        const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+          if (u == 0xFF80u || lo + g * 16 + e >= hi) continue;
+          int sl = cmax - code16(u);
+          sl = sl < kCatch ? sl : kCatch;
+          cnt_b += sl == bslot;
+          cnt_n += sl == nslot;
+        }
+      }
+    }
+    unsigned long long tb, tn;
+    int rank_b = (int)block_exclusive_u64((unsigned long long)cnt_b, s, &tb);
+    int rank_n = (int)block_exclusive_u64((unsigned long long)cnt_n, s, &tn);
+    VT_CTRACE(c, 9);
+    unsigned long long kbest = 0ull;  // ((bits + 1) << 32) | ~index: kept prefix's best
+    int last_j = -1, lastslot_j = -1, cand_j = INT_MAX;
+    uint64_t* lg = cluster.map_shared_rank(c.buf, 0);
+    int* lcount = cluster.map_shared_rank(&s.gcount, 0);
+    for (int g = g0; g < g1; ++g) {
+      const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+        const int j = lo + g * 16 + e;
+        if (u == 0xFF80u || j >= hi) continue;
+        int sl = cmax - code16(u);
+        sl = sl < kCatch ? sl : kCatch;
+        if (sl == bslot) {
+          if (draw && rank_b < kb_r) {
+            const unsigned long long k =
+                ((unsigned long long)(noise_bits(rkey, j) + 1u) << 32) | (0xFFFFFFFFu - (uint32_t)j);
+            kbest = k > kbest ? k : kbest;
+            last_j = j;
+          }
+          ++rank_b;
+        }
+        if (sl == wslot && noise_bits(rkey, j) + 1u == wbits) cand_j = min(cand_j, j);
+        if (sl == lslot) lastslot_j = j;
+        if (want_topn && sl <= nslot) {
+          bool take = true;
+          if (sl == nslot) {
+            take = rank_n < kn_r;
+            ++rank_n;
+          }
+          if (take) {
+            const int pos = atomicAdd(lcount, 1);
+            if (pos < kBufCap)
+              lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)j);
+          }
+        }
+      }
+    }
+    // this CTA's results
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, kbest, o);
+      kbest = k2 > kbest ? k2 : kbest;
+      last_j = max(last_j, __shfl_xor_sync(0xffffffffu, last_j, o));
+      lastslot_j = max(lastslot_j, __shfl_xor_sync(0xffffffffu, lastslot_j, o));
+      cand_j = min(cand_j, __shfl_xor_sync(0xffffffffu, cand_j, o));
+    }
+    if (lane == 0) {
+      s.ru[warp] = kbest;
+      s.ri[warp] = last_j;
+      s.ri[kWarps + warp] = cand_j;
+      s.ri[2 * kWarps + warp] = lastslot_j;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long kb2 = 0ull;
+      int lj = -1, cj = INT_MAX, lsj = -1;
+      for (int w = 0; w < kWarps; ++w) {
+        kb2 = s.ru[w] > kb2 ? s.ru[w] : kb2;
+        lj = max(lj, s.ri[w]);
+        cj = min(cj, s.ri[kWarps + w]);
+        lsj = max(lsj, s.ri[2 * kWarps + w]);
+      }
+      s.part.cb_key = kb2;
+      s.part.cb_last = lj;
+      s.part.cw_j = cj;
+      s.part.last_j = lsj;
+    }
+    VT_CTRACE(c, 14);
+    cluster.sync();  // (d) pass-2 parts and top-n keys complete
+
+    // ---- the leader: draw, outputs -------------------------------------------
+    if (leader) {
+      if (want_topn) {
+        const int N = min(s.gcount, kBufCap);
+        block_sort_desc(c.buf, N);
+        int32_t* out_ids = a.out_topk_ids + (int64_t)row * n;
+        float* out_lps = a.out_topk_logprobs + (int64_t)row * n;
+        for (int t = tid; t < n; t += kThreads) {
+          if (t < N) {
+            const uint64_t k = c.buf[t];
+            out_ids[t] = (int)key_idx(k);
+            out_lps[t] = (key_z(k) - m_t) - lnS;
+          } else {
+            out_ids[t] = -1;
+            out_lps[t] = -INFINITY;
+          }
+        }
+      }
+      if (tid == 0) {
+        int tok = s.rs.bi;
+        float ztok = m_t;
+        int kept = 1;
+        float kth_v = m_t;
+        int kth_i = s.rs.bi;
+        int er = 0;
+        if (draw) {
+          unsigned long long cbk = 0ull;
+          int cbl = -1, cwj = INT_MAX, lsj = -1;
+          for (int r = 0; r < C; ++r) {
+            const Part* pr = cluster.map_shared_rank(&s.part, r);
+            cbk = pr->cb_key > cbk ? pr->cb_key : cbk;
+            cbl = max(cbl, pr->cb_last);
+            cwj = min(cwj, pr->cw_j);
+            lsj = max(lsj, pr->last_j);
+          }
+          float bs = -INFINITY;
+          int bi = INT_MAX;
+          auto offer = [&](float sc, int j) {
+            if (j != INT_MAX && pair_better(sc, j, bs, bi)) {
+              bs = sc;
+              bi = j;
+            }
+          };
+          if (wslot >= 0) {
+            if (cwj == INT_MAX)
+              er |= kErrInternal;  // the winning slot's best element must exist
+            else
+              offer(wscore, cwj);
+          }
+          if (bslot >= 0 && cbk != 0ull) {
+            const uint32_t bits = (uint32_t)(cbk >> 32) - 1u;
+            offer(gumbel_score(zq_value(cmax, bslot, inv_t), bits), (int)(0xFFFFFFFFu - (uint32_t)cbk));
+          }
+          if (sp_kept0 && sp_k0 != 0ull) offer(key_z(sp_k0), (int)key_idx(sp_k0));
+          if (sp_kept1 && sp_k1 != 0ull) offer(key_z(sp_k1), (int)key_idx(sp_k1));
+          if (bi == INT_MAX) {
+            er |= kErrInternal;
+            bi = s.rs.bi;
+          }
+          tok = bi;
+          // the winner's tempered value, from its logit
+          ztok = __fmul_rn(Elt<T>::load1(reinterpret_cast<const T*>(c.rowp) + tok), inv_t);
+          if (bslot >= 0) {
+            kept = (int)(above + (unsigned long long)bkp);
+            kth_v = zq_value(cmax, bslot, inv_t);
+            kth_i = cbl;
+          } else {
+            kept = (int)tot_cnt;
+            kth_v = zq_value(cmax, lslot, inv_t);
+            kth_i = lsj;
+          }
+        }
+        s.bcast_i[0] = tok;
+        a.out_tokens[row] = tok;
+        if (a.out_logprobs) a.out_logprobs[row] = (ztok - m_t) - lnS;
+        a.row_status[row] = kRowOk;
+        a.dbg_kth_value[row] = kth_v;
+        a.dbg_kth_index[row] = kth_i;
+        a.dbg_kept[row] = kept;
+        a.seeds[row] += kSeedStep;
+        er |= s.rs.err | s.part.err;
+        if (er) atomicOr(a.err_word, er);
+      }
+    }
+    cluster.sync();  // (e) no DSMEM access after this
+    if (leader && a.update_counts) {
+      __syncthreads();
+      append_token(a.hist + (int64_t)row * a.hist_cap, a.hist_len + row, a.hist_cap,
+                   s.bcast_i[0], s, a.row_status + row);
+    }
+    VT_CTRACE(c, 15);
+    return true;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1684,11 +2522,13 @@ __device__ __noinline__ void slow_row(Ctx& c, Smem& s, const SampleArgs& a, cg::
   const bool leader = c.rank == 0;
   int32_t* out_ids = n > 0 ? a.out_topk_ids + (int64_t)c.row * n : nullptr;
   float* out_lps = n > 0 ? a.out_topk_logprobs + (int64_t)c.row * n : nullptr;
+  // level-0 bins by bf16 code for bf16 rows whose values are all bf16
+  const bool codes = sizeof(T) == 2 && !c.pen;
   if (n > 0 && !topn_done) {
     {
       // rank n-1 of every element (the -inf ones included, by index)
       SelOut so = cluster_select<T>(c, s, cluster, kPredAll, 0ull, false,
-                                    (unsigned long long)(n - 1), 0.f, false);
+                                    (unsigned long long)(n - 1), 0.f, false, codes);
       const unsigned long long kb = so.all ? 0ull : so.kb;
       if (leader && c.tid == 0) s.gcount = 0;
       cluster.sync();
@@ -1739,7 +2579,7 @@ __device__ __noinline__ void slow_row(Ctx& c, Smem& s, const SampleArgs& a, cg::
       unsigned long long kbk = 0ull;
       if (c.topk) {
         SelOut so = cluster_select<T>(c, s, cluster, kPredSurv, 0ull, false,
-                                      (unsigned long long)(c.top_k - 1), 0.f, !c.topp);
+                                      (unsigned long long)(c.top_k - 1), 0.f, !c.topp, codes);
         if (!so.all) {
           kbk = so.kb;
           bounded = true;
@@ -1754,7 +2594,8 @@ __device__ __noinline__ void slow_row(Ctx& c, Smem& s, const SampleArgs& a, cg::
         }
       }
       if (c.topp) {
-        SelOut so = cluster_select<T>(c, s, cluster, kPredSurv, kbk, true, 0ull, c.top_p, true);
+        SelOut so =
+            cluster_select<T>(c, s, cluster, kPredSurv, kbk, true, 0ull, c.top_p, true, codes);
         if (!so.all) {
           bounded = true;
           kb = so.kb;
@@ -1985,11 +2826,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
       s.part.err = 0;
       s.nloc = 0;
       s.gcount = 0;
-      s.rs.bi = rec.bi;
+      s.rs.bi = (int)(rec.bi_topn & 0x7FFFFFFFu);
       s.rs.err = 0;
     }
     c.m_t = rec.m_t;
     c.lnS = rec.lnS;
+    c.xmax = rec.xmax;
     const int hist_len = a.hist_len[row];
     if (p.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0)
       setup_penalties<T>(c, s, a, P, dsm, p.off_bitmap, p.off_prefix, hist_len);
@@ -2008,7 +2850,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
       __syncthreads();
     }
     VT_CTRACE(c, 1);
-    slow_row<T>(c, s, a, cluster, rec.topn_done != 0);
+    const bool topn_done = (rec.bi_topn >> 31) != 0;
+    bool done = false;
+    if (sizeof(T) == 2 && !c.pen && p.staged && p.off_code != 0u)
+      done = code_row<T>(c, s, a, cluster, topn_done, dsm + p.off_code);
+    if (!done) slow_row<T>(c, s, a, cluster, topn_done);
   }
   // The last CTA to finish clears the hand-over counters for the next call.
   __syncthreads();
@@ -2029,7 +2875,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
 // ---------------------------------------------------------------------------
 // host side: plans and launches
 // ---------------------------------------------------------------------------
-LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties) {
+LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties, bool select) {
   LaunchPlan p;
   p.cluster = cluster;
   int slice = (V + cluster - 1) / cluster;
@@ -2038,13 +2884,15 @@ LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties) {
   p.pen_smem = penalties ? 1 : 0;
   const int E = kGroupBytes / elem_size;
   const size_t ngroups = (size_t)slice / E;
-  // [0, 32 KB): the pass-A bulk-copy ring, later the candidate buffer (16 KB)
-  // and the selection histograms (12 KB)
-  size_t off = (size_t)kRingBytes;
+  // Streaming kernel: [0, 32 KB) the pass-A bulk-copy ring, later the
+  // candidate buffer (16 KB).  Selection kernel: [0, 16 KB) the gather buffer,
+  // aliased by the selection histograms (4 x kBins words), then the merged
+  // bins of this CTA's digit range.
+  size_t off = select ? (size_t)kBufCap * 8 : (size_t)kRingBytes;
   p.off_gmax = (uint32_t)off;
   off += (ngroups * 2 + 15) & ~(size_t)15;
   p.off_mrg = (uint32_t)off;
-  if (cluster > 1) off += (size_t)(kBins / cluster) * 20;
+  if (select) off += (size_t)(kCodeSlots / cluster) * 12;
   off = (off + 15) & ~(size_t)15;
   p.off_bitmap = (uint32_t)off;
   p.off_prefix = (uint32_t)off;
@@ -2064,7 +2912,7 @@ LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties) {
 // then (when staged) the slice itself.
 static SelectPlan plan_select_layout(int V, int elem_size, int cluster, bool penalties,
                                      bool staged) {
-  const LaunchPlan q = plan_layout(V, elem_size, cluster, penalties);
+  const LaunchPlan q = plan_layout(V, elem_size, cluster, penalties, true);
   SelectPlan p{};
   p.cluster = cluster;
   p.slice = q.slice;
@@ -2074,6 +2922,11 @@ static SelectPlan plan_select_layout(int V, int elem_size, int cluster, bool pen
   p.off_bitmap = q.off_bitmap;
   p.off_prefix = q.off_prefix;
   size_t off = (q.smem + 127) & ~(size_t)127;
+  p.off_code = 0u;
+  if (elem_size == 2) {  // bf16 code slots: counts and best noise bits
+    p.off_code = (uint32_t)off;
+    off += (size_t)kCodeSlots * 8;
+  }
   p.off_stage = (uint32_t)off;
   p.staged = staged ? 1 : 0;
   if (staged) off += (size_t)q.slice * elem_size;
@@ -2189,7 +3042,7 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
   const size_t max_slice = 256 * 1024, min_slice = 8 * 1024;
   int cmin = 1;
   while (cmin < kMaxCluster && (size_t)((V + cmin - 1) / cmin) * elem_size > max_slice) cmin <<= 1;
-  LaunchPlan best = plan_layout(V, elem_size, cmin, penalties);
+  LaunchPlan best = plan_layout(V, elem_size, cmin, penalties, false);
   if (prepare_sample(best, dtype) != cudaSuccess) return best;
   if ((int64_t)B > best.active_clusters) {  // several waves even so
     best.sel = plan_select(B, V, elem_size, penalties, dtype, best.cluster);
@@ -2197,7 +3050,7 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
   }
   for (int C = cmin * 2; C <= kMaxCluster; C <<= 1) {
     if ((size_t)((V + C - 1) / C) * elem_size < min_slice) break;
-    LaunchPlan p = plan_layout(V, elem_size, C, penalties);
+    LaunchPlan p = plan_layout(V, elem_size, C, penalties, false);
     if (prepare_sample(p, dtype) != cudaSuccess) break;
     if ((int64_t)B > p.active_clusters) break;  // would no longer fit in one wave
     best = p;

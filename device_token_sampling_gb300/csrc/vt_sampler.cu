@@ -165,7 +165,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   if (!cfg || !out) return VT_ERR_INVALID_ARG;
   *out = nullptr;
   if (cfg->max_batch < 1 || cfg->max_batch > (1 << 20) || cfg->max_vocab < 1 ||
-      cfg->max_vocab > (1 << 26) || cfg->max_logprobs < 0 || cfg->max_logprobs > 32 ||
+      cfg->max_vocab > (1 << 20) || cfg->max_logprobs < 0 || cfg->max_logprobs > 32 ||
       cfg->max_history < 0 || cfg->max_history > 32768 || cfg->device < 0)
     return VT_ERR_INVALID_ARG;
   vt_sampler* h = new (std::nothrow) vt_sampler();
@@ -182,7 +182,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return bail(VT_ERR_CUDA);
   if (!(prop.major == 10 && prop.minor == 3)) return bail(VT_ERR_CUDA);  // built for sm_103a only
   // the largest row must fit the shared-memory plan (16 CTAs per row at most)
-  const vt::LaunchPlan worst = vt::plan_layout(cfg->max_vocab, 4, 16, true);
+  const vt::LaunchPlan worst = vt::plan_layout(cfg->max_vocab, 4, 16, true, true);
   if (worst.smem > (size_t)prop.sharedMemPerBlockOptin) return bail(VT_ERR_CAPACITY);
   h->num_sms = prop.multiProcessorCount;
 

@@ -77,7 +77,7 @@ typedef struct vt_sampler vt_sampler; /* opaque handle */
 
 typedef struct vt_sampler_config {
   int32_t max_batch;    /* largest B of any call, >= 1                          */
-  int32_t max_vocab;    /* largest V of any call, >= 1                          */
+  int32_t max_vocab;    /* largest V of any call, 1..1048576                     */
   int32_t max_logprobs; /* largest num_logprobs, 0..32                          */
   int32_t max_history;  /* per-row capacity of the count table in distinct ids,
                            and the largest prompt + output length per row at a
