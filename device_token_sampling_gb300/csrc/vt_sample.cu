@@ -2310,9 +2310,9 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
       return false;
     }
 
-    // ---- pass 2: index-ordered over contiguous group ranges -------------------
-    const int per = (ngroups + kThreads - 1) / kThreads;
-    const int g0 = min(ngroups, tid * per), g1 = min(ngroups, g0 + per);
+    // ---- pass 2: in index order, a round of kThreads consecutive groups at a
+    // time (thread t takes the round's group t), so one block scan per round
+    // ranks the elements of the boundary slot and of the top-n slot ----------
     int pre_b = 0, pre_n = 0;
     for (int r = 0; r < rank; ++r) {
       const unsigned int* hr = cluster.map_shared_rank(hc, r);
@@ -2321,61 +2321,94 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     }
     const int kb_r = bslot >= 0 ? max(0, min(bkp - pre_b, (int)hc[bslot])) : 0;
     const int kn_r = nslot >= 0 ? max(0, min(nkn - pre_n, (int)hc[nslot])) : 0;
-    int cnt_b = 0, cnt_n = 0;
-    if (bslot >= 0 || nslot >= 0) {
-      for (int g = g0; g < g1; ++g) {
-        const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-          if (u == 0xFF80u || lo + g * 16 + e >= hi) continue;
-          int sl = cmax - code16(u);
-          sl = sl < kCatch ? sl : kCatch;
-          cnt_b += sl == bslot;
-          cnt_n += sl == nslot;
-        }
-      }
-    }
-    unsigned long long tb, tn;
-    int rank_b = (int)block_exclusive_u64((unsigned long long)cnt_b, s, &tb);
-    int rank_n = (int)block_exclusive_u64((unsigned long long)cnt_n, s, &tn);
+    const bool need_rank = (draw && bslot >= 0) || (want_topn && nslot >= 0);
     VT_CTRACE(c, 9);
     unsigned long long kbest = 0ull;  // ((bits + 1) << 32) | ~index: kept prefix's best
     int last_j = -1, lastslot_j = -1, cand_j = INT_MAX;
     uint64_t* lg = cluster.map_shared_rank(c.buf, 0);
     int* lcount = cluster.map_shared_rank(&s.gcount, 0);
-    for (int g = g0; g < g1; ++g) {
-      const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    int base_b = 0, base_n = 0;  // elements of those slots in earlier rounds
+    for (int k0 = 0; k0 < ngroups; k0 += kThreads) {
+      const int g = k0 + tid;
+      uint32_t w[8];
+      int sl16[16];
+      int cb = 0, cn = 0;
+      if (g < ngroups) {
+        const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
+        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-        const int j = lo + g * 16 + e;
-        if (u == 0xFF80u || j >= hi) continue;
-        int sl = cmax - code16(u);
-        sl = sl < kCatch ? sl : kCatch;
-        if (sl == bslot) {
-          if (draw && rank_b < kb_r) {
-            const unsigned long long k =
-                ((unsigned long long)(noise_bits(rkey, j) + 1u) << 32) | (0xFFFFFFFFu - (uint32_t)j);
-            kbest = k > kbest ? k : kbest;
-            last_j = j;
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+          int sl = -1;  // -1: -inf or past the row
+          if (u != 0xFF80u && lo + g * 16 + e < hi) {
+            sl = cmax - code16(u);
+            sl = sl < kCatch ? sl : kCatch;
           }
-          ++rank_b;
+          sl16[e] = sl;
+          cb += sl >= 0 && sl == bslot;
+          cn += sl >= 0 && sl == nslot;
         }
-        if (sl == wslot && noise_bits(rkey, j) + 1u == wbits) cand_j = min(cand_j, j);
-        if (sl == lslot) lastslot_j = j;
-        if (want_topn && sl <= nslot) {
-          bool take = true;
-          if (sl == nslot) {
-            take = rank_n < kn_r;
-            ++rank_n;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sl16[e] = -1;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = 0u;
+      }
+      int rb = base_b, rn = base_n;
+      if (need_rank) {
+        // block exclusive scan of (cb, cn), packed into one word
+        const unsigned int v = (unsigned int)cb | ((unsigned int)cn << 16);
+        unsigned int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned int x = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += x;
+        }
+        if (lane == 31) s.ri[warp] = (int)inc;
+        __syncthreads();
+        unsigned int before = 0u, total = 0u;
+        for (int ww = 0; ww < kWarps; ++ww) {
+          const unsigned int t = (unsigned int)s.ri[ww];
+          if (ww < warp) before += t;
+          total += t;
+        }
+        __syncthreads();
+        const unsigned int ex = before + inc - v;
+        rb += (int)(ex & 0xFFFFu);
+        rn += (int)(ex >> 16);
+        base_b += (int)(total & 0xFFFFu);
+        base_n += (int)(total >> 16);
+      }
+      if (g < ngroups) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int sl = sl16[e];
+          if (sl < 0) continue;
+          const int j = lo + g * 16 + e;
+          if (sl == bslot) {
+            if (draw && rb < kb_r) {
+              const unsigned long long k =
+                  ((unsigned long long)(noise_bits(rkey, j) + 1u) << 32) | (0xFFFFFFFFu - (uint32_t)j);
+              kbest = k > kbest ? k : kbest;
+              last_j = j;
+            }
+            ++rb;
           }
-          if (take) {
-            const int pos = atomicAdd(lcount, 1);
-            if (pos < kBufCap)
-              lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)j);
+          if (sl == wslot && noise_bits(rkey, j) + 1u == wbits) cand_j = min(cand_j, j);
+          if (sl == lslot) lastslot_j = j;
+          if (want_topn && sl <= nslot) {
+            bool take = true;
+            if (sl == nslot) {
+              take = rn < kn_r;
+              ++rn;
+            }
+            if (take) {
+              const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+              const int pos = atomicAdd(lcount, 1);
+              if (pos < kBufCap)
+                lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)j);
+            }
           }
         }
       }
