@@ -208,6 +208,7 @@ struct __align__(16) Smem {
   CodeWalk cw;
   int nloc;    // candidates in this CTA's buffer
   int gcount;  // band keys gathered in the leader (selection)
+  int gcount2;  // boundary-slot indices gathered in the leader (code selection)
   int bcast_i[4];
   float bcast_f[4];
   unsigned long long bcast_u[4];
@@ -415,6 +416,10 @@ __device__ unsigned long long block_min_u64(unsigned long long v, Smem& s) {
   const unsigned long long r = s.ru[kWarps];
   __syncthreads();
   return r;
+}
+
+__device__ unsigned long long block_max_u64(unsigned long long v, Smem& s) {
+  return ~block_min_u64(~v, s);
 }
 
 // Exclusive prefix of one u64 per thread over the CTA; *total gets the sum.
@@ -1913,7 +1918,10 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
       s.part.sp_mass[tid] = 0ull;
       s.part.sp_key[tid] = 0ull;
     }
-    if (leader && tid == 0) s.gcount = 0;
+    if (leader && tid == 0) {
+      s.gcount = 0;
+      s.gcount2 = 0;
+    }
     __syncthreads();
     VT_CTRACE(c, 4);
 
@@ -1922,26 +1930,41 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
       const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       const int j0 = lo + g * 16;
-      // SplitMix64 counter of the column pair (j0 + 2q, j0 + 2q + 1)
-      const uint64_t base = rkey + kSeedStep * ((uint64_t)(j0 >> 1) + 1ull);
+      // slots of the 16 elements first (no branches), then the updates
+      int sl[16];
+      unsigned int special = 0u;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint64_t h = draw ? sm64_mix(base + kSeedStep * (uint64_t)q) : 0ull;
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+        const int d = cmax - code16(u);
+        const int v = d < kCatch ? d : kCatch;
+        const bool live = u != 0xFF80u && j0 + e < hi;  // -inf is never a survivor
+        sl[e] = live ? v : -1;
+        special |= (live && (v == tiny || v == kCatch)) ? (1u << e) : 0u;
+      }
+      uint32_t bits[16];
+      if (draw) {
+        // SplitMix64 counter of the column pair (j0 + 2q, j0 + 2q + 1)
+        const uint64_t base = rkey + kSeedStep * ((uint64_t)(j0 >> 1) + 1ull);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t u = e ? (w[q] >> 16) : (w[q] & 0xFFFFu);
-          const uint32_t bits = e ? bits_odd(h) : bits_even(h);
-          const int j = j0 + 2 * q + e;
-          if (u == 0xFF80u || j >= hi) continue;  // -inf is never a survivor
-          int sl = cmax - code16(u);
-          sl = sl < kCatch ? sl : kCatch;
-          if (sl == tiny || sl == kCatch) {
-            code_special(s.part, sl == tiny ? 0 : 1, u, j, bits, inv_t, m_t, minp, lmp, draw);
-          } else {
-            atomicAdd(&hc[sl], 1u);
-            if (draw) atomicMax(&hb[sl], bits + 1u);
-          }
+        for (int q = 0; q < 8; ++q) {
+          const uint64_t h = sm64_mix(base + kSeedStep * (uint64_t)q);
+          bits[2 * q] = bits_even(h);
+          bits[2 * q + 1] = bits_odd(h);
         }
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (sl[e] < 0 || (special >> e) & 1u) continue;
+        atomicAdd(&hc[sl[e]], 1u);
+        if (draw) atomicMax(&hb[sl[e]], bits[e] + 1u);
+      }
+      while (special) {
+        const int e = __ffs(special) - 1;
+        special &= special - 1u;
+        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+        code_special(s.part, sl[e] == tiny ? 0 : 1, u, j0 + e, draw ? bits[e] : 0u, inv_t, m_t,
+                     minp, lmp, draw);
       }
     }
     VT_CTRACE(c, 12);
@@ -2106,7 +2129,8 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         if (run <= tg && run + na > tg) {
           lw->slot_n = sl;
           lw->kn = (int)(tg + 1 - run);
-          if (sl == tiny || sl == kCatch) lw->fallback = 1;
+          // every element up to and including this slot is gathered
+          if (sl == tiny || sl == kCatch || run + na > (unsigned long long)kBufCap) lw->fallback = 1;
         }
         run += na;
       }
@@ -2122,8 +2146,8 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         vals(sl, na, ns, ms);
         if (run <= tg && run + ns > tg) {
           const unsigned int kk = (unsigned int)(tg + 1 - run);
-          if (sl == tiny || sl == kCatch) {
-            lw->fallback = 1;
+          if (sl == tiny || sl == kCatch || na > (unsigned int)kBufCap) {
+            lw->fallback = 1;  // a boundary slot is gathered whole
           } else {
             lw->k_slot = sl;
             lw->k_kept = (int)kk;
@@ -2177,8 +2201,8 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         if (nc == 0u) continue;
         const unsigned long long mc2 = part_mass(sl, nc, ns, ms);
         if (A <= tgt_m && A + mc2 > tgt_m) {
-          if (sl == tiny || sl == kCatch) {
-            lw->fallback = 1;
+          if (sl == tiny || sl == kCatch || na > (unsigned int)kBufCap) {
+            lw->fallback = 1;  // a boundary slot is gathered whole
           } else {
             const unsigned long long kq = (tgt_m - A) / mass_fixed(zq(sl), m_t) + 1ull;
             lw->slot = sl;
@@ -2279,7 +2303,7 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     cluster.sync();  // (w3) range bests visible
     VT_CTRACE(c, 13);
     const int fallback = lw->fallback;
-    const int nslot = lw->slot_n, nkn = lw->kn;
+    const int nslot = lw->slot_n;
     const unsigned long long above = lw->above;
     float wscore = -INFINITY;
     int wslot = -1;
@@ -2310,107 +2334,56 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
       return false;
     }
 
-    // ---- pass 2: in index order, a round of kThreads consecutive groups at a
-    // time (thread t takes the round's group t), so one block scan per round
-    // ranks the elements of the boundary slot and of the top-n slot ----------
-    int pre_b = 0, pre_n = 0;
-    for (int r = 0; r < rank; ++r) {
-      const unsigned int* hr = cluster.map_shared_rank(hc, r);
-      if (bslot >= 0) pre_b += (int)hr[bslot];
-      if (nslot >= 0) pre_n += (int)hr[nslot];
-    }
-    const int kb_r = bslot >= 0 ? max(0, min(bkp - pre_b, (int)hc[bslot])) : 0;
-    const int kn_r = nslot >= 0 ? max(0, min(nkn - pre_n, (int)hc[nslot])) : 0;
-    const bool need_rank = (draw && bslot >= 0) || (want_topn && nslot >= 0);
+    // ---- pass 2: gather the boundary slot's indices and the top-n keys into the
+    // leader; find the winning slot's best element and the last survivor ----------
     VT_CTRACE(c, 9);
-    unsigned long long kbest = 0ull;  // ((bits + 1) << 32) | ~index: kept prefix's best
+    unsigned long long kbest = 0ull;  // filled by the leader from the gathered indices
     int last_j = -1, lastslot_j = -1, cand_j = INT_MAX;
     uint64_t* lg = cluster.map_shared_rank(c.buf, 0);
     int* lcount = cluster.map_shared_rank(&s.gcount, 0);
-    int base_b = 0, base_n = 0;  // elements of those slots in earlier rounds
-    for (int k0 = 0; k0 < ngroups; k0 += kThreads) {
-      const int g = k0 + tid;
-      uint32_t w[8];
-      int sl16[16];
-      int cb = 0, cn = 0;
-      if (g < ngroups) {
-        const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
-        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
-        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    uint64_t* lbnd = cluster.map_shared_rank(reinterpret_cast<uint64_t*>(code_mem), 0);
+    int* lbcount = cluster.map_shared_rank(&s.gcount2, 0);
+    const bool gather_b = draw && bslot >= 0;
+    const int bsel = gather_b ? bslot : -2;  // -2 matches nothing
+    const int nsel = want_topn ? nslot : -2;
+    for (int g = tid; g < ngroups; g += kThreads) {
+      const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const int j0 = lo + g * 16;
+      // match masks of the 16 elements first (no branches), then the rare work
+      unsigned int mb = 0u, mw = 0u, ml = 0u, mn = 0u;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-          int sl = -1;  // -1: -inf or past the row
-          if (u != 0xFF80u && lo + g * 16 + e < hi) {
-            sl = cmax - code16(u);
-            sl = sl < kCatch ? sl : kCatch;
-          }
-          sl16[e] = sl;
-          cb += sl >= 0 && sl == bslot;
-          cn += sl >= 0 && sl == nslot;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sl16[e] = -1;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = 0u;
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+        const int d = cmax - code16(u);
+        const int v = d < kCatch ? d : kCatch;
+        const bool live = u != 0xFF80u && j0 + e < hi;
+        mb |= (live && v == bsel) ? (1u << e) : 0u;
+        mw |= (live && v == wslot) ? (1u << e) : 0u;
+        ml |= (live && v == lslot) ? (1u << e) : 0u;
+        mn |= (live && v <= nsel) ? (1u << e) : 0u;
       }
-      int rb = base_b, rn = base_n;
-      if (need_rank) {
-        // block exclusive scan of (cb, cn), packed into one word
-        const unsigned int v = (unsigned int)cb | ((unsigned int)cn << 16);
-        unsigned int inc = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned int x = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += x;
-        }
-        if (lane == 31) s.ri[warp] = (int)inc;
-        __syncthreads();
-        unsigned int before = 0u, total = 0u;
-        for (int ww = 0; ww < kWarps; ++ww) {
-          const unsigned int t = (unsigned int)s.ri[ww];
-          if (ww < warp) before += t;
-          total += t;
-        }
-        __syncthreads();
-        const unsigned int ex = before + inc - v;
-        rb += (int)(ex & 0xFFFFu);
-        rn += (int)(ex >> 16);
-        base_b += (int)(total & 0xFFFFu);
-        base_n += (int)(total >> 16);
+      if ((mb | mw | ml | mn) == 0u) continue;
+      if (ml) lastslot_j = max(lastslot_j, j0 + 31 - __clz(ml));
+      while (mb) {
+        const int e = __ffs(mb) - 1;
+        mb &= mb - 1u;
+        // descending order of 0xFFFFFFFF - j is ascending index order
+        const int pos = atomicAdd(lbcount, 1);
+        if (pos < kBufCap) lbnd[pos] = (unsigned long long)(0xFFFFFFFFu - (uint32_t)(j0 + e));
       }
-      if (g < ngroups) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int sl = sl16[e];
-          if (sl < 0) continue;
-          const int j = lo + g * 16 + e;
-          if (sl == bslot) {
-            if (draw && rb < kb_r) {
-              const unsigned long long k =
-                  ((unsigned long long)(noise_bits(rkey, j) + 1u) << 32) | (0xFFFFFFFFu - (uint32_t)j);
-              kbest = k > kbest ? k : kbest;
-              last_j = j;
-            }
-            ++rb;
-          }
-          if (sl == wslot && noise_bits(rkey, j) + 1u == wbits) cand_j = min(cand_j, j);
-          if (sl == lslot) lastslot_j = j;
-          if (want_topn && sl <= nslot) {
-            bool take = true;
-            if (sl == nslot) {
-              take = rn < kn_r;
-              ++rn;
-            }
-            if (take) {
-              const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-              const int pos = atomicAdd(lcount, 1);
-              if (pos < kBufCap)
-                lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)j);
-            }
-          }
-        }
+      while (mw) {
+        const int e = __ffs(mw) - 1;
+        mw &= mw - 1u;
+        if (noise_bits(rkey, j0 + e) + 1u == wbits) cand_j = min(cand_j, j0 + e);
+      }
+      while (mn) {
+        const int e = __ffs(mn) - 1;
+        mn &= mn - 1u;
+        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+        const int pos = atomicAdd(lcount, 1);
+        if (pos < kBufCap)
+          lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)(j0 + e));
       }
     }
     // this CTA's results
@@ -2448,6 +2421,26 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
 
     // ---- the leader: draw, outputs -------------------------------------------
     if (leader) {
+      if (gather_b) {
+        // the kept prefix of the boundary slot: its bkp lowest indices
+        uint64_t* bk = reinterpret_cast<uint64_t*>(code_mem);
+        const int nbk = min(s.gcount2, kBufCap);
+        block_sort_desc(bk, nbk);
+        unsigned long long kb = 0ull;
+        for (int t = tid; t < bkp && t < nbk; t += kThreads) {
+          const int j = (int)(0xFFFFFFFFu - (uint32_t)bk[t]);
+          const unsigned long long k =
+              ((unsigned long long)(noise_bits(rkey, j) + 1u) << 32) | (0xFFFFFFFFu - (uint32_t)j);
+          kb = k > kb ? k : kb;
+        }
+        kb = block_max_u64(kb, s);
+        if (tid == 0) {
+          s.part.cb_key = kb;
+          s.part.cb_last = (bkp >= 1 && bkp <= nbk) ? (int)(0xFFFFFFFFu - (uint32_t)bk[bkp - 1]) : -1;
+          if (s.gcount2 > kBufCap || bkp > nbk) s.part.err |= kErrInternal;
+        }
+        __syncthreads();
+      }
       if (want_topn) {
         const int N = min(s.gcount, kBufCap);
         block_sort_desc(c.buf, N);
@@ -2474,10 +2467,10 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         if (draw) {
           unsigned long long cbk = 0ull;
           int cbl = -1, cwj = INT_MAX, lsj = -1;
+          cbk = s.part.cb_key;
+          cbl = s.part.cb_last;
           for (int r = 0; r < C; ++r) {
             const Part* pr = cluster.map_shared_rank(&s.part, r);
-            cbk = pr->cb_key > cbk ? pr->cb_key : cbk;
-            cbl = max(cbl, pr->cb_last);
             cwj = min(cwj, pr->cw_j);
             lsj = max(lsj, pr->last_j);
           }
