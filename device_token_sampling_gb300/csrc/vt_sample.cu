@@ -1909,7 +1909,30 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     const double lmp = c.lmp;
     const int hi = c.hi, lo = c.lo, ngroups = c.ngroups, row = c.row;
     const uint64_t rkey = c.rkey;
+    // the 8 words (16 bf16) of group g: from the staged slice, else from global
+    // memory (a group reaching past the row end reads -inf there)
     const uint4* stage = c.stage;
+    const uint16_t* gsrc = reinterpret_cast<const uint16_t*>(c.rowp) + lo;
+    auto group_words = [&](int g, uint32_t* w) {
+      uint4 v0, v1;
+      if (stage) {
+        v0 = stage[2 * g];
+        v1 = stage[2 * g + 1];
+      } else if (lo + (g + 1) * 16 <= hi) {
+        const uint4* q = reinterpret_cast<const uint4*>(gsrc + g * 16);
+        v0 = __ldg(q);
+        v1 = __ldg(q + 1);
+      } else {
+        uint32_t h[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) h[e] = lo + g * 16 + e < hi ? (uint32_t)__ldg(gsrc + g * 16 + e) : 0xFF80u;
+        v0 = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+        v1 = make_uint4(h[8] | h[9] << 16, h[10] | h[11] << 16, h[12] | h[13] << 16,
+                        h[14] | h[15] << 16);
+      }
+      w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+      w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    };
 
     for (int b = tid; b < 2 * kCodeSlots; b += kThreads) hc[b] = 0u;
     if (tid < 2) {
@@ -1926,9 +1949,10 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     VT_CTRACE(c, 4);
 
     // ---- pass 1: counts and best noise bits per slot --------------------------
-    for (int g = tid; g < ngroups; g += kThreads) {
-      const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const int ngroups_live = min(ngroups, (hi - lo + 15) / 16);  // groups holding row elements
+    for (int g = tid; g < ngroups_live; g += kThreads) {
+      uint32_t w[8];
+      group_words(g, w);
       const int j0 = lo + g * 16;
       // slots of the 16 elements first (no branches), then the updates
       int sl[16];
@@ -2346,9 +2370,9 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     const bool gather_b = draw && bslot >= 0;
     const int bsel = gather_b ? bslot : -2;  // -2 matches nothing
     const int nsel = want_topn ? nslot : -2;
-    for (int g = tid; g < ngroups; g += kThreads) {
-      const uint4 v0 = stage[2 * g], v1 = stage[2 * g + 1];
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    for (int g = tid; g < ngroups_live; g += kThreads) {
+      uint32_t w[8];
+      group_words(g, w);
       const int j0 = lo + g * 16;
       // match masks of the 16 elements first (no branches), then the rare work
       unsigned int mb = 0u, mw = 0u, ml = 0u, mn = 0u;
@@ -2862,25 +2886,29 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
     if (p.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0)
       setup_penalties<T>(c, s, a, P, dsm, p.off_bitmap, p.off_prefix, hist_len);
     VT_CTRACE(c, 5);
-    if (p.staged) {
-      stage_slice<T>(c, dsm + p.off_stage);
-    } else {
-      for (int g = c.tid; g < c.ngroups; g += kThreads) {
-        float x[Elt<T>::E];
-        load_group<T>(c, g, x);
-        float gm = x[0];
-#pragma unroll
-        for (int q = 1; q < Elt<T>::E; ++q) gm = fmaxf(gm, x[q]);
-        c.gmax[g] = bf16_down(gm);
-      }
-      __syncthreads();
-    }
+    // bf16 rows without penalties take the code selection, from the staged slice
+    // or straight from (aligned) global memory; the rest, or a row the code
+    // selection gives back, the generic selection over group maxima
+    const bool codes = sizeof(T) == 2 && !c.pen && p.off_code != 0u && (p.staged || c.aligned);
+    if (p.staged) stage_slice<T>(c, dsm + p.off_stage);
     VT_CTRACE(c, 1);
     const bool topn_done = (rec.bi_topn >> 31) != 0;
     bool done = false;
-    if (sizeof(T) == 2 && !c.pen && p.staged && p.off_code != 0u)
-      done = code_row<T>(c, s, a, cluster, topn_done, dsm + p.off_code);
-    if (!done) slow_row<T>(c, s, a, cluster, topn_done);
+    if (codes) done = code_row<T>(c, s, a, cluster, topn_done, dsm + p.off_code);
+    if (!done) {
+      if (!p.staged) {
+        for (int g = c.tid; g < c.ngroups; g += kThreads) {
+          float x[Elt<T>::E];
+          load_group<T>(c, g, x);
+          float gm = x[0];
+#pragma unroll
+          for (int q = 1; q < Elt<T>::E; ++q) gm = fmaxf(gm, x[q]);
+          c.gmax[g] = bf16_down(gm);
+        }
+        __syncthreads();
+      }
+      slow_row<T>(c, s, a, cluster, topn_done);
+    }
   }
   // The last CTA to finish clears the hand-over counters for the next call.
   __syncthreads();
@@ -3046,9 +3074,18 @@ cudaError_t prepare_sample(LaunchPlan& plan, int dtype) {
 static SelectPlan plan_select(int B, int V, int elem_size, bool penalties, int dtype,
                               int kernel1_cluster) {
   int C = kMaxCluster;
-  while (C > 1 && (V + C - 1) / C < 16384) C >>= 1;
-  while (C < kMaxCluster && (size_t)((V + C - 1) / C) * elem_size > 96 * 1024) C <<= 1;
-  const bool staged = (size_t)((V + C - 1) / C + 31) * elem_size <= 96 * 1024;
+  bool staged;
+  if (elem_size == 2) {
+    // bf16: the code selection reads each slice twice from global memory, so
+    // no staging; slices of at least 32K elements keep the cluster small and
+    // many clusters resident
+    while (C > 1 && (V + C - 1) / C < 32768) C >>= 1;
+    staged = false;
+  } else {
+    while (C > 1 && (V + C - 1) / C < 16384) C >>= 1;
+    while (C < kMaxCluster && (size_t)((V + C - 1) / C) * elem_size > 96 * 1024) C <<= 1;
+    staged = (size_t)((V + C - 1) / C + 31) * elem_size <= 96 * 1024;
+  }
   SelectPlan p = plan_select_layout(V, elem_size, C, penalties, staged);
   p.kernel1_cluster = kernel1_cluster;
   const cudaError_t e = dtype == 0 ? prepare_select_one<float>(p) : prepare_select_one<uint16_t>(p);
