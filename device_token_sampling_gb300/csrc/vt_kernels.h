@@ -19,9 +19,11 @@ struct __align__(16) SlowRow {
 
 // Everything one sampling launch needs.  Device pointers unless noted.
 struct SampleArgs {
-  const void* logits;        // [B][ld] elements
+  const void* logits;        // [rows][ld] elements
   int64_t ld;                // row stride in elements
-  int32_t B, V;
+  int32_t B, V;              // B: rows of this launch (the grid is B * cluster CTAs)
+  const int32_t* rows;       // [B] the rows of this launch, or null for rows 0..B-1
+  int32_t early;             // hand every row over after its statistics
   int32_t n_logprobs;
   int32_t update_counts;
   int32_t slice;             // elements per CTA (multiple of 32)

@@ -250,11 +250,9 @@ struct Ctx {
   } while (0)
 
 // Optional phase trace: thread 0 stamps the global timer into slot k.
-#define VT_TRACE(k)                                                        \
-  do {                                                                     \
-    if (a.trace && threadIdx.x == 0)                                       \
-      a.trace[(size_t)blockIdx.x * kTraceSlots + (k)] = global_timer_ns(); \
-  } while (0)
+// Phase stamp of the streaming kernel (slot k of this CTA's trace, laid out
+// by row and rank).
+#define VT_TRACE(k) VT_CTRACE(c, k)
 
 // ---------------------------------------------------------------------------
 // loading one 32-byte group of the slice into registers
@@ -1318,9 +1316,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
 
   Ctx c;
   const int C = (int)cluster_nctarank();
-  const RowParams P = init_row<T>(c, a, dsm, blockIdx.x / C, C, (int)cluster_ctarank(), a.slice,
+  const int row = a.rows ? a.rows[blockIdx.x / C] : (int)(blockIdx.x / C);
+  const RowParams P = init_row<T>(c, a, dsm, row, C, (int)cluster_ctarank(), a.slice,
                                   a.off_gmax, a.off_mrg);
-  c.trace = a.trace ? a.trace + (size_t)blockIdx.x * kTraceSlots : nullptr;
+  c.trace = a.trace ? a.trace + ((size_t)row * C + c.rank) * kTraceSlots : nullptr;
   const int n = a.n_logprobs;
   const int hist_len = a.hist_len[c.row];
   VT_TRACE(0);
@@ -1481,7 +1480,9 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     // This CTA's candidate thresholds: at least Kc of its elements are >= them.
     // Up to kThreads, the Kc-th largest thread maximum; beyond, a two-round
     // radix select over the bf16 lower bounds of the group maxima.
-    const int Kc = (K_main + c.C - 1) / c.C, Kn = (n + c.C - 1) / c.C;
+    // (rows handed over after their statistics need no thresholds)
+    const int Kc = a.early ? 0 : (K_main + c.C - 1) / c.C;
+    const int Kn = a.early ? 0 : (n + c.C - 1) / c.C;
     if (c.tid == 0) {
       s.part.tau = INFINITY;
       s.part.tau_n = INFINITY;
@@ -1647,6 +1648,23 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
         if (s.rs.err) atomicOr(a.err_word, s.rs.err);
       }
     }
+    return;
+  }
+
+  // ---- rows routed to the selection kernel: hand over after the statistics ----
+  if (a.early) {
+    cluster.sync();  // every CTA has read the others' pass-A partials
+    if (leader && c.tid == 0) {
+      SlowRow r;
+      r.m_t = c.m_t;
+      r.lnS = c.lnS;
+      r.xmax = s.rs.bv;
+      r.bi_topn = (uint32_t)s.rs.bi | (n == 0 ? 0x80000000u : 0u);
+      a.slow[c.row] = r;
+      a.slow_list[atomicAdd(a.slow_ctl, 1u)] = c.row;
+      if (s.rs.err) atomicOr(a.err_word, s.rs.err);
+    }
+    VT_TRACE(15);
     return;
   }
 

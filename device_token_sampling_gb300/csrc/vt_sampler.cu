@@ -40,14 +40,21 @@ struct vt_sampler {
   int32_t* d_kept = nullptr;
   int32_t* d_err = nullptr;
   vt::SlowRow* d_slow = nullptr;  // rows handed from the streaming to the selection kernel
-  int32_t* d_slow_list = nullptr;
-  uint32_t* d_slow_ctl = nullptr;
+  int32_t* d_slow_list = nullptr;  // [2][max_batch]: one list per launch pair
+  uint32_t* d_slow_ctl = nullptr;  // [2][4]
+  int32_t* d_rows = nullptr;       // [max_batch]: main rows, then side rows
+  // the side stream: rows routed straight to the selection kernel run there,
+  // beside the main stream's launches (fork and join through events)
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  int n_main = 0, n_side = 0;
   // pinned host staging
   vt::RowParams* h_params = nullptr;
   uint64_t* h_seeds = nullptr;
   int32_t* h_raw = nullptr;
   int64_t* h_raw_offs = nullptr;
   int32_t* h_err = nullptr;
+  int32_t* h_rows = nullptr;
   cudaEvent_t ev_params = nullptr, ev_counts = nullptr;
   bool params_pending = false, counts_pending = false;
   // staging for vt_sample_host
@@ -127,6 +134,11 @@ void free_all(vt_sampler* h) {
   dfree(h->d_slow);
   dfree(h->d_slow_list);
   dfree(h->d_slow_ctl);
+  dfree(h->d_rows);
+  if (h->h_rows) cudaFreeHost(h->h_rows);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
   dfree(h->d_io_logits);
   dfree(h->d_io_tokens);
   dfree(h->d_io_lp);
@@ -142,6 +154,7 @@ void free_all(vt_sampler* h) {
 }
 
 bool finite(float x) { return std::isfinite(x); }
+
 
 }  // namespace
 
@@ -209,8 +222,10 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_kept, B * sizeof(int32_t));
   dal((void**)&h->d_err, sizeof(int32_t));
   dal((void**)&h->d_slow, B * sizeof(vt::SlowRow));
-  dal((void**)&h->d_slow_list, B * sizeof(int32_t));
-  dal((void**)&h->d_slow_ctl, 4 * sizeof(uint32_t));
+  dal((void**)&h->d_slow_list, 2 * B * sizeof(int32_t));
+  dal((void**)&h->d_slow_ctl, 8 * sizeof(uint32_t));
+  dal((void**)&h->d_rows, B * sizeof(int32_t));
+  hal((void**)&h->h_rows, B * sizeof(int32_t));
   hal((void**)&h->h_params, B * sizeof(vt::RowParams));
   hal((void**)&h->h_seeds, B * sizeof(uint64_t));
   hal((void**)&h->h_raw, B * H * sizeof(int32_t));
@@ -226,11 +241,14 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   }
   if (!ok) return bail(VT_ERR_CUDA);
   if (cudaEventCreateWithFlags(&h->ev_params, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->ev_counts, cudaEventDisableTiming) != cudaSuccess)
+      cudaEventCreateWithFlags(&h->ev_counts, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
     return bail(VT_ERR_CUDA);
   if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(int32_t)) != cudaSuccess ||
-      cudaMemset(h->d_slow_ctl, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_slow_ctl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_seeds, 0, B * sizeof(uint64_t)) != cudaSuccess ||
       cudaMemset(h->d_status, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
@@ -304,9 +322,26 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
     h->h_seeds[r] = seed[r];
     h->row_flags[r] = rp.flags;
   }
+  // Route the rows that will most likely need selection straight to the
+  // selection kernel: sampled top-p rows without top-k and without penalties
+  // (their nucleus is usually far beyond what one candidate pass gathers).
+  // Used for bf16 calls over all B rows; main rows first, then side rows.
+  auto to_side = [&](int r) {
+    const uint32_t f = h->row_flags[r];
+    return !(f & vt::kRowGreedy) && !(f & vt::kRowPenalty) && (f & vt::kRowTopP) && top_k[r] <= 1;
+  };
+  int nm = 0, ns = 0;
+  for (int r = 0; r < B; ++r)
+    if (!to_side(r)) h->h_rows[nm++] = r;
+  for (int r = 0; r < B; ++r)
+    if (to_side(r)) h->h_rows[nm + ns++] = r;
+  h->n_main = nm;
+  h->n_side = ns;
   VT_CK(h, cudaMemcpyAsync(h->d_params, h->h_params, (size_t)B * sizeof(vt::RowParams),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_seeds, h->h_seeds, (size_t)B * sizeof(uint64_t),
+                           cudaMemcpyHostToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(h->d_rows, h->h_rows, (size_t)B * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaEventRecord(h->ev_params, st));
   h->params_pending = true;
@@ -406,52 +441,86 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
   const int es = dtype == VT_DTYPE_F32 ? 4 : 2;
   bool any_pen = false;
   for (int r = 0; r < B && !any_pen; ++r) any_pen = (h->row_flags[r] & vt::kRowPenalty) != 0;
-  auto key = std::make_pair(std::make_pair(B, V), std::make_pair(dtype, any_pen ? 1 : 0));
-  auto it = h->plans.find(key);
-  if (it == h->plans.end()) {
-    vt::LaunchPlan plan = vt::plan_sample(B, V, es, any_pen, dtype, h->num_sms);
-    const cudaError_t e = vt::prepare_sample(plan, dtype);
-    if (e != cudaSuccess)
-      return set_err(h, VT_ERR_CUDA, "cannot prepare a %d-CTA cluster plan: %s", plan.cluster,
-                     cudaGetErrorString(e));
-    it = h->plans.emplace(key, plan).first;
+  auto get_plan = [&](int rows, const vt::LaunchPlan** out) -> int {
+    auto key = std::make_pair(std::make_pair(rows, V), std::make_pair(dtype, any_pen ? 1 : 0));
+    auto it = h->plans.find(key);
+    if (it == h->plans.end()) {
+      vt::LaunchPlan plan = vt::plan_sample(rows, V, es, any_pen, dtype, h->num_sms);
+      const cudaError_t e = vt::prepare_sample(plan, dtype);
+      if (e != cudaSuccess)
+        return set_err(h, VT_ERR_CUDA, "cannot prepare a %d-CTA cluster plan: %s", plan.cluster,
+                       cudaGetErrorString(e));
+      it = h->plans.emplace(key, plan).first;
+    }
+    *out = &it->second;
+    return VT_OK;
+  };
+  auto make_args = [&](const vt::LaunchPlan& plan, int rows, const int32_t* row_list, int early,
+                       int pair) {
+    vt::SampleArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.logits = logits;
+    a.ld = ld;
+    a.B = rows;
+    a.V = V;
+    a.rows = row_list;
+    a.early = early;
+    a.n_logprobs = n;
+    a.update_counts = update_counts ? 1 : 0;
+    a.slice = plan.slice;
+    a.aligned = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
+    a.pen_smem = plan.pen_smem;
+    a.off_gmax = plan.off_gmax;
+    a.off_mrg = plan.off_mrg;
+    a.off_bitmap = plan.off_bitmap;
+    a.off_prefix = plan.off_prefix;
+    a.params = h->d_params;
+    a.seeds = h->d_seeds;
+    a.hist = h->d_hist;
+    a.hist_len = h->d_hist_len;
+    a.hist_cap = h->cfg.max_history > 0 ? h->cfg.max_history : 1;
+    a.zside = h->d_zside;
+    a.out_tokens = out_tokens;
+    a.out_logprobs = out_logprobs;
+    a.out_topk_ids = out_topk_ids;
+    a.out_topk_logprobs = out_topk_logprobs;
+    a.row_status = h->d_status;
+    a.dbg_kth_value = h->d_kth_v;
+    a.dbg_kth_index = h->d_kth_i;
+    a.dbg_kept = h->d_kept;
+    a.err_word = h->d_err;
+    a.slow = h->d_slow;
+    a.slow_list = h->d_slow_list + (size_t)pair * h->cfg.max_batch;
+    a.slow_ctl = h->d_slow_ctl + 4 * pair;
+    // the phase trace is laid out by row (B rows of `plan.cluster` CTAs)
+    a.trace = (h->trace && (int64_t)B * plan.cluster <= h->trace_ctas) ? h->trace : nullptr;
+    a.trace_ctas = a.trace ? h->trace_ctas : 0;
+    return a;
+  };
+  // bf16 calls over every row split the rows between the two streams
+  const bool split = dtype == VT_DTYPE_BF16 && B == h->params_B && h->n_side > 0 && h->n_main > 0;
+  if (!split) {
+    const vt::LaunchPlan* plan = nullptr;
+    const int rc = get_plan(B, &plan);
+    if (rc != VT_OK) return rc;
+    const vt::SampleArgs a = make_args(*plan, B, nullptr, 0, 0);
+    VT_CK(h, vt::launch_sample(a, *plan, dtype, st, h->phase_event));
+  } else {
+    // both launches keep the whole batch's slices, so that every row's sums
+    // (and so its results) do not depend on how the rows are split
+    const vt::LaunchPlan* pm = nullptr;
+    const int rc = get_plan(B, &pm);
+    if (rc != VT_OK) return rc;
+    const vt::LaunchPlan* ps = pm;
+    const vt::SampleArgs am = make_args(*pm, h->n_main, h->d_rows, 0, 0);
+    const vt::SampleArgs as = make_args(*ps, h->n_side, h->d_rows + h->n_main, 1, 1);
+    VT_CK(h, cudaEventRecord(h->ev_fork, st));
+    VT_CK(h, cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+    VT_CK(h, vt::launch_sample(as, *ps, dtype, h->side, nullptr));
+    VT_CK(h, vt::launch_sample(am, *pm, dtype, st, h->phase_event));
+    VT_CK(h, cudaEventRecord(h->ev_join, h->side));
+    VT_CK(h, cudaStreamWaitEvent(st, h->ev_join, 0));
   }
-  const vt::LaunchPlan& plan = it->second;
-  vt::SampleArgs a;
-  a.logits = logits;
-  a.ld = ld;
-  a.B = B;
-  a.V = V;
-  a.n_logprobs = n;
-  a.update_counts = update_counts ? 1 : 0;
-  a.slice = plan.slice;
-  a.aligned = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
-  a.pen_smem = plan.pen_smem;
-  a.off_gmax = plan.off_gmax;
-  a.off_mrg = plan.off_mrg;
-  a.off_bitmap = plan.off_bitmap;
-  a.off_prefix = plan.off_prefix;
-  a.params = h->d_params;
-  a.seeds = h->d_seeds;
-  a.hist = h->d_hist;
-  a.hist_len = h->d_hist_len;
-  a.hist_cap = h->cfg.max_history > 0 ? h->cfg.max_history : 1;
-  a.zside = h->d_zside;
-  a.out_tokens = out_tokens;
-  a.out_logprobs = out_logprobs;
-  a.out_topk_ids = out_topk_ids;
-  a.out_topk_logprobs = out_topk_logprobs;
-  a.row_status = h->d_status;
-  a.dbg_kth_value = h->d_kth_v;
-  a.dbg_kth_index = h->d_kth_i;
-  a.dbg_kept = h->d_kept;
-  a.err_word = h->d_err;
-  a.slow = h->d_slow;
-  a.slow_list = h->d_slow_list;
-  a.slow_ctl = h->d_slow_ctl;
-  a.trace = (h->trace && (int64_t)B * plan.cluster <= h->trace_ctas) ? h->trace : nullptr;
-  a.trace_ctas = a.trace ? h->trace_ctas : 0;
-  VT_CK(h, vt::launch_sample(a, plan, dtype, st, h->phase_event));
   h->last_B = B;
   h->last_stream = st;
   h->err.clear();
@@ -574,9 +643,9 @@ int vt_debug_last_handover(vt_sampler* h, int32_t* rows) {
   if (!h || !rows) return VT_ERR_INVALID_ARG;
   DeviceGuard guard(h->cfg.device);
   VT_CK(h, cudaStreamSynchronize(h->last_stream));
-  uint32_t v = 0;
-  VT_CK(h, cudaMemcpy(&v, h->d_slow_ctl + 2, sizeof v, cudaMemcpyDeviceToHost));
-  *rows = (int32_t)v;
+  uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  VT_CK(h, cudaMemcpy(v, h->d_slow_ctl, sizeof v, cudaMemcpyDeviceToHost));
+  *rows = (int32_t)(v[2] + v[6]);
   return VT_OK;
 }
 
