@@ -98,14 +98,14 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    """DRAM bytes of one step (all its launches) from the committed ncu summary,
+    if it was taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", f"vt_sample_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_h = re.search(r"source_hash:\s*([0-9a-f]+)", text)
-    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    m_t = re.search(r"dram_bytes_per_step:\s*([0-9]+)", text)
     if not m_h or not m_t or m_h.group(1) != kernel_source_hash():
         return None
     return int(m_t.group(1))
@@ -316,6 +316,7 @@ def run_gpu(args, w: W.Workload):
     elapsed_ms = ev0.elapsed_time(ev1)
     s.check_device_errors()
     handed = s.last_handover()
+    launches_per_step = s.last_launches()
 
     # the two launches of a step timed apart: events on the launching stream
     # before the step, between its launches (recorded by the library) and after
@@ -370,15 +371,13 @@ def run_gpu(args, w: W.Workload):
         peak, peak_kind = load_peaks()
         per_row = algorithmic_bytes_per_row(w)
         alg = int(per_row.sum())
-        # the dominant launch: the streaming kernel reads every row once; the
-        # selection kernel re-reads the rows handed to it
-        if k1_ms >= k2_ms:
-            kernel, kernel_ms, kbytes = "sample_kernel", k1_ms, alg
-            traffic = profiled_traffic(w.name)
-        else:
-            kernel, kernel_ms = "select_kernel", k2_ms
-            kbytes = int(handed * w.V * w.elem_size)
-            traffic = None
+        # A step is one vt_sample: the streaming kernel over every row and the
+        # selection kernel over the rows handed to it, on the caller's stream and
+        # (bf16 batches with top-p-only rows) a second stream beside it.  The
+        # launches overlap, so the roofline is taken over the whole step: the
+        # step's algorithmic bytes over its device time.
+        kernel, kernel_ms, kbytes = "vt_sample step (sample_kernel + select_kernel)", ms_per_step, alg
+        traffic = profiled_traffic(w.name)
         achieved = kbytes / (kernel_ms * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -388,16 +387,15 @@ def run_gpu(args, w: W.Workload):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} (hbm_gbs)",
-                         "algorithmic_bytes_per_launch": kbytes, "kernel": kernel,
+                         "algorithmic_bytes_per_step": kbytes, "kernel": kernel,
                          "kernel_ms": kernel_ms},
-            "launch_split_ms": {"sample_kernel": k1_ms, "select_kernel": k2_ms,
-                                "rows_handed_to_select_kernel": handed,
-                                "step_bytes_over_step_time_gbs":
-                                    alg / (ms_per_step * 1e-3) / 1e9},
+            "launch_split_ms": {"to_end_of_main_sample_kernel": k1_ms,
+                                "rest_of_step": k2_ms,
+                                "rows_handed_to_select_kernel": handed},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "api": "vt_sample_host (pinned host logits in, host outputs back)"},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
             "ns_per_row": 1e6 * ms_per_step / B,
         }

@@ -48,6 +48,7 @@ struct vt_sampler {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int n_main = 0, n_side = 0;
+  int last_launches = 0;  // kernels the last vt_sample launched
   // pinned host staging
   vt::RowParams* h_params = nullptr;
   uint64_t* h_seeds = nullptr;
@@ -505,6 +506,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     if (rc != VT_OK) return rc;
     const vt::SampleArgs a = make_args(*plan, B, nullptr, 0, 0);
     VT_CK(h, vt::launch_sample(a, *plan, dtype, st, h->phase_event));
+    h->last_launches = 2;
   } else {
     // both launches keep the whole batch's slices, so that every row's sums
     // (and so its results) do not depend on how the rows are split
@@ -520,6 +522,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     VT_CK(h, vt::launch_sample(am, *pm, dtype, st, h->phase_event));
     VT_CK(h, cudaEventRecord(h->ev_join, h->side));
     VT_CK(h, cudaStreamWaitEvent(st, h->ev_join, 0));
+    h->last_launches = 4;
   }
   h->last_B = B;
   h->last_stream = st;
@@ -646,6 +649,12 @@ int vt_debug_last_handover(vt_sampler* h, int32_t* rows) {
   uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   VT_CK(h, cudaMemcpy(v, h->d_slow_ctl, sizeof v, cudaMemcpyDeviceToHost));
   *rows = (int32_t)(v[2] + v[6]);
+  return VT_OK;
+}
+
+int vt_debug_last_launches(vt_sampler* h, int32_t* launches) {
+  if (!h || !launches) return VT_ERR_INVALID_ARG;
+  *launches = h->last_launches;
   return VT_OK;
 }
 

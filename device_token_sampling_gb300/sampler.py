@@ -70,6 +70,7 @@ SIGNATURES = {
     "vt_debug_launch_shape": (C.c_int, [P, I32, I32, P, P, P]),
     "vt_debug_set_phase_event": (C.c_int, [P, P]),
     "vt_debug_last_handover": (C.c_int, [P, P]),
+    "vt_debug_last_launches": (C.c_int, [P, P]),
     "vt_sample_noalloc": (C.c_int, [I32, P, I32, I32, I32, I64, P, P, P, P, P, I32, P, P, P, P,
                                     P, I32, P, C.c_char_p, I32]),
     "vt_last_error": (C.c_char_p, [P]),
@@ -318,6 +319,13 @@ class Sampler:
         """Rows the last ``sample`` handed to the selection kernel."""
         v = C.c_int32()
         self._check(self._lib.vt_debug_last_handover(self._h, C.byref(v)), "vt_debug_last_handover")
+        return int(v.value)
+
+    def last_launches(self) -> int:
+        """Kernels the last ``sample`` launched (2, or 4 when its rows were split
+        between the two streams)."""
+        v = C.c_int32()
+        self._check(self._lib.vt_debug_last_launches(self._h, C.byref(v)), "vt_debug_last_launches")
         return int(v.value)
 
     def seeds(self, B: int):

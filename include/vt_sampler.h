@@ -213,6 +213,12 @@ int vt_debug_set_phase_event(vt_sampler* handle, void* event);
  * in one pass could not settle).  Synchronises the handle's last stream. */
 int vt_debug_last_handover(vt_sampler* handle, int32_t* rows);
 
+/* Debug: how many kernels the last vt_sample launched: 2 on one stream (the
+ * streaming kernel, then the selection kernel), or 4 when the call split its
+ * rows between the handle's two streams (a pair on each).  0 before the first
+ * call.  Does not synchronise. */
+int vt_debug_last_launches(vt_sampler* handle, int32_t* launches);
+
 /* Read the current per-row seeds of rows 0..B-1 into a host array (B of the
  * last vt_reset_params).  Synchronises the handle's last stream. */
 int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
