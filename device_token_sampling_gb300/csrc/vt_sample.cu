@@ -1307,6 +1307,101 @@ __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowP
 // ---------------------------------------------------------------------------
 // kernel 1: stream every row once; finish the rows its candidates can finish
 // ---------------------------------------------------------------------------
+// This CTA's candidate thresholds (s.part.tau for the kept set, s.part.tau_n
+// for the top-n): at least Kc (Kn) of its elements are >= them.  Up to
+// kThreads, the Kc-th largest thread maximum (s.tmax); beyond, a two-round
+// radix select over the bf16 lower bounds of the group maxima.  bv is the
+// CTA's maximum.  All threads of the CTA call it.
+__device__ __noinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int Kn, float bv) {
+  if (c.tid == 0) {
+    s.part.tau = INFINITY;
+    s.part.tau_n = INFINITY;
+  }
+  __syncthreads();
+  if ((Kc > 0 && Kc <= kSmallK) || Kn > 0) {
+    const float v = s.tmax[c.tid];
+    int rank = 0;
+    const float4* t4 = reinterpret_cast<const float4*>(s.tmax);
+#pragma unroll 4
+    for (int u = 0; u < kThreads / 4; ++u) {
+      const float4 w = t4[u];
+      const int b = 4 * u;
+      rank += (w.x > v) || (w.x == v && b < c.tid);
+      rank += (w.y > v) || (w.y == v && b + 1 < c.tid);
+      rank += (w.z > v) || (w.z == v && b + 2 < c.tid);
+      rank += (w.w > v) || (w.w == v && b + 3 < c.tid);
+    }
+    if (Kc > 0 && Kc <= kSmallK && rank == Kc - 1) s.part.tau = v;
+    if (Kn > 0 && rank == Kn - 1) s.part.tau_n = v;
+  }
+  if (Kc > kSmallK) {
+    if (Kc > c.ngroups || bv == -INFINITY) {
+      if (c.tid == 0) s.part.tau = -INFINITY;
+    } else {
+      // The Kc-th largest group-maximum lower bound, exactly: a two-round
+      // radix select over the order-preserving 16-bit keys of the bf16
+      // values (high byte, then low byte inside the chosen high byte).
+      auto gkey = [&](int g) -> uint32_t {
+        const uint32_t u = c.gmax[g];
+        return (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u);
+      };
+      uint32_t above = 0u;  // groups whose key is above the chosen prefix
+      int hi_byte = 0;
+      for (int round = 0; round < 2; ++round) {
+        s.hist256[c.tid] = 0u;
+        __syncthreads();
+        for (int g = c.tid; g < c.ngroups; g += kThreads) {
+          const uint32_t k = gkey(g);
+          if (round == 1 && (int)(k >> 8) != hi_byte) continue;
+          const uint32_t bin = round == 0 ? (k >> 8) : (k & 0xFFu);
+          // lanes with the same bin add once (most keys share a few high bytes)
+          const uint32_t peers = __match_any_sync(__activemask(), bin);
+          if ((peers & ((1u << c.lane) - 1u)) == 0u) atomicAdd(&s.hist256[bin], __popc(peers));
+        }
+        __syncthreads();
+        if (c.warp == 0) {
+          // lane l holds bins 255-8l .. 248-8l (descending)
+          uint32_t cnt[8], tot = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            cnt[q] = s.hist256[255 - 8 * c.lane - q];
+            tot += cnt[q];
+          }
+          uint32_t inc = tot;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t w = __shfl_up_sync(0xffffffffu, inc, o);
+            if (c.lane >= o) inc += w;
+          }
+          const uint32_t before = above + inc - tot;
+          if (before < (uint32_t)Kc && above + inc >= (uint32_t)Kc) {
+            uint32_t run = before;
+            for (int q = 0; q < 8; ++q) {
+              if (run + cnt[q] >= (uint32_t)Kc) {
+                s.bcast_i[2] = 255 - 8 * c.lane - q;
+                s.bcast_i[3] = (int)run;
+                break;
+              }
+              run += cnt[q];
+            }
+          }
+        }
+        __syncthreads();
+        const int bsel = s.bcast_i[2];
+        above = (uint32_t)s.bcast_i[3];
+        if (round == 0) {
+          hi_byte = bsel;
+        } else if (c.tid == 0) {
+          const uint32_t k = ((uint32_t)hi_byte << 8) | (uint32_t)bsel;
+          const uint32_t u = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+          s.part.tau = bf16_val((uint16_t)u);
+        }
+        __syncthreads();  // the histogram is cleared again only after every read
+      }
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];
@@ -1477,90 +1572,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     float dz = 0.f;
     block_argmax(bv, bi, dz, s);  // also a barrier: s.tmax is complete after it
     const int nf = __syncthreads_or(nonfin);
-    // This CTA's candidate thresholds: at least Kc of its elements are >= them.
-    // Up to kThreads, the Kc-th largest thread maximum; beyond, a two-round
-    // radix select over the bf16 lower bounds of the group maxima.
-    // (rows handed over after their statistics need no thresholds)
+    // (rows handed over after their statistics take no thresholds here)
     const int Kc = a.early ? 0 : (K_main + c.C - 1) / c.C;
     const int Kn = a.early ? 0 : (n + c.C - 1) / c.C;
-    if (c.tid == 0) {
-      s.part.tau = INFINITY;
-      s.part.tau_n = INFINITY;
-    }
-    __syncthreads();
-    if ((Kc > 0 && Kc <= kSmallK) || Kn > 0) {
-      const float v = s.tmax[c.tid];
-      int rank = 0;
-      const float4* t4 = reinterpret_cast<const float4*>(s.tmax);
-#pragma unroll 4
-      for (int u = 0; u < kThreads / 4; ++u) {
-        const float4 w = t4[u];
-        const int b = 4 * u;
-        rank += (w.x > v) || (w.x == v && b < c.tid);
-        rank += (w.y > v) || (w.y == v && b + 1 < c.tid);
-        rank += (w.z > v) || (w.z == v && b + 2 < c.tid);
-        rank += (w.w > v) || (w.w == v && b + 3 < c.tid);
-      }
-      if (Kc > 0 && Kc <= kSmallK && rank == Kc - 1) s.part.tau = v;
-      if (Kn > 0 && rank == Kn - 1) s.part.tau_n = v;
-    }
-    if (Kc > kSmallK) {
-      if (Kc > c.ngroups || bv == -INFINITY) {
-        if (c.tid == 0) s.part.tau = -INFINITY;
-      } else {
-        // bins of 1/16 (tempered units) below this CTA's max: the first bin
-        // where the count of group maxima reaches Kc, then the smallest group
-        // maximum inside it and above (an exact lower bound)
-        const float scale = 16.0f * c.inv_t;
-        auto gbin = [&](int g) {
-          const float d = __fmul_rn(__fsub_rn(bv, bf16_val(c.gmax[g])), scale);
-          return d < 255.0f ? (int)d : 255;
-        };
-        s.hist256[c.tid] = 0u;
-        __syncthreads();
-        for (int g = c.tid; g < c.ngroups; g += kThreads) atomicAdd(&s.hist256[gbin(g)], 1u);
-        __syncthreads();
-        if (c.warp == 0) {
-          uint32_t cnt[8], tot = 0;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            cnt[q] = s.hist256[8 * c.lane + q];
-            tot += cnt[q];
-          }
-          uint32_t inc = tot;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t w = __shfl_up_sync(0xffffffffu, inc, o);
-            if (c.lane >= o) inc += w;
-          }
-          const uint32_t before = inc - tot;
-          if (before < (uint32_t)Kc && inc >= (uint32_t)Kc) {
-            uint32_t run = before;
-            for (int q = 0; q < 8; ++q) {
-              run += cnt[q];
-              if (run >= (uint32_t)Kc) {
-                s.bcast_i[2] = 8 * c.lane + q;
-                break;
-              }
-            }
-          }
-        }
-        __syncthreads();
-        const int bsel = s.bcast_i[2];
-        float mn = INFINITY;
-        for (int g = c.tid; g < c.ngroups; g += kThreads)
-          if (gbin(g) <= bsel) mn = fminf(mn, bf16_val(c.gmax[g]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        if (c.lane == 0) s.rf[2 * kWarps + 2 + c.warp] = mn;
-        __syncthreads();
-        if (c.tid == 0) {
-          float t = INFINITY;
-          for (int w = 0; w < kWarps; ++w) t = fminf(t, s.rf[2 * kWarps + 2 + w]);
-          s.part.tau = t;
-        }
-      }
-    }
+    cta_thresholds(c, s, Kc, Kn, bv);
     if (c.lane == 0) {
       s.rf[c.warp] = m;
       s.rf[kWarps + c.warp] = sm;
@@ -1667,7 +1682,6 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     VT_TRACE(15);
     return;
   }
-
   // ---- pass B: candidates at or above the cluster threshold ----------------
   // A top-p row without top-k keeps at least p * S elements (none weighs more
   // than the maximum): past the buffer it cannot stay on the candidates, so
