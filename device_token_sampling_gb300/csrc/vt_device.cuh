@@ -198,10 +198,17 @@ __device__ __forceinline__ uint32_t key_idx(uint64_t k) { return ~(uint32_t)k; }
 
 // Mass of an element relative to the row max, in 2^-40 fixed point (exact,
 // order-independent sums).  Explicitly rounded operations: the same element
-// must get the same mass in every pass, whatever the compiler fuses.
+// must get the same mass in every pass, whatever the compiler fuses.  The
+// value floor(w 2^40), w in [0, 1], comes from two 32-bit conversions (one
+// 64-bit conversion runs at a small fraction of their rate): a = w 2^8 is
+// exact, so are its integer part hi and its fraction a - hi, and the
+// fraction times 2^32 is an exact value below 2^32.
 __device__ __forceinline__ unsigned long long mass_fixed(float zt, float m_t) {
   const float w = ex2_approx(__fmul_rn(__fsub_rn(zt, m_t), kLog2e));
-  return __float2ull_rz(w * 0x1p40f);
+  const float a = __fmul_rn(w, 256.0f);
+  const unsigned int hi = __float2uint_rz(a);
+  const unsigned int lo = __float2uint_rz(__fmul_rn(__fsub_rn(a, __uint2float_rn(hi)), 0x1p32f));
+  return ((unsigned long long)hi << 32) | lo;
 }
 
 // ---- warp reductions -------------------------------------------------------

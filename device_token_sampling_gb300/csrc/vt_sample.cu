@@ -2015,12 +2015,16 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         atomicAdd(&hc[sl[e]], 1u);
         if (draw) atomicMax(&hb[sl[e]], bits[e] + 1u);
       }
-      while (special) {
-        const int e = __ffs(special) - 1;
-        special &= special - 1u;
-        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-        code_special(s.part, sl[e] == tiny ? 0 : 1, u, j0 + e, draw ? bits[e] : 0u, inv_t, m_t,
-                     minp, lmp, draw);
+      // (element indices fixed at compile time: the arrays stay in registers)
+      if (special) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          if ((special >> e) & 1u) {
+            const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+            code_special(s.part, sl[e] == tiny ? 0 : 1, u, j0 + e, draw ? bits[e] : 0u, inv_t,
+                         m_t, minp, lmp, draw);
+          }
+        }
       }
     }
     VT_CTRACE(c, 12);
@@ -2433,13 +2437,16 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         mw &= mw - 1u;
         if (noise_bits(rkey, j0 + e) + 1u == wbits) cand_j = min(cand_j, j0 + e);
       }
-      while (mn) {
-        const int e = __ffs(mn) - 1;
-        mn &= mn - 1u;
-        const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-        const int pos = atomicAdd(lcount, 1);
-        if (pos < kBufCap)
-          lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)(j0 + e));
+      if (mn) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          if ((mn >> e) & 1u) {
+            const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
+            const int pos = atomicAdd(lcount, 1);
+            if (pos < kBufCap)
+              lg[pos] = elem_key(__fmul_rn(__uint_as_float(u << 16), inv_t), (uint32_t)(j0 + e));
+          }
+        }
       }
     }
     // this CTA's results
