@@ -1338,33 +1338,36 @@ __device__ __noinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int K
     if (Kc > c.ngroups || bv == -INFINITY) {
       if (c.tid == 0) s.part.tau = -INFINITY;
     } else {
-      // The Kc-th largest group-maximum lower bound, exactly: a two-round
-      // radix select over the order-preserving 16-bit keys of the bf16
-      // values (high byte, then low byte inside the chosen high byte).
-      auto gkey = [&](int g) -> uint32_t {
-        const uint32_t u = c.gmax[g];
+      // The Kc-th largest group-maximum lower bound, exactly: the distance of
+      // each group's order-preserving 16-bit key below the CTA maximum's, in
+      // bins of 16 keys (256 bins, the last one open), then inside the chosen
+      // bin by the low 4 bits.  Distances spread over many bins, so the
+      // shared-memory counts rarely collide.
+      auto gkey = [&](uint32_t u) -> uint32_t {
         return (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u);
       };
-      uint32_t above = 0u;  // groups whose key is above the chosen prefix
-      int hi_byte = 0;
+      const uint32_t kmax = gkey(bf16_down(bv));
+      int dsel = 0;      // chosen distance (bins of 16, then exact)
+      uint32_t below = 0u;  // groups nearer the maximum than the chosen bin
       for (int round = 0; round < 2; ++round) {
         s.hist256[c.tid] = 0u;
         __syncthreads();
         for (int g = c.tid; g < c.ngroups; g += kThreads) {
-          const uint32_t k = gkey(g);
-          if (round == 1 && (int)(k >> 8) != hi_byte) continue;
-          const uint32_t bin = round == 0 ? (k >> 8) : (k & 0xFFu);
-          // lanes with the same bin add once (most keys share a few high bytes)
-          const uint32_t peers = __match_any_sync(__activemask(), bin);
-          if ((peers & ((1u << c.lane) - 1u)) == 0u) atomicAdd(&s.hist256[bin], __popc(peers));
+          const uint32_t k = gkey(c.gmax[g]);
+          const uint32_t d = k <= kmax ? kmax - k : 0u;
+          if (round == 0) {
+            atomicAdd(&s.hist256[d >= 255u * 16u ? 255u : d >> 4], 1u);
+          } else if ((int)(d >> 4) == dsel) {
+            atomicAdd(&s.hist256[d & 15u], 1u);
+          }
         }
         __syncthreads();
         if (c.warp == 0) {
-          // lane l holds bins 255-8l .. 248-8l (descending)
+          // lane l holds bins 8l .. 8l+7 (ascending distance)
           uint32_t cnt[8], tot = 0;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            cnt[q] = s.hist256[255 - 8 * c.lane - q];
+            cnt[q] = s.hist256[8 * c.lane + q];
             tot += cnt[q];
           }
           uint32_t inc = tot;
@@ -1373,12 +1376,12 @@ __device__ __noinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int K
             const uint32_t w = __shfl_up_sync(0xffffffffu, inc, o);
             if (c.lane >= o) inc += w;
           }
-          const uint32_t before = above + inc - tot;
-          if (before < (uint32_t)Kc && above + inc >= (uint32_t)Kc) {
+          const uint32_t before = below + inc - tot;
+          if (before < (uint32_t)Kc && below + inc >= (uint32_t)Kc) {
             uint32_t run = before;
             for (int q = 0; q < 8; ++q) {
               if (run + cnt[q] >= (uint32_t)Kc) {
-                s.bcast_i[2] = 255 - 8 * c.lane - q;
+                s.bcast_i[2] = 8 * c.lane + q;
                 s.bcast_i[3] = (int)run;
                 break;
               }
@@ -1388,15 +1391,19 @@ __device__ __noinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int K
         }
         __syncthreads();
         const int bsel = s.bcast_i[2];
-        above = (uint32_t)s.bcast_i[3];
+        below = (uint32_t)s.bcast_i[3];
+        __syncthreads();  // the histogram is cleared again only after every read
         if (round == 0) {
-          hi_byte = bsel;
+          if (bsel == 255) {  // the open bin: every group is a candidate group
+            if (c.tid == 0) s.part.tau = -INFINITY;
+            break;
+          }
+          dsel = bsel;
         } else if (c.tid == 0) {
-          const uint32_t k = ((uint32_t)hi_byte << 8) | (uint32_t)bsel;
+          const uint32_t k = kmax - (uint32_t)(dsel * 16 + bsel);
           const uint32_t u = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
           s.part.tau = bf16_val((uint16_t)u);
         }
-        __syncthreads();  // the histogram is cleared again only after every read
       }
     }
   }
@@ -1573,6 +1580,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
     block_argmax(bv, bi, dz, s);  // also a barrier: s.tmax is complete after it
     const int nf = __syncthreads_or(nonfin);
     // (rows handed over after their statistics take no thresholds here)
+    // (rows handed over after their statistics take no thresholds)
     const int Kc = a.early ? 0 : (K_main + c.C - 1) / c.C;
     const int Kn = a.early ? 0 : (n + c.C - 1) / c.C;
     cta_thresholds(c, s, Kc, Kn, bv);
