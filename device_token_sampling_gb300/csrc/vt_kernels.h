@@ -79,6 +79,8 @@ struct LaunchPlan {
   size_t smem;        // dynamic shared memory per CTA
   int active_clusters;  // clusters resident at once (filled by prepare_sample)
   SelectPlan sel;       // the selection kernel that finishes handed-over rows
+  SelectPlan own;       // the selection kernel taking its rows' statistics itself
+                        // (bf16 only; cluster 0 otherwise)
 };
 
 // Shared-memory layout for V elements of elem_size bytes split over `cluster`
@@ -98,6 +100,12 @@ cudaError_t prepare_sample(LaunchPlan& plan, int dtype);
 // then the selection kernel for the rows it handed over.
 cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dtype,
                           cudaStream_t stream, cudaEvent_t between = nullptr);
+
+// The selection kernel alone over the rows args.rows[0, args.B) (args.early
+// set): one cluster per row streams its slices for the row statistics (the
+// same slices and arithmetic as the streaming kernel), then selects and draws.
+cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, int dtype,
+                              cudaStream_t stream);
 
 // Build the per-row sorted (id, count) tables from raw ids.
 //   raw, offs  CSR: row r owns raw[offs[r] .. offs[r+1]) (prompt then output)

@@ -1409,199 +1409,196 @@ __device__ __noinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int K
   }
 }
 
+// ---------------------------------------------------------------------------
+// pass A of a row slice: statistics while streaming it once
+// ---------------------------------------------------------------------------
+// Streams this CTA's slice (bulk copies through a ring of kStages slots in
+// `ring` for aligned rows, else plain loads) and leaves in s.part its tempered
+// maximum m, sum of exp(z_t - m) s, the lowest-index argmax (bv, bi) and the
+// non-finite flag; s.tmax holds each thread's maximum and c.gmax each group's
+// (a bf16 lower bound).  Returns this CTA's maximum bv.  All threads call it.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];
-  __shared__ Smem s;
-  cg::cluster_group cluster = cg::this_cluster();
+__device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
   constexpr int E = Elt<T>::E;
-
-  Ctx c;
-  const int C = (int)cluster_nctarank();
-  const int row = a.rows ? a.rows[blockIdx.x / C] : (int)(blockIdx.x / C);
-  const RowParams P = init_row<T>(c, a, dsm, row, C, (int)cluster_ctarank(), a.slice,
-                                  a.off_gmax, a.off_mrg);
-  c.trace = a.trace ? a.trace + ((size_t)row * C + c.rank) * kTraceSlots : nullptr;
-  const int n = a.n_logprobs;
-  const int hist_len = a.hist_len[c.row];
-  VT_TRACE(0);
-
-  if (c.tid == 0) {
-    s.part.err = 0;
-    s.nloc = 0;
-    s.gcount = 0;
-  }
-
-  if (a.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0)
-    setup_penalties<T>(c, s, a, P, dsm, a.off_bitmap, a.off_prefix, hist_len);
-
-  // ---- pass A: stream the slice ----------------------------------------------
-  // Candidates the kept set may need (K_main) and the top-n alone (n).
-  int K_main = c.greedy ? n : max(n, c.topk ? c.top_k : ((c.topp || c.minp) ? kDefaultCand : 0));
-  bool topk_beyond = false;
-  if (K_main > kBufCap) {
-    K_main = n;
-    topk_beyond = true;
-  }
-  {
-    // rm: this thread's running maximum (pre-temperature); rmt = fl(rm / T),
-    // the tempered reference of rsum = sum of exp(z_t - rmt).
-    float rm = -INFINITY, rmt = -INFINITY, rsum = 0.f, bv = -INFINITY;
-    int bi = INT_MAX;
-    bool nanf = false;
-    auto consume = [&](float* x, int g) {
-      float gm = x[0];
+  // rm: this thread's running maximum (pre-temperature); rmt = fl(rm / T),
+  // the tempered reference of rsum = sum of exp(z_t - rmt).
+  float rm = -INFINITY, rmt = -INFINITY, rsum = 0.f, bv = -INFINITY;
+  int bi = INT_MAX;
+  bool nanf = false;
+  auto consume = [&](float* x, int g) {
+    float gm = x[0];
 #pragma unroll
-      for (int i = 1; i < E; ++i) gm = fmaxf(gm, x[i]);
-      c.gmax[g] = bf16_down(gm);
-      if (gm > bv) {
-        int first = 0;
+    for (int i = 1; i < E; ++i) gm = fmaxf(gm, x[i]);
+    c.gmax[g] = bf16_down(gm);
+    if (gm > bv) {
+      int first = 0;
 #pragma unroll
-        for (int i = E - 1; i >= 0; --i)
-          if (x[i] == gm) first = i;
-        bv = gm;
-        bi = c.lo + g * E + first;
-      }
-      if (gm > rm) {
-        const float gmt = __fmul_rn(gm, c.inv_t);
-        rsum = (rm == -INFINITY) ? 0.f
-                                 : rsum * ex2_approx(__fmul_rn(__fsub_rn(rmt, gmt), kLog2e));
-        rm = gm;
-        rmt = gmt;
-      }
-      if (rm > -INFINITY) {
-        // exponentials in place, then a pairwise sum of the group.  Near zero
-        // one FFMA per element, 2^(x a - rm a) with a = log2(e) / T; once the
-        // reference is large, the rounding of rm a would show, and the
-        // tempered difference fl(fl(x / T) - rmt) is formed instead (exact
-        // where it matters, by Sterbenz).
-        if (fabsf(rmt) <= 16.0f) {
-          const float nb = -rm * c.ax;
+      for (int i = E - 1; i >= 0; --i)
+        if (x[i] == gm) first = i;
+      bv = gm;
+      bi = c.lo + g * E + first;
+    }
+    if (gm > rm) {
+      const float gmt = __fmul_rn(gm, c.inv_t);
+      rsum = (rm == -INFINITY) ? 0.f
+                               : rsum * ex2_approx(__fmul_rn(__fsub_rn(rmt, gmt), kLog2e));
+      rm = gm;
+      rmt = gmt;
+    }
+    if (rm > -INFINITY) {
+      // exponentials in place, then a pairwise sum of the group.  Near zero
+      // one FFMA per element, 2^(x a - rm a) with a = log2(e) / T; once the
+      // reference is large, the rounding of rm a would show, and the
+      // tempered difference fl(fl(x / T) - rmt) is formed instead (exact
+      // where it matters, by Sterbenz).
+      if (fabsf(rmt) <= 16.0f) {
+        const float nb = -rm * c.ax;
 #pragma unroll
-          for (int i = 0; i < E; ++i) x[i] = ex2_approx(fmaf(x[i], c.ax, nb));
-        } else {
-#pragma unroll
-          for (int i = 0; i < E; ++i)
-            x[i] = ex2_approx(__fmul_rn(__fsub_rn(__fmul_rn(x[i], c.inv_t), rmt), kLog2e));
-        }
-#pragma unroll
-        for (int w = 1; w < E; w <<= 1)
-#pragma unroll
-          for (int i = 0; i + w < E; i += 2 * w) x[i] += x[i + w];
-        rsum += x[0];
+        for (int i = 0; i < E; ++i) x[i] = ex2_approx(fmaf(x[i], c.ax, nb));
       } else {
 #pragma unroll
-        for (int i = 0; i < E; ++i) nanf |= x[i] != x[i];
+        for (int i = 0; i < E; ++i)
+          x[i] = ex2_approx(__fmul_rn(__fsub_rn(__fmul_rn(x[i], c.inv_t), rmt), kLog2e));
       }
-    };
-    if (c.aligned) {
-      // bulk copies through a ring of kStages 8 KB slots: one group per thread
-      // per stage, kStages - 1 stages in flight while one is consumed
-      const uint32_t bulk = ((uint32_t)(c.hi > c.lo ? c.hi - c.lo : 0) * (uint32_t)sizeof(T)) & ~15u;
-      const int nstage = (c.ngroups + kThreads - 1) / kThreads;
-      const char* src = reinterpret_cast<const char*>(reinterpret_cast<const T*>(c.rowp) + c.lo);
-      uint8_t* ring = reinterpret_cast<uint8_t*>(c.buf);
-      auto stage_bytes = [&](int k) -> uint32_t {
-        const int64_t b = (int64_t)bulk - (int64_t)k * kStageBytes;
-        return b <= 0 ? 0u : (b > kStageBytes ? (uint32_t)kStageBytes : (uint32_t)b);
-      };
-      if (c.tid == 0) {
-        for (int st = 0; st < kStages; ++st) mbar_init(&s.full[st], 1);
-        fence_mbar_init();
-      }
-      __syncthreads();
-      if (c.tid == 0) {
-        for (int k = 0; k < min(kStages, nstage); ++k) {
-          const uint32_t by = stage_bytes(k);
-          if (by) {
-            mbar_arrive_expect_tx(&s.full[k], by);
-            bulk_copy_g2s(ring + k * kStageBytes, src + (size_t)k * kStageBytes, by, &s.full[k]);
-          }
-        }
-      }
-      for (int k = 0; k < nstage; ++k) {
-        const int slot = k % kStages;
-        const uint32_t by = stage_bytes(k);
-        if (by && !mbar_wait_bounded(&s.full[slot], (uint32_t)((k / kStages) & 1)))
-          atomicOr(&s.part.err, kErrTimeout);
-        const int g = k * kThreads + c.tid;
-        if (g < c.ngroups) {
-          float x[E];
-          if ((uint32_t)(c.tid + 1) * kGroupBytes <= by) {
-            const uint4* q = reinterpret_cast<const uint4*>(ring + slot * kStageBytes) + 2 * c.tid;
-            if constexpr (E == 8) {
-              const uint4 u0 = q[0], u1 = q[1];
-              x[0] = __uint_as_float(u0.x); x[1] = __uint_as_float(u0.y);
-              x[2] = __uint_as_float(u0.z); x[3] = __uint_as_float(u0.w);
-              x[4] = __uint_as_float(u1.x); x[5] = __uint_as_float(u1.y);
-              x[6] = __uint_as_float(u1.z); x[7] = __uint_as_float(u1.w);
-            } else {
-              const uint4 u0 = q[0], u1 = q[1];
-              const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                x[2 * i] = __uint_as_float(w[i] << 16);
-                x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-              }
-            }
-            patch_group<T>(c, g, x);
-          } else {
-            load_group<T>(c, g, x);  // the ragged tail, from global memory
-          }
-          consume(x, g);
-        }
-        __syncthreads();  // slot free
-        if (c.tid == 0 && k + kStages < nstage) {
-          const uint32_t nb = stage_bytes(k + kStages);
-          if (nb) {
-            mbar_arrive_expect_tx(&s.full[slot], nb);
-            bulk_copy_g2s(ring + slot * kStageBytes, src + (size_t)(k + kStages) * kStageBytes,
-                          nb, &s.full[slot]);
-          }
-        }
-      }
+      for (int w = 1; w < E; w <<= 1)
+#pragma unroll
+        for (int i = 0; i + w < E; i += 2 * w) x[i] += x[i + w];
+      rsum += x[0];
     } else {
-      for (int g = c.tid; g < c.ngroups; g += kThreads) {
-        float x[E];
-        load_group<T>(c, g, x);
-        consume(x, g);
-      }
-    }
-    const bool nonfin = nanf || (rsum != rsum) || rm == INFINITY;
-    s.tmax[c.tid] = rm;
-    float m = rmt, sm = rsum;  // partials combine in tempered units
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-      lse_combine(m, sm, m2, s2, kLog2e);
+      for (int i = 0; i < E; ++i) nanf |= x[i] != x[i];
     }
-    float dz = 0.f;
-    block_argmax(bv, bi, dz, s);  // also a barrier: s.tmax is complete after it
-    const int nf = __syncthreads_or(nonfin);
-    // (rows handed over after their statistics take no thresholds here)
-    // (rows handed over after their statistics take no thresholds)
-    const int Kc = a.early ? 0 : (K_main + c.C - 1) / c.C;
-    const int Kn = a.early ? 0 : (n + c.C - 1) / c.C;
-    cta_thresholds(c, s, Kc, Kn, bv);
-    if (c.lane == 0) {
-      s.rf[c.warp] = m;
-      s.rf[kWarps + c.warp] = sm;
+  };
+  if (c.aligned) {
+    // bulk copies through a ring of kStages 8 KB slots: one group per thread
+    // per stage, kStages - 1 stages in flight while one is consumed
+    const uint32_t bulk = ((uint32_t)(c.hi > c.lo ? c.hi - c.lo : 0) * (uint32_t)sizeof(T)) & ~15u;
+    const int nstage = (c.ngroups + kThreads - 1) / kThreads;
+    const char* src = reinterpret_cast<const char*>(reinterpret_cast<const T*>(c.rowp) + c.lo);
+    auto stage_bytes = [&](int k) -> uint32_t {
+      const int64_t b = (int64_t)bulk - (int64_t)k * kStageBytes;
+      return b <= 0 ? 0u : (b > kStageBytes ? (uint32_t)kStageBytes : (uint32_t)b);
+    };
+    if (c.tid == 0) {
+      for (int st = 0; st < kStages; ++st) mbar_init(&s.full[st], 1);
+      fence_mbar_init();
     }
     __syncthreads();
     if (c.tid == 0) {
-      float mm = -INFINITY, ss = 0.f;
-      for (int w = 0; w < kWarps; ++w) lse_combine(mm, ss, s.rf[w], s.rf[kWarps + w], kLog2e);
-      s.part.m = mm;
-      s.part.s = ss;
-      s.part.bv = bv;
-      s.part.bi = bi;
-      s.part.nonfinite = nf;
+      for (int k = 0; k < min(kStages, nstage); ++k) {
+        const uint32_t by = stage_bytes(k);
+        if (by) {
+          mbar_arrive_expect_tx(&s.full[k], by);
+          bulk_copy_g2s(ring + k * kStageBytes, src + (size_t)k * kStageBytes, by, &s.full[k]);
+        }
+      }
+    }
+    for (int k = 0; k < nstage; ++k) {
+      const int slot = k % kStages;
+      const uint32_t by = stage_bytes(k);
+      if (by && !mbar_wait_bounded(&s.full[slot], (uint32_t)((k / kStages) & 1)))
+        atomicOr(&s.part.err, kErrTimeout);
+      const int g = k * kThreads + c.tid;
+      if (g < c.ngroups) {
+        float x[E];
+        if ((uint32_t)(c.tid + 1) * kGroupBytes <= by) {
+          const uint4* q = reinterpret_cast<const uint4*>(ring + slot * kStageBytes) + 2 * c.tid;
+          if constexpr (E == 8) {
+            const uint4 u0 = q[0], u1 = q[1];
+            x[0] = __uint_as_float(u0.x); x[1] = __uint_as_float(u0.y);
+            x[2] = __uint_as_float(u0.z); x[3] = __uint_as_float(u0.w);
+            x[4] = __uint_as_float(u1.x); x[5] = __uint_as_float(u1.y);
+            x[6] = __uint_as_float(u1.z); x[7] = __uint_as_float(u1.w);
+          } else {
+            const uint4 u0 = q[0], u1 = q[1];
+            const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              x[2 * i] = __uint_as_float(w[i] << 16);
+              x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+          }
+          patch_group<T>(c, g, x);
+        } else {
+          load_group<T>(c, g, x);  // the ragged tail, from global memory
+        }
+        consume(x, g);
+      }
+      __syncthreads();  // slot free
+      if (c.tid == 0 && k + kStages < nstage) {
+        const uint32_t nb = stage_bytes(k + kStages);
+        if (nb) {
+          mbar_arrive_expect_tx(&s.full[slot], nb);
+          bulk_copy_g2s(ring + slot * kStageBytes, src + (size_t)(k + kStages) * kStageBytes,
+                        nb, &s.full[slot]);
+        }
+      }
+    }
+  } else {
+    for (int g = c.tid; g < c.ngroups; g += kThreads) {
+      float x[E];
+      load_group<T>(c, g, x);
+      consume(x, g);
     }
   }
-  VT_TRACE(2);
-  cluster.sync();  // (1) pass-A partials and thresholds visible
-  VT_TRACE(3);
+  const bool nonfin = nanf || (rsum != rsum) || rm == INFINITY;
+  s.tmax[c.tid] = rm;
+  float m = rmt, sm = rsum;  // partials combine in tempered units
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
+    lse_combine(m, sm, m2, s2, kLog2e);
+  }
+  float dz = 0.f;
+  block_argmax(bv, bi, dz, s);  // also a barrier: s.tmax is complete after it
+  const int nf = __syncthreads_or(nonfin);
+  // (rows handed over after their statistics take no thresholds here)
+  if (c.lane == 0) {
+    s.rf[c.warp] = m;
+    s.rf[kWarps + c.warp] = sm;
+  }
+  __syncthreads();
+  if (c.tid == 0) {
+    float mm = -INFINITY, ss = 0.f;
+    for (int w = 0; w < kWarps; ++w) lse_combine(mm, ss, s.rf[w], s.rf[kWarps + w], kLog2e);
+    s.part.m = mm;
+    s.part.s = ss;
+    s.part.bv = bv;
+    s.part.bi = bi;
+    s.part.nonfinite = nf;
+  }
+  __syncthreads();
+  return bv;
+}
+
+// Outputs of a row whose statistics make it unsampleable (non-finite values,
+// or no finite value): token -1, NaN log-probs, the status; the seed still
+// advances.  The row's leader CTA calls it.
+__device__ __forceinline__ void write_bad_row(const SampleArgs& a, const Smem& s, int row,
+                                              int status) {
+  const int n = a.n_logprobs;
+  if ((int)threadIdx.x < n) {
+    a.out_topk_ids[(int64_t)row * n + threadIdx.x] = -1;
+    a.out_topk_logprobs[(int64_t)row * n + threadIdx.x] = __int_as_float(0x7fc00000);
+  }
+  if (threadIdx.x == 0) {
+    a.out_tokens[row] = -1;
+    if (a.out_logprobs) a.out_logprobs[row] = __int_as_float(0x7fc00000);
+    a.row_status[row] = status;
+    a.dbg_kth_value[row] = __int_as_float(0x7fc00000);
+    a.dbg_kth_index[row] = -1;
+    a.dbg_kept[row] = 0;
+    a.seeds[row] += kSeedStep;
+    if (s.rs.err) atomicOr(a.err_word, s.rs.err);
+  }
+}
+
+// The row's statistics from every CTA's pass-A partials (warp 0; the caller
+// synchronises): tempered maximum, sum and its log, argmax, flags, and the
+// smallest candidate thresholds.
+__device__ __forceinline__ void cluster_stats(const Ctx& c, Smem& s, cg::cluster_group& cluster) {
   if (c.warp == 0) {
     float m = -INFINITY, sm = 0.f, bv = -INFINITY, tau = INFINITY, tau_n = INFINITY;
     int bi = INT_MAX, nf = 0, er = 0;
@@ -1645,6 +1642,53 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
       s.rs.tau_n = tau_n;
     }
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ Smem s;
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int E = Elt<T>::E;
+
+  Ctx c;
+  const int C = (int)cluster_nctarank();
+  const int row = a.rows ? a.rows[blockIdx.x / C] : (int)(blockIdx.x / C);
+  const RowParams P = init_row<T>(c, a, dsm, row, C, (int)cluster_ctarank(), a.slice,
+                                  a.off_gmax, a.off_mrg);
+  c.trace = a.trace ? a.trace + ((size_t)row * C + c.rank) * kTraceSlots : nullptr;
+  const int n = a.n_logprobs;
+  const int hist_len = a.hist_len[c.row];
+  VT_TRACE(0);
+
+  if (c.tid == 0) {
+    s.part.err = 0;
+    s.nloc = 0;
+    s.gcount = 0;
+  }
+
+  if (a.pen_smem && (P.flags & kRowPenalty) != 0 && hist_len > 0)
+    setup_penalties<T>(c, s, a, P, dsm, a.off_bitmap, a.off_prefix, hist_len);
+
+  // ---- pass A: stream the slice ----------------------------------------------
+  // Candidates the kept set may need (K_main) and the top-n alone (n).
+  int K_main = c.greedy ? n : max(n, c.topk ? c.top_k : ((c.topp || c.minp) ? kDefaultCand : 0));
+  bool topk_beyond = false;
+  if (K_main > kBufCap) {
+    K_main = n;
+    topk_beyond = true;
+  }
+  const float cta_max = stream_stats<T>(c, s, reinterpret_cast<uint8_t*>(c.buf));
+  {
+    // (rows handed over after their statistics take no thresholds)
+    const int Kc = a.early ? 0 : (K_main + c.C - 1) / c.C;
+    const int Kn = a.early ? 0 : (n + c.C - 1) / c.C;
+    cta_thresholds(c, s, Kc, Kn, cta_max);
+  }
+  VT_TRACE(2);
+  cluster.sync();  // (1) pass-A partials and thresholds visible
+  VT_TRACE(3);
+  cluster_stats(c, s, cluster);
   __syncthreads();
   c.m_t = s.rs.m_t;
   c.lnS = s.rs.lnS;
@@ -1655,22 +1699,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
 
   if (status0 != kRowOk) {
     cluster.sync();  // nobody reads another CTA's shared memory after this
-    if (leader) {
-      if (c.tid < n) {
-        out_ids[c.tid] = -1;
-        out_lps[c.tid] = __int_as_float(0x7fc00000);
-      }
-      if (c.tid == 0) {
-        a.out_tokens[c.row] = -1;
-        if (a.out_logprobs) a.out_logprobs[c.row] = __int_as_float(0x7fc00000);
-        a.row_status[c.row] = status0;
-        a.dbg_kth_value[c.row] = __int_as_float(0x7fc00000);
-        a.dbg_kth_index[c.row] = -1;
-        a.dbg_kept[c.row] = 0;
-        a.seeds[c.row] += kSeedStep;
-        if (s.rs.err) atomicOr(a.err_word, s.rs.err);
-      }
-    }
+    if (leader) write_bad_row(a, s, c.row, status0);
     return;
   }
 
@@ -2909,10 +2938,15 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
   const int cid = (int)blockIdx.x / C, G = (int)gridDim.x / C;
-  const int count = (int)a.slow_ctl[0];
+  // Rows handed over by the streaming kernel (a list and their statistics),
+  // or, when a.early is set, the rows a.rows[0, B) whose statistics this
+  // kernel takes itself in a first streaming pass over the slice.
+  const bool own_stats = a.early != 0;
+  const int count = own_stats ? a.B : (int)a.slow_ctl[0];
   for (int i = cid; i < count; i += G) {
-    const int row = a.slow_list[i];
-    const SlowRow rec = a.slow[row];
+    const int row = own_stats ? (a.rows ? a.rows[i] : i) : a.slow_list[i];
+    SlowRow rec;
+    if (!own_stats) rec = a.slow[row];
     cluster.sync();  // every CTA of the cluster is done with the previous row
     Ctx c;
     const RowParams P = init_row<T>(c, a, dsm, row, C, rank, p.slice, p.off_gmax, p.off_mrg);
@@ -2923,9 +2957,33 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
       s.part.err = 0;
       s.nloc = 0;
       s.gcount = 0;
-      s.rs.bi = (int)(rec.bi_topn & 0x7FFFFFFFu);
       s.rs.err = 0;
     }
+    if (own_stats) {
+      // the row's statistics: pass A through the bulk-copy ring (in the code
+      // slots' region, free until the selection starts), then the cluster's
+      VT_CTRACE(c, 0);
+      __syncthreads();
+      stream_stats<T>(c, s, dsm + p.off_code);
+      VT_CTRACE(c, 2);
+      cluster.sync();  // every CTA's partials visible
+      VT_CTRACE(c, 3);
+      cluster_stats(c, s, cluster);
+      __syncthreads();
+      const int status0 =
+          s.rs.nonfinite ? kRowNonfinite : (s.rs.m_t == -INFINITY ? kRowEmpty : kRowOk);
+      rec.m_t = s.rs.m_t;
+      rec.lnS = s.rs.lnS;
+      rec.xmax = s.rs.bv;
+      rec.bi_topn = (uint32_t)s.rs.bi | (a.n_logprobs == 0 ? 0x80000000u : 0u);
+      cluster.sync();  // every CTA has read the others' partials
+      if (status0 != kRowOk) {
+        if (rank == 0) write_bad_row(a, s, row, status0);
+        continue;
+      }
+      if (c.tid == 0) atomicOr(&s.part.err, s.rs.err);
+    }
+    if (c.tid == 0) s.rs.bi = (int)(rec.bi_topn & 0x7FFFFFFFu);
     c.m_t = rec.m_t;
     c.lnS = rec.lnS;
     c.xmax = rec.xmax;
@@ -2963,7 +3021,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
     __threadfence();
     const unsigned int done = atomicAdd(&a.slow_ctl[1], 1u);
     if (done == gridDim.x - 1) {
-      a.slow_ctl[2] = a.slow_ctl[0];  // kept for vt_debug_last_handover
+      a.slow_ctl[2] = own_stats ? (unsigned int)count : a.slow_ctl[0];  // for vt_debug_last_handover
       a.slow_ctl[0] = 0u;
       a.slow_ctl[1] = 0u;
       __threadfence();
@@ -3144,6 +3202,22 @@ static SelectPlan plan_select(int B, int V, int elem_size, bool penalties, int d
   return p;
 }
 
+// The selection kernel that takes its rows' statistics itself (bf16 rows
+// without penalties): the streaming kernel's cluster, so that its slices, and
+// the statistics summed over them, are the streaming kernel's exactly.
+static SelectPlan plan_select_own(int V, int elem_size, int dtype, const LaunchPlan& k1) {
+  SelectPlan p{};
+  if (elem_size != 2 || dtype == 0) return p;
+  p = plan_select_layout(V, elem_size, k1.cluster, false, false);
+  p.kernel1_cluster = k1.cluster;
+  if (p.off_code == 0u || p.slice != k1.slice ||
+      prepare_select_one<uint16_t>(p) != cudaSuccess) {
+    SelectPlan none{};
+    return none;
+  }
+  return p;
+}
+
 LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, int num_sms) {
   // Slices of at most 256 KB (so the per-group structures stay small) and at
   // least 8 KB of logits; among those, the largest cluster that still lets
@@ -3156,6 +3230,7 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
   if (prepare_sample(best, dtype) != cudaSuccess) return best;
   if ((int64_t)B > best.active_clusters) {  // several waves even so
     best.sel = plan_select(B, V, elem_size, penalties, dtype, best.cluster);
+    best.own = plan_select_own(V, elem_size, dtype, best);
     return best;
   }
   for (int C = cmin * 2; C <= kMaxCluster; C <<= 1) {
@@ -3166,6 +3241,7 @@ LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, i
     best = p;
   }
   best.sel = plan_select(B, V, elem_size, penalties, dtype, best.cluster);
+  best.own = plan_select_own(V, elem_size, dtype, best);
   return best;
 }
 
@@ -3202,6 +3278,17 @@ cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dt
                           cudaStream_t stream, cudaEvent_t between) {
   return dtype == 0 ? launch_one<float>(args, plan, stream, between)
                     : launch_one<uint16_t>(args, plan, stream, between);
+}
+
+cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, int dtype,
+                              cudaStream_t stream) {
+  if (dtype == 0 || plan.own.cluster < 1 || !args.early) return cudaErrorInvalidValue;
+  if (args.B < 1) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = select_config<uint16_t>(plan.own, attr);
+  cfg.gridDim = dim3((unsigned)(args.B * plan.own.cluster), 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, select_kernel<uint16_t>, args, plan.own);
 }
 
 }  // namespace vt

@@ -518,11 +518,16 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     const vt::SampleArgs as = make_args(*ps, h->n_side, h->d_rows + h->n_main, 1, 1);
     VT_CK(h, cudaEventRecord(h->ev_fork, st));
     VT_CK(h, cudaStreamWaitEvent(h->side, h->ev_fork, 0));
-    VT_CK(h, vt::launch_sample(as, *ps, dtype, h->side, nullptr));
+    // the side rows: the selection kernel alone, taking their statistics
+    // itself (else the streaming kernel hands them over at once)
+    if (ps->own.cluster >= 1)
+      VT_CK(h, vt::launch_select_own(as, *ps, dtype, h->side));
+    else
+      VT_CK(h, vt::launch_sample(as, *ps, dtype, h->side, nullptr));
     VT_CK(h, vt::launch_sample(am, *pm, dtype, st, h->phase_event));
     VT_CK(h, cudaEventRecord(h->ev_join, h->side));
     VT_CK(h, cudaStreamWaitEvent(st, h->ev_join, 0));
-    h->last_launches = 4;
+    h->last_launches = ps->own.cluster >= 1 ? 3 : 4;
   }
   h->last_B = B;
   h->last_stream = st;

@@ -322,7 +322,7 @@ class Sampler:
         return int(v.value)
 
     def last_launches(self) -> int:
-        """Kernels the last ``sample`` launched (2, or 4 when its rows were split
+        """Kernels the last ``sample`` launched (2, or 3 when its rows were split
         between the two streams)."""
         v = C.c_int32()
         self._check(self._lib.vt_debug_last_launches(self._h, C.byref(v)), "vt_debug_last_launches")

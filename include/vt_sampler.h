@@ -214,9 +214,10 @@ int vt_debug_set_phase_event(vt_sampler* handle, void* event);
 int vt_debug_last_handover(vt_sampler* handle, int32_t* rows);
 
 /* Debug: how many kernels the last vt_sample launched: 2 on one stream (the
- * streaming kernel, then the selection kernel), or 4 when the call split its
- * rows between the handle's two streams (a pair on each).  0 before the first
- * call.  Does not synchronise. */
+ * streaming kernel, then the selection kernel), or 3 when the call split its
+ * rows between the handle's two streams (the selection kernel alone, taking
+ * its rows' statistics itself, on the second stream; the pair on the first).
+ * 0 before the first call.  Does not synchronise. */
 int vt_debug_last_launches(vt_sampler* handle, int32_t* launches);
 
 /* Read the current per-row seeds of rows 0..B-1 into a host array (B of the
