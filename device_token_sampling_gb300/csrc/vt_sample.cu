@@ -2443,22 +2443,40 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     const bool gather_b = draw && bslot >= 0;
     const int bsel = gather_b ? bslot : -2;  // -2 matches nothing
     const int nsel = want_topn ? nslot : -2;
+    // A regular slot holds one bf16 value, so the matches are on the raw bits:
+    // the boundary, winning and last slots by equality, the top-n slots by
+    // order (every value at least the value of slot nsel).  A slot that is
+    // not regular matches nothing (the last slot is then unused, and a top-n
+    // or boundary slot never is one here).
+    auto slot_bits = [&](int sl) -> uint32_t {
+      if (sl < 0 || sl == tiny || sl >= kCatch) return 0xFFFFu;  // a NaN: matches no element
+      const int code = cmax - sl;
+      const uint32_t mag = (uint32_t)((code < 0 ? -code : code) - 1 + (kCodeEmin << 7));
+      return (code < 0 ? 0x8000u : 0u) | mag;
+    };
+    auto ord16 = [](uint32_t u) -> uint32_t { return (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u); };
+    const uint32_t ub = slot_bits(bsel), uw = slot_bits(wslot), ul = slot_bits(lslot);
+    const uint32_t un = slot_bits(nsel);
+    const uint32_t kn = un == 0xFFFFu ? 0x10000u : ord16(un);  // 0x10000: no top-n
+    // the next group's words are loaded while this one is matched
+    uint32_t wnext[8];
+    if (tid < ngroups_live) group_words(tid, wnext);
     for (int g = tid; g < ngroups_live; g += kThreads) {
       uint32_t w[8];
-      group_words(g, w);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) w[q] = wnext[q];
+      if (g + kThreads < ngroups_live) group_words(g + kThreads, wnext);
       const int j0 = lo + g * 16;
       // match masks of the 16 elements first (no branches), then the rare work
+      // (-inf, and the -inf padding past the row end, match nothing)
       unsigned int mb = 0u, mw = 0u, ml = 0u, mn = 0u;
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const uint32_t u = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-        const int d = cmax - code16(u);
-        const int v = d < kCatch ? d : kCatch;
-        const bool live = u != 0xFF80u && j0 + e < hi;
-        mb |= (live && v == bsel) ? (1u << e) : 0u;
-        mw |= (live && v == wslot) ? (1u << e) : 0u;
-        ml |= (live && v == lslot) ? (1u << e) : 0u;
-        mn |= (live && v <= nsel) ? (1u << e) : 0u;
+        mb |= (u == ub) ? (1u << e) : 0u;
+        mw |= (u == uw) ? (1u << e) : 0u;
+        ml |= (u == ul) ? (1u << e) : 0u;
+        mn |= (ord16(u) >= kn) ? (1u << e) : 0u;
       }
       if ((mb | mw | ml | mn) == 0u) continue;
       if (ml) lastslot_j = max(lastslot_j, j0 + 31 - __clz(ml));
