@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <new>
 #include <string>
@@ -336,6 +337,15 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
     if (!to_side(r)) h->h_rows[nm++] = r;
   for (int r = 0; r < B; ++r)
     if (to_side(r)) h->h_rows[nm + ns++] = r;
+  // Clusters start in launch order, and the last ones may wait for room on
+  // the SMs: the main rows go heaviest first (most candidates: top-k rows by
+  // k, then the other filtered rows, greedy rows last), stable in row order.
+  auto weight = [&](int r) {
+    const uint32_t f = h->row_flags[r];
+    if (f & vt::kRowGreedy) return 0;
+    return top_k[r] > 1 ? top_k[r] : 1;
+  };
+  std::stable_sort(h->h_rows, h->h_rows + nm, [&](int x, int y) { return weight(x) > weight(y); });
   h->n_main = nm;
   h->n_side = ns;
   VT_CK(h, cudaMemcpyAsync(h->d_params, h->h_params, (size_t)B * sizeof(vt::RowParams),
