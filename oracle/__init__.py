@@ -22,7 +22,7 @@ MAX_ALT = 8
 
 # Planted mistakes the mutation tests compile in, one per variant.
 MUTANTS = ("HASH", "TIE_HIGH", "PEN_ORDER", "PROMPT_ONLY", "TOPP_INCL", "TOPP_NO_RENORM",
-           "SCORE_MUL")
+           "SCORE_MUL", "IGNORE_ALL")
 
 
 def lib_path(mutant: str | None = None) -> str:
@@ -71,6 +71,14 @@ def load(mutant: str | None = None) -> C.CDLL:
     lib.oracle_sample.argtypes = [C.c_int64, C.c_int, C.c_int, C.c_int64, C.c_int, P, P, P, P, P, P,
                                   P, P,
                                   P, P, P, P, P, C.c_int, P, P, P, P]
+    lib.oracle_sample_ex.restype = C.c_int
+    lib.oracle_sample_ex.argtypes = [C.c_int64, C.c_int, C.c_int, C.c_int64, C.c_int, P, P, P, P,
+                                     P, P, P, P, P, P, P, P, P, P, C.c_int, P, P, P, P, P]
+    lib.oracle_topp_decay.restype = C.c_float
+    lib.oracle_topp_decay.argtypes = [C.c_float, C.c_float, C.c_float, C.c_float, C.c_int32,
+                                      C.c_int32]
+    lib.oracle_filtered_probs.restype = C.c_int
+    lib.oracle_filtered_probs.argtypes = [P, C.c_int, C.c_int64, P]
     lib.oracle_mix64.restype = C.c_uint64
     lib.oracle_mix64.argtypes = [C.c_uint64]
     lib.oracle_uniform.restype = C.c_double
@@ -103,6 +111,7 @@ class OracleOut:
     topn_ids: np.ndarray
     topn_logprobs: np.ndarray
     zt: np.ndarray | None
+    probs: np.ndarray | None = None
 
 
 def _ptr(a):
@@ -111,11 +120,14 @@ def _ptr(a):
 
 def sample(logits, V, dtype, temperature, top_k, top_p, min_p, presence, frequency, repetition,
            seed, prompt_ids, prompt_offsets, output_ids, output_offsets, num_logprobs,
-           want_zt=False, mutant=None, rows=None, first_row=0) -> OracleOut:
+           want_zt=False, mutant=None, rows=None, first_row=0, prompt_ignore=None,
+           want_probs=False) -> OracleOut:
     """Run the oracle on host arrays.  ``logits`` is [B, ld] (fp32, or uint16 bf16 bits).
 
     ``rows`` (optional) restricts the call to a subset of rows; each row keeps its
-    batch index as the key of its noise stream."""
+    batch index as the key of its noise stream.  ``prompt_ignore`` (optional [B])
+    is each row's prompt_ignore_length; ``want_probs`` returns the filtered
+    distribution of every row in ``probs`` ([B, V] float64)."""
     lib = load(mutant)
     logits = np.ascontiguousarray(logits)
     B, ld = logits.shape
@@ -126,7 +138,9 @@ def sample(logits, V, dtype, temperature, top_k, top_p, min_p, presence, frequen
                        repetition[r:r + 1], seed[r:r + 1],
                        *_row_hist(prompt_ids, prompt_offsets, r),
                        *_row_hist(output_ids, output_offsets, r), num_logprobs,
-                       want_zt=want_zt, mutant=mutant, first_row=first_row + int(r))
+                       want_zt=want_zt, mutant=mutant, first_row=first_row + int(r),
+                       prompt_ignore=None if prompt_ignore is None else prompt_ignore[r:r + 1],
+                       want_probs=want_probs)
                 for r in rows]
         return _concat(outs)
     f32 = lambda a: np.ascontiguousarray(a, dtype=np.float32)
@@ -141,12 +155,15 @@ def sample(logits, V, dtype, temperature, top_k, top_p, min_p, presence, frequen
     tid = np.zeros((B, n), np.int32)
     tlp = np.zeros((B, n), np.float64)
     zt = np.zeros((B, V), np.float32) if want_zt else None
-    rc = lib.oracle_sample(int(first_row), B, V, ld, dtype, _ptr(logits), _ptr(args["t"]), _ptr(args["k"]),
-                           _ptr(args["p"]), _ptr(args["mp"]), _ptr(args["pr"]),
-                           _ptr(args["fr"]), _ptr(args["rp"]), _ptr(args["sd"]),
-                           _ptr(args["pi"]), _ptr(args["po"]), _ptr(args["oi"]),
-                           _ptr(args["oo"]), n, C.cast(res, C.c_void_p),
-                           _ptr(tid) if n else None, _ptr(tlp) if n else None, _ptr(zt))
+    probs = np.zeros((B, V), np.float64) if want_probs else None
+    ign = None if prompt_ignore is None else i32(prompt_ignore)
+    rc = lib.oracle_sample_ex(int(first_row), B, V, ld, dtype, _ptr(logits), _ptr(args["t"]),
+                              _ptr(args["k"]), _ptr(args["p"]), _ptr(args["mp"]),
+                              _ptr(args["pr"]), _ptr(args["fr"]), _ptr(args["rp"]),
+                              _ptr(args["sd"]), _ptr(args["pi"]), _ptr(args["po"]),
+                              _ptr(args["oi"]), _ptr(args["oo"]), _ptr(ign), n,
+                              C.cast(res, C.c_void_p), _ptr(tid) if n else None,
+                              _ptr(tlp) if n else None, _ptr(zt), _ptr(probs))
     if rc != 0:
         raise ValueError("oracle_sample rejected its arguments")
     g = lambda f, dt: np.array([getattr(res[r], f) for r in range(B)], dtype=dt)
@@ -160,7 +177,7 @@ def sample(logits, V, dtype, temperature, top_k, top_p, min_p, presence, frequen
         topp_near=g("topp_near", np.int32), kept_lo=g("kept_lo", np.int32),
         kept_hi=g("kept_hi", np.int32),
         alt_tokens=[list(res[r].alt_tokens[:res[r].n_alt]) for r in range(B)],
-        topn_ids=tid, topn_logprobs=tlp, zt=zt)
+        topn_ids=tid, topn_logprobs=tlp, zt=zt, probs=probs)
 
 
 def _row_hist(ids, offs, r):
@@ -182,12 +199,33 @@ def _concat(outs):
     return OracleOut(**d)
 
 
-def sample_workload(w, want_zt=False, rows=None, mutant=None, seed=None) -> OracleOut:
-    """Run the oracle on a ``workloads.Workload`` (optionally on a subset of rows)."""
-    return sample(w.logits, w.V, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.presence,
+def sample_workload(w, want_zt=False, rows=None, mutant=None, seed=None, top_p=None,
+                    want_probs=False) -> OracleOut:
+    """Run the oracle on a ``workloads.Workload`` (optionally on a subset of rows;
+    ``top_p`` overrides the rows' top_p, e.g. with a decayed effective one)."""
+    return sample(w.logits, w.V, w.dtype, w.temperature, w.top_k,
+                  w.top_p if top_p is None else top_p, w.min_p, w.presence,
                   w.frequency, w.repetition, w.seed if seed is None else seed, w.prompt_ids,
                   w.prompt_offsets, w.output_ids, w.output_offsets, w.num_logprobs,
-                  want_zt=want_zt, mutant=mutant, rows=rows)
+                  want_zt=want_zt, mutant=mutant, rows=rows,
+                  prompt_ignore=getattr(w, "prompt_ignore", None), want_probs=want_probs)
+
+
+def topp_decay(p: float, p_init: float, decay: float, p_min: float, reset_id: int, token: int,
+               mutant=None) -> float:
+    """One top-p decay step after a sampled token (fp32)."""
+    return float(load(mutant).oracle_topp_decay(p, p_init, decay, p_min, reset_id, token))
+
+
+def filtered_probs(zt_row, kept: int, mutant=None) -> np.ndarray:
+    """The filtered distribution of one row of tempered logits whose kept set is
+    the first ``kept`` entries of the total order."""
+    zt_row = np.ascontiguousarray(zt_row, dtype=np.float32)
+    out = np.zeros(zt_row.shape[0], np.float64)
+    rc = load(mutant).oracle_filtered_probs(_ptr(zt_row), zt_row.shape[0], int(kept), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_filtered_probs rejected its arguments")
+    return out
 
 
 def mix64(z: int, mutant=None) -> int:

@@ -88,16 +88,31 @@ void add_alt(oracle_row_result* res, int32_t tok) {
 
 void sample_row(int64_t r, int V, const float* x, float T, int32_t k, float p, float mp,
                 float pres, float freq, float rep, uint64_t seed, const int32_t* pids,
-                int64_t np, const int32_t* oids, int64_t no, int n, oracle_row_result* res,
-                int32_t* topn_ids, double* topn_lp, float* zt_out) {
+                int64_t np, const int32_t* oids, int64_t no, int64_t ignore, int n,
+                oracle_row_result* res, int32_t* topn_ids, double* topn_lp, float* zt_out,
+                double* probs_out) {
   const double nan = std::numeric_limits<double>::quiet_NaN();
   const float finf = std::numeric_limits<float>::infinity();
 
-  // Occurrence counts over the prompt plus the generated output.
-  std::vector<int32_t> c(V, 0);
-  for (int64_t i = 0; i < np; ++i) c[pids[i]]++;
+  // Occurrence counts over the prompt plus the generated output: c for the
+  // repetition penalty, cpf for presence and frequency, which leave out the
+  // first `ignore` prompt tokens (prompt_ignore_length; <= 0 leaves none out,
+  // beyond the prompt it is the whole prompt).
+  const int64_t skip = std::min<int64_t>(std::max<int64_t>(ignore, 0), np);
+  std::vector<int32_t> c(V, 0), cpf(V, 0);
+  for (int64_t i = 0; i < np; ++i) {
+#ifdef ORACLE_MUTANT_IGNORE_ALL
+    if (i >= skip) c[pids[i]]++;  // planted: the ignored prefix skips repetition too
+#else
+    c[pids[i]]++;
+#endif
+    if (i >= skip) cpf[pids[i]]++;
+  }
 #ifndef ORACLE_MUTANT_PROMPT_ONLY
-  for (int64_t i = 0; i < no; ++i) c[oids[i]]++;
+  for (int64_t i = 0; i < no; ++i) {
+    c[oids[i]]++;
+    cpf[oids[i]]++;
+  }
 #endif
 
   // Greedy route: any one of these settings, whatever the others.
@@ -108,17 +123,19 @@ void sample_row(int64_t r, int V, const float* x, float T, int32_t k, float p, f
   std::vector<float> zt(V);
   for (int j = 0; j < V; ++j) {
     float z = x[j];
-    if (c[j] > 0) {
 #ifdef ORACLE_MUTANT_PEN_ORDER
+    if (cpf[j] > 0) {
       z = z - pres;  // planted: presence first
-      z = z - freq * (float)c[j];
-      if (rep != 1.0f) z = (z >= 0.0f) ? z / rep : z * rep;
-#else
-      if (rep != 1.0f) z = (z >= 0.0f) ? z / rep : z * rep;
-      z = z - freq * (float)c[j];
-      z = z - pres;
-#endif
+      z = z - freq * (float)cpf[j];
     }
+    if (c[j] > 0 && rep != 1.0f) z = (z >= 0.0f) ? z / rep : z * rep;
+#else
+    if (c[j] > 0 && rep != 1.0f) z = (z >= 0.0f) ? z / rep : z * rep;
+    if (cpf[j] > 0) {
+      z = z - freq * (float)cpf[j];
+      z = z - pres;
+    }
+#endif
     zt[j] = z * inv_t;
   }
   if (zt_out) std::memcpy(zt_out, zt.data(), sizeof(float) * (size_t)V);
@@ -145,6 +162,8 @@ void sample_row(int64_t r, int V, const float* x, float T, int32_t k, float p, f
     else if (zt[j] != -finf)
       ++finite;
   }
+  if (probs_out)
+    for (int j = 0; j < V; ++j) probs_out[j] = nan;
   if (nonfinite) {
     res->status = ORACLE_ROW_NONFINITE;
     return;
@@ -153,6 +172,8 @@ void sample_row(int64_t r, int V, const float* x, float T, int32_t k, float p, f
     res->status = ORACLE_ROW_EMPTY;
     return;
   }
+  if (probs_out)
+    for (int j = 0; j < V; ++j) probs_out[j] = 0.0;
   res->status = ORACLE_ROW_OK;
 
   // Log-softmax over the full row: global max, then sum of exponentials.
@@ -188,6 +209,7 @@ void sample_row(int64_t r, int V, const float* x, float T, int32_t k, float p, f
     res->logprob = (double)all[0].v - lse;
     res->kept_lo = res->kept_hi = 1;
     add_alt(res, res->token);
+    if (probs_out) probs_out[res->token] = 1.0;
     return;
   }
 
@@ -237,6 +259,13 @@ void sample_row(int64_t r, int V, const float* x, float T, int32_t k, float p, f
   res->kept_count = (int32_t)L3;
   res->kth_value = all[L3 - 1].v;
   res->kth_index = all[L3 - 1].i;
+  // The filtered distribution the draw samples from: the kept prefix,
+  // renormalised (exp(z_t - m) / its sum), zero elsewhere.
+  if (probs_out) {
+    double W = 0.0;
+    for (int64_t i = 0; i < L3; ++i) W += std::exp((double)all[i].v - m);
+    for (int64_t i = 0; i < L3; ++i) probs_out[all[i].i] = std::exp((double)all[i].v - m) / W;
+  }
   res->topp_near = topp_near ? 1 : 0;
   res->kept_lo = (int32_t)lo;
   res->kept_hi = (int32_t)hi;
@@ -324,6 +353,41 @@ int oracle_sample(int64_t first_row, int B, int V, int64_t ld, int dtype, const 
                   const int64_t* prompt_offsets, const int32_t* output_ids,
                   const int64_t* output_offsets, int num_logprobs, oracle_row_result* results,
                   int32_t* topn_ids, double* topn_logprobs, float* zt_out) {
+  return oracle_sample_ex(first_row, B, V, ld, dtype, logits, temperature, top_k, top_p, min_p,
+                          presence, frequency, repetition, seed, prompt_ids, prompt_offsets,
+                          output_ids, output_offsets, nullptr, num_logprobs, results, topn_ids,
+                          topn_logprobs, zt_out, nullptr);
+}
+
+float oracle_topp_decay(float p, float p_init, float decay, float p_min, int32_t reset_id,
+                        int32_t token) {
+  if (token == reset_id) return p_init;
+  const float q = p * decay;
+  return q < p_min ? p_min : q;
+}
+
+int oracle_filtered_probs(const float* zt, int V, int64_t kept, double* probs) {
+  if (!zt || !probs || V <= 0 || kept < 1 || kept > V) return -1;
+  std::vector<Elem> all(V);
+  for (int j = 0; j < V; ++j) all[j] = Elem{zt[j], j};
+  std::sort(all.begin(), all.end(), before);
+  if (!std::isfinite(all[kept - 1].v)) return -1;
+  const double m = (double)all[0].v;
+  double W = 0.0;
+  for (int64_t i = 0; i < kept; ++i) W += std::exp((double)all[i].v - m);
+  for (int j = 0; j < V; ++j) probs[j] = 0.0;
+  for (int64_t i = 0; i < kept; ++i) probs[all[i].i] = std::exp((double)all[i].v - m) / W;
+  return 0;
+}
+
+int oracle_sample_ex(int64_t first_row, int B, int V, int64_t ld, int dtype, const void* logits,
+                     const float* temperature, const int32_t* top_k, const float* top_p,
+                     const float* min_p, const float* presence, const float* frequency,
+                     const float* repetition, const uint64_t* seed, const int32_t* prompt_ids,
+                     const int64_t* prompt_offsets, const int32_t* output_ids,
+                     const int64_t* output_offsets, const int32_t* prompt_ignore,
+                     int num_logprobs, oracle_row_result* results, int32_t* topn_ids,
+                     double* topn_logprobs, float* zt_out, double* probs) {
   if (first_row < 0 || B < 0 || V <= 0 || ld < V || num_logprobs < 0 || !results) return -1;
   if (B > 0 && (!logits || !temperature || !top_k || !top_p || !min_p || !presence ||
                 !frequency || !repetition || !seed || !prompt_offsets || !output_offsets))
@@ -354,10 +418,11 @@ int oracle_sample(int64_t first_row, int B, int V, int64_t ld, int dtype, const 
     const int64_t pa = prompt_offsets[r], oa = output_offsets[r];
     sample_row(first_row + r, V, x.data(), temperature[r], top_k[r], top_p[r], min_p[r], presence[r],
                frequency[r], repetition[r], seed[r], prompt_ids + pa, prompt_offsets[r + 1] - pa,
-               output_ids + oa, output_offsets[r + 1] - oa, num_logprobs, &results[r],
+               output_ids + oa, output_offsets[r + 1] - oa, prompt_ignore ? prompt_ignore[r] : 0,
+               num_logprobs, &results[r],
                num_logprobs ? topn_ids + (int64_t)r * num_logprobs : nullptr,
                num_logprobs ? topn_logprobs + (int64_t)r * num_logprobs : nullptr,
-               zt_out ? zt_out + (int64_t)r * V : nullptr);
+               zt_out ? zt_out + (int64_t)r * V : nullptr, probs ? probs + (int64_t)r * V : nullptr);
   }
   return 0;
 }

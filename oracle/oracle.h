@@ -8,7 +8,9 @@
  * What it computes, per row r (sources named by page and section):
  *   counts       c_j = occurrences of j in the prompt ids plus the output ids
  *                (TensorRT-LLM "Sampling", occurrence penalties: the history is
- *                the prompt plus everything generated so far);
+ *                the prompt plus everything generated so far); presence and
+ *                frequency count without the first prompt_ignore_length prompt
+ *                tokens, which still count for repetition (same section);
  *   greedy route T == 0 or top_k == 1 or top_p == 0 or min_p == 1 (same page,
  *                "LLM API sampling behavior": greedy whatever the rest);
  *   penalties    repetition, then frequency, then presence, fp32, no FMA;
@@ -21,7 +23,13 @@
  *   draw         argmax over kept j of z_t - ln(-ln u_j), u_j from a SplitMix64
  *                stream keyed by (seed, row, j); lowest index on equal scores
  *                (vllm.cpp PR "the Gumbel draw that scanned 248,320 tokens on
- *                one thread": GumbelScore, ExpNoise, ArgReduce).
+ *                one thread": GumbelScore, ExpNoise, ArgReduce);
+ *   probabilities the filtered distribution the draw samples from, on request
+ *                (TensorRT-LLM "Sampling", Performance: the sampling
+ *                probabilities after the top-k / top-p masking);
+ *   top-p decay  after each sampled token the effective top_p becomes
+ *                max(top_p * decay, top_p_min), or the initial top_p when the
+ *                token is top_p_reset_ids (same page, "Top-P decay").
  */
 #ifndef VT_ORACLE_H
 #define VT_ORACLE_H
@@ -82,6 +90,34 @@ int oracle_sample(int64_t first_row, int B, int V, int64_t ld, int dtype, const 
                   const int32_t* output_ids, const int64_t* output_offsets,
                   int num_logprobs, oracle_row_result* results, int32_t* topn_ids,
                   double* topn_logprobs, float* zt_out);
+
+/* oracle_sample with two more inputs and one more output:
+ *   prompt_ignore  optional [B]: per row, the first prompt_ignore[r] prompt ids
+ *                  count for the repetition penalty only (<= 0: none; beyond
+ *                  the prompt: the whole prompt); NULL for none.
+ *   probs          optional [B][V] output: the filtered distribution the draw
+ *                  samples from (the kept prefix of the total order, each
+ *                  exp(z_t - m) over their sum; zero elsewhere; one-hot on a
+ *                  greedy row; NaN on a row with status != 0). */
+int oracle_sample_ex(int64_t first_row, int B, int V, int64_t ld, int dtype, const void* logits,
+                     const float* temperature, const int32_t* top_k, const float* top_p,
+                     const float* min_p, const float* presence, const float* frequency,
+                     const float* repetition, const uint64_t* seed,
+                     const int32_t* prompt_ids, const int64_t* prompt_offsets,
+                     const int32_t* output_ids, const int64_t* output_offsets,
+                     const int32_t* prompt_ignore, int num_logprobs,
+                     oracle_row_result* results, int32_t* topn_ids, double* topn_logprobs,
+                     float* zt_out, double* probs);
+
+/* One top-p decay step after a sampled token, in fp32: the initial top_p when
+ * token == reset_id, else max(p * decay, p_min). */
+float oracle_topp_decay(float p, float p_init, float decay, float p_min, int32_t reset_id,
+                        int32_t token);
+
+/* The filtered distribution of one row of tempered logits zt[V] whose kept
+ * set is the first `kept` entries of the total order (z_t descending, index
+ * ascending): probs[V].  Returns 0, or -1 on bad arguments. */
+int oracle_filtered_probs(const float* zt, int V, int64_t kept, double* probs);
 
 /* The SplitMix64 finaliser (Steele, Lea and Flood 2014; the public-domain
  * splitmix64.c generator applies it to state += 0x9E3779B97F4A7C15). */

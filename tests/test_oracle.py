@@ -43,7 +43,8 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 # --------------------------------------------------------------------------
 
 def run_rows(x, *, T=1.0, k=0, p=1.0, mp=0.0, pres=0.0, freq=0.0, rep=1.0, seeds=None,
-             prompt=None, output=None, n=0, mutant=None, want_zt=False, first_row=0):
+             prompt=None, output=None, n=0, mutant=None, want_zt=False, first_row=0,
+             ignore=None, want_probs=False):
     """Oracle on fp32 rows ``x[B, V]`` with scalar or per-row params."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     B, V = x.shape
@@ -56,7 +57,9 @@ def run_rows(x, *, T=1.0, k=0, p=1.0, mp=0.0, pres=0.0, freq=0.0, rep=1.0, seeds
                     full(p, np.float32), full(mp, np.float32), full(pres, np.float32),
                     full(freq, np.float32), full(rep, np.float32),
                     np.asarray(seeds, dtype=np.uint64), pi, po, oi, oo, n, want_zt=want_zt,
-                    mutant=mutant, first_row=first_row)
+                    mutant=mutant, first_row=first_row,
+                    prompt_ignore=None if ignore is None else full(ignore, np.int32),
+                    want_probs=want_probs)
 
 
 def total_order(z):
@@ -162,6 +165,23 @@ def check_penalty_cases(mutant=None):
         assert got == want, (x, c, rep, freq, pres, got, want)
         assert math.copysign(1.0, got) == math.copysign(1.0, want)
         assert list(o.zt[0, 1:]) == [0.5, -0.5, 1.0]  # unseen tokens untouched
+
+
+def check_prompt_ignore_cases(mutant=None):
+    # TensorRT-LLM "Sampling", occurrence penalties: prompt_ignore_length
+    rows = []
+    for line in open(os.path.join(GOLDEN, "prompt_ignore_cases.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            rows.append(line.split())
+    assert len(rows) == 8
+    for x, npr, nout, N, rep, freq, pres, want in rows:
+        row = np.array([[float(x), 0.5, -0.5, 1.0]], np.float32)
+        o = run_rows(row, rep=float(rep), freq=float(freq), pres=float(pres),
+                     prompt=[np.zeros(int(npr), np.int32)], output=[np.zeros(int(nout), np.int32)],
+                     ignore=int(N), want_zt=True, mutant=mutant)
+        assert float(o.zt[0, 0]) == float(want), (x, npr, nout, N, float(o.zt[0, 0]), want)
+        assert list(o.zt[0, 1:]) == [0.5, -0.5, 1.0]
 
 
 def check_counts(mutant=None):
@@ -416,6 +436,7 @@ MUTANT_CHECKS = {
     "TOPP_INCL": [check_filters_bruteforce, check_two_value_closed_form],
     "TOPP_NO_RENORM": [check_filters_bruteforce],
     "SCORE_MUL": [lambda mutant: check_draw_distribution(mutant, n_draws=200_000)],
+    "IGNORE_ALL": [check_prompt_ignore_cases],
 }
 
 
@@ -425,3 +446,85 @@ def test_planted_mistakes_are_caught(oracle_mod, mutant):
     for chk in MUTANT_CHECKS[mutant]:
         with pytest.raises(AssertionError):
             chk(mutant=mutant)
+
+
+# --------------------------------------------------------------------------
+# prompt_ignore_length, the filtered distribution, top-p decay
+# --------------------------------------------------------------------------
+
+def test_prompt_ignore_hand_cases(oracle_mod):
+    check_prompt_ignore_cases()
+
+
+def test_prompt_ignore_token_only_in_the_ignored_prefix(oracle_mod):
+    # token 1 only in the ignored prefix: repetition alone; token 2 once after
+    # it: all three penalties; token 3 unseen
+    row = np.array([[0.0, 3.0, 3.0, 3.0]], np.float32)
+    o = run_rows(row, rep=2.0, freq=0.5, pres=0.25, prompt=[np.array([1, 1, 2], np.int32)],
+                 ignore=2, want_zt=True)
+    assert list(o.zt[0]) == [0.0, 1.5, 0.75, 3.0]  # 3/2 ; 3/2 - 0.5 - 0.25 ; untouched
+
+
+def test_prompt_ignore_zero_matches_no_ignore(oracle_mod):
+    rng = np.random.default_rng(31)
+    x = rng.normal(0, 2, size=(3, 200)).astype(np.float32)
+    pr = [rng.integers(0, 200, 50).astype(np.int32) for _ in range(3)]
+    ou = [rng.integers(0, 200, 20).astype(np.int32) for _ in range(3)]
+    a = run_rows(x, rep=1.2, freq=0.3, pres=0.4, prompt=pr, output=ou, want_zt=True, n=4)
+    b = run_rows(x, rep=1.2, freq=0.3, pres=0.4, prompt=pr, output=ou, want_zt=True, n=4,
+                 ignore=[0, -5, 0])
+    assert np.array_equal(a.zt, b.zt) and np.array_equal(a.token, b.token)
+
+
+def check_probs(mutant=None):
+    rng = np.random.default_rng(41)
+    for trial in range(60):
+        V = int(rng.integers(3, 9))
+        z = np.round(rng.normal(0, 1.5, size=(1, V)), 1).astype(np.float32)
+        k = int(rng.choice([0, 2, V - 1, V]))  # k == 1 is the greedy route, checked apart
+        p = float(rng.choice([1.0, 0.3, 0.6, 0.9]))
+        mp = float(rng.choice([0.0, 0.1, 0.4]))
+        o = run_rows(z, k=k, p=p, mp=mp, want_probs=True, want_zt=True, mutant=mutant)
+        if o.topp_near[0]:
+            continue
+        kept = kept_by_definition(o.zt[0], k, p, mp)
+        pr = o.probs[0]
+        assert set(np.nonzero(pr)[0]) == set(kept), (trial, kept, pr)
+        assert abs(pr.sum() - 1.0) <= 1e-12
+        i0 = kept[0]
+        for i in kept:  # each kept token's weight relative to the most probable one
+            assert abs(pr[i] / pr[i0] - math.exp(float(o.zt[0, i]) - float(o.zt[0, i0]))) <= 1e-12
+
+
+def test_filtered_distribution_by_definition(oracle_mod):
+    # TensorRT-LLM "Sampling", Performance: the sampling probabilities after the
+    # top-k / top-p masking, i.e. the kept set renormalised
+    check_probs()
+
+
+def test_filtered_distribution_greedy_and_helper(oracle_mod):
+    rng = np.random.default_rng(43)
+    z = rng.normal(0, 1, size=(2, 50)).astype(np.float32)
+    g = run_rows(z, T=0.0, want_probs=True)
+    for r in range(2):
+        assert g.probs[r, g.token[r]] == 1.0 and g.probs[r].sum() == 1.0
+    o = run_rows(z, T=0.7, k=10, p=0.8, want_probs=True, want_zt=True)
+    for r in range(2):
+        np.testing.assert_array_equal(O.filtered_probs(o.zt[r], o.kept_count[r]), o.probs[r])
+    bad = z.copy()
+    bad[0, 3] = np.nan
+    b = run_rows(bad, T=1.0, want_probs=True)
+    assert np.isnan(b.probs[0]).all() and not np.isnan(b.probs[1]).any()
+
+
+def test_topp_decay_steps(oracle_mod):
+    # TensorRT-LLM "Sampling", Top-P decay: multiplied by the decay after every
+    # sampled token, bounded below by top_p_min, reset to the initial top_p
+    # when the token top_p_reset_ids is sampled (-1 never matches)
+    p, seq = 0.5, []
+    for tok in [3, 3, 3, 7, 3]:
+        p = O.topp_decay(p, 0.5, 0.5, 0.1, 7, tok)
+        seq.append(p)
+    assert seq == [0.25, 0.125, float(np.float32(0.1)), 0.5, 0.25]
+    assert O.topp_decay(0.3, 0.9, 1.0, 1e-6, -1, 0) == float(np.float32(0.3))
+    assert O.topp_decay(0.3, 0.9, 0.5, 1e-6, -1, -1) == float(np.float32(0.9))
