@@ -1,11 +1,15 @@
 // vt_counts.cu -- per-row token-count tables for the occurrence penalties.
 //
 // The penalties of the TensorRT-LLM "Sampling" page use c_j, the number of
-// times token j occurs in the prompt plus everything generated so far.  At a
-// counts reset each row's raw ids (prompt then output, CSR) are sorted in
-// shared memory and run-length encoded into a table of distinct ids in
-// increasing order with their counts.  The sampling kernel reads the slice of
-// the table that falls in each CTA's part of the row and appends drawn tokens.
+// times token j occurs in the prompt plus everything generated so far; the
+// first prompt_ignore_length prompt tokens count for the repetition penalty
+// only.  At a counts reset each row's raw occurrences (prompt then output,
+// CSR; each (id << 1) | ignored) are sorted in shared memory and run-length
+// encoded into a table of distinct ids in increasing order, each with the
+// number of its occurrences that count for presence and frequency (possibly
+// 0: an id in the table is seen, for repetition).  The sampling kernel reads
+// the slice of the table that falls in each CTA's part of the row and
+// appends drawn tokens.
 #include "vt_device.cuh"
 #include "vt_kernels.h"
 
@@ -50,7 +54,7 @@ __global__ void __launch_bounds__(kCountThreads)
   const int per = (len + kCountThreads - 1) / kCountThreads;
   const int i0 = min(len, (int)threadIdx.x * per), i1 = min(len, i0 + per);
   int starts = 0;
-  for (int i = i0; i < i1; ++i) starts += (i == 0 || keys[i] != keys[i - 1]);
+  for (int i = i0; i < i1; ++i) starts += (i == 0 || (keys[i] >> 1) != (keys[i - 1] >> 1));
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int inc = starts;
 #pragma unroll
@@ -75,15 +79,16 @@ __global__ void __launch_bounds__(kCountThreads)
   int pos = warp_off[warp] + inc - starts;
   int2* out = hist + (int64_t)row * hist_cap;
   for (int i = i0; i < i1; ++i) {
-    if (i == 0 || keys[i] != keys[i - 1]) {
-      // run length: first index whose key is larger (binary search)
-      int lo = i + 1, hi = len;
-      const int key = keys[i];
+    if (i == 0 || (keys[i] >> 1) != (keys[i - 1] >> 1)) {
+      // the id's counted occurrences (flag 0) sort first: they end at the
+      // first key above (id << 1) (binary search)
+      int lo = i, hi = len;
+      const int key = keys[i] & ~1;
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         if (keys[mid] > key) hi = mid; else lo = mid + 1;
       }
-      out[pos++] = make_int2(key, lo - i);
+      out[pos++] = make_int2(key >> 1, lo - i);
     }
   }
 }

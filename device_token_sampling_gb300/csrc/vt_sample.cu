@@ -582,14 +582,17 @@ __device__ __forceinline__ bool minp_pass(float zt, float m_t, double lmp) {
   return (double)zt - (double)m_t >= lmp;
 }
 
-// Occurrence penalties of one seen token: repetition, frequency, presence
-// (fp32, each operation rounded once).
+// Occurrence penalties of one seen token (fp32, each operation rounded
+// once): repetition for any occurrence, then frequency and presence when
+// `count` (its occurrences outside the ignored prompt prefix) is positive.
 __device__ __forceinline__ float penalize(float x, int count, const RowParams& P) {
   float z = x;
   if (P.repetition != 1.0f)
     z = (z >= 0.0f) ? __fdiv_rn(z, P.repetition) : __fmul_rn(z, P.repetition);
-  z = __fsub_rn(z, __fmul_rn(P.frequency, (float)count));
-  z = __fsub_rn(z, P.presence);
+  if (count > 0) {
+    z = __fsub_rn(z, __fmul_rn(P.frequency, (float)count));
+    z = __fsub_rn(z, P.presence);
+  }
   return z;
 }
 

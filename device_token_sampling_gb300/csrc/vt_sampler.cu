@@ -365,6 +365,14 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
 int vt_reset_token_counts(vt_sampler* h, int32_t B, const int32_t* prompt_ids,
                           const int64_t* prompt_offsets, const int32_t* output_ids,
                           const int64_t* output_offsets, void* stream) {
+  return vt_reset_token_counts_ex(h, B, prompt_ids, prompt_offsets, output_ids, output_offsets,
+                                  nullptr, stream);
+}
+
+int vt_reset_token_counts_ex(vt_sampler* h, int32_t B, const int32_t* prompt_ids,
+                             const int64_t* prompt_offsets, const int32_t* output_ids,
+                             const int64_t* output_offsets, const int32_t* prompt_ignore_length,
+                             void* stream) {
   if (!h) return VT_ERR_INVALID_ARG;
   if (B < 1) return set_err(h, VT_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
   if (B > h->cfg.max_batch)
@@ -392,20 +400,25 @@ int vt_reset_token_counts(vt_sampler* h, int32_t B, const int32_t* prompt_ids,
     VT_CK(h, cudaEventSynchronize(h->ev_counts));
     h->counts_pending = false;
   }
+  // Each occurrence goes up as (id << 1) | ignored: ignored occurrences (the
+  // first prompt_ignore_length prompt ids) count for repetition only.
   int64_t w = 0;
   h->h_raw_offs[0] = 0;
   for (int r = 0; r < B; ++r) {
+    const int64_t skip = prompt_ignore_length && prompt_ignore_length[r] > 0
+                             ? (int64_t)prompt_ignore_length[r]
+                             : 0;
     for (int64_t i = prompt_offsets[r]; i < prompt_offsets[r + 1]; ++i) {
       const int32_t id = prompt_ids[i];
       if (id < 0 || id >= h->cfg.max_vocab)
         return set_err(h, VT_ERR_INVALID_ARG, "row %d: prompt id %d out of range", r, id);
-      h->h_raw[w++] = id;
+      h->h_raw[w++] = (id << 1) | (i - prompt_offsets[r] < skip ? 1 : 0);
     }
     for (int64_t i = output_offsets[r]; i < output_offsets[r + 1]; ++i) {
       const int32_t id = output_ids[i];
       if (id < 0 || id >= h->cfg.max_vocab)
         return set_err(h, VT_ERR_INVALID_ARG, "row %d: output id %d out of range", r, id);
-      h->h_raw[w++] = id;
+      h->h_raw[w++] = id << 1;
     }
     h->h_raw_offs[r + 1] = w;
   }

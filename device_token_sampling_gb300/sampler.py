@@ -59,6 +59,7 @@ SIGNATURES = {
     "vt_sampler_destroy": (None, [P]),
     "vt_reset_params": (C.c_int, [P, I32, P, P, P, P, P, P, P, P, P]),
     "vt_reset_token_counts": (C.c_int, [P, I32, P, P, P, P, P]),
+    "vt_reset_token_counts_ex": (C.c_int, [P, I32, P, P, P, P, P, P]),
     "vt_sample": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
     "vt_sample_host": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
     "vt_check_device_errors": (C.c_int, [P]),
@@ -174,7 +175,7 @@ class Sampler:
         self._check(rc, "vt_reset_params")
 
     def reset_token_counts(self, prompt_ids, prompt_offsets, output_ids, output_offsets,
-                           stream=None):
+                           stream=None, prompt_ignore=None):
         pi = np.ascontiguousarray(prompt_ids, np.int32)
         po = np.ascontiguousarray(prompt_offsets, np.int64)
         oi = np.ascontiguousarray(output_ids, np.int32)
@@ -182,9 +183,17 @@ class Sampler:
         B = po.shape[0] - 1
         if oo.shape[0] != B + 1:
             raise ValueError("prompt and output offsets disagree on B")
-        rc = self._lib.vt_reset_token_counts(self._h, B, _np_ptr(pi), _np_ptr(po), _np_ptr(oi),
-                                             _np_ptr(oo), _stream_ptr(stream))
-        self._check(rc, "vt_reset_token_counts")
+        if prompt_ignore is None:
+            rc = self._lib.vt_reset_token_counts(self._h, B, _np_ptr(pi), _np_ptr(po),
+                                                 _np_ptr(oi), _np_ptr(oo), _stream_ptr(stream))
+            self._check(rc, "vt_reset_token_counts")
+            return
+        ig = np.ascontiguousarray(prompt_ignore, np.int32)
+        if ig.shape != (B,):
+            raise ValueError("prompt_ignore must have shape (B,)")
+        rc = self._lib.vt_reset_token_counts_ex(self._h, B, _np_ptr(pi), _np_ptr(po), _np_ptr(oi),
+                                                _np_ptr(oo), _np_ptr(ig), _stream_ptr(stream))
+        self._check(rc, "vt_reset_token_counts_ex")
 
     def reset_workload(self, w, stream=None):
         """Reset params, seeds and counts from a ``workloads.Workload``."""
@@ -192,7 +201,8 @@ class Sampler:
                           w.repetition, w.seed, stream=stream)
         if self.cfg.max_history > 0:
             self.reset_token_counts(w.prompt_ids, w.prompt_offsets, w.output_ids,
-                                    w.output_offsets, stream=stream)
+                                    w.output_offsets, stream=stream,
+                                    prompt_ignore=getattr(w, "prompt_ignore", None))
 
     # -- sampling ------------------------------------------------------------
     def sample(self, logits, V: int | None = None, num_logprobs: int = 0,

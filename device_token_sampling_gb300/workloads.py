@@ -66,6 +66,9 @@ class Workload:
     output_offsets: np.ndarray
     num_logprobs: int
     notes: dict = field(default_factory=dict)
+    # per row: the first prompt_ignore[r] prompt ids count for the repetition
+    # penalty only (None: 0 on every row)
+    prompt_ignore: np.ndarray | None = None
 
     @property
     def elem_size(self) -> int:

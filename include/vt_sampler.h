@@ -124,6 +124,19 @@ int vt_reset_token_counts(vt_sampler* handle, int32_t B, const int32_t* prompt_i
                           const int64_t* prompt_offsets, const int32_t* output_ids,
                           const int64_t* output_offsets, void* stream);
 
+/* vt_reset_token_counts with each row's prompt_ignore_length (TensorRT-LLM
+ * "Sampling", occurrence penalties): the first prompt_ignore_length[r] prompt
+ * ids of row r are left out of the presence and frequency counts and still
+ * count for the repetition penalty.  Values <= 0 leave none out; values
+ * beyond the row's prompt leave the whole prompt out.  prompt_ignore_length
+ * is a host array of B entries, or NULL (none left out: vt_reset_token_counts).
+ * A token the call appends to the counts (update_counts) always counts for
+ * all three.  Errors as vt_reset_token_counts. */
+int vt_reset_token_counts_ex(vt_sampler* handle, int32_t B, const int32_t* prompt_ids,
+                             const int64_t* prompt_offsets, const int32_t* output_ids,
+                             const int64_t* output_offsets, const int32_t* prompt_ignore_length,
+                             void* stream);
+
 /* Sample one token for each of rows 0..B-1.
  *   logits            device [B][ld] elements of `dtype`; row r starts at
  *                     logits + r*ld; only columns [0, V) are read.  Rows whose
