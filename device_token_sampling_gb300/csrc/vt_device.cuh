@@ -29,6 +29,7 @@ enum : uint32_t {
   kRowTopP = 2u,     // 0 < top_p < 1
   kRowMinP = 4u,     // 0 < min_p < 1
   kRowPenalty = 8u,  // any of presence, frequency, repetition is active
+  kRowDecay = 16u,   // top-p decay: the effective top_p lives in the row's DecayState
 };
 
 struct __align__(16) RowParams {
@@ -42,6 +43,19 @@ struct __align__(16) RowParams {
   float min_p;
   double log_min_p;   // log((double)min_p), computed on the host
   double pad_;
+};
+
+// Row status codes (match VT_ROW_* in the public header).
+constexpr int kRowOk = 0, kRowNonfinite = 1, kRowEmpty = 2, kRowHistoryFull = 3;
+
+// Top-p decay state of one row [TensorRT-LLM "Sampling", top-p decay]: the
+// effective top_p the next call samples with, and the rule that moves it
+// after each sampled token (the initial top_p is RowParams::top_p).
+struct __align__(16) DecayState {
+  float p;            // effective top_p
+  float decay;        // (0, 1]
+  float p_min;        // (0, 1]
+  int32_t reset_id;   // >= -1; -1 never matches
 };
 
 // ---- small PTX wrappers ----------------------------------------------------
@@ -176,6 +190,20 @@ __device__ __forceinline__ bool may_beat(float zt, float s_cur, uint32_t b) {
   const float one_minus_u = (float)(2u * (0xFFFFFFu - b) + 1u) * 0x1p-25f;
   const float t = ex2_approx(__fmul_rn(__fsub_rn(zt, s_cur), kLog2e));
   return one_minus_u < t * 1.00390625f;
+}
+
+// Occurrence penalties of one seen token (fp32, each operation rounded
+// once): repetition for any occurrence, then frequency and presence when
+// `count` (its occurrences outside the ignored prompt prefix) is positive.
+__device__ __forceinline__ float penalize(float x, int count, const RowParams& P) {
+  float z = x;
+  if (P.repetition != 1.0f)
+    z = (z >= 0.0f) ? __fdiv_rn(z, P.repetition) : __fmul_rn(z, P.repetition);
+  if (count > 0) {
+    z = __fsub_rn(z, __fmul_rn(P.frequency, (float)count));
+    z = __fsub_rn(z, P.presence);
+  }
+  return z;
 }
 
 // ---- order-preserving keys -------------------------------------------------

@@ -8,6 +8,7 @@
 namespace vt {
 
 struct RowParams;
+struct DecayState;
 
 // A row the streaming kernel hands to the selection kernel.
 struct __align__(16) SlowRow {
@@ -35,6 +36,7 @@ struct SampleArgs {
   uint32_t off_prefix;
   const RowParams* params;   // [B]
   uint64_t* seeds;           // [B], advanced by the kernel
+  DecayState* decay;         // [B] top-p decay state (rows with kRowDecay), may be null
   int2* hist;                // [B][hist_cap] sorted (id, count)
   int32_t* hist_len;         // [B]
   int32_t hist_cap;
@@ -114,5 +116,42 @@ cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, in
 cudaError_t launch_build_counts(const int32_t* raw, const int64_t* offs, int max_len, int B,
                                 int2* hist, int32_t* hist_len, int32_t hist_cap,
                                 cudaStream_t stream);
+
+// Append each sampled row's token to its count table (rows whose status is
+// not ok are left alone; a full table sets status VT_ROW_HISTORY_FULL), as
+// the sampling kernels do when they update the counts themselves.
+cudaError_t launch_append(int2* hist, int32_t* hist_len, int32_t hist_cap, const int32_t* tokens,
+                          int32_t* row_status, int B, cudaStream_t stream);
+
+// ---- the filtered distribution on request (vt_probs.cu) ---------------------
+constexpr int kProbsMaxRange = 65536;  // elements per CTA at most
+constexpr int kProbsMaxSplits = 64;    // CTAs per row at most (unless V needs more)
+constexpr int kProbsCtasPerSm = 6;     // the grid aims at this many CTAs per SM
+
+struct ProbsArgs {
+  const void* logits;          // [B][ld] elements, as sampled
+  int64_t ld;
+  int32_t B, V;
+  int32_t splits, range;       // CTAs per row, elements per CTA (multiple of 64)
+  int32_t vec_in;              // rows 16-byte aligned: 16-byte loads
+  int32_t vec_out;             // output rows 16-byte aligned: 16-byte stores
+  const RowParams* params;     // [B]
+  const int2* hist;            // [B][hist_cap] sorted (id, count), may be null
+  const int32_t* hist_len;
+  int32_t hist_cap;
+  const int32_t* tokens;       // [B] the drawn tokens
+  const int32_t* row_status;   // [B]
+  const float* kth_value;      // [B] the last kept element: value, index
+  const int32_t* kth_index;
+  float2* part;                // [B * splits] (max, exp-sum) partials
+  float* probs;                // [B][ld_probs] fp32 output
+  int64_t ld_probs;
+};
+
+// CTAs per row and elements per CTA for B rows of V.
+void plan_probs(int B, int V, int num_sms, int* splits, int* range);
+
+// The two launches (partials, then the probabilities) on `stream`.
+cudaError_t launch_probs(const ProbsArgs& args, int dtype, cudaStream_t stream);
 
 }  // namespace vt

@@ -252,6 +252,7 @@ extern "C" int vt_sample_noalloc(int32_t device, const void* logits, int32_t dty
   a.off_prefix = plan.off_prefix;
   a.params = d_params;
   a.seeds = d_seeds;
+  a.decay = nullptr;  // no top-p decay on this path
   a.hist = nullptr;  // read only for rows with penalties or with update_counts
   a.hist_len = d_hist_len;
   a.hist_cap = 1;

@@ -55,9 +55,6 @@ constexpr int kSmallK = 32;  // up to this many per CTA, thresholds come from th
 static_assert(kBufCap * 8 <= kRingBytes, "the candidate buffer lives in the ring region");
 static_assert((1 << 10) * 16 <= kBufCap * 8, "selection histograms exceed the gather buffer");
 
-// Row status codes (match VT_ROW_* in the public header).
-constexpr int kRowOk = 0, kRowNonfinite = 1, kRowEmpty = 2, kRowHistoryFull = 3;
-
 template <typename T>
 struct Elt;
 
@@ -580,20 +577,6 @@ __device__ __forceinline__ bool minp_pass(float zt, float m_t, double lmp) {
   if (d > l + margin) return true;
   if (d < l - margin) return false;
   return (double)zt - (double)m_t >= lmp;
-}
-
-// Occurrence penalties of one seen token (fp32, each operation rounded
-// once): repetition for any occurrence, then frequency and presence when
-// `count` (its occurrences outside the ignored prompt prefix) is positive.
-__device__ __forceinline__ float penalize(float x, int count, const RowParams& P) {
-  float z = x;
-  if (P.repetition != 1.0f)
-    z = (z >= 0.0f) ? __fdiv_rn(z, P.repetition) : __fmul_rn(z, P.repetition);
-  if (count > 0) {
-    z = __fsub_rn(z, __fmul_rn(P.frequency, (float)count));
-    z = __fsub_rn(z, P.presence);
-  }
-  return z;
 }
 
 // ---------------------------------------------------------------------------
@@ -1241,8 +1224,13 @@ __device__ RowParams init_row(Ctx& c, const SampleArgs& a, uint8_t* dsm, int row
   c.ax = P.inv_t * kLog2e;
   c.top_k = P.top_k;
   c.top_p = P.top_p;
+  bool topp = (P.flags & kRowTopP) != 0;
+  if (P.flags & kRowDecay) {  // the decayed top_p; 1 (the start) filters nothing
+    c.top_p = a.decay[row].p;
+    topp = c.top_p < 1.0f;
+  }
   c.topk = !c.greedy && P.top_k > 1 && P.top_k < a.V;
-  c.topp = !c.greedy && (P.flags & kRowTopP) != 0;
+  c.topp = !c.greedy && topp;
   c.minp = !c.greedy && (P.flags & kRowMinP) != 0;
   c.lmp = P.log_min_p;
   c.rkey = row_key(a.seeds[row], row);
@@ -1578,7 +1566,18 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
 
 // Outputs of a row whose statistics make it unsampleable (non-finite values,
 // or no finite value): token -1, NaN log-probs, the status; the seed still
-// advances.  The row's leader CTA calls it.
+// advances and the top-p decay state stays.  The row's leader CTA calls it.
+// Top-p decay after the row's sampled token [TensorRT-LLM "Sampling", top-p
+// decay]: back to the initial top_p when the token is the reset id, else
+// max(top_p * decay, top_p_min), in fp32.  One thread of the row calls it.
+__device__ __forceinline__ void decay_top_p(const SampleArgs& a, int row, int tok) {
+  const RowParams& P = a.params[row];
+  if (!(P.flags & kRowDecay)) return;
+  DecayState& d = a.decay[row];
+  const float q = __fmul_rn(d.p, d.decay);
+  d.p = tok == d.reset_id ? P.top_p : (q < d.p_min ? d.p_min : q);
+}
+
 __device__ __forceinline__ void write_bad_row(const SampleArgs& a, const Smem& s, int row,
                                               int status) {
   const int n = a.n_logprobs;
@@ -1882,6 +1881,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
       a.dbg_kth_index[c.row] = c.greedy ? tok : (int)key_idx(kk);
       a.dbg_kept[c.row] = L3;
       a.seeds[c.row] += kSeedStep;
+      decay_top_p(a, c.row, tok);
       if (s.rs.err) atomicOr(a.err_word, s.rs.err);
     }
     VT_TRACE(9);
@@ -2640,6 +2640,7 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         a.dbg_kth_index[row] = kth_i;
         a.dbg_kept[row] = kept;
         a.seeds[row] += kSeedStep;
+        decay_top_p(a, row, tok);
         er |= s.rs.err | s.part.err;
         if (er) atomicOr(a.err_word, er);
       }
@@ -2891,6 +2892,7 @@ __device__ __noinline__ void slow_row(Ctx& c, Smem& s, const SampleArgs& a, cg::
     a.dbg_kth_index[c.row] = kth_i;
     a.dbg_kept[c.row] = kept;
     a.seeds[c.row] += kSeedStep;
+    decay_top_p(a, c.row, tok);
     const int er = s.rs.err | s.part.err;
     if (er) atomicOr(a.err_word, er);
   }
@@ -3048,6 +3050,17 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const SampleArgs a,
       __threadfence();
     }
   }
+}
+
+// The count-table append on its own (one CTA per row): used when the call
+// exports the filtered distribution, which needs the counts the draw saw.
+__global__ void __launch_bounds__(kThreads) append_kernel(int2* hist, int32_t* hist_len,
+                                                          int32_t cap, const int32_t* tokens,
+                                                          int32_t* row_status) {
+  __shared__ Smem s;
+  const int row = blockIdx.x;
+  if (row_status[row] != kRowOk) return;  // uniform over the CTA
+  append_token(hist + (int64_t)row * cap, hist_len + row, cap, tokens[row], s, row_status + row);
 }
 
 }  // namespace
@@ -3310,6 +3323,13 @@ cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, in
   cfg.gridDim = dim3((unsigned)(args.B * plan.own.cluster), 1, 1);
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, select_kernel<uint16_t>, args, plan.own);
+}
+
+cudaError_t launch_append(int2* hist, int32_t* hist_len, int32_t hist_cap, const int32_t* tokens,
+                          int32_t* row_status, int B, cudaStream_t stream) {
+  if (B < 1) return cudaSuccess;
+  append_kernel<<<B, kThreads, 0, stream>>>(hist, hist_len, hist_cap, tokens, row_status);
+  return cudaGetLastError();
 }
 
 }  // namespace vt

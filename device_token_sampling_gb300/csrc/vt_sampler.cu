@@ -30,6 +30,7 @@ struct vt_sampler {
   // device state and scratch
   vt::RowParams* d_params = nullptr;
   uint64_t* d_seeds = nullptr;
+  vt::DecayState* d_decay = nullptr;  // [max_batch] top-p decay state
   int2* d_hist = nullptr;
   int32_t* d_hist_len = nullptr;
   float* d_zside = nullptr;
@@ -44,6 +45,8 @@ struct vt_sampler {
   int32_t* d_slow_list = nullptr;  // [2][max_batch]: one list per launch pair
   uint32_t* d_slow_ctl = nullptr;  // [2][4]
   int32_t* d_rows = nullptr;       // [max_batch]: main rows, then side rows
+  float2* d_probs_part = nullptr;  // (max, exp-sum) partials of the filtered distribution
+  size_t probs_part_cap = 0;
   // the side stream: rows routed straight to the selection kernel run there,
   // beside the main stream's launches (fork and join through events)
   cudaStream_t side = nullptr;
@@ -53,6 +56,7 @@ struct vt_sampler {
   // pinned host staging
   vt::RowParams* h_params = nullptr;
   uint64_t* h_seeds = nullptr;
+  vt::DecayState* h_decay = nullptr;
   int32_t* h_raw = nullptr;
   int64_t* h_raw_offs = nullptr;
   int32_t* h_err = nullptr;
@@ -123,6 +127,7 @@ void free_all(vt_sampler* h) {
   };
   dfree(h->d_params);
   dfree(h->d_seeds);
+  dfree(h->d_decay);
   dfree(h->d_hist);
   dfree(h->d_hist_len);
   dfree(h->d_zside);
@@ -137,6 +142,7 @@ void free_all(vt_sampler* h) {
   dfree(h->d_slow_list);
   dfree(h->d_slow_ctl);
   dfree(h->d_rows);
+  dfree(h->d_probs_part);
   if (h->h_rows) cudaFreeHost(h->h_rows);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
@@ -148,6 +154,7 @@ void free_all(vt_sampler* h) {
   dfree(h->d_io_tlp);
   hfree(h->h_params);
   hfree(h->h_seeds);
+  hfree(h->h_decay);
   hfree(h->h_raw);
   hfree(h->h_raw_offs);
   hfree(h->h_err);
@@ -213,6 +220,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   };
   dal((void**)&h->d_params, B * sizeof(vt::RowParams));
   dal((void**)&h->d_seeds, B * sizeof(uint64_t));
+  dal((void**)&h->d_decay, B * sizeof(vt::DecayState));
   dal((void**)&h->d_hist, B * H * sizeof(int2));
   dal((void**)&h->d_hist_len, B * sizeof(int32_t));
   dal((void**)&h->d_zside, B * H * sizeof(float));
@@ -227,9 +235,16 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_slow_list, 2 * B * sizeof(int32_t));
   dal((void**)&h->d_slow_ctl, 8 * sizeof(uint32_t));
   dal((void**)&h->d_rows, B * sizeof(int32_t));
+  // B rows of ceil(V / max range) + 1 splits, plus the splits that small
+  // batches add to fill the GPU (plan_probs never asks for more)
+  h->probs_part_cap = B * (size_t)((cfg->max_vocab + vt::kProbsMaxRange - 1) /
+                                       vt::kProbsMaxRange + 1) +
+                      (size_t)vt::kProbsCtasPerSm * h->num_sms;
+  dal((void**)&h->d_probs_part, h->probs_part_cap * sizeof(float2));
   hal((void**)&h->h_rows, B * sizeof(int32_t));
   hal((void**)&h->h_params, B * sizeof(vt::RowParams));
   hal((void**)&h->h_seeds, B * sizeof(uint64_t));
+  hal((void**)&h->h_decay, B * sizeof(vt::DecayState));
   hal((void**)&h->h_raw, B * H * sizeof(int32_t));
   hal((void**)&h->h_raw_offs, (B + 1) * sizeof(int64_t));
   hal((void**)&h->h_err, sizeof(int32_t));
@@ -274,6 +289,15 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
                     const float* top_p, const float* min_p, const float* presence,
                     const float* frequency, const float* repetition, const uint64_t* seed,
                     void* stream) {
+  return vt_reset_params_ex(h, B, temperature, top_k, top_p, min_p, presence, frequency,
+                            repetition, seed, nullptr, nullptr, nullptr, stream);
+}
+
+int vt_reset_params_ex(vt_sampler* h, int32_t B, const float* temperature, const int32_t* top_k,
+                       const float* top_p, const float* min_p, const float* presence,
+                       const float* frequency, const float* repetition, const uint64_t* seed,
+                       const float* top_p_decay, const float* top_p_min,
+                       const int32_t* top_p_reset_ids, void* stream) {
   if (!h) return VT_ERR_INVALID_ARG;
   if (B < 1) return set_err(h, VT_ERR_INVALID_ARG, "B must be >= 1 (got %d)", B);
   if (B > h->cfg.max_batch)
@@ -292,6 +316,14 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
       return set_err(h, VT_ERR_INVALID_ARG, "row %d: min_p %g not in [0,1]", r, mp);
     if (!finite(presence[r]) || !finite(frequency[r]) || !finite(rep) || !(rep > 0.0f))
       return set_err(h, VT_ERR_INVALID_ARG, "row %d: penalties out of range", r);
+    if (top_p_decay && !(top_p_decay[r] > 0.0f && top_p_decay[r] <= 1.0f))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: top_p_decay %g not in (0,1]", r,
+                     top_p_decay[r]);
+    if (top_p_min && !(top_p_min[r] > 0.0f && top_p_min[r] <= 1.0f))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: top_p_min %g not in (0,1]", r, top_p_min[r]);
+    if (top_p_reset_ids && top_p_reset_ids[r] < -1)
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: top_p_reset_ids %d < -1", r,
+                     top_p_reset_ids[r]);
   }
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
@@ -315,6 +347,15 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
     if (mp > 0.0f && mp < 1.0f) rp.flags |= vt::kRowMinP;
     if (presence[r] != 0.0f || frequency[r] != 0.0f || repetition[r] != 1.0f)
       rp.flags |= vt::kRowPenalty;
+    // An active decay makes a sampled row a top-p row from its top_p (1 when
+    // unset); the explicit greedy triggers take precedence.
+    vt::DecayState ds;
+    ds.p = p;
+    ds.decay = top_p_decay ? top_p_decay[r] : 1.0f;
+    ds.p_min = top_p_min ? top_p_min[r] : 1e-6f;
+    ds.reset_id = top_p_reset_ids ? top_p_reset_ids[r] : -1;
+    if (!greedy && ds.decay < 1.0f) rp.flags |= vt::kRowDecay;
+    h->h_decay[r] = ds;
     rp.presence = presence[r];
     rp.frequency = frequency[r];
     rp.repetition = repetition[r];
@@ -330,7 +371,8 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
   // Used for bf16 calls over all B rows; main rows first, then side rows.
   auto to_side = [&](int r) {
     const uint32_t f = h->row_flags[r];
-    return !(f & vt::kRowGreedy) && !(f & vt::kRowPenalty) && (f & vt::kRowTopP) && top_k[r] <= 1;
+    return !(f & vt::kRowGreedy) && !(f & vt::kRowPenalty) && !(f & vt::kRowDecay) &&
+           (f & vt::kRowTopP) && top_k[r] <= 1;
   };
   int nm = 0, ns = 0;
   for (int r = 0; r < B; ++r)
@@ -351,6 +393,8 @@ int vt_reset_params(vt_sampler* h, int32_t B, const float* temperature, const in
   VT_CK(h, cudaMemcpyAsync(h->d_params, h->h_params, (size_t)B * sizeof(vt::RowParams),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_seeds, h->h_seeds, (size_t)B * sizeof(uint64_t),
+                           cudaMemcpyHostToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(h->d_decay, h->h_decay, (size_t)B * sizeof(vt::DecayState),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_rows, h->h_rows, (size_t)B * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st));
@@ -441,7 +485,7 @@ int vt_reset_token_counts_ex(vt_sampler* h, int32_t B, const int32_t* prompt_ids
 static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t B, int32_t V,
                        int64_t ld, int32_t n, int32_t update_counts, int32_t* out_tokens,
                        float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
-                       cudaStream_t st) {
+                       float* out_probs, int64_t ld_probs, cudaStream_t st) {
   if (h->params_B == 0) return set_err(h, VT_ERR_STATE, "vt_sample before vt_reset_params");
   if (B < 1 || B > h->params_B)
     return set_err(h, B < 1 ? VT_ERR_INVALID_ARG : VT_ERR_STATE,
@@ -459,6 +503,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     return set_err(h, VT_ERR_INVALID_ARG, "top-k log-prob outputs are null");
   if ((update_counts && h->cfg.max_history == 0))
     return set_err(h, VT_ERR_CAPACITY, "update_counts needs max_history > 0");
+  if (out_probs && ld_probs < V) return set_err(h, VT_ERR_INVALID_ARG, "ld_probs < V");
   for (int r = 0; r < B; ++r)
     if ((h->row_flags[r] & vt::kRowPenalty) && r >= h->counts_B)
       return set_err(h, VT_ERR_STATE, "row %d has penalties but its counts were never reset", r);
@@ -490,7 +535,8 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     a.rows = row_list;
     a.early = early;
     a.n_logprobs = n;
-    a.update_counts = update_counts ? 1 : 0;
+    // with the distribution exported, the counts are updated after it
+    a.update_counts = update_counts && !out_probs ? 1 : 0;
     a.slice = plan.slice;
     a.aligned = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
     a.pen_smem = plan.pen_smem;
@@ -500,6 +546,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     a.off_prefix = plan.off_prefix;
     a.params = h->d_params;
     a.seeds = h->d_seeds;
+    a.decay = h->d_decay;
     a.hist = h->d_hist;
     a.hist_len = h->d_hist_len;
     a.hist_cap = h->cfg.max_history > 0 ? h->cfg.max_history : 1;
@@ -552,6 +599,38 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     VT_CK(h, cudaStreamWaitEvent(st, h->ev_join, 0));
     h->last_launches = ps->own.cluster >= 1 ? 3 : 4;
   }
+  if (out_probs) {
+    vt::ProbsArgs pa;
+    std::memset(&pa, 0, sizeof pa);
+    pa.logits = logits;
+    pa.ld = ld;
+    pa.B = B;
+    pa.V = V;
+    vt::plan_probs(B, V, h->num_sms, &pa.splits, &pa.range);
+    if ((size_t)B * pa.splits > h->probs_part_cap)
+      return set_err(h, VT_ERR_CAPACITY, "probability partials exceed their buffer");
+    pa.vec_in = ((uintptr_t)logits % 16 == 0) && (((uint64_t)ld * es) % 16 == 0);
+    pa.vec_out = ((uintptr_t)out_probs % 16 == 0) && (((uint64_t)ld_probs * 4) % 16 == 0);
+    pa.params = h->d_params;
+    const bool has_counts = h->counts_B > 0 && h->cfg.max_history > 0;
+    pa.hist = has_counts ? h->d_hist : nullptr;
+    pa.hist_len = h->d_hist_len;
+    pa.hist_cap = h->cfg.max_history > 0 ? h->cfg.max_history : 1;
+    pa.tokens = out_tokens;
+    pa.row_status = h->d_status;
+    pa.kth_value = h->d_kth_v;
+    pa.kth_index = h->d_kth_i;
+    pa.part = h->d_probs_part;
+    pa.probs = out_probs;
+    pa.ld_probs = ld_probs;
+    VT_CK(h, vt::launch_probs(pa, dtype, st));
+    h->last_launches += 2;
+    if (update_counts) {
+      VT_CK(h, vt::launch_append(h->d_hist, h->d_hist_len, pa.hist_cap, out_tokens, h->d_status,
+                                 B, st));
+      h->last_launches += 1;
+    }
+  }
   h->last_B = B;
   h->last_stream = st;
   h->err.clear();
@@ -566,7 +645,20 @@ int vt_sample(vt_sampler* h, const void* logits, int32_t dtype, int32_t B, int32
   DeviceGuard guard(h->cfg.device);
   if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
   return sample_impl(h, logits, dtype, B, V, ld, num_logprobs, update_counts, out_tokens,
-                     out_logprobs, out_topk_ids, out_topk_logprobs, (cudaStream_t)stream);
+                     out_logprobs, out_topk_ids, out_topk_logprobs, nullptr, 0,
+                     (cudaStream_t)stream);
+}
+
+int vt_sample_ex(vt_sampler* h, const void* logits, int32_t dtype, int32_t B, int32_t V,
+                 int64_t ld, int32_t num_logprobs, int32_t update_counts, int32_t* out_tokens,
+                 float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
+                 float* out_probs, int64_t ld_probs, void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
+  return sample_impl(h, logits, dtype, B, V, ld, num_logprobs, update_counts, out_tokens,
+                     out_logprobs, out_topk_ids, out_topk_logprobs, out_probs, ld_probs,
+                     (cudaStream_t)stream);
 }
 
 int vt_check_device_errors(vt_sampler* h) {
@@ -600,7 +692,8 @@ int vt_sample_host(vt_sampler* h, const void* host_logits, int32_t dtype, int32_
   cudaStream_t st = (cudaStream_t)stream;
   VT_CK(h, cudaMemcpyAsync(h->d_io_logits, host_logits, bytes, cudaMemcpyHostToDevice, st));
   const int rc = sample_impl(h, h->d_io_logits, dtype, B, V, ld, n, update_counts, h->d_io_tokens,
-                             h->d_io_lp, n ? h->d_io_tid : nullptr, n ? h->d_io_tlp : nullptr, st);
+                             h->d_io_lp, n ? h->d_io_tid : nullptr, n ? h->d_io_tlp : nullptr,
+                             nullptr, 0, st);
   if (rc != VT_OK) return rc;
   VT_CK(h, cudaMemcpyAsync(host_tokens, h->d_io_tokens, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
   if (host_logprobs)
@@ -712,6 +805,17 @@ int vt_debug_get_seeds(vt_sampler* h, uint64_t* host_seeds) {
   DeviceGuard guard(h->cfg.device);
   VT_CK(h, cudaStreamSynchronize(h->last_stream));
   VT_CK(h, cudaMemcpy(host_seeds, h->d_seeds, (size_t)h->params_B * 8, cudaMemcpyDeviceToHost));
+  return VT_OK;
+}
+
+int vt_read_top_p(vt_sampler* h, float* host_top_p) {
+  if (!h || !host_top_p) return VT_ERR_INVALID_ARG;
+  if (h->params_B == 0) return set_err(h, VT_ERR_STATE, "no vt_reset_params yet");
+  DeviceGuard guard(h->cfg.device);
+  VT_CK(h, cudaStreamSynchronize(h->last_stream));
+  VT_CK(h, cudaMemcpy(h->h_decay, h->d_decay, (size_t)h->params_B * sizeof(vt::DecayState),
+                      cudaMemcpyDeviceToHost));
+  for (int r = 0; r < h->params_B; ++r) host_top_p[r] = h->h_decay[r].p;
   return VT_OK;
 }
 

@@ -58,9 +58,12 @@ SIGNATURES = {
     "vt_sampler_create": (C.c_int, [C.POINTER(Config), C.POINTER(P)]),
     "vt_sampler_destroy": (None, [P]),
     "vt_reset_params": (C.c_int, [P, I32, P, P, P, P, P, P, P, P, P]),
+    "vt_reset_params_ex": (C.c_int, [P, I32, P, P, P, P, P, P, P, P, P, P, P, P]),
+    "vt_read_top_p": (C.c_int, [P, P]),
     "vt_reset_token_counts": (C.c_int, [P, I32, P, P, P, P, P]),
     "vt_reset_token_counts_ex": (C.c_int, [P, I32, P, P, P, P, P, P]),
     "vt_sample": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
+    "vt_sample_ex": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P, I64, P]),
     "vt_sample_host": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
     "vt_check_device_errors": (C.c_int, [P]),
     "vt_get_row_status": (C.c_int, [P, P, P]),
@@ -158,7 +161,9 @@ class Sampler:
 
     # -- state ---------------------------------------------------------------
     def reset_params(self, temperature, top_k, top_p, min_p, presence, frequency, repetition,
-                     seed, stream=None):
+                     seed, stream=None, top_p_decay=None, top_p_min=None, top_p_reset_ids=None):
+        """Per-row parameters and seeds; the three top-p decay arrays are
+        optional (None: the library's default for every row)."""
         t = np.ascontiguousarray(temperature, np.float32)
         B = t.shape[0]
         arrs = [t, np.ascontiguousarray(top_k, np.int32), np.ascontiguousarray(top_p, np.float32),
@@ -170,9 +175,21 @@ class Sampler:
         for a in arrs:
             if a.shape != (B,):
                 raise ValueError("every parameter array must have shape (B,)")
-        rc = self._lib.vt_reset_params(self._h, B, *[_np_ptr(a) for a in arrs],
-                                       _stream_ptr(stream))
-        self._check(rc, "vt_reset_params")
+        decay = [None if a is None else np.ascontiguousarray(a, dt)
+                 for a, dt in ((top_p_decay, np.float32), (top_p_min, np.float32),
+                               (top_p_reset_ids, np.int32))]
+        if all(a is None for a in decay):
+            rc = self._lib.vt_reset_params(self._h, B, *[_np_ptr(a) for a in arrs],
+                                           _stream_ptr(stream))
+            self._check(rc, "vt_reset_params")
+            return
+        for a in decay:
+            if a is not None and a.shape != (B,):
+                raise ValueError("every top-p decay array must have shape (B,)")
+        rc = self._lib.vt_reset_params_ex(self._h, B, *[_np_ptr(a) for a in arrs],
+                                          *[_np_ptr(a) for a in decay],
+                                          _stream_ptr(stream))
+        self._check(rc, "vt_reset_params_ex")
 
     def reset_token_counts(self, prompt_ids, prompt_offsets, output_ids, output_offsets,
                            stream=None, prompt_ignore=None):
@@ -206,12 +223,15 @@ class Sampler:
 
     # -- sampling ------------------------------------------------------------
     def sample(self, logits, V: int | None = None, num_logprobs: int = 0,
-               update_counts: bool = False, out=None, stream=None, dtype: int | None = None):
+               update_counts: bool = False, out=None, stream=None, dtype: int | None = None,
+               probs=None):
         """Sample one token per row of a CUDA tensor ``logits`` [B, ld] (float32 or
         bfloat16, or a uint16 tensor of bf16 bits with ``dtype=DTYPE_BF16``).
 
         Returns ``(tokens, logprobs, topk_ids, topk_logprobs)`` CUDA tensors (the
-        last two have shape [B, num_logprobs]).  Stream-ordered; nothing waits."""
+        last two have shape [B, num_logprobs]).  ``probs`` (a float32 CUDA tensor
+        [B, >= V] with contiguous rows) also receives the filtered distribution of
+        each row.  Stream-ordered; nothing waits."""
         import torch
         if logits.dim() != 2 or not logits.is_cuda:
             raise ValueError("logits must be a 2-D CUDA tensor")
@@ -234,12 +254,19 @@ class Sampler:
                    torch.empty((B, n), dtype=torch.int32, device=dev),
                    torch.empty((B, n), dtype=torch.float32, device=dev))
         tok, lp, tid, tlp = out
-        rc = self._lib.vt_sample(self._h, P(logits.data_ptr()), dtype, B, V, ld, n,
-                                 1 if update_counts else 0, P(tok.data_ptr()),
-                                 P(lp.data_ptr()) if lp is not None else None,
-                                 P(tid.data_ptr()) if n else None,
-                                 P(tlp.data_ptr()) if n else None, _stream_ptr(stream))
-        self._check(rc, "vt_sample")
+        args = (self._h, P(logits.data_ptr()), dtype, B, V, ld, n, 1 if update_counts else 0,
+                P(tok.data_ptr()), P(lp.data_ptr()) if lp is not None else None,
+                P(tid.data_ptr()) if n else None, P(tlp.data_ptr()) if n else None)
+        if probs is None:
+            rc = self._lib.vt_sample(*args, _stream_ptr(stream))
+            self._check(rc, "vt_sample")
+            return out
+        if (probs.dim() != 2 or not probs.is_cuda or probs.dtype != torch.float32
+                or probs.shape[0] != B or probs.shape[1] < V or probs.stride(1) != 1):
+            raise ValueError("probs must be a float32 CUDA tensor [B, >= V] with contiguous rows")
+        rc = self._lib.vt_sample_ex(*args, P(probs.data_ptr()), probs.stride(0),
+                                    _stream_ptr(stream))
+        self._check(rc, "vt_sample_ex")
         return out
 
     def sample_ptr(self, logits_ptr: int, dtype: int, B: int, V: int, ld: int, num_logprobs: int,
@@ -337,6 +364,12 @@ class Sampler:
         v = C.c_int32()
         self._check(self._lib.vt_debug_last_launches(self._h, C.byref(v)), "vt_debug_last_launches")
         return int(v.value)
+
+    def top_p(self, B: int):
+        """The effective top_p of rows 0..B-1 (decayed on rows with top-p decay)."""
+        p = np.zeros(self.cfg.max_batch, np.float32)
+        self._check(self._lib.vt_read_top_p(self._h, _np_ptr(p)), "vt_read_top_p")
+        return p[:B]
 
     def seeds(self, B: int):
         s = np.zeros(self.cfg.max_batch, np.uint64)  # the call writes up to max_batch seeds

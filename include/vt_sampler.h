@@ -113,6 +113,33 @@ int vt_reset_params(vt_sampler* handle, int32_t B, const float* temperature,
                     const float* presence, const float* frequency,
                     const float* repetition, const uint64_t* seed, void* stream);
 
+/* vt_reset_params plus top-p decay [TensorRT-LLM "Sampling", LLM API sampling
+ * behaviour, top-p decay].  Each of the three arrays is a host array of B
+ * entries, or NULL for its default:
+ *   top_p_decay      in (0, 1]; 1 disables (default 1).
+ *   top_p_min        in (0, 1]; the floor of the decayed top_p (default 1e-6).
+ *   top_p_reset_ids  >= -1; -1 never matches a token (default -1).
+ * A row with top_p_decay < 1 that is not greedy (the greedy triggers above take
+ * precedence) samples as a top-p row with an effective top_p that starts at its
+ * top_p (1 when top_p is 1).  After each vt_sample that draws a token for the
+ * row, the effective top_p becomes the row's top_p when the token equals
+ * top_p_reset_ids, else max(top_p_eff * top_p_decay, top_p_min), in fp32; a
+ * row the call could not sample (status != 0) keeps it.  The state lives on
+ * the device and carries across vt_sample calls until the next reset.
+ * Errors as vt_reset_params (any value out of range: nothing uploaded). */
+int vt_reset_params_ex(vt_sampler* handle, int32_t B, const float* temperature,
+                       const int32_t* top_k, const float* top_p, const float* min_p,
+                       const float* presence, const float* frequency,
+                       const float* repetition, const uint64_t* seed,
+                       const float* top_p_decay, const float* top_p_min,
+                       const int32_t* top_p_reset_ids, void* stream);
+
+/* Read the effective top_p of rows 0..B-1 into a host array (B of the last
+ * reset): the decayed value for rows with top-p decay, top_p for the others.
+ * Synchronises the handle's last stream.  Errors: VT_ERR_INVALID_ARG (null
+ * pointer), VT_ERR_STATE (no reset yet), VT_ERR_CUDA. */
+int vt_read_top_p(vt_sampler* handle, float* host_top_p);
+
 /* Rebuild the token counts of rows 0..B-1 from host CSR arrays: row r's prompt
  * ids are prompt_ids[prompt_offsets[r] .. prompt_offsets[r+1]), likewise its
  * output ids (offsets: B+1 entries, non-decreasing, starting at 0).  The counts
@@ -166,6 +193,27 @@ int vt_sample(vt_sampler* handle, const void* logits, int32_t dtype, int32_t B, 
               int64_t ld, int32_t num_logprobs, int32_t update_counts, int32_t* out_tokens,
               float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
               void* stream);
+
+/* vt_sample plus the filtered distribution each row drew from, on request
+ * [TensorRT-LLM "Sampling", Performance: the full set of token probabilities
+ * after the top-k / top-p masking, computed only when the user asks for it,
+ * e.g. for rejection sampling].
+ *   out_probs  device fp32 [B][ld_probs] (ld_probs >= V; columns [V, ld_probs)
+ *              are not written), or NULL (then this is vt_sample).  Row r
+ *              receives exp(z_t,j - m) / sum over the kept set of
+ *              exp(z_t - m) for j in the row's kept set after min-p, top-k
+ *              and top-p (m the row maximum of z_t), 0 elsewhere; a one-hot
+ *              vector at the token on a greedy row; NaN everywhere on a row
+ *              with status VT_ROW_NONFINITE or VT_ROW_EMPTY.  fp32 arithmetic:
+ *              each entry within a relative 3e-5 of the exact value.
+ * The distribution uses the counts the draw saw: with update_counts the
+ * tokens are appended after it.  Two extra launches (three with
+ * update_counts) read the logits twice more.  Errors as vt_sample, plus
+ * VT_ERR_INVALID_ARG for ld_probs < V. */
+int vt_sample_ex(vt_sampler* handle, const void* logits, int32_t dtype, int32_t B, int32_t V,
+                 int64_t ld, int32_t num_logprobs, int32_t update_counts, int32_t* out_tokens,
+                 float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
+                 float* out_probs, int64_t ld_probs, void* stream);
 
 /* vt_sample from host memory: copies host logits [B][ld] into the handle's
  * device staging (created with host_io = 1), samples, copies the outputs back
@@ -238,8 +286,8 @@ int vt_debug_last_launches(vt_sampler* handle, int32_t* launches);
 int vt_debug_get_seeds(vt_sampler* handle, uint64_t* host_seeds);
 
 /* ---- sampling without any allocation -------------------------------------
- * The paper has no counterpart of this entry point.  It serves callers that
- * may not allocate device memory: an engine that reserves nearly all of it
+ * The sampling pages have no counterpart of this entry point.  It serves
+ * callers that may not allocate device memory: an engine that reserves nearly all of it
  * for its KV cache at start-up, a host whose device memory belongs to a
  * framework's caching allocator, a decode loop that keeps cudaMalloc and
  * cudaFree (which waits for the whole device) out of its step.  Such callers

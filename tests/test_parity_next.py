@@ -14,7 +14,8 @@ torch = pytest.importorskip("torch")
 import oracle as O
 from device_token_sampling_gb300 import workloads as W
 
-from paritylib import check_workload, custom_workload, make_sampler
+from paritylib import (check_workload, compare, custom_workload, device_logits, make_sampler,
+                       run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,5 +73,233 @@ def test_prompt_ignore_counts_table():
             seen = np.unique(np.concatenate([prompt[r], output[r]]))
             np.testing.assert_array_equal(ids, seen)  # every seen id, for repetition
             np.testing.assert_array_equal(cnt, [counted.get(int(i), 0) for i in ids])
+    finally:
+        s.close()
+
+
+# --------------------------------------------------------------------------
+# top-p decay
+# --------------------------------------------------------------------------
+
+# per row: T, top_k, initial top_p, decay, top_p_min, reset id (-1: never)
+DECAY_ROWS = [
+    (1.0, 0, 1.0, 0.9, 1e-6, -1),    # top_p unset: decay alone makes it a top-p row
+    (1.2, 0, 0.95, 0.5, 0.3, 17),    # floor reached at step 2, then a reset
+    (0.9, 0, 0.9, 0.5, 1e-6, 17),    # toward the floor: nearly greedy
+    (1.1, 50, 0.99, 0.7, 0.2, 17),   # top-k then the decayed top-p
+    (0.0, 0, 0.9, 0.5, 0.1, -1),     # greedy takes precedence: no decay
+    (1.0, 0, 0.8, 1.0, 0.5, 17),     # decay 1: off
+    (1.3, 0, 0.7, 0.95, 0.6, -1),    # slow decay, never reset
+    (1.0, 1, 0.9, 0.5, 0.1, 17),     # top_k = 1 is greedy: no decay
+]
+RESET_STEPS = (3, 6)  # steps whose logits make the reset id (17) the clear winner
+
+
+def decay_step_logits(rng, B, V, step):
+    x = W.peaked_rows(rng, B, V)
+    if step in RESET_STEPS:
+        x[:, 17] = x.max(axis=1) + 12.0
+    return x
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+def test_top_p_decay_steps(dtype):
+    """Eight calls on one handle: each call samples with the effective top_p the
+    state holds, which must follow the oracle's decay rule bit for bit."""
+    rng = np.random.default_rng(63)
+    B, V, steps = len(DECAY_ROWS), 40_000, 8
+    T, k, p0, decay, pmin, reset = (np.array(c) for c in zip(*DECAY_ROWS))
+    x0 = decay_step_logits(rng, B, V, 0)
+    w = custom_workload(x0, dtype=dtype, T=T, k=k, p=p0, n=4, name="top-p decay")
+    s = make_sampler(w)
+    try:
+        s.reset_params(w.temperature, w.top_k, w.top_p, w.min_p, w.presence, w.frequency,
+                       w.repetition, w.seed, top_p_decay=decay.astype(np.float32),
+                       top_p_min=pmin.astype(np.float32), top_p_reset_ids=reset.astype(np.int32))
+        s.reset_token_counts(w.prompt_ids, w.prompt_offsets, w.output_ids, w.output_offsets)
+        active = (decay < 1.0) & (T > 0.0) & (k != 1)
+        p_eff = p0.astype(np.float32).copy()
+        seed = w.seed.copy()
+        resets = 0
+        for step in range(steps):
+            np.testing.assert_array_equal(s.top_p(B), p_eff, err_msg=f"step {step}")
+            x = x0 if step == 0 else decay_step_logits(rng, B, V, step)
+            ws = custom_workload(x, dtype=dtype, T=T, k=k, p=p0, n=4, name=f"decay step {step}")
+            ws.seed = seed.copy()
+            g = run_gpu(s, ws, reset=False)
+            o = O.sample_workload(ws, want_zt=True, top_p=p_eff)
+            compare(g, o, where=ws.name)
+            for r in np.flatnonzero(active):
+                if g["status"][r] == 0:
+                    resets += int(g["token"][r] == reset[r])
+                    p_eff[r] = O.topp_decay(float(p_eff[r]), float(p0[r]), float(decay[r]),
+                                            float(pmin[r]), int(reset[r]), int(g["token"][r]))
+            seed = np.array([O.next_seed(int(v)) for v in seed], np.uint64)
+        np.testing.assert_array_equal(s.top_p(B), p_eff, err_msg="after the last step")
+        np.testing.assert_array_equal(s.seeds(B), seed)
+        assert resets >= 4, "the reset id was drawn too rarely to test the reset"
+        assert p_eff[6] == np.float32(0.6)  # the floor
+    finally:
+        s.close()
+
+
+def test_top_p_decay_rejects_out_of_range():
+    rng = np.random.default_rng(64)
+    w = custom_workload(rng.normal(0, 1, size=(2, 1000)), p=0.9)
+    s = make_sampler(w)
+    try:
+        base = (w.temperature, w.top_k, w.top_p, w.min_p, w.presence, w.frequency, w.repetition,
+                w.seed)
+        for kw in (dict(top_p_decay=[0.0, 0.9]), dict(top_p_decay=[1.5, 0.9]),
+                   dict(top_p_min=[0.0, 0.5]), dict(top_p_min=[0.5, 1.01]),
+                   dict(top_p_reset_ids=[-2, 3])):
+            with pytest.raises(Exception, match="VT_ERR_INVALID_ARG|out of range|not in|< -1"):
+                s.reset_params(*base, **{kk: np.asarray(v) for kk, v in kw.items()})
+        # defaults: decay 0.5 alone, floor 1e-6, no reset id
+        s.reset_params(*base, top_p_decay=np.array([0.5, 1.0], np.float32))
+        np.testing.assert_array_equal(s.top_p(2), np.float32([0.9, 0.9]))
+    finally:
+        s.close()
+
+
+# --------------------------------------------------------------------------
+# the filtered distribution on request
+# --------------------------------------------------------------------------
+
+# fp32 arithmetic against the oracle's double: the exponent argument z_t - m
+# is rounded once (relative error |z_t - m| 2^-24, at most about 6e-6 where
+# the probability is still a normal fp32 number), expf adds a few ulp, the
+# kept set's exp-sum a relative error that grows with the terms a thread
+# adds in sequence (about 150 here, 9e-6 at worst); the bound takes 3e-5.
+PROBS_RTOL = 3e-5
+PROBS_ATOL = 1e-37  # below the smallest normal fp32 number the relative bound stops
+
+
+def sample_with_probs(s, w, x=None, update_counts=False, ld_probs=None):
+    if x is None:
+        x = device_logits(w)
+    dt = W.DTYPE_BF16 if w.dtype == W.DTYPE_BF16 else W.DTYPE_F32
+    ldp = w.V if ld_probs is None else ld_probs
+    probs = torch.full((w.B, ldp), -7.0, dtype=torch.float32, device=x.device)
+    tok, lp, tid, tlp = s.sample(x, V=w.V, num_logprobs=w.num_logprobs,
+                                 update_counts=update_counts, dtype=dt, probs=probs)
+    st = s.row_status(w.B)
+    kv, ki, kept = s.filter_boundary(w.B)
+    torch.cuda.synchronize()
+    s.check_device_errors()
+    g = dict(token=tok.cpu().numpy(), logprob=lp.cpu().numpy(), topn_ids=tid.cpu().numpy(),
+             topn_lp=tlp.cpu().numpy(), status=st.cpu().numpy(), kth_value=kv.cpu().numpy(),
+             kth_index=ki.cpu().numpy(), kept=kept.cpu().numpy())
+    return g, probs.cpu().numpy()
+
+
+def check_probs(g, probs, o, where):
+    B, V = o.probs.shape
+    for r in range(B):
+        tag = f"{where} row {r}"
+        got = probs[r, :V]
+        if o.status[r] != 0:
+            assert np.isnan(got).all(), tag
+            continue
+        if o.greedy[r]:
+            want = np.zeros(V)
+            want[g["token"][r]] = 1.0
+            np.testing.assert_array_equal(got, want, err_msg=tag)
+            continue
+        kept = int(g["kept"][r])
+        want = o.probs[r] if kept == o.kept_count[r] else O.filtered_probs(o.zt[r], kept)
+        assert ((got > 0) == (want > 0)).all(), (tag, "support")
+        np.testing.assert_allclose(got, want, rtol=PROBS_RTOL, atol=PROBS_ATOL, err_msg=tag)
+        assert abs(float(got.astype(np.float64).sum()) - 1.0) < 1e-4, tag
+    if probs.shape[1] > V:
+        assert (probs[:, V:] == -7.0).all(), f"{where}: columns beyond V written"
+
+
+def mixed_probs_workload(rng, dtype, B=12, V=50_003, ld=None, name="probs mixed"):
+    x = W.peaked_rows(rng, B, V)
+    x[B - 2, 11] = np.nan         # status 1
+    x[B - 1, :] = -np.inf         # status 2
+    prompt, output = history(rng, B, V, 120, 30)
+    return custom_workload(
+        x, dtype=dtype, ld=ld, name=name, n=6, prompt=prompt, output=output,
+        T=[0.0, 0.7, 1.0, 1.3, 0.9, 2.0, 1.0, 0.8, 1.5, 1.1, 1.0, 1.0][:B],
+        k=[0, 0, 50, 0, 300, 0, 1000, 20, 0, 0, 0, 0][:B],
+        p=[1.0, 0.9, 1.0, 0.95, 0.8, 1.0, 0.5, 1.0, 0.99, 1.0, 0.9, 0.9][:B],
+        mp=[0.0, 0.0, 0.0, 0.05, 0.0, 0.01, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0][:B],
+        pres=[0.0, 0.5, 0.0, 0.0, 0.3, 0.0, 0.0, 0.2, 0.0, 0.0, 0.0, 0.0][:B],
+        freq=[0.0, 0.2, 0.0, 0.0, 0.1, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0][:B],
+        rep=[1.0, 1.2, 1.0, 1.0, 0.9, 1.0, 1.0, 1.1, 1.0, 1.0, 1.0, 1.0][:B])
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+def test_probs_mixed(dtype):
+    rng = np.random.default_rng(65)
+    w = mixed_probs_workload(rng, dtype)
+    s = make_sampler(w)
+    try:
+        s.reset_workload(w)
+        g, probs = sample_with_probs(s, w)
+        o = O.sample_workload(w, want_zt=True, want_probs=True)
+        compare(g, o, where=w.name)
+        check_probs(g, probs, o, w.name)
+        assert s.last_launches() in (4, 5)  # the sampling pair, then the two passes
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("ld_extra", [3, 8])
+def test_probs_unaligned_and_padded(ld_extra):
+    # odd row strides: element-wise loads and stores; columns past V untouched
+    rng = np.random.default_rng(66 + ld_extra)
+    V = 30_001
+    w = mixed_probs_workload(rng, W.DTYPE_BF16, B=8, V=V, ld=V + ld_extra, name="probs ld")
+    s = make_sampler(w)
+    try:
+        s.reset_workload(w)
+        g, probs = sample_with_probs(s, w, ld_probs=V + ld_extra)
+        o = O.sample_workload(w, want_zt=True, want_probs=True)
+        compare(g, o, where=w.name)
+        check_probs(g, probs, o, w.name)
+    finally:
+        s.close()
+
+
+def test_probs_with_update_counts():
+    """The distribution uses the counts the draw saw; the counts then gain the
+    token exactly as a call without the export leaves them."""
+    rng = np.random.default_rng(67)
+    w = mixed_probs_workload(rng, W.DTYPE_F32, B=10, V=20_000)
+    x = device_logits(w)
+    a, b = make_sampler(w), make_sampler(w)
+    try:
+        a.reset_workload(w)
+        b.reset_workload(w)
+        for step in range(3):
+            ga, probs = sample_with_probs(a, w, x=x, update_counts=True)
+            gb = run_gpu(b, w, x=x, update_counts=True, reset=False)
+            for k in ("token", "status", "kept", "kth_index"):
+                np.testing.assert_array_equal(ga[k], gb[k], err_msg=f"step {step} {k}")
+            for r in range(w.B):
+                np.testing.assert_array_equal(a.counts(r)[0], b.counts(r)[0])
+                np.testing.assert_array_equal(a.counts(r)[1], b.counts(r)[1])
+            if step == 0:
+                o = O.sample_workload(w, want_zt=True, want_probs=True)
+                check_probs(ga, probs, o, "update_counts")
+    finally:
+        a.close()
+        b.close()
+
+
+def test_probs_full_vocab_batch():
+    # the b256 mix at full vocabulary, the oracle on a sample of its rows
+    w = W.b256(seed=5)
+    rows = np.array([0, 1, 2, 63, 64, 127, 128, 191, 200, 255])
+    s = make_sampler(w)
+    try:
+        s.reset_workload(w)
+        g, probs = sample_with_probs(s, w)
+        o = O.sample_workload(w, want_zt=True, want_probs=True, rows=rows)
+        compare(g, o, rows=rows, where="b256")
+        check_probs({k: v[rows] for k, v in g.items()}, probs[rows], o, "b256")
     finally:
         s.close()
