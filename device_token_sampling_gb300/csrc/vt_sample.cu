@@ -508,15 +508,22 @@ __device__ void block_sort_desc_impl(uint64_t* keys) {
   for (int k = 2; k <= N; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j < KPT) {
+        // partners within the thread: one unrolled case per distance, so that
+        // every index into v is known at compile time (v stays in registers)
 #pragma unroll
-        for (int q = 0; q < KPT; ++q) {
-          const int p = q ^ j;
-          if (p > q) {
-            const bool up = ((base + q) & k) == 0;
-            const uint64_t a = v[q], b = v[p];
-            if (up ? (a < b) : (a > b)) {
-              v[q] = b;
-              v[p] = a;
+        for (int jj = KPT / 2; jj > 0; jj >>= 1) {
+          if (jj == j) {
+#pragma unroll
+            for (int q = 0; q < KPT; ++q) {
+              const int p = q ^ jj;
+              if (p > q) {
+                const bool up = ((base + q) & k) == 0;
+                const uint64_t a = v[q], b = v[p];
+                if (up ? (a < b) : (a > b)) {
+                  v[q] = b;
+                  v[p] = a;
+                }
+              }
             }
           }
         }
@@ -566,6 +573,105 @@ __device__ void block_sort_desc(uint64_t* keys, int n) {
     block_sort_desc_impl<4>(keys);
   else
     block_sort_desc_impl<8>(keys);
+}
+
+// The K-th largest of N distinct keys (1 <= K <= N), most significant byte
+// first: a 256-bin count of the keys that share the prefix found so far, the
+// bin holding rank K, then the next byte.  Ends as soon as that bin holds one
+// key.  All threads of the CTA call it and get the key.
+__device__ uint64_t block_select_desc(const uint64_t* keys, int N, int K, Smem& s) {
+  uint64_t prefix = 0ull, mask = 0ull;
+  int need = K;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += kThreads) s.hist256[b] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += kThreads) {
+      const uint64_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&s.hist256[(uint32_t)(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // lane l takes bins 255 - 8l down to 248 - 8l: descending key order
+      const int lane = threadIdx.x;
+      unsigned int cnt[8], tot = 0u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        cnt[q] = s.hist256[255 - 8 * lane - q];
+        tot += cnt[q];
+      }
+      unsigned int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int w = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += w;
+      }
+      const unsigned int excl = incl - tot;
+      if (excl < (unsigned int)need && (unsigned int)need <= incl) {
+        unsigned int run = excl;
+        int bin = -1, nn = 0, bc = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (bin < 0 && run + cnt[q] >= (unsigned int)need) {
+            bin = 255 - 8 * lane - q;
+            nn = need - (int)run;
+            bc = (int)cnt[q];
+          }
+          run += cnt[q];
+        }
+        s.bcast_i[0] = bin;
+        s.bcast_i[1] = nn;
+        s.bcast_i[2] = bc;
+      }
+    }
+    __syncthreads();
+    const int bin = s.bcast_i[0];
+    need = s.bcast_i[1];
+    const int bc = s.bcast_i[2];
+    prefix |= (uint64_t)(uint32_t)bin << shift;
+    mask |= 255ull << shift;
+    __syncthreads();  // the broadcast is read before anyone writes it again
+    if (bc == 1 || shift == 0) {
+      for (int i = threadIdx.x; i < N; i += kThreads)
+        if ((keys[i] & mask) == prefix) s.bcast_u[0] = keys[i];
+      __syncthreads();
+      const uint64_t r = s.bcast_u[0];
+      __syncthreads();
+      return r;
+    }
+  }
+  return prefix;  // not reached: the last byte leaves one key
+}
+
+// Descending bitonic sort of keys[0, n), n <= 32, by one warp (keys past n
+// read as 0, the smallest key).
+__device__ __forceinline__ void warp_sort_desc32(uint64_t* keys, int n, int lane) {
+  uint64_t v = lane < n ? keys[lane] : 0ull;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool lower = (lane & j) == 0;
+      const bool up = (lane & k) == 0;
+      v = (lower == up) ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  if (lane < n) keys[lane] = v;
+}
+
+// The q largest of N distinct keys (q <= 32), sorted descending into out[0, q):
+// a selection of the q-th, a gather of the keys at or above it, a warp sort.
+__device__ void block_top_desc(const uint64_t* keys, int N, int q, uint64_t* out, Smem& s) {
+  const uint64_t kq = block_select_desc(keys, N, q, s);
+  if (threadIdx.x == 0) s.bcast_i[3] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += kThreads) {
+    const uint64_t k = keys[i];
+    if (k >= kq) out[atomicAdd(&s.bcast_i[3], 1)] = k;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) warp_sort_desc32(out, q, threadIdx.x);
+  __syncthreads();
 }
 
 // min-p test z_t - m >= ln(min_p), decided exactly in double; fp32 decides
@@ -1192,6 +1298,38 @@ __device__ int leader_draw(Ctx& c, Smem& s, int N, bool L2_inside, double S_fixe
   return L3;
 }
 
+// The same without top-p, on the unsorted candidates: the kept set is the
+// L2 = min(top_k, min-p survivors) largest keys, found by selection.  Returns
+// L2; *kk is the last kept key.
+__device__ int leader_draw_unordered(Ctx& c, Smem& s, int N, int* tok, float* ztok,
+                                     uint64_t* kk) {
+  int pass = 0;
+  if (c.minp)
+    for (int i = c.tid; i < N; i += kThreads) pass += minp_pass(key_z(c.buf[i]), c.m_t, c.lmp);
+  const int L1 = c.minp ? block_sum_int(pass, s) : N;
+  const int L2 = max(1, c.topk ? min(c.top_k, L1) : L1);
+  const uint64_t kb = block_select_desc(c.buf, N, L2, s);
+  float bs = -INFINITY, bz = 0.f;
+  int bidx = INT_MAX;
+  for (int i = c.tid; i < N; i += kThreads) {
+    const uint64_t k = c.buf[i];
+    if (k < kb) continue;
+    const int j = (int)key_idx(k);
+    const float zt = key_z(k);
+    const float sc = gumbel_score(zt, noise_bits(c.rkey, j));
+    if (pair_better(sc, j, bs, bidx)) {
+      bs = sc;
+      bidx = j;
+      bz = zt;
+    }
+  }
+  block_argmax(bs, bidx, bz, s);
+  *tok = bidx;
+  *ztok = bz;
+  *kk = kb;
+  return L2;
+}
+
 // ---------------------------------------------------------------------------
 // per-row set-up shared by both kernels
 // ---------------------------------------------------------------------------
@@ -1564,9 +1702,6 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
   return bv;
 }
 
-// Outputs of a row whose statistics make it unsampleable (non-finite values,
-// or no finite value): token -1, NaN log-probs, the status; the seed still
-// advances and the top-p decay state stays.  The row's leader CTA calls it.
 // Top-p decay after the row's sampled token [TensorRT-LLM "Sampling", top-p
 // decay]: back to the initial top_p when the token is the reset id, else
 // max(top_p * decay, top_p_min), in fp32.  One thread of the row calls it.
@@ -1578,6 +1713,9 @@ __device__ __forceinline__ void decay_top_p(const SampleArgs& a, int row, int to
   d.p = tok == d.reset_id ? P.top_p : (q < d.p_min ? d.p_min : q);
 }
 
+// Outputs of a row whose statistics make it unsampleable (non-finite values,
+// or no finite value): token -1, NaN log-probs, the status; the seed still
+// advances and the top-p decay state stays.  The row's leader CTA calls it.
 __device__ __forceinline__ void write_bad_row(const SampleArgs& a, const Smem& s, int row,
                                               int status) {
   const int n = a.n_logprobs;
@@ -1856,24 +1994,40 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
       return;
     }
     const int N = nc;
-    block_sort_desc(c.buf, N);
-    for (int t = c.tid; t < n; t += kThreads) {
-      const uint64_t k = c.buf[t];
-      out_ids[t] = (int)key_idx(k);
-      out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
-    }
     int tok;
     float ztok;
     int L3;
-    if (c.greedy) {
-      tok = s.rs.bi;
-      ztok = c.m_t;
-      L3 = 1;
-    } else {
+    uint64_t kk = 0ull;  // the last kept key
+    if (c.topp) {
+      // top-p needs the masses in order: the whole candidate set sorted
+      block_sort_desc(c.buf, N);
+      for (int t = c.tid; t < n; t += kThreads) {
+        const uint64_t k = c.buf[t];
+        out_ids[t] = (int)key_idx(k);
+        out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
+      }
       L3 = leader_draw(c, s, N, L2_inside, S_fixed, &tok, &ztok);
+      kk = c.buf[L3 - 1];
+    } else {
+      // no order beyond the top-n: the kept boundary is a selection
+      if (n > 0) {
+        uint64_t* top = reinterpret_cast<uint64_t*>(s.tmax);
+        block_top_desc(c.buf, N, n, top, s);
+        for (int t = c.tid; t < n; t += kThreads) {
+          const uint64_t k = top[t];
+          out_ids[t] = (int)key_idx(k);
+          out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
+        }
+      }
+      if (c.greedy) {
+        tok = s.rs.bi;
+        ztok = c.m_t;
+        L3 = 1;
+      } else {
+        L3 = leader_draw_unordered(c, s, N, &tok, &ztok, &kk);
+      }
     }
     if (c.tid == 0) {
-      const uint64_t kk = c.buf[L3 - 1];
       a.out_tokens[c.row] = tok;
       if (a.out_logprobs) a.out_logprobs[c.row] = (ztok - c.m_t) - c.lnS;
       a.row_status[c.row] = kRowOk;
@@ -1896,9 +2050,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   // ---- rows the candidates cannot finish go to the selection kernel ---------
   if (leader) {
     if (n > 0 && topn_ok) {
-      block_sort_desc(c.buf, nc);
+      uint64_t* top = reinterpret_cast<uint64_t*>(s.tmax);
+      block_top_desc(c.buf, nc, n, top, s);
       for (int t = c.tid; t < n; t += kThreads) {
-        const uint64_t k = c.buf[t];
+        const uint64_t k = top[t];
         out_ids[t] = (int)key_idx(k);
         out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
       }
@@ -2103,26 +2258,38 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
       sp_k0 = v[6];
       sp_k1 = v[7];
     }
-    for (int b = tid; b < nb; b += kThreads) {
-      unsigned int cnt[kMaxCluster], bst[kMaxCluster];
+    // (nb is a multiple of kThreads: 8 slots of a thread per round, every
+    // CTA's values for them loaded before any is combined)
+    for (int b = tid; b < nb; b += 8 * kThreads) {
+      unsigned int sc[8], sbm[8];
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < C) {
-          const unsigned int* hr = cluster.map_shared_rank(hc, r);
-          cnt[r] = hr[b0 + b];
-          bst[r] = hr[kCodeSlots + b0 + b];
+      for (int u = 0; u < 8; ++u) {
+        sc[u] = 0u;
+        sbm[u] = 0u;
+      }
+      for (int r = 0; r < C; ++r) {
+        const unsigned int* hr = cluster.map_shared_rank(hc, r) + b0;
+        unsigned int cnt[8], bst[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int bb = b + u * kThreads;
+          cnt[u] = bb < nb ? hr[bb] : 0u;
+          bst[u] = bb < nb ? hr[kCodeSlots + bb] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          sc[u] += cnt[u];
+          sbm[u] = bst[u] > sbm[u] ? bst[u] : sbm[u];
         }
       }
-      unsigned int sc = 0u, sbm = 0u;
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < C) {
-          sc += cnt[r];
-          sbm = bst[r] > sbm ? bst[r] : sbm;
+      for (int u = 0; u < 8; ++u) {
+        const int bb = b + u * kThreads;
+        if (bb < nb) {
+          mc[bb] = sc[u];
+          mb[bb] = sbm[u];
         }
       }
-      mc[b] = sc;
-      mb[b] = sbm;
     }
     __syncthreads();
     VT_CTRACE(c, 11);
@@ -2544,11 +2711,14 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
     if (leader) {
       if (gather_b) {
         // the kept prefix of the boundary slot: its bkp lowest indices
+        // (keys 0xFFFFFFFF - j: the bkp largest are the bkp lowest indices)
         uint64_t* bk = reinterpret_cast<uint64_t*>(code_mem);
         const int nbk = min(s.gcount2, kBufCap);
-        block_sort_desc(bk, nbk);
+        const int kq = min(bkp, nbk);
+        const uint64_t kth = kq >= 1 ? block_select_desc(bk, nbk, kq, s) : ~0ull;
         unsigned long long kb = 0ull;
-        for (int t = tid; t < bkp && t < nbk; t += kThreads) {
+        for (int t = tid; t < nbk; t += kThreads) {
+          if (bk[t] < kth) continue;
           const int j = (int)(0xFFFFFFFFu - (uint32_t)bk[t]);
           const unsigned long long k =
               ((unsigned long long)(noise_bits(rkey, j) + 1u) << 32) | (0xFFFFFFFFu - (uint32_t)j);
@@ -2557,19 +2727,21 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
         kb = block_max_u64(kb, s);
         if (tid == 0) {
           s.part.cb_key = kb;
-          s.part.cb_last = (bkp >= 1 && bkp <= nbk) ? (int)(0xFFFFFFFFu - (uint32_t)bk[bkp - 1]) : -1;
+          s.part.cb_last = (bkp >= 1 && bkp <= nbk) ? (int)(0xFFFFFFFFu - (uint32_t)kth) : -1;
           if (s.gcount2 > kBufCap || bkp > nbk) s.part.err |= kErrInternal;
         }
         __syncthreads();
       }
       if (want_topn) {
         const int N = min(s.gcount, kBufCap);
-        block_sort_desc(c.buf, N);
+        const int q = min(n, N);
+        uint64_t* top = reinterpret_cast<uint64_t*>(s.tmax);
+        if (q > 0) block_top_desc(c.buf, N, q, top, s);
         int32_t* out_ids = a.out_topk_ids + (int64_t)row * n;
         float* out_lps = a.out_topk_logprobs + (int64_t)row * n;
         for (int t = tid; t < n; t += kThreads) {
-          if (t < N) {
-            const uint64_t k = c.buf[t];
+          if (t < q) {
+            const uint64_t k = top[t];
             out_ids[t] = (int)key_idx(k);
             out_lps[t] = (key_z(k) - m_t) - lnS;
           } else {
