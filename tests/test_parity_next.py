@@ -19,6 +19,8 @@ from paritylib import (check_workload, compare, custom_workload, device_logits, 
 
 pytestmark = pytest.mark.gpu
 
+V_FULL = 151_936
+
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -208,7 +210,10 @@ def check_probs(g, probs, o, where):
             continue
         kept = int(g["kept"][r])
         want = o.probs[r] if kept == o.kept_count[r] else O.filtered_probs(o.zt[r], kept)
-        assert ((got > 0) == (want > 0)).all(), (tag, "support")
+        # the kept set: nothing outside it; inside, fp32 holds every entry that
+        # is not below its smallest subnormal
+        assert (got[want == 0] == 0).all(), (tag, "outside the kept set")
+        assert (got[want >= 1e-44] > 0).all(), (tag, "inside the kept set")
         np.testing.assert_allclose(got, want, rtol=PROBS_RTOL, atol=PROBS_ATOL, err_msg=tag)
         assert abs(float(got.astype(np.float64).sum()) - 1.0) < 1e-4, tag
     if probs.shape[1] > V:
@@ -301,5 +306,42 @@ def test_probs_full_vocab_batch():
         o = O.sample_workload(w, want_zt=True, want_probs=True, rows=rows)
         compare(g, o, rows=rows, where="b256")
         check_probs({k: v[rows] for k, v in g.items()}, probs[rows], o, "b256")
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("V", [1, 7, 17, 100, 4097, 200_003])
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+def test_probs_vocab_widths(V, dtype):
+    # ragged tails, one to many CTAs per row, splits of one element to 64 K
+    rng = np.random.default_rng(70 + V)
+    B = 6
+    x = rng.normal(0, 2.0, size=(B, V)).astype(np.float32)
+    w = custom_workload(x, dtype=dtype, T=[0.0, 0.9, 1.2, 0.7, 1.0, 0.5],
+                        k=[0, 0, 5, 0, 40, 3], p=[1.0, 1.0, 1.0, 0.8, 0.9, 1.0],
+                        mp=[0.0, 0.0, 0.0, 0.0, 0.0, 0.2], n=min(5, V), name=f"probs V{V}")
+    s = make_sampler(w)
+    try:
+        s.reset_workload(w)
+        g, probs = sample_with_probs(s, w)
+        o = O.sample_workload(w, want_zt=True, want_probs=True)
+        compare(g, o, where=w.name)
+        check_probs(g, probs, o, w.name)
+    finally:
+        s.close()
+
+
+def test_probs_single_row_many_splits():
+    # one row: the grid spreads it over the most CTAs the plan allows
+    rng = np.random.default_rng(77)
+    x = W.peaked_rows(rng, 1, V_FULL)
+    w = custom_workload(x, dtype=W.DTYPE_BF16, T=1.3, p=0.97, n=3, name="probs B1")
+    s = make_sampler(w)
+    try:
+        s.reset_workload(w)
+        g, probs = sample_with_probs(s, w)
+        o = O.sample_workload(w, want_zt=True, want_probs=True)
+        compare(g, o, where=w.name)
+        check_probs(g, probs, o, w.name)
     finally:
         s.close()
