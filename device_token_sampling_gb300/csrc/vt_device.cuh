@@ -161,10 +161,8 @@ __device__ __forceinline__ uint32_t noise_bits(uint64_t key, int64_t j) {
 }
 
 // ln(e) with e = -ln(u), u = (b + 1/2) 2^-24, evaluated through inputs that are
-// exact in fp32: u itself below 1/2, 1 - u from 1/2 up.  Kept out of line: the
-// scans call it rarely (behind may_beat) from unrolled loops, where inlined
-// copies of the logarithms would crowd the instruction cache.
-static __device__ __noinline__ float log_exp_noise(uint32_t b) {
+// exact in fp32: u itself below 1/2, 1 - u from 1/2 up.
+__device__ __forceinline__ float log_exp_noise_inl(uint32_t b) {
   float e;
   if (b < (1u << 23)) {
     const float u = (float)(2u * b + 1u) * 0x1p-25f;
@@ -176,10 +174,19 @@ static __device__ __noinline__ float log_exp_noise(uint32_t b) {
   }
   return logf(e);
 }
+// The same kept out of line: the scans call it rarely (behind may_beat) from
+// unrolled loops, where inlined copies of the logarithms would crowd the
+// instruction cache.
+static __device__ __noinline__ float log_exp_noise(uint32_t b) { return log_exp_noise_inl(b); }
 
 // Gumbel score z_t - ln(-ln u).
 __device__ __forceinline__ float gumbel_score(float zt, uint32_t b) {
   return __fsub_rn(zt, log_exp_noise(b));
+}
+// The same inline, for loops that score every element they visit (a call
+// would save and restore registers through local memory each time).
+__device__ __forceinline__ float gumbel_score_inl(float zt, uint32_t b) {
+  return __fsub_rn(zt, log_exp_noise_inl(b));
 }
 
 // A cheap certificate that an element cannot beat the score `s_cur`:

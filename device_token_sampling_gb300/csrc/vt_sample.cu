@@ -1285,7 +1285,7 @@ __device__ int leader_draw(Ctx& c, Smem& s, int N, bool L2_inside, double S_fixe
     const uint64_t k = c.buf[i];
     const int j = (int)key_idx(k);
     const float zt = key_z(k);
-    const float sc = gumbel_score(zt, noise_bits(c.rkey, j));
+    const float sc = gumbel_score_inl(zt, noise_bits(c.rkey, j));
     if (pair_better(sc, j, bs, bidx)) {
       bs = sc;
       bidx = j;
@@ -1316,7 +1316,7 @@ __device__ int leader_draw_unordered(Ctx& c, Smem& s, int N, int* tok, float* zt
     if (k < kb) continue;
     const int j = (int)key_idx(k);
     const float zt = key_z(k);
-    const float sc = gumbel_score(zt, noise_bits(c.rkey, j));
+    const float sc = gumbel_score_inl(zt, noise_bits(c.rkey, j));
     if (pair_better(sc, j, bs, bidx)) {
       bs = sc;
       bidx = j;
@@ -2471,7 +2471,13 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
           if (sl == tiny || sl == kCatch || na > (unsigned int)kBufCap) {
             lw->fallback = 1;  // a boundary slot is gathered whole
           } else {
-            const unsigned long long kq = (tgt_m - A) / mass_fixed(zq(sl), m_t) + 1ull;
+            // kq = floor((tgt_m - A) / mass) + 1, below the slot's count: a
+            // float quotient corrected to the exact one by integer products
+            const unsigned long long num = tgt_m - A, den = mass_fixed(zq(sl), m_t);
+            unsigned long long q = (unsigned long long)__fdiv_rz((float)num, (float)den);
+            while (q > 0ull && q * den > num) --q;
+            while ((q + 1ull) * den <= num) ++q;
+            const unsigned long long kq = q + 1ull;
             lw->slot = sl;
             lw->kp = kq < (unsigned long long)nc ? (int)kq : (int)nc;
             lw->above = run;
@@ -2517,7 +2523,7 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
           const float z = zq(sl);
           if (minp && !minp_pass(z, m_t, lmp)) continue;
           if (approx_score(z, bbits - 1u) < cmax_a - margin) continue;
-          const float sc = gumbel_score(z, bbits - 1u);
+          const float sc = gumbel_score_inl(z, bbits - 1u);
           if (sc > emax) {
             emax = sc;
             eslot = sl;
@@ -2767,33 +2773,41 @@ __device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
             cwj = min(cwj, pr->cw_j);
             lsj = max(lsj, pr->last_j);
           }
-          float bs = -INFINITY;
+          // candidates: (score, index) and the tempered value when its slot
+          // holds one value (else it is read from the logits)
+          float bs = -INFINITY, bz = 0.f;
           int bi = INT_MAX;
-          auto offer = [&](float sc, int j) {
+          bool bz_known = false;
+          auto offer = [&](float sc, int j, float zt, bool known) {
             if (j != INT_MAX && pair_better(sc, j, bs, bi)) {
               bs = sc;
               bi = j;
+              bz = zt;
+              bz_known = known;
             }
           };
           if (wslot >= 0) {
             if (cwj == INT_MAX)
               er |= kErrInternal;  // the winning slot's best element must exist
             else
-              offer(wscore, cwj);
+              offer(wscore, cwj, zq(wslot), true);
           }
           if (bslot >= 0 && cbk != 0ull) {
             const uint32_t bits = (uint32_t)(cbk >> 32) - 1u;
-            offer(gumbel_score(zq_value(cmax, bslot, inv_t), bits), (int)(0xFFFFFFFFu - (uint32_t)cbk));
+            const float zb = zq_value(cmax, bslot, inv_t);
+            offer(gumbel_score(zb, bits), (int)(0xFFFFFFFFu - (uint32_t)cbk), zb, true);
           }
-          if (sp_kept0 && sp_k0 != 0ull) offer(key_z(sp_k0), (int)key_idx(sp_k0));
-          if (sp_kept1 && sp_k1 != 0ull) offer(key_z(sp_k1), (int)key_idx(sp_k1));
+          if (sp_kept0 && sp_k0 != 0ull) offer(key_z(sp_k0), (int)key_idx(sp_k0), 0.f, false);
+          if (sp_kept1 && sp_k1 != 0ull) offer(key_z(sp_k1), (int)key_idx(sp_k1), 0.f, false);
           if (bi == INT_MAX) {
             er |= kErrInternal;
             bi = s.rs.bi;
+            bz_known = false;
           }
           tok = bi;
-          // the winner's tempered value, from its logit
-          ztok = __fmul_rn(Elt<T>::load1(reinterpret_cast<const T*>(c.rowp) + tok), inv_t);
+          // the winner's tempered value: its slot's value, or from its logit
+          ztok = bz_known ? bz
+                          : __fmul_rn(Elt<T>::load1(reinterpret_cast<const T*>(c.rowp) + tok), inv_t);
           if (bslot >= 0) {
             kept = (int)(above + (unsigned long long)bkp);
             kth_v = zq_value(cmax, bslot, inv_t);
