@@ -106,8 +106,9 @@ cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dt
 // The selection kernel alone over the rows args.rows[0, args.B) (args.early
 // set): one cluster per row streams its slices for the row statistics (the
 // same slices and arithmetic as the streaming kernel), then selects and draws.
+// `launched`, when not null, is recorded once every CTA of the launch has begun.
 cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, int dtype,
-                              cudaStream_t stream);
+                              cudaStream_t stream, cudaEvent_t launched = nullptr);
 
 // Build the per-row sorted (id, count) tables from raw ids.
 //   raw, offs  CSR: row r owns raw[offs[r] .. offs[r+1]) (prompt then output)

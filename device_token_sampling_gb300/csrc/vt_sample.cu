@@ -3501,13 +3501,19 @@ cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dt
 }
 
 cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, int dtype,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, cudaEvent_t launched) {
   if (dtype == 0 || plan.own.cluster < 1 || !args.early) return cudaErrorInvalidValue;
-  if (args.B < 1) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
+  if (args.B < 1) return launched ? cudaEventRecord(launched, stream) : cudaSuccess;
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = select_config<uint16_t>(plan.own, attr);
   cfg.gridDim = dim3((unsigned)(args.B * plan.own.cluster), 1, 1);
   cfg.stream = stream;
+  if (launched) {  // fires once every CTA of the launch has begun
+    attr[1].id = cudaLaunchAttributeLaunchCompletionEvent;
+    attr[1].val.launchCompletionEvent.event = launched;
+    attr[1].val.launchCompletionEvent.flags = 0;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, select_kernel<uint16_t>, args, plan.own);
 }
 

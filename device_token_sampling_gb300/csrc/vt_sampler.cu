@@ -51,6 +51,7 @@ struct vt_sampler {
   // beside the main stream's launches (fork and join through events)
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_launched = nullptr;  // every side CTA has begun
   int n_main = 0, n_side = 0;
   int last_launches = 0;  // kernels the last vt_sample launched
   // pinned host staging
@@ -146,6 +147,7 @@ void free_all(vt_sampler* h) {
   if (h->h_rows) cudaFreeHost(h->h_rows);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_launched) cudaEventDestroy(h->ev_launched);
   if (h->side) cudaStreamDestroy(h->side);
   dfree(h->d_io_logits);
   dfree(h->d_io_tokens);
@@ -261,6 +263,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
       cudaEventCreateWithFlags(&h->ev_counts, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_launched, cudaEventDisableTiming) != cudaSuccess ||
       cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess)
     return bail(VT_ERR_CUDA);
   if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
@@ -590,10 +593,14 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     VT_CK(h, cudaStreamWaitEvent(h->side, h->ev_fork, 0));
     // the side rows: the selection kernel alone, taking their statistics
     // itself (else the streaming kernel hands them over at once)
-    if (ps->own.cluster >= 1)
-      VT_CK(h, vt::launch_select_own(as, *ps, dtype, h->side));
-    else
+    // The side rows are the step's longest: the main rows' CTAs wait until
+    // every side CTA has begun, so that the side ones never wait for room.
+    if (ps->own.cluster >= 1) {
+      VT_CK(h, vt::launch_select_own(as, *ps, dtype, h->side, h->ev_launched));
+      VT_CK(h, cudaStreamWaitEvent(st, h->ev_launched, 0));
+    } else {
       VT_CK(h, vt::launch_sample(as, *ps, dtype, h->side, nullptr));
+    }
     VT_CK(h, vt::launch_sample(am, *pm, dtype, st, h->phase_event));
     VT_CK(h, cudaEventRecord(h->ev_join, h->side));
     VT_CK(h, cudaStreamWaitEvent(st, h->ev_join, 0));
