@@ -52,6 +52,7 @@ struct vt_sampler {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   cudaEvent_t ev_launched = nullptr;  // every side CTA has begun
+  bool launch_order = true;           // main rows wait for ev_launched (while it works)
   int n_main = 0, n_side = 0;
   int last_launches = 0;  // kernels the last vt_sample launched
   // pinned host staging
@@ -595,9 +596,24 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     // itself (else the streaming kernel hands them over at once)
     // The side rows are the step's longest: the main rows' CTAs wait until
     // every side CTA has begun, so that the side ones never wait for room.
+    // The order is a preference: where the launch-completion event or the
+    // wait on it is refused (a profiler that serialises kernels refuses the
+    // wait), the handle stops asking for it.
     if (ps->own.cluster >= 1) {
-      VT_CK(h, vt::launch_select_own(as, *ps, dtype, h->side, h->ev_launched));
-      VT_CK(h, cudaStreamWaitEvent(st, h->ev_launched, 0));
+      bool launched = false;
+      if (h->launch_order) {
+        if (vt::launch_select_own(as, *ps, dtype, h->side, h->ev_launched) == cudaSuccess) {
+          launched = true;
+          if (cudaStreamWaitEvent(st, h->ev_launched, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            h->launch_order = false;
+          }
+        } else {
+          (void)cudaGetLastError();
+          h->launch_order = false;
+        }
+      }
+      if (!launched) VT_CK(h, vt::launch_select_own(as, *ps, dtype, h->side, nullptr));
     } else {
       VT_CK(h, vt::launch_sample(as, *ps, dtype, h->side, nullptr));
     }
