@@ -345,3 +345,61 @@ def test_probs_single_row_many_splits():
         check_probs(g, probs, o, w.name)
     finally:
         s.close()
+
+
+def test_features_together_over_steps():
+    """prompt_ignore_length, top-p decay, update_counts and the filtered
+    distribution in one multi-call run over a bf16 batch whose top-p-only rows
+    take the second stream; each call is checked against the oracle with the
+    history and effective top_p the previous calls left (teacher forced)."""
+    rng = np.random.default_rng(80)
+    B, V, steps = 12, 40_000, 3
+    T = np.array([0.0, 0.8, 1.1, 0.9, 1.3, 1.0, 0.7, 1.2, 1.0, 0.9, 1.4, 0.6], np.float32)
+    k = np.array([0, 30, 0, 0, 0, 100, 0, 0, 1, 0, 0, 0], np.int32)
+    p = np.array([1.0, 0.9, 0.8, 0.95, 0.9, 1.0, 0.7, 0.99, 1.0, 1.0, 0.85, 0.9], np.float32)
+    pres = np.array([0.3, 0.0, 0.0, 0.5, 0.0, 0.2, 0.0, 0.0, 0.0, 0.4, 0.0, 0.0], np.float32)
+    rep = np.array([1.1, 1.0, 1.0, 1.2, 1.0, 1.0, 1.0, 1.0, 1.0, 0.9, 1.0, 1.0], np.float32)
+    decay = np.array([1, 1, 1, 0.8, 1, 0.7, 0.9, 1, 1, 1, 1, 1], np.float32)
+    pmin = np.full(B, 0.3, np.float32)
+    reset = np.full(B, -1, np.int32)
+    ignore = np.array([0, 0, 0, 10, 0, 50, 0, 0, 0, 200, 0, 0], np.int32)
+    prompt, output = history(rng, B, V, 60, 20)
+    output = [list(o) for o in output]
+    x0 = W.peaked_rows(rng, B, V)
+    w0 = custom_workload(x0, dtype=W.DTYPE_BF16, T=T, k=k, p=p, pres=pres, freq=0.1 * (pres > 0),
+                         rep=rep, n=4, prompt=prompt, output=output, name="together")
+    w0.prompt_ignore = ignore
+    s = make_sampler(w0, max_history=256)
+    try:
+        s.reset_params(w0.temperature, w0.top_k, w0.top_p, w0.min_p, w0.presence, w0.frequency,
+                       w0.repetition, w0.seed, top_p_decay=decay, top_p_min=pmin,
+                       top_p_reset_ids=reset)
+        s.reset_token_counts(w0.prompt_ids, w0.prompt_offsets, w0.output_ids, w0.output_offsets,
+                             prompt_ignore=ignore)
+        active = (decay < 1) & (T > 0) & (k != 1)
+        p_eff = p.copy()
+        seed = w0.seed.copy()
+        for step in range(steps):
+            x = x0 if step == 0 else W.peaked_rows(rng, B, V)
+            ws = custom_workload(x, dtype=W.DTYPE_BF16, T=T, k=k, p=p, pres=pres,
+                                 freq=0.1 * (pres > 0), rep=rep, n=4, prompt=prompt,
+                                 output=[np.array(o, np.int32) for o in output],
+                                 name=f"together step {step}")
+            ws.prompt_ignore = ignore
+            ws.seed = seed.copy()
+            g, probs = sample_with_probs(s, ws, update_counts=True)
+            # the split step (3 or 4 launches), the two export passes, the append
+            assert s.last_launches() in (6, 7), s.last_launches()
+            o = O.sample_workload(ws, want_zt=True, top_p=p_eff, want_probs=True)
+            compare(g, o, where=ws.name)
+            check_probs(g, probs, o, ws.name)
+            for r in range(B):
+                if g["status"][r] == 0:
+                    output[r].append(int(g["token"][r]))
+                    if active[r]:
+                        p_eff[r] = O.topp_decay(float(p_eff[r]), float(p[r]), float(decay[r]),
+                                                float(pmin[r]), int(reset[r]), int(g["token"][r]))
+            seed = np.array([O.next_seed(int(v)) for v in seed], np.uint64)
+            np.testing.assert_array_equal(s.top_p(B), p_eff, err_msg=ws.name)
+    finally:
+        s.close()
