@@ -183,7 +183,10 @@ int vt_reset_token_counts_ex(vt_sampler* handle, int32_t B, const int32_t* promp
  *                     and their log-probs; -1 / NaN for a row without a token;
  *                     may be NULL only when num_logprobs == 0.
  * The call enqueues device work only: it allocates nothing, does not
- * synchronise, and may be captured into a CUDA graph.
+ * synchronise, and may be captured into a CUDA graph.  A bf16 call over all
+ * the rows of the last vt_reset_params may run its top-p-only rows on a
+ * stream of the handle: it forks from `stream` and joins back into it through
+ * events, so that all of the call's work is ordered on `stream`.
  * Errors: VT_ERR_STATE (no vt_reset_params yet, B larger than the rows given
  * there, or a row with penalties whose counts were never reset),
  * VT_ERR_INVALID_ARG, VT_ERR_CAPACITY, VT_ERR_CUDA (launch failure).  Device-
