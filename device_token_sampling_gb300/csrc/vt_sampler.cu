@@ -598,10 +598,12 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     // every side CTA has begun, so that the side ones never wait for room.
     // The order is a preference: where the launch-completion event or the
     // wait on it is refused (a profiler that serialises kernels refuses the
-    // wait), the handle stops asking for it.
+    // wait), the handle stops asking for it.  It is asked for only when every
+    // side cluster fits on the GPU at once; else the main rows would wait for
+    // the side kernel's last wave to begin.
     if (ps->own.cluster >= 1) {
       bool launched = false;
-      if (h->launch_order) {
+      if (h->launch_order && h->n_side <= ps->own.clusters) {
         if (vt::launch_select_own(as, *ps, dtype, h->side, h->ev_launched) == cudaSuccess) {
           launched = true;
           if (cudaStreamWaitEvent(st, h->ev_launched, 0) != cudaSuccess) {
