@@ -833,6 +833,12 @@ int vt_debug_get_seeds(vt_sampler* h, uint64_t* host_seeds) {
   return VT_OK;
 }
 
+int vt_debug_probs_plan(int32_t B, int32_t V, int32_t num_sms, int32_t* splits, int32_t* range) {
+  if (B < 1 || V < 1 || num_sms < 1 || !splits || !range) return VT_ERR_INVALID_ARG;
+  vt::plan_probs(B, V, num_sms, splits, range);
+  return VT_OK;
+}
+
 int vt_read_top_p(vt_sampler* h, float* host_top_p) {
   if (!h || !host_top_p) return VT_ERR_INVALID_ARG;
   if (h->params_B == 0) return set_err(h, VT_ERR_STATE, "no vt_reset_params yet");

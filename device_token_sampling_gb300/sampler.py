@@ -60,6 +60,7 @@ SIGNATURES = {
     "vt_reset_params": (C.c_int, [P, I32, P, P, P, P, P, P, P, P, P]),
     "vt_reset_params_ex": (C.c_int, [P, I32, P, P, P, P, P, P, P, P, P, P, P, P]),
     "vt_read_top_p": (C.c_int, [P, P]),
+    "vt_debug_probs_plan": (C.c_int, [I32, I32, I32, P, P]),
     "vt_reset_token_counts": (C.c_int, [P, I32, P, P, P, P, P]),
     "vt_reset_token_counts_ex": (C.c_int, [P, I32, P, P, P, P, P, P]),
     "vt_sample": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),

@@ -258,6 +258,14 @@ int vt_debug_get_counts(vt_sampler* handle, int32_t row, int32_t* ids, int32_t* 
 int vt_debug_launch_shape(vt_sampler* handle, int32_t dtype, int32_t V, int32_t* ctas_per_row,
                           int32_t* slice_elems, int64_t* smem_bytes);
 
+/* Debug, no device needed: the grid vt_sample_ex uses for the filtered
+ * distribution of B rows of V on a GPU of num_sms SMs: CTAs per row
+ * (*splits) and elements per CTA (*range, a multiple of 64).  A handle
+ * created for (max_batch, max_vocab) holds the partials of every B <= max_batch
+ * and V <= max_vocab.  Errors: VT_ERR_INVALID_ARG (a size below 1, null
+ * pointer). */
+int vt_debug_probs_plan(int32_t B, int32_t V, int32_t num_sms, int32_t* splits, int32_t* range);
+
 /* Debug: phase trace.  With a device buffer of capacity_ctas * slots_per_cta
  * uint64 entries set, each later vt_sample whose grid fits writes, per CTA,
  * the GPU global timer (ns) at each phase boundary (slots not reached keep

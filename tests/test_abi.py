@@ -81,3 +81,37 @@ def test_product_package_does_not_import_the_oracle():
             text = open(path, errors="ignore").read()
             assert "import oracle" not in text and "from oracle" not in text, path
             assert "oracle.h" not in text, path
+
+
+def test_probs_plan_without_gpu(lib_path):
+    """The filtered distribution's grid: every split holds 1 to 64 K elements (a
+    multiple of 64 wide), the splits cover the row exactly, and B x splits stays
+    within the partials a handle allocates at create: max_batch x (ceil(max_vocab
+    / 64 K) + 1) + 6 per SM."""
+    from device_token_sampling_gb300 import sampler
+    lib = sampler.load_library()
+    sp, rg = ctypes.c_int32(), ctypes.c_int32()
+
+    def plan(B, V, sms):
+        assert lib.vt_debug_probs_plan(B, V, sms, ctypes.byref(sp), ctypes.byref(rg)) == 0
+        return sp.value, rg.value
+
+    def cap(max_b, max_v, sms):
+        return max_b * ((max_v + 65535) // 65536 + 1) + 6 * sms
+
+    sizes_b = [1, 2, 7, 64, 255, 256, 1000, 4096, 1 << 20]
+    sizes_v = [1, 63, 64, 65, 1000, 65536, 65537, 151_936, 248_320, 1 << 20]
+    for sms in (1, 152):
+        for B in sizes_b:
+            for V in sizes_v:
+                s, r = plan(B, V, sms)
+                assert r % 64 == 0 and 64 <= r <= 65536, (B, V, r)
+                assert (s - 1) * r < V <= s * r, (B, V, s, r)
+                assert B * s <= cap(B, V, sms), (B, V, s)
+        for mb in sizes_b:
+            for mv in sizes_v:
+                for B in [b for b in sizes_b if b <= mb][-3:]:
+                    for V in [v for v in sizes_v if v <= mv][-3:]:
+                        assert B * plan(B, V, sms)[0] <= cap(mb, mv, sms), (mb, mv, B, V)
+    assert lib.vt_debug_probs_plan(0, 10, 152, ctypes.byref(sp), ctypes.byref(rg)) == \
+        sampler.VT_ERR_INVALID_ARG
