@@ -64,6 +64,19 @@ def make_workload(name: str, rank: int) -> W.Workload:
     raise ValueError(name)
 
 
+def whole_job_rate(local_s: float, rows_per_rank: int, world: int, device) -> tuple:
+    """The slowest rank's time (seconds) and the whole job's rows per second:
+    every rank samples rows_per_rank rows in its own time; the job takes the
+    longest of them."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_s], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    slowest = float(t.item())
+    return slowest, rows_per_rank * world / slowest
+
+
 def algorithmic_bytes_per_row(w: W.Workload) -> np.ndarray:
     """Bytes one row must move at minimum: its logits once, its distinct
     (id, count) history pairs, its parameters and seed (read + write), and its
@@ -338,13 +351,9 @@ def run_gpu(args, w: W.Workload):
     s.check_device_errors()
     k1_ms = float(np.mean([ea.elapsed_time(em) for ea, em, _ in evs]))
     k2_ms = float(np.mean([em.elapsed_time(eb) for _, em, eb in evs]))
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_s, value = whole_job_rate(elapsed_ms / 1e3, B * args.steps, world, dev)
+    max_ms = max_s * 1e3
     ms_per_step = max_ms / args.steps
-    rows_total = B * args.steps * world
-    value = rows_total / (max_ms / 1e3)
 
     # end to end through the C ABI with host buffers: H2D of the step's logits
     # from pinned memory, sampling, D2H of the step's outputs, every step
@@ -360,10 +369,7 @@ def run_gpu(args, w: W.Workload):
     for i in range(e2e_steps):
         s.sample_host(host, V, dt, n, update, stream=stream, out=ho)
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = B * e2e_steps * world / float(te.item())
+    _, e2e_value = whole_job_rate(e2e_s, B * e2e_steps, world, dev)
     h2d = int(host.nbytes)
     d2h = int(sum(a.nbytes for a in ho))
 
