@@ -28,3 +28,12 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_single_and_all_cores():
+    sys.path.insert(0, ROOT)
+    import bench
+    from device_token_sampling_gb300 import workloads as W
+    d = bench.cpu_baseline(W.tiny(), budget_rows=4)
+    assert d["kind"] == "oracle" and d["cores"] == 1 and d["value"] > 0
+    assert d["all_cores"]["cores"] == (os.cpu_count() or 1) and d["all_cores"]["value"] > 0
