@@ -22,7 +22,7 @@ MAX_ALT = 8
 
 # Planted mistakes the mutation tests compile in, one per variant.
 MUTANTS = ("HASH", "TIE_HIGH", "PEN_ORDER", "PROMPT_ONLY", "TOPP_INCL", "TOPP_NO_RENORM",
-           "SCORE_MUL", "IGNORE_ALL")
+           "SCORE_MUL", "IGNORE_ALL", "PAIR_OVERLAP", "ROW_IGNORED", "STEP_IS_ROW")
 
 
 def lib_path(mutant: str | None = None) -> str:
@@ -85,6 +85,8 @@ def load(mutant: str | None = None) -> C.CDLL:
     lib.oracle_uniform.argtypes = [C.c_uint64, C.c_int64, C.c_int64]
     lib.oracle_next_seed.restype = C.c_uint64
     lib.oracle_next_seed.argtypes = [C.c_uint64]
+    lib.oracle_noise_bits.restype = C.c_int
+    lib.oracle_noise_bits.argtypes = [C.c_uint64, C.c_int64, C.c_int64, C.c_int64, P]
     _libs[key] = lib
     return lib
 
@@ -234,6 +236,16 @@ def mix64(z: int, mutant=None) -> int:
 
 def uniform(seed: int, row: int, j: int, mutant=None) -> float:
     return float(load(mutant).oracle_uniform(C.c_uint64(seed), row, j))
+
+
+def noise_bits(seed: int, row: int, j0: int, n: int, mutant=None) -> np.ndarray:
+    """The 24-bit noise integers b_j of columns j0 .. j0 + n - 1 of ``row``."""
+    out = np.zeros(int(n), np.uint32)
+    rc = load(mutant).oracle_noise_bits(C.c_uint64(seed % 2**64), int(row), int(j0), int(n),
+                                        _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_noise_bits rejected its arguments")
+    return out
 
 
 def next_seed(seed: int) -> int:

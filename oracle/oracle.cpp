@@ -36,15 +36,32 @@ uint64_t mix64(uint64_t z) {
 
 // Row key: the seed mixed with the (1-based) row number.
 uint64_t row_key(uint64_t seed, int64_t row) {
+#if defined(ORACLE_MUTANT_ROW_IGNORED)
+  (void)row;
+  return mix64(seed);  // planted: every row of one seed shares a stream
+#elif defined(ORACLE_MUTANT_STEP_IS_ROW)
+  return seed + kGamma * ((uint64_t)row + 1);  // planted: (seed + step, r) == (seed, r + 1)
+#else
   return mix64(seed ^ mix64((uint64_t)row + 1));
+#endif
 }
 
-// One SplitMix64 output serves the column pair (2i, 2i+1): the even column
-// takes bits 63..40, the odd column bits 31..8.  u = (b + 1/2) / 2^24.
-double uniform_from_key(uint64_t key, int64_t j) {
+// The 24-bit integer b_j of column j: one SplitMix64 output serves the column
+// pair (2i, 2i+1), the even column taking bits 63..40 and the odd column bits
+// 31..8.
+uint32_t noise_bits_from_key(uint64_t key, int64_t j) {
   const uint64_t x = mix64(key + kGamma * ((uint64_t)(j >> 1) + 1));
-  const uint32_t b = (j & 1) ? (uint32_t)((x >> 8) & 0xFFFFFFu) : (uint32_t)(x >> 40);
-  return ((double)b + 0.5) / 16777216.0;
+  if (!(j & 1)) return (uint32_t)(x >> 40);
+#ifdef ORACLE_MUTANT_PAIR_OVERLAP
+  return (uint32_t)((x >> 36) & 0xFFFFFFu);  // planted: the odd field overlaps the even one
+#else
+  return (uint32_t)((x >> 8) & 0xFFFFFFu);
+#endif
+}
+
+// u = (b + 1/2) / 2^24, strictly inside (0, 1) and exact in double.
+double uniform_from_key(uint64_t key, int64_t j) {
+  return ((double)noise_bits_from_key(key, j) + 0.5) / 16777216.0;
 }
 
 float bf16_to_f32(uint16_t b) {
@@ -345,6 +362,13 @@ double oracle_uniform(uint64_t seed, int64_t row, int64_t j) {
 }
 
 uint64_t oracle_next_seed(uint64_t seed) { return seed + kGamma; }
+
+int oracle_noise_bits(uint64_t seed, int64_t row, int64_t j0, int64_t n, uint32_t* out) {
+  if (row < 0 || j0 < 0 || n < 0 || (n > 0 && !out)) return -1;
+  const uint64_t key = row_key(seed, row);
+  for (int64_t i = 0; i < n; ++i) out[i] = noise_bits_from_key(key, j0 + i);
+  return 0;
+}
 
 int oracle_sample(int64_t first_row, int B, int V, int64_t ld, int dtype, const void* logits,
                   const float* temperature, const int32_t* top_k, const float* top_p,

@@ -129,6 +129,11 @@ double oracle_uniform(uint64_t seed, int64_t row, int64_t j);
 /* The seed a row carries into the next step: seed + 0x9E3779B97F4A7C15 mod 2^64. */
 uint64_t oracle_next_seed(uint64_t seed);
 
+/* The 24-bit noise integers b_j of row `row` under `seed` for the n columns
+ * j0 .. j0 + n - 1 (u_j = (b_j + 0.5) * 2^-24) into out[n].  Returns 0, or -1
+ * on bad arguments. */
+int oracle_noise_bits(uint64_t seed, int64_t row, int64_t j0, int64_t n, uint32_t* out);
+
 #ifdef __cplusplus
 }
 #endif

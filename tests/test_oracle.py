@@ -16,9 +16,18 @@ What pins what:
   min-p / top-k / top-p      subset enumeration of the page's definitions on V <= 8,
                              closed form on two-value rows
   noise                      KS test of u against U(0,1); -ln u against Exp(1)
+  key schedule               independence, not values: the even and odd 24-bit
+                             fields of one hash (16x16 contingency tables over
+                             every nibble pairing, 1e6 pairs); rows of one seed
+                             and consecutive steps of one row (no shared or
+                             shifted stream: value-overlap counts against the
+                             n^2 / 2^24 of independent streams, and same-column
+                             contingency tables)
   draw formula               chi-square of 1e6 draws against the filtered softmax
-The key schedule (which SplitMix64 output feeds which column) and the
-log-prob convention are this implementation's own reading: parity unpinned.
+Which SplitMix64 output feeds which column, and the log-prob convention, are
+this implementation's own reading: the pages fix no value for them, so their
+values are parity unpinned; the independence checks above pin the properties a
+plausible mistake in the schedule would break.
 """
 from __future__ import annotations
 
@@ -268,6 +277,53 @@ Z16 = np.array([2.1, 0.3, -0.7, 1.4, 0.0, -2.2, 1.9, 0.8, -0.1, 0.5, -1.3, 1.1, 
                 0.9, -3.0], np.float32)
 
 
+def _contingency_p(a, b, bins=16):
+    """p-value of a chi-square independence test of two nibble streams."""
+    t = np.zeros((bins, bins), np.int64)
+    np.add.at(t, (a.astype(np.int64), b.astype(np.int64)), 1)
+    return scipy.stats.chi2_contingency(t)[1]
+
+
+def check_pair_fields_independent(mutant=None, n_pairs=1_000_000):
+    """The even and odd columns of one hash output use disjoint, independent
+    bit fields: every nibble of one field against the top nibble of the other."""
+    b = O.noise_bits(0x5EED5EED, 11, 0, 2 * n_pairs, mutant=mutant)
+    even, odd = b[0::2], b[1::2]
+    for s in range(0, 24, 4):
+        assert _contingency_p((even >> s) & 15, odd >> 20) >= 1e-4, ("even nibble", s)
+        assert _contingency_p((odd >> s) & 15, even >> 20) >= 1e-4, ("odd nibble", s)
+
+
+def _streams_independent(b1, b2, tag):
+    n = len(b1)
+    overlap = len(np.intersect1d(b1, b2))
+    expect = n * n / 2**24  # distinct values two independent uniform streams share
+    assert overlap < expect + 10 * math.sqrt(expect) + 10, (tag, "overlap", overlap, expect)
+    assert _contingency_p(b1 >> 20, b2 >> 20) >= 1e-4, (tag, "same-column nibbles")
+
+
+def check_rows_independent(mutant=None, n=65_536):
+    """Rows of one seed draw independent streams, at any row distance."""
+    seed = 0xC0FFEE
+    for r in (0, 5, 1024):
+        b1 = O.noise_bits(seed, r, 0, n, mutant=mutant)
+        for d in (1, 2, 3, 64, 1000):
+            _streams_independent(b1, O.noise_bits(seed, r + d, 0, n, mutant=mutant), (r, d))
+
+
+def check_steps_independent(mutant=None, n=65_536):
+    """The stream a row draws after its seed advanced once shares nothing with
+    this step's streams of the same or a neighbouring row."""
+    seed = 0xABCDEF12345
+    nxt = O.next_seed(seed)
+    for r in (1, 77):
+        b1 = O.noise_bits(seed, r, 0, n, mutant=mutant)
+        for r2 in (r - 1, r, r + 1):
+            _streams_independent(b1, O.noise_bits(nxt, r2, 0, n, mutant=mutant), (r, r2))
+            _streams_independent(O.noise_bits(seed, r2, 0, n, mutant=mutant),
+                                 O.noise_bits(nxt, r, 0, n, mutant=mutant), (r2, r))
+
+
 def check_draw_distribution(mutant=None, n_draws=1_000_000):
     for k, p, mp in ((0, 1.0, 0.0), (8, 1.0, 0.0), (0, 0.5, 0.0), (0, 1.0, 0.1)):
         chi_square_case(Z16, k, p, mp, n_draws, mutant=mutant)
@@ -294,6 +350,24 @@ def test_uniform_noise_is_uniform(oracle_mod):
     # neighbouring columns share one hash output but are not equal
     pair = [(O.uniform(77, 3, 2 * i), O.uniform(77, 3, 2 * i + 1)) for i in range(2000)]
     assert sum(a == c for a, c in pair) <= 2
+
+
+def test_noise_bits_match_uniforms(oracle_mod):
+    b = O.noise_bits(123, 4, 1000, 64)
+    for i in range(64):
+        assert O.uniform(123, 4, 1000 + i) == (float(b[i]) + 0.5) / 2**24
+
+
+def test_pair_fields_independent(oracle_mod):
+    check_pair_fields_independent()
+
+
+def test_rows_of_one_seed_independent(oracle_mod):
+    check_rows_independent()
+
+
+def test_steps_of_one_row_independent(oracle_mod):
+    check_steps_independent()
 
 
 def test_greedy_lowest_index_ties(oracle_mod):
@@ -437,6 +511,9 @@ MUTANT_CHECKS = {
     "TOPP_NO_RENORM": [check_filters_bruteforce],
     "SCORE_MUL": [lambda mutant: check_draw_distribution(mutant, n_draws=200_000)],
     "IGNORE_ALL": [check_prompt_ignore_cases],
+    "PAIR_OVERLAP": [check_pair_fields_independent],
+    "ROW_IGNORED": [check_rows_independent],
+    "STEP_IS_ROW": [check_rows_independent, check_steps_independent],
 }
 
 
