@@ -213,6 +213,18 @@ __device__ __forceinline__ float penalize(float x, int count, const RowParams& P
   return z;
 }
 
+// min-p test z_t - m >= ln(min_p) [TensorRT-LLM "Sampling", min-p], decided
+// exactly in double; fp32 decides whenever it is far from the threshold.
+// Monotone in zt.
+__device__ __forceinline__ bool minp_pass(float zt, float m_t, double lmp) {
+  const float d = __fsub_rn(zt, m_t);
+  const float l = (float)lmp;
+  const float margin = 1e-4f * (1.0f + fabsf(l));
+  if (d > l + margin) return true;
+  if (d < l - margin) return false;
+  return (double)zt - (double)m_t >= lmp;
+}
+
 // ---- order-preserving keys -------------------------------------------------
 // Monotone map of a non-NaN float to uint32 (-0 and +0 map together).
 __device__ __forceinline__ uint32_t ord_key(float f) {
@@ -231,20 +243,37 @@ __device__ __forceinline__ uint64_t elem_key(float zt, uint32_t idx) {
 __device__ __forceinline__ float key_z(uint64_t k) { return key_value((uint32_t)(k >> 32)); }
 __device__ __forceinline__ uint32_t key_idx(uint64_t k) { return ~(uint32_t)k; }
 
-// Mass of an element relative to the row max, in 2^-40 fixed point (exact,
-// order-independent sums).  Explicitly rounded operations: the same element
-// must get the same mass in every pass, whatever the compiler fuses.  The
-// value floor(w 2^40), w in [0, 1], comes from two 32-bit conversions (one
-// 64-bit conversion runs at a small fraction of their rate): a = w 2^8 is
-// exact, so are its integer part hi and its fraction a - hi, and the
-// fraction times 2^32 is an exact value below 2^32.
+// Mass of an element relative to the row max, w = exp(zt - m_t) in [0, 1], in
+// 2^-43 fixed point (exact, order-independent sums of up to 2^20 elements).
+// The top-p decision compares prefix sums of these masses, so their error is
+// bounded, not just small:
+//   * the difference zt - m_t is kept exactly as d + lo (Knuth's TwoSum), and
+//     w = e^d (1 + lo), whose first-order remainder lo^2 / 2 is below 2^-48 d^2;
+//   * e^d is CUDA's expf, within 2 ulp (the CUDA Math API's stated maximum
+//     error), and the FMA rounds once more: |w / exp(zt - m_t) - 1| < 3.1e-7;
+//   * the fixed point truncates each mass by less than 2^-43.
+// A prefix ratio P / W (W >= 1: the row maximum has mass 1) over N <= 2^20
+// elements is then within 2 * 3.1e-7 + N 2^-43 < 7.4e-7 of the exact ratio,
+// inside the 1e-6 window in which a top-p decision counts as a tie.
+// Explicitly rounded operations: the same element gets the same mass in every
+// pass.  floor(w 2^43) comes from two 32-bit conversions (one 64-bit conversion
+// runs at a small fraction of their rate): a = w 2^11 is exact, so are its
+// integer part hi and the fraction a - hi, and the fraction times 2^32 is an
+// exact integer below 2^32.
 __device__ __forceinline__ unsigned long long mass_fixed(float zt, float m_t) {
-  const float w = ex2_approx(__fmul_rn(__fsub_rn(zt, m_t), kLog2e));
-  const float a = __fmul_rn(w, 256.0f);
+  const float d = __fsub_rn(zt, m_t);
+  const float e = expf(d);
+  if (!(e > 0.0f)) return 0ull;  // -inf, or below the fixed point's range
+  const float bb = __fsub_rn(d, zt);
+  const float aa = __fsub_rn(d, bb);
+  const float lo = __fadd_rn(__fsub_rn(zt, aa), __fsub_rn(-m_t, bb));
+  const float w = fminf(__fmaf_rn(e, lo, e), 1.0f);
+  const float a = __fmul_rn(w, 2048.0f);
   const unsigned int hi = __float2uint_rz(a);
-  const unsigned int lo = __float2uint_rz(__fmul_rn(__fsub_rn(a, __uint2float_rn(hi)), 0x1p32f));
-  return ((unsigned long long)hi << 32) | lo;
+  const unsigned int fr = __float2uint_rz(__fmul_rn(__fsub_rn(a, __uint2float_rn(hi)), 0x1p32f));
+  return ((unsigned long long)hi << 32) | fr;
 }
+constexpr double kMassScale = 8796093022208.0;  // 2^43, the scale of mass_fixed
 
 // ---- warp reductions -------------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {

@@ -124,6 +124,59 @@ cudaError_t launch_build_counts(const int32_t* raw, const int64_t* offs, int max
 cudaError_t launch_append(int2* hist, int32_t* hist_len, int32_t hist_cap, const int32_t* tokens,
                           int32_t* row_status, int B, cudaStream_t stream);
 
+// ---- the persistent row kernel (vt_rows.cu) ----------------------------------
+// bf16 rows without penalties: persistent thread-block clusters, each looping
+// over rows with every CTA's slice of the row resident in shared memory
+// (double-buffered: the next row's slice is copied in while this one is
+// processed).  Rows it cannot settle exactly are handed to the selection
+// kernel through the SlowRow records, as the streaming kernel does.
+struct RowArgs {
+  const void* logits;        // [rows][ld] bf16
+  int64_t ld;
+  int32_t B, V;
+  const int32_t* order;      // [norder] rows in processing order; rows >= B are skipped
+  int32_t norder;
+  int32_t n_logprobs;
+  int32_t slice;             // elements per CTA (a multiple of 8)
+  int32_t aligned;           // rows 16-byte aligned: slices arrive by bulk copy
+  uint32_t buf_bytes;        // bytes of one slice buffer (a multiple of 128)
+  const RowParams* params;   // [B]
+  uint64_t* seeds;           // [B], advanced by the kernel
+  DecayState* decay;         // [B]
+  int32_t* out_tokens;
+  float* out_logprobs;       // may be null
+  int32_t* out_topk_ids;     // [B][n]
+  float* out_topk_logprobs;
+  int32_t* row_status;
+  float* dbg_kth_value;
+  int32_t* dbg_kth_index;
+  int32_t* dbg_kept;
+  int32_t* err_word;
+  SlowRow* slow;             // hand-over records and list, as in SampleArgs
+  int32_t* slow_list;
+  uint32_t* slow_ctl;
+  unsigned long long* trace; // optional [B][cluster][kTraceSlots] phase stamps (ns)
+};
+
+struct RowPlan {
+  int cluster;        // CTAs per row (0: the row kernel does not take this call)
+  int slice;          // elements per CTA
+  uint32_t buf_bytes; // one slice buffer
+  size_t smem;        // dynamic shared memory per CTA
+  int clusters;       // persistent clusters launched (resident at once)
+};
+
+// Plan the row kernel for B rows of V bf16 elements: the cluster size whose
+// double-buffered slices fit one CTA per SM; cluster = 0 when V is too large.
+RowPlan plan_rows(int B, int V);
+
+// Launch the row kernel (grid: plan.clusters clusters of plan.cluster CTAs).
+cudaError_t launch_rows(const RowArgs& args, const RowPlan& plan, cudaStream_t stream);
+
+// The selection kernel alone over the rows the row kernel handed over.
+cudaError_t launch_select_handed(const SampleArgs& args, const LaunchPlan& plan, int dtype,
+                                 cudaStream_t stream);
+
 // ---- the filtered distribution on request (vt_probs.cu) ---------------------
 constexpr int kProbsMaxRange = 65536;  // elements per CTA at most
 constexpr int kProbsMaxSplits = 64;    // CTAs per row at most (unless V needs more)

@@ -674,16 +674,6 @@ __device__ void block_top_desc(const uint64_t* keys, int N, int q, uint64_t* out
   __syncthreads();
 }
 
-// min-p test z_t - m >= ln(min_p), decided exactly in double; fp32 decides
-// whenever it is far from the threshold.
-__device__ __forceinline__ bool minp_pass(float zt, float m_t, double lmp) {
-  const float d = __fsub_rn(zt, m_t);
-  const float l = (float)lmp;
-  const float margin = 1e-4f * (1.0f + fabsf(l));
-  if (d > l + margin) return true;
-  if (d < l - margin) return false;
-  return (double)zt - (double)m_t >= lmp;
-}
 
 // ---------------------------------------------------------------------------
 // cluster-wide radix selection on (value, index) keys
@@ -700,7 +690,7 @@ enum Pred { kPredAll = 0, kPredSurv = 1 };
 // catches everything from 16 down), which spreads any row's mass over many
 // bins; deeper levels split the surviving bin's 64-bit key range 1024 ways.
 // A band of at most kBufCap keys is then gathered, sorted and walked.  Bin
-// masses are exact sums of the elements' 2^-40 fixed-point masses, kept as
+// masses are exact sums of the elements' 2^-43 fixed-point masses, kept as
 // three 32-bit partial sums per bin so that every update is a 32-bit shared
 // atomic (slices of at most 65536 elements cannot overflow them).
 //
@@ -1254,8 +1244,7 @@ __device__ void append_token(int2* tab, int32_t* len_p, int cap, int tok, Smem& 
 
 // Kept-set processing on the sorted candidates in the leader's buffer.
 // Returns L3 (kept count); writes the drawn token and its tempered logit.
-__device__ int leader_draw(Ctx& c, Smem& s, int N, bool L2_inside, double S_fixed, int* tok,
-                           float* ztok) {
+__device__ int leader_draw(Ctx& c, Smem& s, int N, int* tok, float* ztok) {
   int pass = 0;
   if (c.minp)
     for (int i = c.tid; i < N; i += kThreads) pass += minp_pass(key_z(c.buf[i]), c.m_t, c.lmp);
@@ -1269,8 +1258,7 @@ __device__ int leader_draw(Ctx& c, Smem& s, int N, bool L2_inside, double S_fixe
     for (int i = i0; i < i1; ++i) lm += mass_fixed(key_z(c.buf[i]), c.m_t);
     unsigned long long tot;
     const unsigned long long ex = block_exclusive_u64(lm, s, &tot);
-    const unsigned long long W2 = L2_inside ? tot : (unsigned long long)S_fixed;
-    const unsigned long long Tm = (unsigned long long)((double)W2 * (double)c.top_p);
+    const unsigned long long Tm = (unsigned long long)((double)tot * (double)c.top_p);
     int kept = 0;
     unsigned long long run = ex;
     for (int i = i0; i < i1; ++i) {
@@ -1958,10 +1946,10 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   const int nc = s.rs.nc;
   const bool cand_ok = K_need > 0 ? (nc <= kBufCap && !s.rs.overflow) : true;
   const bool topn_ok = n == 0 || (cand_ok && nc >= n);
-  const double S_fixed = (double)s.rs.S * 1099511627776.0;  // 2^40
   // The kept prefix is known from the candidates when every min-p survivor is
-  // a candidate, or when top-k ends inside them; a top-p-only row also stays
-  // on the candidates when they already hold more than p of the row's mass.
+  // a candidate, or when top-k ends inside them.  A top-p row needs the exact
+  // mass of the survivors it renormalises over, so it stays on the candidates
+  // only when they hold every survivor of min-p and top-k.
   const bool surv_inside = complete || (c.minp && s.rs.nc_minp < nc);
   const bool L2_inside = surv_inside || (c.topk && !topk_beyond && c.top_k <= nc);
   bool fast;
@@ -1970,10 +1958,6 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
   } else {
     if (!c.topk && !c.topp && !c.minp)
       fast = complete && cand_ok;
-    else if (c.topp)
-      fast = cand_ok && (L2_inside || (!c.minp && !c.topk &&
-                                       (double)s.rs.cand_mass >
-                                           (double)c.top_p * S_fixed * (1.0 + 1e-5)));
     else
       fast = cand_ok && L2_inside;
     fast = fast && topn_ok && K_need > 0;
@@ -2006,7 +1990,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const SampleArgs a)
         out_ids[t] = (int)key_idx(k);
         out_lps[t] = (key_z(k) - c.m_t) - c.lnS;
       }
-      L3 = leader_draw(c, s, N, L2_inside, S_fixed, &tok, &ztok);
+      L3 = leader_draw(c, s, N, &tok, &ztok);
       kk = c.buf[L3 - 1];
     } else {
       // no order beyond the top-n: the kept boundary is a selection
@@ -3498,6 +3482,22 @@ cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dt
                           cudaStream_t stream, cudaEvent_t between) {
   return dtype == 0 ? launch_one<float>(args, plan, stream, between)
                     : launch_one<uint16_t>(args, plan, stream, between);
+}
+
+cudaError_t launch_select_handed(const SampleArgs& args, const LaunchPlan& plan, int dtype,
+                                 cudaStream_t stream) {
+  if (plan.sel.clusters < 1) return cudaErrorInvalidConfiguration;
+  cudaLaunchAttribute attr[1];
+  if (dtype == 0) {
+    cudaLaunchConfig_t cfg = select_config<float>(plan.sel, attr);
+    cfg.gridDim = dim3((unsigned)(plan.sel.clusters * plan.sel.cluster), 1, 1);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, select_kernel<float>, args, plan.sel);
+  }
+  cudaLaunchConfig_t cfg = select_config<uint16_t>(plan.sel, attr);
+  cfg.gridDim = dim3((unsigned)(plan.sel.clusters * plan.sel.cluster), 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, select_kernel<uint16_t>, args, plan.sel);
 }
 
 cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, int dtype,

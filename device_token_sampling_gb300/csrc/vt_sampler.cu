@@ -45,6 +45,7 @@ struct vt_sampler {
   int32_t* d_slow_list = nullptr;  // [2][max_batch]: one list per launch pair
   uint32_t* d_slow_ctl = nullptr;  // [2][4]
   int32_t* d_rows = nullptr;       // [max_batch]: main rows, then side rows
+  int32_t* d_order = nullptr;      // [max_batch]: rows in the row kernel's order
   float2* d_probs_part = nullptr;  // (max, exp-sum) partials of the filtered distribution
   size_t probs_part_cap = 0;
   // the side stream: rows routed straight to the selection kernel run there,
@@ -55,6 +56,9 @@ struct vt_sampler {
   bool launch_order = true;           // main rows wait for ev_launched (while it works)
   int n_main = 0, n_side = 0;
   int last_launches = 0;  // kernels the last vt_sample launched
+  int last_pairs = 1;     // hand-over lists the last vt_sample used
+  int path = 1;           // 0: the row kernel where it applies; 1: always the streaming kernel
+  std::map<std::pair<int, int>, vt::RowPlan> row_plans;
   // pinned host staging
   vt::RowParams* h_params = nullptr;
   uint64_t* h_seeds = nullptr;
@@ -63,6 +67,7 @@ struct vt_sampler {
   int64_t* h_raw_offs = nullptr;
   int32_t* h_err = nullptr;
   int32_t* h_rows = nullptr;
+  int32_t* h_order = nullptr;
   cudaEvent_t ev_params = nullptr, ev_counts = nullptr;
   bool params_pending = false, counts_pending = false;
   // staging for vt_sample_host
@@ -144,8 +149,10 @@ void free_all(vt_sampler* h) {
   dfree(h->d_slow_list);
   dfree(h->d_slow_ctl);
   dfree(h->d_rows);
+  dfree(h->d_order);
   dfree(h->d_probs_part);
   if (h->h_rows) cudaFreeHost(h->h_rows);
+  if (h->h_order) cudaFreeHost(h->h_order);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_launched) cudaEventDestroy(h->ev_launched);
@@ -238,6 +245,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_slow_list, 2 * B * sizeof(int32_t));
   dal((void**)&h->d_slow_ctl, 8 * sizeof(uint32_t));
   dal((void**)&h->d_rows, B * sizeof(int32_t));
+  dal((void**)&h->d_order, B * sizeof(int32_t));
   // B rows of ceil(V / max range) + 1 splits, plus the splits that small
   // batches add to fill the GPU (plan_probs never asks for more)
   h->probs_part_cap = B * (size_t)((cfg->max_vocab + vt::kProbsMaxRange - 1) /
@@ -245,6 +253,7 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
                       (size_t)vt::kProbsCtasPerSm * h->num_sms;
   dal((void**)&h->d_probs_part, h->probs_part_cap * sizeof(float2));
   hal((void**)&h->h_rows, B * sizeof(int32_t));
+  hal((void**)&h->h_order, B * sizeof(int32_t));
   hal((void**)&h->h_params, B * sizeof(vt::RowParams));
   hal((void**)&h->h_seeds, B * sizeof(uint64_t));
   hal((void**)&h->h_decay, B * sizeof(vt::DecayState));
@@ -394,6 +403,22 @@ int vt_reset_params_ex(vt_sampler* h, int32_t B, const float* temperature, const
   std::stable_sort(h->h_rows, h->h_rows + nm, [&](int x, int y) { return weight(x) > weight(y); });
   h->n_main = nm;
   h->n_side = ns;
+  // The row kernel's order: its clusters take rows round-robin from this
+  // list, so the costliest rows go first -- top-p rows whose kept set can
+  // reach far (every element counted and many drawn), then rows that draw
+  // over many elements (large top-k, min-p alone, no filter), then top-k rows
+  // by k, greedy rows last.
+  auto cost = [&](int r) -> long long {
+    const uint32_t f = h->row_flags[r];
+    if (f & vt::kRowGreedy) return 0;
+    const int k = top_k[r];
+    const bool kcut = k > 1;
+    if ((f & (vt::kRowTopP | vt::kRowDecay)) && !kcut) return 3LL << 40;
+    if (!kcut || k > 2048) return 2LL << 40;
+    return (1LL << 40) + k;
+  };
+  for (int r = 0; r < B; ++r) h->h_order[r] = r;
+  std::stable_sort(h->h_order, h->h_order + B, [&](int x, int y) { return cost(x) > cost(y); });
   VT_CK(h, cudaMemcpyAsync(h->d_params, h->h_params, (size_t)B * sizeof(vt::RowParams),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_seeds, h->h_seeds, (size_t)B * sizeof(uint64_t),
@@ -401,6 +426,8 @@ int vt_reset_params_ex(vt_sampler* h, int32_t B, const float* temperature, const
   VT_CK(h, cudaMemcpyAsync(h->d_decay, h->h_decay, (size_t)B * sizeof(vt::DecayState),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_rows, h->h_rows, (size_t)B * sizeof(int32_t),
+                           cudaMemcpyHostToDevice, st));
+  VT_CK(h, cudaMemcpyAsync(h->d_order, h->h_order, (size_t)B * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaEventRecord(h->ev_params, st));
   h->params_pending = true;
@@ -572,9 +599,66 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     a.trace_ctas = a.trace ? h->trace_ctas : 0;
     return a;
   };
-  // bf16 calls over every row split the rows between the two streams
-  const bool split = dtype == VT_DTYPE_BF16 && B == h->params_B && h->n_side > 0 && h->n_main > 0;
-  if (!split) {
+  // bf16 rows without penalties: the persistent row kernel, then the selection
+  // kernel for the rows it hands over (counts appended by a third launch)
+  const vt::RowPlan* rplan = nullptr;
+  if (dtype == VT_DTYPE_BF16 && !any_pen && h->path == 0) {
+    auto key = std::make_pair(B, V);
+    auto it = h->row_plans.find(key);
+    if (it == h->row_plans.end()) it = h->row_plans.emplace(key, vt::plan_rows(B, V)).first;
+    if (it->second.cluster > 0) rplan = &it->second;
+  }
+  // other bf16 calls over every row split the rows between the two streams
+  const bool split = !rplan && dtype == VT_DTYPE_BF16 && B == h->params_B && h->n_side > 0 &&
+                     h->n_main > 0;
+  h->last_pairs = split ? 2 : 1;
+  if (rplan) {
+    const vt::LaunchPlan* plan = nullptr;
+    const int rc = get_plan(B, &plan);
+    if (rc != VT_OK) return rc;
+    vt::SampleArgs sa = make_args(*plan, B, nullptr, 0, 0);
+    sa.update_counts = 0;
+    sa.trace = nullptr;
+    sa.trace_ctas = 0;
+    vt::RowArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    ra.logits = logits;
+    ra.ld = ld;
+    ra.B = B;
+    ra.V = V;
+    ra.order = h->d_order;
+    ra.norder = h->params_B;
+    ra.n_logprobs = n;
+    ra.slice = rplan->slice;
+    ra.aligned = sa.aligned;
+    ra.buf_bytes = rplan->buf_bytes;
+    ra.params = h->d_params;
+    ra.seeds = h->d_seeds;
+    ra.decay = h->d_decay;
+    ra.out_tokens = out_tokens;
+    ra.out_logprobs = out_logprobs;
+    ra.out_topk_ids = out_topk_ids;
+    ra.out_topk_logprobs = out_topk_logprobs;
+    ra.row_status = h->d_status;
+    ra.dbg_kth_value = h->d_kth_v;
+    ra.dbg_kth_index = h->d_kth_i;
+    ra.dbg_kept = h->d_kept;
+    ra.err_word = h->d_err;
+    ra.slow = h->d_slow;
+    ra.slow_list = sa.slow_list;
+    ra.slow_ctl = sa.slow_ctl;
+    // the phase trace is laid out by row (B rows of rplan->cluster CTAs)
+    ra.trace = (h->trace && (int64_t)B * rplan->cluster <= h->trace_ctas) ? h->trace : nullptr;
+    VT_CK(h, vt::launch_rows(ra, *rplan, st));
+    if (h->phase_event) VT_CK(h, cudaEventRecord(h->phase_event, st));
+    VT_CK(h, vt::launch_select_handed(sa, *plan, dtype, st));
+    h->last_launches = 2;
+    if (update_counts && !out_probs) {
+      VT_CK(h, vt::launch_append(h->d_hist, h->d_hist_len, sa.hist_cap, out_tokens, h->d_status,
+                                 B, st));
+      h->last_launches += 1;
+    }
+  } else if (!split) {
     const vt::LaunchPlan* plan = nullptr;
     const int rc = get_plan(B, &plan);
     if (rc != VT_OK) return rc;
@@ -794,7 +878,26 @@ int vt_debug_last_handover(vt_sampler* h, int32_t* rows) {
   VT_CK(h, cudaStreamSynchronize(h->last_stream));
   uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   VT_CK(h, cudaMemcpy(v, h->d_slow_ctl, sizeof v, cudaMemcpyDeviceToHost));
-  *rows = (int32_t)(v[2] + v[6]);
+  *rows = (int32_t)(v[2] + (h->last_pairs > 1 ? v[6] : 0u));
+  return VT_OK;
+}
+
+int vt_debug_row_plan(vt_sampler* h, int32_t B, int32_t V, int32_t* cluster,
+                      int32_t* clusters, int32_t* slice, int64_t* smem_bytes) {
+  if (!h || !cluster || !clusters || !slice || !smem_bytes || B < 1 || V < 1)
+    return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  const vt::RowPlan p = vt::plan_rows(B, V);
+  *cluster = p.cluster;
+  *clusters = p.clusters;
+  *slice = p.slice;
+  *smem_bytes = (int64_t)p.smem;
+  return VT_OK;
+}
+
+int vt_debug_set_path(vt_sampler* h, int32_t path) {
+  if (!h || path < 0 || path > 1) return VT_ERR_INVALID_ARG;
+  h->path = path;
   return VT_OK;
 }
 

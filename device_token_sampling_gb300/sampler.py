@@ -76,6 +76,8 @@ SIGNATURES = {
     "vt_debug_set_phase_event": (C.c_int, [P, P]),
     "vt_debug_last_handover": (C.c_int, [P, P]),
     "vt_debug_last_launches": (C.c_int, [P, P]),
+    "vt_debug_set_path": (C.c_int, [P, I32]),
+    "vt_debug_row_plan": (C.c_int, [P, I32, I32, P, P, P, P]),
     "vt_sample_noalloc": (C.c_int, [I32, P, I32, I32, I32, I64, P, P, P, P, P, I32, P, P, P, P,
                                     P, I32, P, C.c_char_p, I32]),
     "vt_last_error": (C.c_char_p, [P]),
@@ -358,6 +360,19 @@ class Sampler:
         v = C.c_int32()
         self._check(self._lib.vt_debug_last_handover(self._h, C.byref(v)), "vt_debug_last_handover")
         return int(v.value)
+
+    def row_plan(self, B: int, V: int):
+        """The row kernel's plan for B rows of V bf16 logits: (CTAs per row,
+        resident clusters, elements per CTA, dynamic shared memory bytes)."""
+        c, n, sl, sm = C.c_int32(), C.c_int32(), C.c_int32(), C.c_int64()
+        self._check(self._lib.vt_debug_row_plan(self._h, B, V, C.byref(c), C.byref(n),
+                                                C.byref(sl), C.byref(sm)), "vt_debug_row_plan")
+        return int(c.value), int(n.value), int(sl.value), int(sm.value)
+
+    def set_path(self, path: int):
+        """0: the row kernel for bf16 calls without penalties; 1 (the default):
+        the streaming kernel for every call."""
+        self._check(self._lib.vt_debug_set_path(self._h, int(path)), "vt_debug_set_path")
 
     def last_launches(self) -> int:
         """Kernels the last ``sample`` launched (2, or 3 when its rows were split

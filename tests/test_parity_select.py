@@ -33,16 +33,22 @@ def _built():
 
 
 def check(w, expect_handover=True):
-    s = make_sampler(w)
-    try:
-        g = run_gpu(s, w)
-        if expect_handover:
-            assert s.last_handover() > 0, "no row reached the selection kernel"
-        o = O.sample_workload(w, want_zt=True)
-        compare(g, o, where=w.name)
-        return g, o
-    finally:
-        s.close()
+    """Both sampling paths against the oracle: the streaming kernel (which must
+    hand rows to the selection kernel here) and, for bf16 rows without
+    penalties, the row kernel (which settles most rows itself)."""
+    o = O.sample_workload(w, want_zt=True)
+    g = None
+    for path in (1, 0):
+        s = make_sampler(w)
+        try:
+            s.set_path(path)
+            g = run_gpu(s, w)
+            if expect_handover and path == 1:
+                assert s.last_handover() > 0, "no row reached the selection kernel"
+            compare(g, o, where=f"{w.name} path {path}")
+        finally:
+            s.close()
+    return g, o
 
 
 def bulk(rng, B, V, sigma=1.5):
@@ -153,6 +159,7 @@ def test_repeat_calls_reuse_handover_state():
     w = custom_workload(x, dtype=W.DTYPE_BF16, T=1.5, p=0.95, n=5, name="repeat")
     s = make_sampler(w)
     try:
+        s.set_path(1)
         xd = device_logits(w)
         first = run_gpu(s, w, x=xd)
         for _ in range(2):
