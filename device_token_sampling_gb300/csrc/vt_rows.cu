@@ -1,65 +1,64 @@
-// vt_rows.cu -- the persistent row kernel: bf16 rows without penalties.
+// vt_rows.cu -- the row kernels: bf16 rows without penalties.
 //
 // The per-step decode sampler of the pages (TensorRT-LLM "Sampling": the
 // temperature, min-p, top-k and top-p formulas; vllm.cpp pull request "the
 // Gumbel draw that scanned 248,320 tokens on one thread": the seeded Gumbel
 // draw over true global indices, lowest index on ties; Tenstorrent sampling
 // README: log-softmax log-probs, one seed advance per sampled token), laid out
-// for sm_103a so that HBM streams each logit once while every later pass reads
-// shared memory:
+// for sm_103a as independent CTAs that never wait for one another:
 //
-//   * persistent thread-block clusters of C CTAs loop over the rows (heaviest
-//     first, in a host-made order); CTA r of a cluster owns elements
-//     [r * slice, (r + 1) * slice) of each of its rows;
-//   * each CTA holds its slice of the current row in one shared-memory
-//     buffer while one bulk copy fills the other with the slice of the
-//     cluster's next row (double buffering, one mbarrier per buffer);
-//   * pass A (statistics): row maximum, sum of exponentials, lowest-index
-//     argmax, and four group maxima per thread;
-//   * pass H (counts): bf16 codes are exact bins -- every element with one
-//     bf16 pattern has the same tempered value and the same mass -- so a count
-//     per code slot below the CTA's own maximum settles min-p, top-k, top-p
-//     and the top-n exactly.  Rows whose kept set is small count only the
-//     elements above a local lower bound of their k-th (n-th) largest value,
-//     taken from the group maxima; top-p rows count every element;
-//   * barrier 1; the leader CTA merges the C histograms (each shifted by the
-//     distance of its CTA's maximum below the row's) and walks the slots:
-//     top-n boundary, min-p survivors, top-k boundary, top-p over the top-k
-//     survivors renormalised, with masses summed in exact fixed point;
-//   * barrier 2; pass D draws over the kept elements (Gumbel scores, with a
-//     cheap certificate that skips elements that cannot win) and sends the
-//     top-n to the leader; the kept elements of the boundary slot are the
-//     lowest-indexed ones, selected per CTA;
-//   * barrier 3; the leader writes the row's outputs.
-// Rows whose boundary falls where one slot holds several values (the slot of
-// magnitudes below 2^-12, or the catch-all below the slot window) are handed
-// to the selection kernel with their statistics, exactly as the streaming
-// kernel hands rows over.
+//   pass kernel, one CTA per (row, slice of at most 76 KB):
+//     * the slice arrives in shared memory by one bulk copy (mbarrier);
+//     * pass A: the slice maximum (packed bf16 maxima per 16-byte vector,
+//       kept per vector so later passes skip whole vectors), then the sum of
+//       exponentials against it, the lowest-index argmax, and 8 group maxima
+//       per thread;
+//     * bf16 codes are exact bins: every element with one bf16 pattern has one
+//       tempered value and one mass.  Rows whose kept set lies inside a small
+//       top-k (and greedy rows' top-n) write the records of their elements
+//       above a local lower bound of the k-th (n-th) largest value, taken from
+//       the group maxima; rows whose kept set may reach far (top-p or min-p
+//       without such a top-k) write a count per code slot below the slice
+//       maximum; rows without a filter draw over every element;
+//     * the partial results go to global memory, and the last CTA of the row
+//       to arrive (one atomic per row) completes it: it merges the counts
+//       (each CTA's slots shifted by its maximum's distance below the row's)
+//       and walks them -- top-n boundary, min-p survivors, top-k boundary,
+//       top-p over the top-k survivors renormalised, with masses summed in
+//       exact fixed point -- then draws over the kept records and writes the
+//       row, or leaves the walk for the draw kernel;
+//   draw kernel, for the rows whose kept set needs every element: one CTA per
+//     (row, slice) reads the slice again and scores its kept elements (a cheap
+//     integer prefilter, then a certificate, skip nearly all of them); the
+//     row's last CTA writes the token.
+// Rows whose boundary falls where one slot holds several values (magnitudes
+// below 2^-12, or the catch-all below the slot window), or whose records
+// overflow, are handed to the selection kernel with their statistics.
 #include "vt_device.cuh"
 #include "vt_kernels.h"
 
 #include <climits>
 
-namespace cg = cooperative_groups;
-
 namespace vt {
 namespace {
 
-constexpr int kRT = 512;                 // threads per CTA of the row kernel
+constexpr int kRT = 256;                 // threads per CTA of the row kernels
 constexpr int kRW = kRT / 32;            // warps
-constexpr int kSl = 4096;                // code slots of the count histogram
+constexpr int kSl = kRowSlots;           // code slots of the count histogram
 constexpr int kSlCatch = kSl - 1;        // the last slot: everything below the window
 constexpr int kSlPT = kSl / kRT;         // slots per thread in the walk
 constexpr int kTinyE = 115;              // bf16 exponent field of 2^-12
-constexpr int kGrp = 4;                  // group maxima per thread (thresholds)
+constexpr int kGrp = 8;                  // group maxima per thread (thresholds)
+constexpr int kPCap = 1024;              // top-k up to this: the records settle the row
 constexpr int kListCap = 2048;           // boundary-slot indices one CTA can rank
-constexpr int kGatherCap = 64;           // top-n keys the leader gathers
-constexpr int kRMaxC = 16;               // CTAs per cluster at most
+constexpr int kSliceMax = 38912;         // elements per CTA at most (76 KB)
+constexpr int kFinishRecCap = 5120;      // records the finish kernel holds (40 KB)
 constexpr int kAllKept = -1;             // beta: every finite element is kept
 constexpr int kNoKept = -2;              // beta: greedy row, no draw
-constexpr int kThrAll = INT_MIN;         // histogram threshold: every finite element
-constexpr int kThrNone = INT_MAX;        // no histogram
+constexpr int kThrAll = INT_MIN;         // threshold: every finite element
+constexpr int kThrNone = INT_MAX;        // nothing written
 static_assert(kSl % kRT == 0, "slots split evenly over the threads");
+enum : int { kModeStats = 0, kModeRecords = 1, kModeCounts = 2, kModeAll = 3 };
 
 // Signed code of a bf16 pattern, monotone in the value: magnitudes below
 // 2^-12 and both zeros share code 0, every other value has a code of its own.
@@ -95,60 +94,44 @@ __device__ __forceinline__ uint32_t bits8(const uint4& q, int i) {
   return (i & 1) ? (w >> 16) : (w & 0xFFFFu);
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+// Records of candidate elements: code + 32768 in bits 52..36, 0xFFFFF - j in
+// bits 35..16 and the bf16 pattern in bits 15..0, so that descending records
+// are in the order (value descending, index ascending) wherever codes are
+// single values, and the value is recovered exactly.
+__device__ __forceinline__ uint64_t rec_make(int code, int j, uint32_t bits) {
+  return ((uint64_t)(uint32_t)(code + 32768) << 36) | ((uint64_t)(0xFFFFFu - (uint32_t)j) << 16) |
+         (uint64_t)bits;
 }
+__device__ __forceinline__ int rec_code(uint64_t r) { return (int)(r >> 36) - 32768; }
+__device__ __forceinline__ int rec_j(uint64_t r) { return (int)(0xFFFFFu - ((uint32_t)(r >> 16) & 0xFFFFFu)); }
+__device__ __forceinline__ float rec_x(uint64_t r) { return __uint_as_float(((uint32_t)r & 0xFFFFu) << 16); }
 
-// What a CTA publishes for the row (read by the others over DSMEM).
-struct __align__(16) RPart {
-  float xmax;              // CTA maximum before temperature (-inf: none)
-  float s;                 // sum of exp(z_t - fl(xmax / T)) over the slice
-  int arg;                 // lowest index of xmax (INT_MAX: none)
-  int bad;                 // a NaN or +inf
-  int cmax;                // code of xmax
-  int thr;                 // the histogram counted finite elements with code >= thr
-  unsigned int catch_cnt;  // counted elements below the CTA's slot window
-  int err;
-  // after the draw pass
-  float best_s, best_z;    // best Gumbel score and its tempered value
-  int best_j;
-  int kth_j;               // the row's last kept index when this CTA holds it (-1)
-  unsigned long long last_key;  // rows keeping everything: the order's last element here
-  int fin;                 // rows keeping everything: finite elements here
-  int pad0;
-};
-
-// The leader's walk, read by every CTA after barrier 2.
+// The leader's walk over the merged slots, and what it found.
 struct __align__(16) RRes {
-  int action;              // 0: draw and gather; 1: handed to the selection kernel
+  int action;              // 0: settled; 1: hand the row over
   int beta;                // kept boundary slot, kAllKept or kNoKept
+  int qk;                  // kept elements of slot beta
   int sn;                  // top-n boundary slot (-1: no top-n)
+  int cn;                  // top-n elements of slot sn
   int L3;                  // kept count
-  float kth_z;             // tempered value of the last kept element (slot rows)
-  int last_rank;           // CTA holding the last kept element of slot beta
-  int cb[kRMaxC];          // kept elements of slot beta per CTA
-  int nb[kRMaxC];          // elements of slot beta per CTA
-  int cn[kRMaxC];          // top-n elements of slot sn per CTA
-  int nn[kRMaxC];          // elements of slot sn per CTA
+  float kth_z;             // tempered value of slot beta
+  int pad;
 };
 
 struct __align__(16) RSmem {
-  uint64_t full[2];        // bulk-copy completion, one per slice buffer
-  RPart part[2];           // by row parity
-  RRes res;                // leader: this row's walk
-  RRes rl;                 // every CTA: the leader's walk
-  uint64_t gather[kGatherCap];  // leader: top-n keys
-  int gcount;
-  int nlist, nlistn;       // boundary-slot indices listed by this CTA
-  int flag;
+  uint64_t full;           // bulk-copy completion
+  RRes res;
+  int flag, last, nrec, nlist, nlistn;
   unsigned int h256[256];  // threshold histogram
   float rf[4 * kRW];
   int ri[4 * kRW];
   unsigned long long ru[4 * kRW + 2];
   int bi[16];
   float bf[8];
-  unsigned long long bu[8];
-  int delta[kRMaxC];       // row slot = CTA r's slot + delta[r]
+  unsigned long long top[32];  // the row's top-n records
+  int ntop;
+  int delta[kRowMaxC];     // finisher: row slot = CTA r's slot + delta[r]
 };
 
 // ---------------------------------------------------------------------------
@@ -333,82 +316,137 @@ __device__ uint32_t rblock_kth_smallest(const uint32_t* list, int n, int c, uint
 // ---------------------------------------------------------------------------
 // pass A: statistics of the slice (shared memory)
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 struct Stats {
-  float rm, rmt, rs;   // thread maximum, its tempered value, sum of exp(z_t - rmt)
-  int j;               // lowest index of rm among this thread's elements (INT_MAX: none)
-  bool bad;            // a NaN seen (a +inf shows as rm)
-  float gm[kGrp];      // maxima of the thread's vectors k = 0, 1, 2, 3 (mod 4)
+  float M;            // the slice maximum (every thread)
+  float S;            // sum of exp(z_t - fl(M / T)) over the slice (every thread)
+  int arg;            // lowest index of M (every thread; INT_MAX: none)
+  bool bad;           // a NaN or +inf (every thread)
+  float gm[kGrp];     // this thread's group maxima (vectors tid + k kRT, k = g mod kGrp)
 };
 
-// One pass over the thread's 16-byte vectors v = tid + k * kRT: the running
-// maximum rm with the sum rs of exp(z_t - fl(rm / T)), rescaled when rm grows;
-// the first vector holding rm; a NaN flag; and each vector's maximum into
-// vmax[v] (bf16 bits), which lets the later passes skip whole vectors.  Each
-// term is 2^(z_t log2(e) - fl(rm / T) log2(e)) with the reference product
-// carried exactly as hi + lo: one FFMA (exact product, one rounding) and one
-// add, so the exponent is the tempered difference to within an ulp at any
-// scale.  bf16 tempering fl(x / T) is strictly increasing in x (two bf16
-// values differ by at least 2^-8 relative, far above fp32 rounding), so the
-// maximum and argmax of x are those of z_t.
-__device__ __forceinline__ Stats pass_stats(const uint4* sv, uint16_t* vmax, int nvec, int lo,
-                                            float inv_t) {
+// Two sweeps.  The first takes each 16-byte vector's maximum with packed bf16
+// maxima (kept in vmax[v] as bf16 bits: later passes skip whole vectors), the
+// thread's group maxima and its first vector holding its maximum; the slice
+// maximum M and its lowest index follow.  The second sums
+// 2^(z_t log2(e) - fl(M / T) log2(e)) with the reference product carried
+// exactly as hi + lo: one FFMA (exact product, one rounding) and one add, so
+// every exponent is the tempered difference to within an ulp at any scale.
+// bf16 tempering fl(x / T) is strictly increasing in x (two bf16 values
+// differ by at least 2^-8 relative, far above fp32 rounding), so the maximum
+// and argmax of x are those of z_t.
+__device__ Stats pass_stats(const uint4* sv, uint16_t* vmax, int nvec, int lo, float inv_t,
+                            RSmem& s) {
   Stats o;
-  o.rm = -INFINITY;
-  o.rmt = -INFINITY;
-  o.rs = 0.f;
-  o.j = INT_MAX;
-  o.bad = false;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float rm = -INFINITY;
+  int rv = -1;
 #pragma unroll
   for (int g = 0; g < kGrp; ++g) o.gm[g] = -INFINITY;
-  float nb_hi = 0.f, nb_lo = 0.f;  // -fl(rm / T) log2(e) = nb_hi + nb_lo
-  int rv = -1;
-  for (int v0 = threadIdx.x; v0 < nvec; v0 += kGrp * kRT) {
+  for (int v0 = tid; v0 < nvec; v0 += kGrp * kRT) {
 #pragma unroll
     for (int g = 0; g < kGrp; ++g) {
       const int v = v0 + g * kRT;
       if (v < nvec) {
-        float x[8];
-        unpack8(sv[v], x);
-        const float vm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-                               fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+        const uint4 q = sv[v];
+        const uint32_t m2 = bmax2(bmax2(q.x, q.y), bmax2(q.z, q.w));
+        const float vm = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
         vmax[v] = (uint16_t)(__float_as_uint(vm) >> 16);
         o.gm[g] = fmaxf(o.gm[g], vm);
-        if (vm > o.rm) {
-          const float vmt = __fmul_rn(vm, inv_t);
-          const float nh = __fmul_rn(-vmt, kLog2e);
-          const float nl = __fmaf_rn(-vmt, kLog2e, -nh);
-          o.rs = (o.rm == -INFINITY)
-                     ? 0.f
-                     : o.rs * ex2_approx(__fadd_rn(__fmaf_rn(o.rmt, kLog2e, nh), nl));
-          o.rm = vm;
-          o.rmt = vmt;
-          nb_hi = nh;
-          nb_lo = nl;
+        if (vm > rm) {
+          rm = vm;
           rv = v;
-        }
-        if (o.rm > -INFINITY) {
-          float t[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            t[i] = ex2_approx(__fadd_rn(__fmaf_rn(__fmul_rn(x[i], inv_t), kLog2e, nb_hi), nb_lo));
-          o.rs += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o.bad |= x[i] != x[i];
         }
       }
     }
   }
-  o.bad |= o.rs != o.rs;
-  if (rv >= 0) {
+  // the slice maximum
+  float m = warp_max(rm);
+  if (lane == 0) s.rf[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < kRW ? s.rf[lane] : -INFINITY;
+    t = warp_max(t);
+    if (lane == 0) s.bf[0] = t;
+  }
+  __syncthreads();
+  o.M = s.bf[0];
+  // its lowest index: only threads whose maximum equals it hold one
+  int j = INT_MAX;
+  if (rv >= 0 && rm == o.M) {
+    const uint4 q = sv[rv];
     float x[8];
-    unpack8(sv[rv], x);
-    int first = 7;
+    unpack8(q, x);
 #pragma unroll
     for (int i = 7; i >= 0; --i)
-      if (x[i] == o.rm) first = i;
-    o.j = lo + 8 * rv + first;
+      if (x[i] == o.M) j = lo + 8 * rv + i;
   }
+  // the sum against fl(M / T)
+  float rs = 0.f;
+  bool nanf = false;
+  if (o.M > -INFINITY) {
+    const float Mt = __fmul_rn(o.M, inv_t);
+    const float nh = __fmul_rn(-Mt, kLog2e);
+    const float nl = __fmaf_rn(-Mt, kLog2e, -nh);
+    // A vector whose tempered maximum is more than 30 below Mt adds less than
+    // 8 e^-30 to a sum that is at least 1; over at most 2^20 elements the
+    // skipped terms stay below 1e-7 of it.
+    const float zcut = __fsub_rn(Mt, 30.0f);
+    for (int v = tid; v < nvec; v += kRT) {
+      if (__fmul_rn(__uint_as_float((uint32_t)vmax[v] << 16), inv_t) < zcut) continue;
+      float x[8];
+      unpack8(sv[v], x);
+      float t[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        t[i] = ex2_approx(__fadd_rn(__fmaf_rn(__fmul_rn(x[i], inv_t), kLog2e, nh), nl));
+      rs += ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+    }
+  } else {
+    for (int v = tid; v < nvec; v += kRT) {
+      float x[8];
+      unpack8(sv[v], x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nanf |= x[i] != x[i];
+    }
+  }
+  nanf |= rs != rs;
+  rs = warp_sum_f(rs);
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) j = min(j, __shfl_xor_sync(0xffffffffu, j, o2));
+  const int anybad = __any_sync(0xffffffffu, nanf) ? 1 : 0;
+  if (lane == 0) {
+    s.rf[kRW + warp] = rs;
+    s.ri[warp] = j;
+    s.ri[kRW + warp] = anybad;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < kRW ? s.rf[kRW + lane] : 0.f;
+    int jj = lane < kRW ? s.ri[lane] : INT_MAX;
+    int bb = lane < kRW ? s.ri[kRW + lane] : 0;
+    t = warp_sum_f(t);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      jj = min(jj, __shfl_xor_sync(0xffffffffu, jj, o2));
+      bb |= __shfl_xor_sync(0xffffffffu, bb, o2);
+    }
+    if (lane == 0) {
+      s.bf[1] = t;
+      s.bi[0] = jj;
+      s.bi[1] = bb;
+    }
+  }
+  __syncthreads();
+  o.S = s.bf[1];
+  o.arg = s.bi[0];
+  o.bad = s.bi[1] != 0 || o.M == INFINITY;
+  __syncthreads();
   return o;
 }
 
@@ -520,22 +558,22 @@ __device__ __forceinline__ unsigned int pass_counts(const uint4* sv, const uint1
   return catch_cnt;
 }
 
+
 // ---------------------------------------------------------------------------
-// the leader's walk over the merged code slots
+// the walk over the merged code slots
 // ---------------------------------------------------------------------------
 struct WalkIn {
-  int C;
   int n;                    // top-n
   bool greedy, topk, topp, minp;
+  bool need_cut;            // the counts cover the kept set only if top-k cuts inside them
   int top_k;
   float top_p;
   double lmp;
   float inv_t, m_t;
   int cmax;                 // code of the row maximum
   int Smax;                 // row slots [0, Smax] hold every element of their value
-  bool full;                // every CTA counted every finite element
-  unsigned int catch_tot;   // the CTAs' own catch-all counts
-  int delta[kRMaxC];        // row slot = CTA r's slot + delta[r]
+  bool full;                // every finite element is counted (the catch-all too)
+  unsigned int catch_row;   // counted elements below the window
 };
 
 // Row slot S stands for the bf16 value of code cmax - S (slot 0: the row
@@ -544,9 +582,9 @@ struct WalkIn {
 // values: the code-0 slot (|x| < 2^-12) and the catch-all (everything below
 // the window); their masses are carried as [low, high] bounds, and a
 // boundary that falls in them, or a decision the bounds leave open, hands the
-// row over.  Writes s.res.  Every thread of the leader CTA calls it.
-__device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem& s) {
-  cg::cluster_group cluster = cg::this_cluster();
+// row over.  cnt[S] holds the row's count of slot S for S <= Smax.  Writes
+// s.res.  Every thread of the CTA calls it.
+__device__ __noinline__ void walk_slots(const WalkIn& w, const uint32_t* hist, RSmem& s) {
   const int tid = threadIdx.x;
   const int S0 = tid * kSlPT;
   if (tid == 0) {
@@ -554,24 +592,9 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
 #pragma unroll
     for (int i = 0; i < 16; ++i) s.bi[i] = -1;
   }
-  // ---- merge: row slot S of CTA r is its slot S - delta[r] ----
   uint32_t cnt[kSlPT];
 #pragma unroll
-  for (int q = 0; q < kSlPT; ++q) cnt[q] = 0u;
-  unsigned int extra = 0;
-  for (int r = 0; r < w.C; ++r) {
-    const uint32_t* hr = cluster.map_shared_rank(hist, r);
-    const int d = w.delta[r];
-#pragma unroll
-    for (int q = 0; q < kSlPT; ++q) {
-      const int S = S0 + q, sl = S - d;
-      if (S <= w.Smax && sl >= 0) cnt[q] += hr[sl];
-    }
-    // slots of CTA r that fall below the row's window join the catch-all
-    if (w.full)
-      for (int sl = max(kSlCatch - d, 0) + tid; sl < kSlCatch; sl += kRT) extra += hr[sl];
-  }
-  const unsigned int catch_row = w.full ? w.catch_tot + (unsigned int)rblock_sum((int)extra, s) : 0u;
+  for (int q = 0; q < kSlPT; ++q) cnt[q] = (S0 + q <= w.Smax) ? hist[S0 + q] : 0u;
   __syncthreads();  // s.bi initialised
 
   const float m_t = w.m_t;
@@ -604,11 +627,11 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
   const unsigned long long ea = rblock_excl(ta, s, &TA);
   const unsigned long long es = rblock_excl(ts, s, &TS);
   unsigned long long catch_surv = 0;
-  if (w.full && catch_row > 0u) {
+  if (w.full && w.catch_row > 0u) {
     if (w.minp) {
       if (minp_pass(z_bot, m_t, w.lmp) && tid == 0) atomicOr(&s.flag, 1);
     } else {
-      catch_surv = catch_row;
+      catch_surv = w.catch_row;
     }
   }
 
@@ -631,7 +654,7 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
   };
   if (w.n > 0) {
     if (TA < (unsigned long long)w.n) {
-      if (tid == 0) atomicOr(&s.flag, 1);  // the top-n reaches past the window
+      if (tid == 0) atomicOr(&s.flag, 1);  // the top-n reaches past the counted slots
     } else {
       find_count(ea, cnt, ta, (unsigned long long)w.n, 0);
     }
@@ -642,8 +665,8 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
     if (K <= TS) {
       cut = true;
       find_count(es, cs, ts, K, 2);
-    } else if (K <= TS + catch_surv) {
-      if (tid == 0) atomicOr(&s.flag, 1);  // the top-k boundary in the catch-all
+    } else if (K <= TS + catch_surv || w.need_cut) {
+      if (tid == 0) atomicOr(&s.flag, 1);  // the top-k boundary past the counted slots
     }
   }
   __syncthreads();
@@ -718,7 +741,7 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
     }
     __syncthreads();
     if (tid == 0 && (s.bi[6] < 0 || s.bi[6] != s.bi[8] || s.bi[7] != s.bi[9]))
-      atomicOr(&s.flag, 1);  // past the window, or left open by the bounds
+      atomicOr(&s.flag, 1);  // past the counted slots, or left open by the bounds
     __syncthreads();
     beta = s.bi[6];
     qk = s.bi[7];
@@ -744,34 +767,13 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
     s.bi[11] = (int)(run + (unsigned long long)qk);
   }
   __syncthreads();
-
-  // ---- per-CTA shares of the two boundary slots ----
-  if (tid < w.C) {
-    const uint32_t* hr = cluster.map_shared_rank(hist, tid);
-    const int d = w.delta[tid];
-    s.res.nb[tid] = (beta >= 0 && beta - d >= 0) ? (int)hr[beta - d] : 0;
-    s.res.nn[tid] = (sn >= 0 && sn - d >= 0) ? (int)hr[sn - d] : 0;
-  }
-  __syncthreads();
   if (tid == 0) {
     RRes& R = s.res;
-    int pre = 0, pren = 0, sum_b = 0;
-    R.last_rank = -1;
-    for (int r = 0; r < w.C; ++r) {
-      const int nb = R.nb[r], nn = R.nn[r];
-      const int cb = beta >= 0 ? min(max(qk - pre, 0), nb) : 0;
-      const int cn = sn >= 0 ? min(max(cn_tot - pren, 0), nn) : 0;
-      if (beta >= 0 && pre < qk && qk <= pre + nb) R.last_rank = r;
-      if ((cb > 0 && cb < nb && nb > kListCap) || (cn > 0 && cn < nn && nn > kListCap)) s.flag |= 1;
-      R.cb[r] = cb;
-      R.cn[r] = cn;
-      pre += nb;
-      pren += nn;
-      sum_b += nb;
-    }
-    if (beta >= 0 && (R.last_rank < 0 || qk < 1)) s.flag |= 1;
+    if (beta >= 0 && qk < 1) s.flag |= 1;
     R.beta = beta;
+    R.qk = qk;
     R.sn = sn;
+    R.cn = cn_tot;
     R.L3 = beta >= 0 ? s.bi[11] : (beta == kNoKept ? 1 : 0);
     R.kth_z = beta >= 0 ? slot_z(beta) : 0.f;
     R.action = s.flag ? 1 : 0;
@@ -779,602 +781,863 @@ __device__ __noinline__ void leader_walk(const WalkIn& w, uint32_t* hist, RSmem&
   __syncthreads();
 }
 
+// ---------------------------------------------------------------------------
+// shared pieces of the two kernels
+// ---------------------------------------------------------------------------
+// Row parameters as the kernels use them.
+struct RowCfg {
+  bool greedy, topk, topp, minp;
+  int top_k, n, mode;
+  float inv_t, top_p;
+  double lmp;
+};
+__device__ __forceinline__ RowCfg row_cfg(const RowArgs& a, int row, const RowParams& P) {
+  RowCfg c;
+  c.greedy = (P.flags & kRowGreedy) != 0;
+  c.inv_t = P.inv_t;
+  c.top_p = P.top_p;
+  bool topp = (P.flags & kRowTopP) != 0;
+  if (P.flags & kRowDecay) {  // the decayed top_p; 1 (the start) filters nothing
+    c.top_p = a.decay[row].p;
+    topp = c.top_p < 1.0f;
+  }
+  c.topp = topp && !c.greedy;
+  c.top_k = P.top_k;
+  c.topk = !c.greedy && P.top_k > 1 && P.top_k < a.V;
+  c.minp = !c.greedy && (P.flags & kRowMinP) != 0;
+  c.lmp = P.log_min_p;
+  c.n = a.n_logprobs;
+  if (c.greedy) c.mode = c.n > 0 ? kModeRecords : kModeStats;
+  else if (!c.topk && !c.topp && !c.minp) c.mode = kModeAll;
+  else if (c.topk && c.top_k <= kPCap) c.mode = kModeRecords;
+  else c.mode = kModeCounts;
+  return c;
+}
+
+// Copy CTA `rank`'s slice of `row` into shared memory: one bulk copy of its
+// whole 16-byte units (aligned rows), plain loads for the rest; -inf past the
+// end up to whole vectors.  Returns false when the bounded wait ran out.
+__device__ bool load_slice(const RowArgs& a, int row, int lo, int nel, int nvec, uint8_t* buf,
+                           RSmem& s) {
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(a.logits) + (int64_t)row * a.ld + lo;
+  const uint32_t bulk = a.aligned ? (((uint32_t)nel * 2u) & ~15u) : 0u;
+  if (threadIdx.x == 0 && bulk) {
+    mbar_init(&s.full, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&s.full, bulk);
+    bulk_copy_g2s(buf, src, bulk, &s.full);
+  }
+  uint16_t* e16 = reinterpret_cast<uint16_t*>(buf);
+  for (int k = (int)(bulk >> 1) + threadIdx.x; k < nel; k += kRT) e16[k] = src[k];
+  for (int k = nel + threadIdx.x; k < 8 * nvec; k += kRT) e16[k] = 0xFF80u;
+  __syncthreads();  // the mbarrier initialised, the plain part stored
+  bool ok = true;
+  if (bulk) ok = mbar_wait_bounded(&s.full, 0u);
+  return ok;
+}
+
+// The best Gumbel score over elements offered one at a time: a 24-bit
+// integer prefilter, then the certificate, then the exact score.  An element
+// beats the best bs only if -ln u < e^(z - bs) <= e^(zmax - bs) = E, and
+// -ln u >= 1 - u, so only if u > 1 - E: b >= blo (a 2^-8 margin and one unit
+// cover the fp32 rounding).
+struct Draw {
+  float bs = -INFINITY, bz = 0.f;
+  int bj = INT_MAX;
+  uint32_t blo = 0u;
+  float zmax;
+  __device__ explicit Draw(float zmax_) : zmax(zmax_) {}
+  // The noise bound for elements whose tempered value is at most z.
+  __device__ __forceinline__ uint32_t bound(float z) const {
+    if (bs == -INFINITY) return 0u;
+    const float E = ex2_approx(__fmul_rn(__fsub_rn(z, bs), kLog2e)) * 1.00390625f;
+    const float th = (1.0f - E) * 16777216.0f;
+    return (E < 1.0f && th > 1.0f) ? (uint32_t)th - 1u : 0u;
+  }
+  __device__ __forceinline__ void offer(float z, int j, uint32_t bits) {
+    if (bits < blo) return;
+    if (!may_beat(z, bs, bits)) return;
+    const float sc = gumbel_score(z, bits);
+    if (pair_better(sc, j, bs, bj)) {
+      bs = sc;
+      bj = j;
+      bz = z;
+      const float E = ex2_approx(__fmul_rn(__fsub_rn(zmax, bs), kLog2e)) * 1.00390625f;
+      const float th = (1.0f - E) * 16777216.0f;
+      blo = (E < 1.0f && th > 1.0f) ? (uint32_t)th - 1u : 0u;
+    }
+  }
+};
+
+// Outputs of a row without a token: -1, NaN log-probs, the status; the seed
+// still advances.  All threads of one CTA call it.
+__device__ void write_bad(const RowArgs& a, int row, int status, int err) {
+  const int n = a.n_logprobs;
+  if ((int)threadIdx.x < n) {
+    a.out_topk_ids[(int64_t)row * n + threadIdx.x] = -1;
+    a.out_topk_logprobs[(int64_t)row * n + threadIdx.x] = __int_as_float(0x7fc00000);
+  }
+  if (threadIdx.x == 0) {
+    a.out_tokens[row] = -1;
+    if (a.out_logprobs) a.out_logprobs[row] = __int_as_float(0x7fc00000);
+    a.row_status[row] = status;
+    a.dbg_kth_value[row] = __int_as_float(0x7fc00000);
+    a.dbg_kth_index[row] = -1;
+    a.dbg_kept[row] = 0;
+    a.seeds[row] += kSeedStep;
+    if (err) atomicOr(a.err_word, err);
+  }
+}
+
+// The token and its row data.  One thread calls it.
+__device__ void write_token(const RowArgs& a, int row, const RowParams& P, int tok, float ztok,
+                            float m_t, float lnS, float kz, int kj, int L3, int err) {
+  a.out_tokens[row] = tok;
+  if (a.out_logprobs) a.out_logprobs[row] = (ztok - m_t) - lnS;
+  a.row_status[row] = kRowOk;
+  a.dbg_kth_value[row] = kz;
+  a.dbg_kth_index[row] = kj;
+  a.dbg_kept[row] = L3;
+  a.seeds[row] += kSeedStep;
+  if (P.flags & kRowDecay) {  // [TensorRT-LLM "Sampling", top-p decay]
+    DecayState& d = a.decay[row];
+    const float qd = __fmul_rn(d.p, d.decay);
+    d.p = tok == d.reset_id ? P.top_p : (qd < d.p_min ? d.p_min : qd);
+  }
+  if (err) atomicOr(a.err_word, err);
+}
+
+// Hand a row to the selection kernel with its statistics.  One thread.
+__device__ void hand_over(const RowArgs& a, int row, float m_t, float lnS, float xmax, int arg,
+                          int err) {
+  SlowRow sr;
+  sr.m_t = m_t;
+  sr.lnS = lnS;
+  sr.xmax = xmax;
+  sr.bi_topn = (uint32_t)arg | (a.n_logprobs == 0 ? 0x80000000u : 0u);
+  a.slow[row] = sr;
+  a.slow_list[atomicAdd(a.slow_ctl, 1u)] = row;
+  if (err) atomicOr(a.err_word, err);
+}
 
 // ---------------------------------------------------------------------------
-// the kernel
+// the pass kernel: one CTA per (row, slice); the row's last CTA completes it
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRT, 1) rows_kernel(const RowArgs a) {
+__device__ void finish_row(const RowArgs& a, int row, const RowParams& P, const RowCfg& c,
+                           uint8_t* buf, uint32_t* hist, uint32_t* list, RSmem& s);
+
+__global__ void __launch_bounds__(kRT, 2) row_pass_kernel(const RowArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ RSmem s;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
-  const int cid = (int)blockIdx.x / C, ncl = (int)gridDim.x / C;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool leader = rank == 0;
+  const int tid = threadIdx.x;
+  const int C = a.C;
+  const int q = (int)blockIdx.x / C, rank = (int)blockIdx.x % C;
+  if (q >= a.norder) return;
+  const int row = a.order[q];
+  if (row >= a.B) return;
   const int lo = rank * a.slice;
-  const int hi = min(lo + a.slice, a.V);
-  const int nel = max(0, hi - lo);
+  const int nel = max(0, min(lo + a.slice, a.V) - lo);
   const int nvec = (nel + 7) >> 3;
-  const int n = a.n_logprobs;
-  auto buf_at = [&](int bf) { return dsm + (size_t)bf * a.buf_bytes; };
-  uint32_t* hist = reinterpret_cast<uint32_t*>(dsm + 2 * (size_t)a.buf_bytes);
-  uint32_t* list_b = hist + kSl;
-  uint32_t* list_n = list_b + kListCap;
-  uint16_t* vmax = reinterpret_cast<uint16_t*>(list_n + kListCap);  // [nvec] vector maxima
-  // aligned rows: one bulk copy of the slice's whole 16-byte units, the last
-  // (< 8) elements by plain loads; other rows: plain loads of the whole slice
-  const uint32_t bulk = a.aligned ? (((uint32_t)nel * 2u) & ~15u) : 0u;
-  const int tail0 = a.aligned ? (int)(bulk >> 1) : 0;
-  const int ntail = a.aligned ? nel - tail0 : 0;
-  auto row_src = [&](int row) {
-    return reinterpret_cast<const uint16_t*>(a.logits) + (int64_t)row * a.ld + lo;
-  };
-  auto next_q = [&](int q) {
-    while (q < a.norder && a.order[q] >= a.B) q += ncl;
-    return q;
-  };
-
-  // -inf past the slice's end up to whole vectors (never written again)
-  for (int bf = 0; bf < 2; ++bf) {
-    uint16_t* e = reinterpret_cast<uint16_t*>(buf_at(bf));
-    for (int k = nel + tid; k < 8 * nvec; k += kRT) e[k] = 0xFF80u;
-  }
-  if (tid == 0) {
-    mbar_init(&s.full[0], 1);
-    mbar_init(&s.full[1], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  auto issue = [&](int row, int bf) {  // thread 0
-    if (bulk) {
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&s.full[bf], bulk);
-      bulk_copy_g2s(buf_at(bf), row_src(row), bulk, &s.full[bf]);
-    }
-  };
-  int q = next_q(cid);
-  if (q < a.norder && a.aligned) {
-    const int row = a.order[q];
-    if (tid == 0) issue(row, 0);
-    if (tid < ntail) reinterpret_cast<uint16_t*>(buf_at(0))[tail0 + tid] = row_src(row)[tail0 + tid];
-  }
-  __syncthreads();
-  int err = 0;
-
-  for (int i = 0; q < a.norder; ++i) {
-    const int row = a.order[q];
-    unsigned long long* tr =
-        a.trace ? a.trace + ((size_t)row * C + rank) * kTraceSlots : nullptr;
-#define VT_RTRACE(k)                                      \
-  do {                                                    \
-    if (tr && tid == 0) tr[(k)] = global_timer_ns();      \
+  uint8_t* buf = dsm;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(dsm + a.buf_bytes);
+  uint16_t* vmax = reinterpret_cast<uint16_t*>(hist + kSl);
+  unsigned long long* tr = a.trace ? a.trace + ((size_t)row * C + rank) * kTraceSlots : nullptr;
+#define VT_RTRACE(k)                                 \
+  do {                                               \
+    if (tr && tid == 0) tr[(k)] = global_timer_ns(); \
   } while (0)
-    VT_RTRACE(0);
-    const int b = i & 1, par = i & 1;
-    const int qn = next_q(q + ncl);
-    const int rown = qn < a.norder ? a.order[qn] : -1;
-    uint16_t tail_v = 0;
-    // the next row's slice into the other buffer, whose row ended with a barrier
-    if (a.aligned && rown >= 0) {
-      if (tid == 0) issue(rown, b ^ 1);
-      if (tid < ntail) tail_v = row_src(rown)[tail0 + tid];  // stored at this row's end
-    }
-    if (a.aligned) {
-      if (bulk && !mbar_wait_bounded(&s.full[b], (uint32_t)((i >> 1) & 1))) err |= kErrTimeout;
-    } else {
-      uint16_t* e = reinterpret_cast<uint16_t*>(buf_at(b));
-      const uint16_t* src = row_src(row);
-      for (int k = tid; k < nel; k += kRT) e[k] = src[k];
-      __syncthreads();
-    }
-    const uint4* sv = reinterpret_cast<const uint4*>(buf_at(b));
-    VT_RTRACE(1);
+  VT_RTRACE(0);
+  int err = load_slice(a, row, lo, nel, nvec, buf, s) ? 0 : kErrTimeout;
+  VT_RTRACE(1);
+  const uint4* sv = reinterpret_cast<const uint4*>(buf);
+  const RowParams P = a.params[row];
+  const RowCfg c = row_cfg(a, row, P);
 
-    const RowParams P = a.params[row];
-    const bool greedy = (P.flags & kRowGreedy) != 0;
-    const float inv_t = P.inv_t;
-    float top_p = P.top_p;
-    bool topp = (P.flags & kRowTopP) != 0;
-    if (P.flags & kRowDecay) {  // the decayed top_p; 1 (the start) filters nothing
-      top_p = a.decay[row].p;
-      topp = top_p < 1.0f;
-    }
-    topp = topp && !greedy;
-    const bool topk = !greedy && P.top_k > 1 && P.top_k < a.V;
-    const bool minp = !greedy && (P.flags & kRowMinP) != 0;
-    const bool filtered = topk || topp || minp;
-    const bool need_hist = n > 0 || (!greedy && filtered);
+  // ---- pass A ----
+  const Stats st = pass_stats(sv, vmax, nvec, lo, c.inv_t, s);
+  const int cmax = st.M > -INFINITY ? bcode(__float_as_uint(st.M) >> 16) : -bcode(0x7F80u);
+  const float Mt = st.M > -INFINITY ? __fmul_rn(st.M, c.inv_t) : -INFINITY;
+  VT_RTRACE(2);
 
-    do {  // the row; `break` ends it
-      // ---- pass A ----
-      const Stats st = pass_stats(sv, vmax, nvec, lo, inv_t);
-      {
-        float m = st.rm, mt = st.rmt, sm = st.rs;
-        int j = st.j, bad = st.bad ? 1 : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-          const int j2 = __shfl_xor_sync(0xffffffffu, j, o);
-          const float mt2 = __shfl_xor_sync(0xffffffffu, mt, o);
-          const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-          if (pair_better(m2, j2, m, j)) {
-            m = m2;
-            j = j2;
-          }
-          lse_combine(mt, sm, mt2, s2, kLog2e);
-          bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-        }
-        if (lane == 0) {
-          s.rf[warp] = m;
-          s.rf[kRW + warp] = mt;
-          s.rf[2 * kRW + warp] = sm;
-          s.ri[warp] = j;
-          s.ri[kRW + warp] = bad;
-        }
-        __syncthreads();
-        if (warp == 0) {
-          float bm = lane < kRW ? s.rf[lane] : -INFINITY;
-          float bmt = lane < kRW ? s.rf[kRW + lane] : -INFINITY;
-          float bs = lane < kRW ? s.rf[2 * kRW + lane] : 0.f;
-          int bj = lane < kRW ? s.ri[lane] : INT_MAX;
-          int bb = lane < kRW ? s.ri[kRW + lane] : 0;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, bm, o);
-            const int j2 = __shfl_xor_sync(0xffffffffu, bj, o);
-            const float mt2 = __shfl_xor_sync(0xffffffffu, bmt, o);
-            const float s2 = __shfl_xor_sync(0xffffffffu, bs, o);
-            if (pair_better(m2, j2, bm, bj)) {
-              bm = m2;
-              bj = j2;
-            }
-            lse_combine(bmt, bs, mt2, s2, kLog2e);
-            bb |= __shfl_xor_sync(0xffffffffu, bb, o);
-          }
-          if (lane == 0) {
-          RPart& pt = s.part[par];
-          pt.xmax = bm;
-          pt.s = bs;
-          pt.arg = bj;
-          pt.bad = bb || bm == INFINITY;
-          pt.cmax = bm > -INFINITY ? bcode(__float_as_uint(bm) >> 16) : -bcode(0x7F80u);
-          s.bf[0] = bmt;
-          }
-        }
-        __syncthreads();
-      }
-      const int cmax_cta = s.part[par].cmax;
-      const float mt_cta = s.bf[0];
-      VT_RTRACE(2);
-
-      // ---- thresholds and pass H ----
-      int thr = kThrNone;
-      unsigned int catch_cnt = 0;
-      if (need_hist) {
-        const int Kk = (topk && P.top_k <= kGrp * kRT) ? P.top_k : 0;
-        int tn, tk;
-        local_thresholds(st.gm, cmax_cta, n, Kk, s, &tn, &tk);
-        if (greedy || !filtered) {
-          thr = tn;
-        } else {
-          int tkept = topk ? (Kk > 0 ? tk : kThrAll) : kThrAll;
-          if (minp) {
-            if (warp == 0) {
-              const int mc = mt_cta > -INFINITY ? minp_code_warp(inv_t, mt_cta, P.log_min_p, cmax_cta)
-                                                : kThrAll;
-              if (lane == 0) s.bi[6] = mc;
-            }
-            __syncthreads();
-            tkept = max(tkept, s.bi[6]);
-            __syncthreads();
-          }
-          thr = n > 0 ? min(tn, tkept) : tkept;
-        }
-        uint4* h4 = reinterpret_cast<uint4*>(hist);
-        for (int k = tid; k < kSl / 4; k += kRT) h4[k] = make_uint4(0u, 0u, 0u, 0u);
-        __syncthreads();
-        catch_cnt = (unsigned int)rblock_sum(
-            (int)pass_counts(sv, vmax, nvec, code_floor_value(thr), cmax_cta, hist), s);
-      }
-      if (tid == 0) {
-        RPart& pt = s.part[par];
-        pt.thr = thr;
-        pt.catch_cnt = catch_cnt;
-        pt.err = err;
-      }
-      VT_RTRACE(3);
-      cluster.sync();  // (1) statistics and histograms visible
-      VT_RTRACE(4);
-
-      // ---- the row's statistics from every CTA ----
-      if (warp == 0) {
-        float xm = -INFINITY, mt = -INFINITY, sm = 0.f;
-        int arg = INT_MAX, bd = 0, th = INT_MIN, er = 0, cm = INT_MIN;
-        unsigned int ct = 0u;
-        if (lane < C) {
-          const RPart* pp = cluster.map_shared_rank(&s.part[par], lane);
-          xm = pp->xmax;
-          mt = xm > -INFINITY ? __fmul_rn(xm, inv_t) : -INFINITY;
-          sm = pp->s;
-          arg = pp->arg;
-          bd = pp->bad;
-          th = pp->thr;
-          ct = pp->catch_cnt;
-          er = pp->err;
-          cm = pp->cmax;
-        }
-        const int my_cmax = cm;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float x2 = __shfl_xor_sync(0xffffffffu, xm, o);
-          const int a2 = __shfl_xor_sync(0xffffffffu, arg, o);
-          const float mt2 = __shfl_xor_sync(0xffffffffu, mt, o);
-          const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
-          if (pair_better(x2, a2, xm, arg)) {
-            xm = x2;
-            arg = a2;
-          }
-          lse_combine(mt, sm, mt2, s2, kLog2e);
-          bd |= __shfl_xor_sync(0xffffffffu, bd, o);
-          er |= __shfl_xor_sync(0xffffffffu, er, o);
-          th = max(th, __shfl_xor_sync(0xffffffffu, th, o));
-          ct += __shfl_xor_sync(0xffffffffu, ct, o);
-          cm = max(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-        }
-        if (lane < C) s.delta[lane] = cm - my_cmax;
-        if (lane == 0) {
-          s.bf[1] = xm;
-          s.bf[2] = mt;
-          s.bf[3] = sm;
-          s.bi[0] = arg;
-          s.bi[1] = bd || xm == INFINITY;
-          s.bi[2] = th;
-          s.bi[3] = (int)ct;
-          s.bi[7] = er;
-          s.bi[8] = cm;
-        }
-      }
-      __syncthreads();
-      const float xmax_row = s.bf[1], m_t = s.bf[2], S_row = s.bf[3];
-      const int arg_row = s.bi[0], bad_row = s.bi[1], thr_row = s.bi[2];
-      const unsigned int catch_tot = (unsigned int)s.bi[3];
-      const int err_row = s.bi[7] | err, cmax_row = s.bi[8];
-      const float lnS = logf(S_row);
-      __syncthreads();
-      const int status = bad_row ? kRowNonfinite : (xmax_row == -INFINITY ? kRowEmpty : kRowOk);
-
-      if (status != kRowOk) {  // no token: -1, NaN log-probs; the seed still advances
-        if (leader) {
-          if (tid < n) {
-            a.out_topk_ids[(int64_t)row * n + tid] = -1;
-            a.out_topk_logprobs[(int64_t)row * n + tid] = __int_as_float(0x7fc00000);
-          }
-          if (tid == 0) {
-            a.out_tokens[row] = -1;
-            if (a.out_logprobs) a.out_logprobs[row] = __int_as_float(0x7fc00000);
-            a.row_status[row] = status;
-            a.dbg_kth_value[row] = __int_as_float(0x7fc00000);
-            a.dbg_kth_index[row] = -1;
-            a.dbg_kept[row] = 0;
-            a.seeds[row] += kSeedStep;
-            if (err_row) atomicOr(a.err_word, err_row);
-          }
-        }
-        break;
-      }
-      if (greedy && n == 0) {  // the argmax, nothing else
-        if (leader && tid == 0) {
-          a.out_tokens[row] = arg_row;
-          if (a.out_logprobs) a.out_logprobs[row] = -lnS;
-          a.row_status[row] = kRowOk;
-          a.dbg_kth_value[row] = m_t;
-          a.dbg_kth_index[row] = arg_row;
-          a.dbg_kept[row] = 1;
-          a.seeds[row] += kSeedStep;
-          if (err_row) atomicOr(a.err_word, err_row);
-        }
-        break;
-      }
-
-      // ---- the leader's walk (barrier 2), or every element kept ----
-      const bool walk = need_hist;
-      if (walk) {
-        if (leader) {
-          if (tid == 0) s.gcount = 0;
-          WalkIn w;
-          w.C = C;
-          w.n = n;
-          w.greedy = greedy;
-          w.topk = topk;
-          w.topp = topp;
-          w.minp = minp;
-          w.top_k = P.top_k;
-          w.top_p = top_p;
-          w.lmp = P.log_min_p;
-          w.inv_t = inv_t;
-          w.m_t = m_t;
-          w.cmax = cmax_row;
-          const long long Sstar = thr_row == kThrAll ? (long long)INT_MAX
-                                                     : (long long)cmax_row - (long long)thr_row;
-          w.full = Sstar >= kSlCatch;
-          w.Smax = (int)(Sstar < kSlCatch - 1 ? Sstar : kSlCatch - 1);
-          w.catch_tot = catch_tot;
-          for (int r = 0; r < C; ++r) w.delta[r] = s.delta[r];
-          leader_walk(w, hist, s);
-          if (tid == 0 && s.res.action) {  // to the selection kernel, with the statistics
-            SlowRow sr;
-            sr.m_t = m_t;
-            sr.lnS = lnS;
-            sr.xmax = xmax_row;
-            sr.bi_topn = (uint32_t)arg_row | (n == 0 ? 0x80000000u : 0u);
-            a.slow[row] = sr;
-            a.slow_list[atomicAdd(a.slow_ctl, 1u)] = row;
-            if (err_row) atomicOr(a.err_word, err_row);
-          }
-        }
-        VT_RTRACE(5);
-        cluster.sync();  // (2) the walk visible
-        VT_RTRACE(6);
-        if (tid < (int)(sizeof(RRes) / 4)) {
-          const int* src = reinterpret_cast<const int*>(cluster.map_shared_rank(&s.res, 0));
-          reinterpret_cast<int*>(&s.rl)[tid] = src[tid];
-        }
-        __syncthreads();
-        if (s.rl.action) break;
+  // ---- records, counts, or the draw over every element ----
+  int thr = kThrNone, thr_n = kThrNone, nrec = 0, fin = 0;
+  unsigned int catch_cnt = 0u;
+  unsigned long long lastk = ~0ull;
+  Draw d(Mt);
+  if (c.mode != kModeStats && !st.bad) {
+    int tn = kThrAll, tk = kThrAll;
+    const int Kk = (c.mode == kModeRecords && c.topk && c.top_k <= kGrp * kRT) ? c.top_k : 0;
+    local_thresholds(st.gm, cmax, c.n, Kk, s, &tn, &tk);
+    if (c.mode == kModeRecords) {
+      if (c.greedy) {
+        thr = tn;
       } else {
-        if (tid == 0) {
-          s.rl.action = 0;
-          s.rl.beta = kAllKept;
-          s.rl.sn = -1;
-          s.rl.L3 = 0;
-          s.rl.last_rank = -1;
-          s.rl.cb[rank] = s.rl.nb[rank] = s.rl.cn[rank] = s.rl.nn[rank] = 0;
+        int tkept = Kk > 0 ? tk : kThrAll;
+        if (c.minp) {
+          if ((tid >> 5) == 0) {
+            const int mc = Mt > -INFINITY ? minp_code_warp(c.inv_t, Mt, c.lmp, cmax) : kThrAll;
+            if ((tid & 31) == 0) s.bi[6] = mc;
+          }
+          __syncthreads();
+          tkept = max(tkept, s.bi[6]);
+          __syncthreads();
         }
-        __syncthreads();
+        thr = c.n > 0 ? min(tn, tkept) : tkept;
       }
-
-      // ---- pass D: the draw over the kept elements, the top-n to the leader ----
-      // Slot S < beta holds values above x_b = value(beta) (codes are
-      // monotone; beta is never the code-0 slot), so the tests are value
-      // compares: kept iff x > x_b, or x == x_b and among the first cb of the
-      // boundary slot here; likewise the top-n against x_n.  Vectors whose
-      // maximum is below both are skipped whole.
-      const int beta = s.rl.beta, sn = s.rl.sn;
-      const int cb = s.rl.cb[rank], nb = s.rl.nb[rank];
-      const int cnq = s.rl.cn[rank], nnq = s.rl.nn[rank];
-      const bool bfull = cb == nb, nfull = cnq == nnq;
-      const bool keep_all = beta == kAllKept;
-      const float xb = beta >= 0 ? bcode_value(cmax_row - beta) : INFINITY;
-      const float xn = sn >= 0 ? bcode_value(cmax_row - sn) : INFINITY;
-      const float lim = keep_all ? -INFINITY : fminf(xb, xn);
-      const uint64_t key = row_key(a.seeds[row], row);
-      if (tid == 0) {
-        s.nlist = 0;
-        s.nlistn = 0;
+      thr_n = thr;
+    } else {
+      thr_n = c.n > 0 ? tn : kThrNone;
+    }
+    // records of the elements with code >= the record threshold
+    const int rthr = c.mode == kModeRecords ? thr : thr_n;
+    if (rthr != kThrNone) {
+      const float tx = code_floor_value(rthr);
+      if (tid == 0) s.nrec = 0;
+      __syncthreads();
+      uint64_t* out = a.cand + ((size_t)row * C + rank) * a.cand_cap;
+      const int lane = tid & 31;
+      for (int v0 = tid - lane; v0 < nvec; v0 += kRT) {  // warp-uniform trip count
+        const int v = v0 + lane;
+        uint32_t m = 0u;
+        uint4 qv = make_uint4(0u, 0u, 0u, 0u);
+        if (v < nvec && __uint_as_float((uint32_t)vmax[v] << 16) >= tx) {
+          qv = sv[v];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x = __uint_as_float(bits8(qv, i) << 16);
+            m |= (uint32_t)(x >= tx && x > -INFINITY) << i;
+          }
+        }
+        if (!__any_sync(0xffffffffu, m != 0u)) continue;
+        // one shared atomic per warp: each lane's records at its prefix
+        const int cnt = __popc(m);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+        int base = 0;
+        if (lane == 31 && wtot > 0) base = atomicAdd(&s.nrec, wtot);
+        base = __shfl_sync(0xffffffffu, base, 31);
+        int pos = base + incl - cnt;
+        while (m) {
+          const int i = __ffs(m) - 1;
+          m &= m - 1u;
+          const uint32_t bits = bits8(qv, i);
+          if (pos < a.cand_cap) out[pos] = rec_make(bcode(bits), lo + 8 * v + i, bits);
+          ++pos;
+        }
       }
       __syncthreads();
-      int* gc = cluster.map_shared_rank(&s.gcount, 0);
-      uint64_t* gb = cluster.map_shared_rank(s.gather, 0);
-      auto push = [&](float x, int j) {
-        const int pos = atomicAdd(gc, 1);
-        if (pos < kGatherCap) gb[pos] = elem_key(__fmul_rn(x, inv_t), (uint32_t)j);
-      };
-      float bs = -INFINITY, bz = 0.f;
-      int bj = INT_MAX, kthmax = -1, fin = 0;
-      unsigned long long lastk = ~0ull;
-      // Noise prefilter: an element beats the running best bs only if
-      // -ln u < e^(z - bs) <= e^(m_t - bs) = E, and -ln u >= 1 - u, so only if
-      // u > 1 - E: 24-bit noise b >= blo (a 2^-8 margin and one unit cover
-      // the fp32 rounding).  Those pass to the per-element certificate.
-      uint32_t blo = 0u;
-      auto set_blo = [&]() {
-        const float E = ex2_approx(__fmul_rn(__fsub_rn(m_t, bs), kLog2e)) * 1.00390625f;
-        const float th = (1.0f - E) * 16777216.0f;
-        blo = (E < 1.0f && th > 1.0f) ? (uint32_t)th - 1u : 0u;
-      };
-      auto consider = [&](float x, int j, uint32_t bits) {
-        if (bits < blo) return;
-        const float z = __fmul_rn(x, inv_t);
-        if (!may_beat(z, bs, bits)) return;
-        const float sc = gumbel_score(z, bits);
-        if (pair_better(sc, j, bs, bj)) {
-          bs = sc;
-          bj = j;
-          bz = z;
-          set_blo();
-        }
-      };
+      nrec = s.nrec;
+    }
+    if (c.mode == kModeCounts) {  // a count per code slot below the slice maximum
+      thr = kThrAll;
+      uint4* h4 = reinterpret_cast<uint4*>(hist);
+      for (int k = tid; k < kSl / 4; k += kRT) h4[k] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      catch_cnt =
+          (unsigned int)rblock_sum((int)pass_counts(sv, vmax, nvec, -INFINITY, cmax, hist), s);
+      uint4* g4 = reinterpret_cast<uint4*>(a.ghist + ((size_t)row * C + rank) * kSl);
+      for (int k = tid; k < kSl / 4; k += kRT) g4[k] = h4[k];
+    } else if (c.mode == kModeAll) {  // no filter: every finite element is kept
+      const uint64_t key = row_key(a.seeds[row], row);
       for (int v = tid; v < nvec; v += kRT) {
-        if (!(__uint_as_float((uint32_t)vmax[v] << 16) >= lim)) continue;
         const uint4 qv = sv[v];
         float x[8];
         unpack8(qv, x);
-        uint32_t km = 0u, rare = 0u;
+        uint64_t h[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const bool fin_i = x[i] > -INFINITY;
-          const bool kp = keep_all ? fin_i : x[i] > xb;
-          km |= (uint32_t)kp << i;
-          rare |= (uint32_t)(x[i] == xb || x[i] >= xn) << i;
-        }
-        if (keep_all) {
-          fin += __popc(km);
+        for (int w = 0; w < 4; ++w) h[w] = pair_hash(key, lo + 8 * v + 2 * w);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (km & (1u << i)) {
-              const unsigned long long k =
-                  elem_key(__fmul_rn(x[i], inv_t), (uint32_t)(lo + 8 * v + i));
-              lastk = k < lastk ? k : lastk;
-            }
+        for (int q2 = 0; q2 < 8; ++q2) {
+          if (x[q2] > -INFINITY) {
+            const int j = lo + 8 * v + q2;
+            const float z = __fmul_rn(x[q2], c.inv_t);
+            d.offer(z, j, (q2 & 1) ? bits_odd(h[q2 >> 1]) : bits_even(h[q2 >> 1]));
+            const unsigned long long k = elem_key(z, (uint32_t)j);
+            lastk = k < lastk ? k : lastk;
+            ++fin;
           }
         }
-        while (rare) {  // top-n members and boundary-slot elements (few)
-          const int i = __ffs(rare) - 1;
-          rare &= rare - 1u;
-          const int j = lo + 8 * v + i;
-          const float xe = __uint_as_float(bits8(qv, i) << 16);
-          if (xe > xn || (xe == xn && nfull)) {
-            push(xe, j);
-          } else if (xe == xn && cnq > 0) {
-            const int pos = atomicAdd(&s.nlistn, 1);
-            if (pos < kListCap) list_n[pos] = (uint32_t)(j - lo);
-          }
-          if (xe == xb) {
-            if (bfull) {
-              km |= 1u << i;
-              kthmax = max(kthmax, j);
-            } else if (cb > 0) {
-              const int pos = atomicAdd(&s.nlist, 1);
-              if (pos < kListCap) list_b[pos] = (uint32_t)(j - lo);
-            }
-          }
-        }
-        if (km) {
+      }
+      rblock_argmax(d.bs, d.bj, d.bz, s);
+      lastk = rblock_min_u64(lastk, s);
+      fin = rblock_sum(fin, s);
+    }
+  }
+  VT_RTRACE(3);
+  if (tid == 0) {
+    RowPartG& pt = a.part[(size_t)row * C + rank];
+    pt.xmax = st.M;
+    pt.s = st.S;
+    pt.arg = st.arg;
+    pt.bad = st.bad ? 1 : 0;
+    pt.cmax = cmax;
+    pt.thr = thr;
+    pt.thr_n = thr_n;
+    pt.catch_cnt = catch_cnt;
+    pt.ncand = nrec;
+    pt.err = err;
+    pt.best_s = d.bs;
+    pt.best_z = d.bz;
+    pt.best_j = d.bj;
+    pt.kth_j = -1;
+    pt.last_key = lastk;
+    pt.fin = fin;
+  }
+#undef VT_RTRACE
+}
+
+// ---------------------------------------------------------------------------
+// the finish kernel: one CTA per row, after the pass kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRT, 3) row_finish_kernel(const RowArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ RSmem s;
+  const int q = (int)blockIdx.x;
+  if (q >= a.norder) return;
+  const int row = a.order[q];
+  if (row >= a.B) return;
+  unsigned long long* tr = a.trace ? a.trace + (size_t)row * a.C * kTraceSlots : nullptr;
+  if (tr && threadIdx.x == 0) tr[4] = global_timer_ns();
+  const RowParams P = a.params[row];
+  const RowCfg c = row_cfg(a, row, P);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(dsm);
+  uint32_t* list = hist + kSl;
+  uint8_t* recbuf = reinterpret_cast<uint8_t*>(list + kListCap);
+  finish_row(a, row, P, c, recbuf, hist, list, s);
+  if (tr && threadIdx.x == 0) tr[5] = global_timer_ns();
+}
+
+// The top-n from records whose slot < sn (all) or == sn (the first cn by
+// index), ordered (value descending, index ascending) by their exact values.
+__device__ void write_topn(const RowArgs& a, int row, const RowCfg& c, const uint64_t* recs,
+                           int nrec, int cmax_row, int sn, int cn, int nsn, float m_t, float lnS,
+                           uint32_t* list, uint32_t* bins, RSmem& s, int* err) {
+  const int tid = threadIdx.x;
+  const int code_n = cmax_row - sn;
+  if (tid == 0) {
+    s.ntop = 0;
+    s.nlistn = 0;
+  }
+  __syncthreads();
+  const bool all_sn = cn == nsn;
+  for (int e = tid; e < nrec; e += kRT) {
+    const uint64_t r = recs[e];
+    const int code = rec_code(r);
+    if (code > code_n || (code == code_n && all_sn)) {
+      const int pos = atomicAdd(&s.ntop, 1);
+      if (pos < 32) s.top[pos] = r;
+    } else if (code == code_n) {
+      const int pos = atomicAdd(&s.nlistn, 1);
+      if (pos < kListCap) list[pos] = (uint32_t)rec_j(r);
+    }
+  }
+  __syncthreads();
+  if (!all_sn) {
+    const int nl = min(s.nlistn, kListCap);
+    const uint32_t kth = rblock_kth_smallest(list, nl, cn, bins, s);
+    for (int e = tid; e < nrec; e += kRT) {
+      const uint64_t r = recs[e];
+      if (rec_code(r) == code_n && (uint32_t)rec_j(r) <= kth) {
+        const int pos = atomicAdd(&s.ntop, 1);
+        if (pos < 32) s.top[pos] = r;
+      }
+    }
+    __syncthreads();
+  }
+  const int n = c.n;
+  if (tid < 32) {
+    const int g = min(s.ntop, 32);
+    unsigned long long k = 0ull;
+    float z = 0.f;
+    int j = -1;
+    if (tid < g) {
+      const uint64_t r = s.top[tid];
+      j = rec_j(r);
+      z = __fmul_rn(rec_x(r), c.inv_t);
+      k = elem_key(z, (uint32_t)j);
+    }
+    int rk = 0;
+    for (int t = 0; t < g; ++t) rk += __shfl_sync(0xffffffffu, k, t) > k;
+    if (tid < g && rk < n) {
+      a.out_topk_ids[(int64_t)row * n + rk] = j;
+      a.out_topk_logprobs[(int64_t)row * n + rk] = (z - m_t) - lnS;
+    }
+    if (tid == 0 && g != n) *err |= kErrInternal;
+  }
+  __syncthreads();
+}
+
+__device__ void finish_row(const RowArgs& a, int row, const RowParams& P, const RowCfg& c,
+                           uint8_t* buf, uint32_t* hist, uint32_t* list, RSmem& s) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = a.C;
+  const RowPartG* parts = a.part + (size_t)row * C;
+  // ---- the row's statistics from every CTA's partials ----
+  if (warp == 0) {
+    float xm = -INFINITY, mt = -INFINITY, sm = 0.f, bs = -INFINITY, bz = 0.f;
+    int arg = INT_MAX, bd = 0, th = INT_MIN, thn = INT_MIN, er = 0, cm = INT_MIN, ovf = 0;
+    int bj = INT_MAX, fn = 0;
+    unsigned int ct = 0u;
+    unsigned long long lk = ~0ull;
+    if (lane < C) {
+      const RowPartG* pp = parts + lane;
+      xm = __ldcg(&pp->xmax);
+      mt = xm > -INFINITY ? __fmul_rn(xm, c.inv_t) : -INFINITY;
+      sm = __ldcg(&pp->s);
+      arg = __ldcg(&pp->arg);
+      bd = __ldcg(&pp->bad);
+      th = __ldcg(&pp->thr);
+      thn = __ldcg(&pp->thr_n);
+      ct = __ldcg(&pp->catch_cnt);
+      ovf = __ldcg(&pp->ncand) > a.cand_cap;
+      er = __ldcg(&pp->err);
+      cm = __ldcg(&pp->cmax);
+      bs = __ldcg(&pp->best_s);
+      bz = __ldcg(&pp->best_z);
+      bj = __ldcg(&pp->best_j);
+      lk = __ldcg(&pp->last_key);
+      fn = __ldcg(&pp->fin);
+    }
+    const int my_cmax = cm;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            if (km & (3u << (2 * w))) {
-              const int j0 = lo + 8 * v + 2 * w;
-              const uint64_t h = pair_hash(key, j0);
-              if (km & (1u << (2 * w))) consider(x[2 * w], j0, bits_even(h));
-              if (km & (2u << (2 * w))) consider(x[2 * w + 1], j0 + 1, bits_odd(h));
-            }
-          }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float x2 = __shfl_xor_sync(0xffffffffu, xm, o);
+      const int a2 = __shfl_xor_sync(0xffffffffu, arg, o);
+      const float mt2 = __shfl_xor_sync(0xffffffffu, mt, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sm, o);
+      if (pair_better(x2, a2, xm, arg)) {
+        xm = x2;
+        arg = a2;
+      }
+      lse_combine(mt, sm, mt2, s2, kLog2e);
+      const float b2 = __shfl_xor_sync(0xffffffffu, bs, o);
+      const int j2 = __shfl_xor_sync(0xffffffffu, bj, o);
+      const float z2 = __shfl_xor_sync(0xffffffffu, bz, o);
+      if (pair_better(b2, j2, bs, bj)) {
+        bs = b2;
+        bj = j2;
+        bz = z2;
+      }
+      const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, lk, o);
+      lk = l2 < lk ? l2 : lk;
+      bd |= __shfl_xor_sync(0xffffffffu, bd, o);
+      er |= __shfl_xor_sync(0xffffffffu, er, o);
+      ovf |= __shfl_xor_sync(0xffffffffu, ovf, o);
+      th = max(th, __shfl_xor_sync(0xffffffffu, th, o));
+      thn = max(thn, __shfl_xor_sync(0xffffffffu, thn, o));
+      cm = max(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+      ct += __shfl_xor_sync(0xffffffffu, ct, o);
+      fn += __shfl_xor_sync(0xffffffffu, fn, o);
+    }
+    if (lane < C) s.delta[lane] = cm - my_cmax;
+    if (lane == 0) {
+      s.bf[0] = xm;
+      s.bf[1] = mt;
+      s.bf[2] = sm;
+      s.bf[3] = bz;
+      s.bi[0] = arg;
+      s.bi[1] = bd || xm == INFINITY;
+      s.bi[2] = th;
+      s.bi[3] = thn;
+      s.bi[4] = (int)ct;
+      s.bi[5] = er;
+      s.bi[6] = cm;
+      s.bi[7] = ovf;
+      s.bi[8] = bj;
+      s.bi[9] = fn;
+      s.ru[0] = lk;
+    }
+  }
+  __syncthreads();
+  const float xmax = s.bf[0], m_t = s.bf[1], S = s.bf[2], bz = s.bf[3];
+  const int arg = s.bi[0], bad = s.bi[1], thr = s.bi[2], thrn = s.bi[3];
+  const unsigned int catch_tot = (unsigned int)s.bi[4];
+  int err = s.bi[5];
+  const int cmax = s.bi[6], ovf = s.bi[7], bj = s.bi[8], fn = s.bi[9];
+  const unsigned long long lk = s.ru[0];
+  const float lnS = logf(S);
+  __syncthreads();
+  auto done = [&]() {};
+  if (bad || xmax == -INFINITY) {
+    write_bad(a, row, bad ? kRowNonfinite : kRowEmpty, err);
+    done();
+    return;
+  }
+  if (c.mode == kModeStats) {  // greedy, no top-n
+    if (tid == 0) write_token(a, row, P, arg, m_t, m_t, lnS, m_t, arg, 1, err);
+    done();
+    return;
+  }
+  if (c.mode == kModeAll && c.n == 0) {
+    if (tid == 0) write_token(a, row, P, bj, bz, m_t, lnS, key_z(lk), (int)key_idx(lk), fn, err);
+    done();
+    return;
+  }
+
+  // ---- the records this row needs, in shared memory ----
+  uint64_t* recs = reinterpret_cast<uint64_t*>(buf);
+  const int rcap = kFinishRecCap;
+  const int rthr = c.mode == kModeRecords ? thr : thrn;
+  int nrec = 0;
+  if (rthr != kThrNone) {
+    if (tid == 0) s.nrec = 0;
+    __syncthreads();
+    if (!ovf) {
+      // every CTA's record count, then all records in one flat sweep
+      int* ncum = s.ri;  // [C + 1] exclusive prefix of the counts
+      if (tid < 32) {
+        int v = tid < C ? __ldcg(&parts[tid].ncand) : 0;
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, inc, o);
+          if (tid >= o) inc += t;
         }
+        if (tid == 0) ncum[0] = 0;
+        if (tid < C) ncum[tid + 1] = inc;
       }
       __syncthreads();
-      // the kept (top-n) part of a boundary slot: its lowest indices here
-      const int nl = s.nlist, nln = s.nlistn;
-      const uint16_t* e16 = reinterpret_cast<const uint16_t*>(buf_at(b));
-      if (beta >= 0 && cb > 0 && cb < nb) {
-        if (nl != nb && tid == 0) err |= kErrInternal;
-        const uint32_t kth = rblock_kth_smallest(list_b, min(nl, kListCap), cb, hist, s);
-        for (int e = tid; e < min(nl, kListCap); e += kRT) {
-          const uint32_t off = list_b[e];
-          if (off <= kth) {
-            const int j = lo + (int)off;
-            consider(__uint_as_float((uint32_t)e16[off] << 16), j, noise_bits(key, j));
-          }
-        }
-        if (tid == 0) kthmax = max(kthmax, lo + (int)kth);
-      }
-      if (sn >= 0 && cnq > 0 && cnq < nnq) {
-        if (nln != nnq && tid == 0) err |= kErrInternal;
-        const uint32_t kth = rblock_kth_smallest(list_n, min(nln, kListCap), cnq, hist, s);
-        for (int e = tid; e < min(nln, kListCap); e += kRT) {
-          const uint32_t off = list_n[e];
-          if (off <= kth) push(__uint_as_float((uint32_t)e16[off] << 16), lo + (int)off);
-        }
-      }
-      VT_RTRACE(7);
-      rblock_argmax(bs, bj, bz, s);
-      kthmax = rblock_max(kthmax, s);
-      if (beta == kAllKept) {
-        lastk = rblock_min_u64(lastk, s);
-        fin = rblock_sum(fin, s);
-      }
-      if (tid == 0) {
-        RPart& pt = s.part[par];
-        pt.best_s = bs;
-        pt.best_j = bj;
-        pt.best_z = bz;
-        pt.kth_j = rank == s.rl.last_rank ? kthmax : -1;
-        pt.last_key = lastk;
-        pt.fin = fin;
-        pt.err = err;
-      }
-      VT_RTRACE(8);
-      cluster.sync();  // (3) draw partials and the top-n keys visible
-      VT_RTRACE(9);
-
-      // ---- the leader writes the row ----
-      if (leader) {
-        if (warp == 0) {  // lanes < C read the CTAs' draw partials
-          float best = -INFINITY, bzz = 0.f;
-          int bjj = INT_MAX, nfin = 0, er = 0, kjr = -1;
-          unsigned long long lk = ~0ull;
-          if (lane < C) {
-            const RPart* pp = cluster.map_shared_rank(&s.part[par], lane);
-            best = pp->best_s;
-            bjj = pp->best_j;
-            bzz = pp->best_z;
-            lk = pp->last_key;
-            nfin = pp->fin;
-            er = pp->err;
-            kjr = lane == s.rl.last_rank ? pp->kth_j : -1;
-          }
+      const int total = ncum[C];
+      const uint64_t* base = a.cand + (size_t)row * C * a.cand_cap;
+      for (int e0 = tid; e0 < total; e0 += 4 * kRT) {
+        uint64_t rec[4];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
-            const int j2 = __shfl_xor_sync(0xffffffffu, bjj, o);
-            const float z2 = __shfl_xor_sync(0xffffffffu, bzz, o);
-            if (pair_better(b2, j2, best, bjj)) {
-              best = b2;
-              bjj = j2;
-              bzz = z2;
-            }
-            const unsigned long long l2 = __shfl_xor_sync(0xffffffffu, lk, o);
-            lk = l2 < lk ? l2 : lk;
-            nfin += __shfl_xor_sync(0xffffffffu, nfin, o);
-            er |= __shfl_xor_sync(0xffffffffu, er, o);
-            kjr = max(kjr, __shfl_xor_sync(0xffffffffu, kjr, o));
-          }
-          if (lane == 0) {
-            int tok = arg_row, kj = arg_row, L3 = 1;
-            float ztok = m_t, kz = m_t;
-            er |= err_row;
-            if (!greedy) {
-              tok = bjj;
-              ztok = bzz;
-              if (beta >= 0) {
-                kz = s.rl.kth_z;
-                kj = kjr;
-                L3 = s.rl.L3;
-              } else {
-                kz = key_z(lk);
-                kj = (int)key_idx(lk);
-                L3 = nfin;
-              }
-              if (tok == INT_MAX || kj < 0) er |= kErrInternal;
-            }
-            if (n > 0 && s.gcount != n) er |= kErrInternal;
-            a.out_tokens[row] = tok;
-            if (a.out_logprobs) a.out_logprobs[row] = (ztok - m_t) - lnS;
-            a.row_status[row] = kRowOk;
-            a.dbg_kth_value[row] = kz;
-            a.dbg_kth_index[row] = kj;
-            a.dbg_kept[row] = L3;
-            a.seeds[row] += kSeedStep;
-            if (P.flags & kRowDecay) {  // [TensorRT-LLM "Sampling", top-p decay]
-              DecayState& d = a.decay[row];
-              const float qd = __fmul_rn(d.p, d.decay);
-              d.p = tok == d.reset_id ? P.top_p : (qd < d.p_min ? d.p_min : qd);
-            }
-            if (er) atomicOr(a.err_word, er);
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * kRT;
+          rec[u] = ~0ull;
+          if (e < total) {
+            int r = 0;
+            while (r + 1 < C && e >= ncum[r + 1]) ++r;
+            rec[u] = __ldcg(base + (size_t)r * a.cand_cap + (e - ncum[r]));
           }
         }
-        if (n > 0 && warp == 0) {  // the top-n, ordered (value desc, index asc)
-          const int g = min(s.gcount, kGatherCap);
-          const uint64_t k = lane < g ? s.gather[lane] : 0ull;
-          int rk = 0;
-          for (int t = 0; t < g; ++t) rk += s.gather[t] > k;
-          if (lane < g && rk < n) {
-            a.out_topk_ids[(int64_t)row * n + rk] = (int)key_idx(k);
-            a.out_topk_logprobs[(int64_t)row * n + rk] = (key_z(k) - m_t) - lnS;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (rec[u] != ~0ull && rec_code(rec[u]) >= rthr) {
+            const int pos = atomicAdd(&s.nrec, 1);
+            if (pos < rcap) recs[pos] = rec[u];
           }
         }
       }
-    } while (0);
-    VT_RTRACE(10);
-#undef VT_RTRACE
-
-    // ---- row end: the next row's last elements, then its buffer is complete ----
-    if (a.aligned && rown >= 0 && tid < ntail)
-      reinterpret_cast<uint16_t*>(buf_at(b ^ 1))[tail0 + tid] = tail_v;
+    }
     __syncthreads();
-    q = qn;
+    nrec = s.nrec;
   }
-  if (err) atomicOr(a.err_word, err);
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
+  if (ovf || nrec > rcap) {
+    if (tid == 0) hand_over(a, row, m_t, lnS, xmax, arg, err);
+    done();
+    return;
+  }
+
+  // ---- counts per row slot ----
+  WalkIn w;
+  w.n = c.n;
+  w.greedy = c.greedy || c.mode == kModeAll;
+  w.topk = c.topk && !w.greedy;
+  w.topp = c.topp && !w.greedy;
+  w.minp = c.minp && !w.greedy;
+  w.need_cut = c.mode == kModeRecords && w.topk && !w.minp;
+  w.top_k = c.top_k;
+  w.top_p = c.top_p;
+  w.lmp = c.lmp;
+  w.inv_t = c.inv_t;
+  w.m_t = m_t;
+  w.cmax = cmax;
+  if (c.mode == kModeCounts) {
+    // every CTA's counts, shifted by its maximum's distance below the row's
+    unsigned int extra = 0u;
+    uint32_t cnt[kSlPT];
+#pragma unroll
+    for (int q = 0; q < kSlPT; ++q) cnt[q] = 0u;
+    const int S0 = tid * kSlPT;
+    for (int r = 0; r < C; ++r) {
+      const uint32_t* gh = a.ghist + ((size_t)row * C + r) * kSl;
+      const int d = s.delta[r];
+      uint32_t v[kSlPT];
+#pragma unroll
+      for (int q = 0; q < kSlPT; ++q) {
+        const int sl = S0 + q - d;
+        v[q] = (S0 + q < kSlCatch && sl >= 0) ? __ldcg(gh + sl) : 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < kSlPT; ++q) cnt[q] += v[q];
+      for (int sl = max(kSlCatch - d, 0) + tid; sl < kSlCatch; sl += kRT) extra += __ldcg(gh + sl);
+    }
+#pragma unroll
+    for (int q = 0; q < kSlPT; ++q) hist[S0 + q] = cnt[q];
+    w.catch_row = catch_tot + (unsigned int)rblock_sum((int)extra, s);
+    w.Smax = kSlCatch - 1;
+    w.full = true;
+  } else {
+    uint4* h4 = reinterpret_cast<uint4*>(hist);
+    for (int k = tid; k < kSl / 4; k += kRT) h4[k] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    int beyond = 0;
+    for (int e = tid; e < nrec; e += kRT) {
+      const int sl = cmax - rec_code(recs[e]);
+      if (sl < kSlCatch) atomicAdd(&hist[sl], 1u);
+      else ++beyond;
+    }
+    w.catch_row = (unsigned int)rblock_sum(beyond, s);
+    const long long Sstar = rthr == kThrAll ? (long long)INT_MAX : (long long)cmax - rthr;
+    w.full = Sstar >= kSlCatch;
+    w.Smax = (int)(Sstar < kSlCatch - 1 ? Sstar : kSlCatch - 1);
+  }
+  __syncthreads();
+  walk_slots(w, hist, s);
+  const RRes R = s.res;
+  // counts the later steps need, before the histogram is reused as scratch
+  const int nsn = R.sn >= 0 ? (int)hist[R.sn] : 0;
+  const int nbeta = R.beta >= 0 ? (int)hist[R.beta] : 0;
+  __syncthreads();
+  bool give = R.action != 0;
+  if (R.sn >= 0 && R.cn < nsn && nsn > kListCap) give = true;
+  if (c.mode == kModeRecords && R.beta >= 0 && R.qk < nbeta && nbeta > kListCap) give = true;
+  if (give) {
+    if (tid == 0) hand_over(a, row, m_t, lnS, xmax, arg, err);
+    done();
+    return;
+  }
+  if (c.n > 0) write_topn(a, row, c, recs, nrec, cmax, R.sn, R.cn, nsn, m_t, lnS, list, hist, s, &err);
+
+  if (c.mode == kModeCounts) {
+    // the draw kernel finishes the row: each CTA's share of the boundary slot
+    if (tid < C) {
+      const int d = s.delta[tid];
+      const int sl = R.beta - d;
+      s.ri[tid] = (sl >= 0 && sl < kSlCatch) ? (int)__ldcg(a.ghist + ((size_t)row * C + tid) * kSl + sl) : 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      RowWalk W;
+      W.action = 0;
+      W.beta = R.beta;
+      W.L3 = R.L3;
+      W.kth_z = R.kth_z;
+      W.m_t = m_t;
+      W.lnS = lnS;
+      W.cmax = cmax;
+      W.last_rank = -1;
+      int pre = 0;
+      bool ok = R.beta >= 0;
+      for (int r = 0; r < C; ++r) {
+        const int nb = s.ri[r];
+        const int cb = min(max(R.qk - pre, 0), nb);
+        if (pre < R.qk && R.qk <= pre + nb) W.last_rank = r;
+        if (cb > 0 && cb < nb && nb > kListCap) ok = false;
+        W.cb[r] = cb;
+        W.nb[r] = nb;
+        pre += nb;
+      }
+      if (W.last_rank < 0) ok = false;
+      if (!ok) {
+        hand_over(a, row, m_t, lnS, xmax, arg, err);
+      } else {
+        a.walk[row] = W;
+        __threadfence();
+        a.flist[atomicAdd(&a.fctl[0], 1u)] = row;
+        if (err) atomicOr(a.err_word, err);
+      }
+    }
+    done();
+    return;
+  }
+  if (c.mode == kModeAll || c.greedy) {
+    if (tid == 0) {
+      if (c.greedy) write_token(a, row, P, arg, m_t, m_t, lnS, m_t, arg, 1, err);
+      else write_token(a, row, P, bj, bz, m_t, lnS, key_z(lk), (int)key_idx(lk), fn, err);
+    }
+    done();
+    return;
+  }
+
+  // ---- records: the draw over the kept set ----
+  const int code_b = cmax - R.beta;
+  const bool all_b = R.qk == nbeta;
+  const uint64_t key = row_key(a.seeds[row], row);
+  Draw dr(m_t);
+  int kthj = -1;
+  if (tid == 0) s.nlist = 0;
+  __syncthreads();
+  for (int e = tid; e < nrec; e += kRT) {
+    const uint64_t r = recs[e];
+    const int code = rec_code(r);
+    const int j = rec_j(r);
+    if (code > code_b || (code == code_b && all_b)) {
+      dr.offer(__fmul_rn(rec_x(r), c.inv_t), j, noise_bits(key, j));
+      if (code == code_b) kthj = max(kthj, j);
+    } else if (code == code_b) {
+      const int pos = atomicAdd(&s.nlist, 1);
+      if (pos < kListCap) list[pos] = (uint32_t)j;
+    }
+  }
+  __syncthreads();
+  if (!all_b) {
+    const uint32_t kth = rblock_kth_smallest(list, min(s.nlist, kListCap), R.qk, hist, s);
+    for (int e = tid; e < nrec; e += kRT) {
+      const uint64_t r = recs[e];
+      const int j = rec_j(r);
+      if (rec_code(r) == code_b && (uint32_t)j <= kth)
+        dr.offer(__fmul_rn(rec_x(r), c.inv_t), j, noise_bits(key, j));
+    }
+    kthj = (int)kth;
+  }
+  rblock_argmax(dr.bs, dr.bj, dr.bz, s);
+  kthj = rblock_max(kthj, s);
+  if (tid == 0) {
+    if (dr.bj == INT_MAX || kthj < 0) err |= kErrInternal;
+    write_token(a, row, P, dr.bj, dr.bz, m_t, lnS, R.kth_z, kthj, R.L3, err);
+  }
+  done();
+}
+
+// ---------------------------------------------------------------------------
+// the draw kernel: rows whose kept set needs every element
+// ---------------------------------------------------------------------------
+// One CTA per (listed row, slice).  Elements above the boundary value x_b are
+// kept, and of those equal to it the first cb (by index) of this CTA; the
+// row's last CTA combines the best scores and writes the token.  The grid's
+// last CTA clears the list for the next call.
+__global__ void __launch_bounds__(kRT, 2) row_draw_kernel(const RowArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  __shared__ RSmem s;
+  const int tid = threadIdx.x;
+  const int C = a.C;
+  const int i = (int)blockIdx.x / C, rank = (int)blockIdx.x % C;
+  const int nf = (int)__ldcg(&a.fctl[0]);
+  if (i < nf) {
+    const int row = __ldcg(&a.flist[i]);
+    const RowWalk* wp = a.walk + row;
+    const int beta = __ldcg(&wp->beta), L3 = __ldcg(&wp->L3), cmax = __ldcg(&wp->cmax);
+    const int cb = __ldcg(&wp->cb[rank]), nb = __ldcg(&wp->nb[rank]);
+    const int last_rank = __ldcg(&wp->last_rank);
+    const float m_t = __ldcg(&wp->m_t), lnS = __ldcg(&wp->lnS), kth_z = __ldcg(&wp->kth_z);
+    const int lo = rank * a.slice;
+    const int nel = max(0, min(lo + a.slice, a.V) - lo);
+    const int nvec = (nel + 7) >> 3;
+    uint8_t* buf = dsm;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(dsm + a.buf_bytes);
+    uint32_t* list = hist + kSl;
+    unsigned long long* tr = a.trace ? a.trace + ((size_t)row * C + rank) * kTraceSlots : nullptr;
+    if (tr && tid == 0) tr[6] = global_timer_ns();
+    int err = load_slice(a, row, lo, nel, nvec, buf, s) ? 0 : kErrTimeout;
+    if (tr && tid == 0) tr[7] = global_timer_ns();
+    const RowParams P = a.params[row];
+    const float inv_t = P.inv_t;
+    const uint4* sv = reinterpret_cast<const uint4*>(buf);
+    const float xb = bcode_value(cmax - beta);
+    const bool all_b = cb == nb;
+    const uint64_t key = row_key(a.seeds[row], row);
+    Draw d(m_t);
+    int kthj = -1;
+    if (tid == 0) s.nlist = 0;
+    __syncthreads();
+    for (int v = tid; v < nvec; v += kRT) {
+      const uint4 qv = sv[v];
+      const uint32_t m2 = bmax2(bmax2(qv.x, qv.y), bmax2(qv.z, qv.w));
+      if (!(fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u)) >= xb)) continue;
+      float x[8];
+      unpack8(qv, x);
+      uint32_t km = 0u, eq = 0u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        km |= (uint32_t)(x[q] > xb) << q;
+        eq |= (uint32_t)(x[q] == xb) << q;
+      }
+      while (eq) {  // elements of the boundary slot (few)
+        const int q = __ffs(eq) - 1;
+        eq &= eq - 1u;
+        const int j = lo + 8 * v + q;
+        if (all_b) {
+          km |= 1u << q;
+          kthj = max(kthj, j);
+        } else if (cb > 0) {
+          const int pos = atomicAdd(&s.nlist, 1);
+          if (pos < kListCap) list[pos] = (uint32_t)j;
+        }
+      }
+      if (km) {
+        // the vector's four hashes together (independent chains overlap); an
+        // element can beat the best only if its noise clears the bound the
+        // vector's own maximum sets (one ex2 per vector, one compare each)
+        uint64_t h[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) h[w] = pair_hash(key, lo + 8 * v + 2 * w);
+        const float zv = __fmul_rn(fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u)), inv_t);
+        const uint32_t bv = d.bound(zv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t bits = (q & 1) ? bits_odd(h[q >> 1]) : bits_even(h[q >> 1]);
+          if ((km & (1u << q)) && bits >= bv) d.offer(__fmul_rn(x[q], inv_t), lo + 8 * v + q, bits);
+        }
+      }
+    }
+    __syncthreads();
+    if (!all_b && cb > 0) {
+      const int nl = min(s.nlist, kListCap);
+      if (s.nlist != nb && tid == 0) err |= kErrInternal;
+      const uint32_t kth = rblock_kth_smallest(list, nl, cb, hist, s);
+      const uint16_t* e16 = reinterpret_cast<const uint16_t*>(buf);
+      for (int e = tid; e < nl; e += kRT) {
+        const int j = (int)list[e];
+        if ((uint32_t)j <= kth)
+          d.offer(__fmul_rn(__uint_as_float((uint32_t)e16[j - lo] << 16), inv_t), j,
+                  noise_bits(key, j));
+      }
+      kthj = (int)kth;
+    }
+    if (tr && tid == 0) tr[8] = global_timer_ns();
+    rblock_argmax(d.bs, d.bj, d.bz, s);
+    kthj = rblock_max(kthj, s);
+    if (tid == 0) {
+      RowPartG& pt = a.part[(size_t)row * C + rank];
+      pt.best_s = d.bs;
+      pt.best_j = d.bj;
+      pt.best_z = d.bz;
+      pt.kth_j = rank == last_rank ? kthj : -1;
+      pt.err = err;
+      __threadfence();
+      s.last = atomicAdd(&a.ctl[row], 1u) == (unsigned int)(C - 1);
+    }
+    __syncthreads();
+    if (s.last && tid == 0) {
+      __threadfence();
+      float bs = -INFINITY, bz = 0.f;
+      int bj = INT_MAX, kj = -1, er = 0;
+      for (int r = 0; r < C; ++r) {
+        const RowPartG* pp = a.part + (size_t)row * C + r;
+        const float b2 = __ldcg(&pp->best_s);
+        const int j2 = __ldcg(&pp->best_j);
+        if (pair_better(b2, j2, bs, bj)) {
+          bs = b2;
+          bj = j2;
+          bz = __ldcg(&pp->best_z);
+        }
+        if (r == last_rank) kj = __ldcg(&pp->kth_j);
+        er |= __ldcg(&pp->err);
+      }
+      if (bj == INT_MAX || kj < 0) er |= kErrInternal;
+      write_token(a, row, P, bj, bz, m_t, lnS, kth_z, kj, L3, er);
+      a.ctl[row] = 0u;
+      if (tr) tr[9] = global_timer_ns();
+    }
+  }
+  // the grid's last CTA clears the list for the next call
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&a.fctl[1], 1u) == gridDim.x - 1) {
+      a.fctl[2] = a.fctl[0];
+      a.fctl[0] = 0u;
+      a.fctl[1] = 0u;
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace
@@ -1385,70 +1648,56 @@ __global__ void __launch_bounds__(kRT, 1) rows_kernel(const RowArgs a) {
 // ---------------------------------------------------------------------------
 namespace vt {
 
+constexpr size_t kFinishSmem = (size_t)kSl * 4 + (size_t)kListCap * 4 + (size_t)kFinishRecCap * 8;
+
 RowPlan plan_rows(int B, int V) {
+  (void)B;
   RowPlan p{};
-  int dev = 0, optin = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return p;
-  const size_t fixed = (size_t)kSl * 4 + (size_t)2 * kListCap * 4;
-  const size_t room = (size_t)optin > sizeof(RSmem) ? (size_t)optin - sizeof(RSmem) : 0;
-  for (int C = 1; C <= kRMaxC; C <<= 1) {
-    int slice = (V + C - 1) / C;
-    slice = (slice + 7) & ~7;
-    const uint32_t buf = (uint32_t)(((size_t)slice * 2 + 127) & ~(size_t)127);
-    const size_t smem = 2 * (size_t)buf + fixed + (((size_t)slice / 8 * 2 + 15) & ~(size_t)15);
-    if (smem > room) continue;
-    cudaError_t e = cudaFuncSetAttribute(rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(rows_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) {
-      (void)cudaGetLastError();
-      return p;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C, 1, 1);
-    cfg.blockDim = dim3(kRT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, rows_kernel, &cfg) != cudaSuccess ||
-        nclusters < 1) {
-      (void)cudaGetLastError();
-      continue;
-    }
-    p.cluster = C;
-    p.slice = slice;
-    p.buf_bytes = buf;
-    p.smem = smem;
-    p.clusters = nclusters < B ? nclusters : B;
+  const int C = (V + kSliceMax - 1) / kSliceMax;
+  if (V < 1 || C > kRowMaxC) return p;
+  int slice = (V + C - 1) / C;
+  slice = (slice + 7) & ~7;
+  const uint32_t buf = (uint32_t)(((size_t)slice * 2 + 127) & ~(size_t)127);
+  const size_t vbytes = (((size_t)slice / 8 * 2 + 15) & ~(size_t)15);
+  const size_t smem = buf + (size_t)kSl * 4 + (vbytes > (size_t)kListCap * 4 ? vbytes : (size_t)kListCap * 4);
+  if (cudaFuncSetAttribute(row_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(row_draw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess) {
+    (void)cudaGetLastError();
     return p;
   }
+  if (cudaFuncSetAttribute(row_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kFinishSmem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return p;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_pass_kernel, kRT, smem) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    (void)cudaGetLastError();
+    return p;
+  }
+  p.cluster = C;
+  p.slice = slice;
+  p.buf_bytes = buf;
+  p.smem = smem;
+  p.clusters = per_sm;
   return p;
 }
 
-cudaError_t launch_rows(const RowArgs& args, const RowPlan& plan, cudaStream_t stream) {
-  if (plan.cluster < 1 || plan.clusters < 1) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(plan.clusters * plan.cluster), 1, 1);
-  cfg.blockDim = dim3(kRT, 1, 1);
-  cfg.dynamicSmemBytes = plan.smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = plan.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rows_kernel, args);
+cudaError_t launch_rows(const RowArgs& args, const RowPlan& plan, int draw_rows,
+                        cudaStream_t stream) {
+  if (plan.cluster < 1 || args.norder < 1) return cudaErrorInvalidConfiguration;
+  row_pass_kernel<<<(unsigned)(args.norder * plan.cluster), kRT, plan.smem, stream>>>(args);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  row_finish_kernel<<<(unsigned)args.norder, kRT, kFinishSmem, stream>>>(args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || draw_rows < 1) return e;
+  row_draw_kernel<<<(unsigned)(draw_rows * plan.cluster), kRT, plan.smem, stream>>>(args);
+  return cudaGetLastError();
 }
 
 }  // namespace vt

@@ -45,7 +45,16 @@ struct vt_sampler {
   int32_t* d_slow_list = nullptr;  // [2][max_batch]: one list per launch pair
   uint32_t* d_slow_ctl = nullptr;  // [2][4]
   int32_t* d_rows = nullptr;       // [max_batch]: main rows, then side rows
-  int32_t* d_order = nullptr;      // [max_batch]: rows in the row kernel's order
+  int32_t* d_order = nullptr;      // [max_batch]: rows in the row kernels' order
+  // scratch of the row kernels
+  vt::RowPartG* d_rpart = nullptr;  // [max_batch][row_cmax]
+  uint64_t* d_rcand = nullptr;      // [max_batch][row_cmax][kRowCandCap]
+  uint32_t* d_rhist = nullptr;      // [max_batch][row_cmax][kRowSlots]
+  uint32_t* d_rctl = nullptr;       // [max_batch]
+  int32_t* d_rflist = nullptr;      // [max_batch]
+  uint32_t* d_rfctl = nullptr;      // [4]
+  vt::RowWalk* d_rwalk = nullptr;   // [max_batch]
+  int row_cmax = 0;
   float2* d_probs_part = nullptr;  // (max, exp-sum) partials of the filtered distribution
   size_t probs_part_cap = 0;
   // the side stream: rows routed straight to the selection kernel run there,
@@ -91,6 +100,8 @@ struct vt_sampler {
 };
 
 namespace {
+
+constexpr int kRowCandCap = 4096;  // candidate records per row-kernel CTA
 
 int set_err(vt_sampler* h, int code, const char* fmt, ...) {
   if (h) {
@@ -150,6 +161,13 @@ void free_all(vt_sampler* h) {
   dfree(h->d_slow_ctl);
   dfree(h->d_rows);
   dfree(h->d_order);
+  dfree(h->d_rpart);
+  dfree(h->d_rcand);
+  dfree(h->d_rhist);
+  dfree(h->d_rctl);
+  dfree(h->d_rflist);
+  dfree(h->d_rfctl);
+  dfree(h->d_rwalk);
   dfree(h->d_probs_part);
   if (h->h_rows) cudaFreeHost(h->h_rows);
   if (h->h_order) cudaFreeHost(h->h_order);
@@ -246,6 +264,18 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_slow_ctl, 8 * sizeof(uint32_t));
   dal((void**)&h->d_rows, B * sizeof(int32_t));
   dal((void**)&h->d_order, B * sizeof(int32_t));
+  // the row kernels: CTAs per row of the largest bf16 row (76 KB slices)
+  h->row_cmax = std::min(vt::kRowMaxC, (cfg->max_vocab + 38911) / 38912);
+  {
+    const size_t RC = B * (size_t)h->row_cmax;
+    dal((void**)&h->d_rpart, RC * sizeof(vt::RowPartG));
+    dal((void**)&h->d_rcand, RC * (size_t)kRowCandCap * sizeof(uint64_t));
+    dal((void**)&h->d_rhist, RC * (size_t)vt::kRowSlots * sizeof(uint32_t));
+    dal((void**)&h->d_rctl, B * sizeof(uint32_t));
+    dal((void**)&h->d_rflist, B * sizeof(int32_t));
+    dal((void**)&h->d_rfctl, 4 * sizeof(uint32_t));
+    dal((void**)&h->d_rwalk, B * sizeof(vt::RowWalk));
+  }
   // B rows of ceil(V / max range) + 1 splits, plus the splits that small
   // batches add to fill the GPU (plan_probs never asks for more)
   h->probs_part_cap = B * (size_t)((cfg->max_vocab + vt::kProbsMaxRange - 1) /
@@ -279,6 +309,8 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_slow_ctl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_rctl, 0, B * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(h->d_rfctl, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_seeds, 0, B * sizeof(uint64_t)) != cudaSuccess ||
       cudaMemset(h->d_status, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
@@ -599,14 +631,14 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     a.trace_ctas = a.trace ? h->trace_ctas : 0;
     return a;
   };
-  // bf16 rows without penalties: the persistent row kernel, then the selection
-  // kernel for the rows it hands over (counts appended by a third launch)
+  // bf16 rows without penalties: the row kernels, then the selection kernel for
+  // the rows they hand over (counts appended by one more launch)
   const vt::RowPlan* rplan = nullptr;
   if (dtype == VT_DTYPE_BF16 && !any_pen && h->path == 0) {
     auto key = std::make_pair(B, V);
     auto it = h->row_plans.find(key);
     if (it == h->row_plans.end()) it = h->row_plans.emplace(key, vt::plan_rows(B, V)).first;
-    if (it->second.cluster > 0) rplan = &it->second;
+    if (it->second.cluster > 0 && it->second.cluster <= h->row_cmax) rplan = &it->second;
   }
   // other bf16 calls over every row split the rows between the two streams
   const bool split = !rplan && dtype == VT_DTYPE_BF16 && B == h->params_B && h->n_side > 0 &&
@@ -620,6 +652,17 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     sa.update_counts = 0;
     sa.trace = nullptr;
     sa.trace_ctas = 0;
+    // rows whose kept set may need every element go through the draw kernel:
+    // sampled rows with a filter (top-k, top-p, min-p, top-p decay) other than
+    // a top-k of at most 1024 (a superset of the rows the pass kernel lists)
+    int draw_rows = 0;
+    for (int r = 0; r < B; ++r) {
+      const uint32_t f = h->row_flags[r];
+      const int k = h->h_params[r].top_k;
+      const bool topk = k > 1 && k < V;
+      const bool filtered = topk || (f & (vt::kRowTopP | vt::kRowMinP | vt::kRowDecay));
+      if (!(f & vt::kRowGreedy) && filtered && !(topk && k <= 1024)) ++draw_rows;
+    }
     vt::RowArgs ra;
     std::memset(&ra, 0, sizeof ra);
     ra.logits = logits;
@@ -628,6 +671,7 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     ra.V = V;
     ra.order = h->d_order;
     ra.norder = h->params_B;
+    ra.C = rplan->cluster;
     ra.n_logprobs = n;
     ra.slice = rplan->slice;
     ra.aligned = sa.aligned;
@@ -647,12 +691,21 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     ra.slow = h->d_slow;
     ra.slow_list = sa.slow_list;
     ra.slow_ctl = sa.slow_ctl;
-    // the phase trace is laid out by row (B rows of rplan->cluster CTAs)
-    ra.trace = (h->trace && (int64_t)B * rplan->cluster <= h->trace_ctas) ? h->trace : nullptr;
-    VT_CK(h, vt::launch_rows(ra, *rplan, st));
+    ra.part = h->d_rpart;
+    ra.cand = h->d_rcand;
+    ra.cand_cap = kRowCandCap;
+    ra.ghist = h->d_rhist;
+    ra.ctl = h->d_rctl;
+    ra.flist = h->d_rflist;
+    ra.fctl = h->d_rfctl;
+    ra.walk = h->d_rwalk;
+    // the phase trace is laid out by row (params_B rows of C CTAs)
+    ra.trace = (h->trace && (int64_t)h->params_B * rplan->cluster <= h->trace_ctas) ? h->trace
+                                                                                     : nullptr;
+    VT_CK(h, vt::launch_rows(ra, *rplan, draw_rows, st));
     if (h->phase_event) VT_CK(h, cudaEventRecord(h->phase_event, st));
     VT_CK(h, vt::launch_select_handed(sa, *plan, dtype, st));
-    h->last_launches = 2;
+    h->last_launches = draw_rows > 0 ? 3 : 2;
     if (update_counts && !out_probs) {
       VT_CK(h, vt::launch_append(h->d_hist, h->d_hist_len, sa.hist_cap, out_tokens, h->d_status,
                                  B, st));
