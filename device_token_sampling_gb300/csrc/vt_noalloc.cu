@@ -22,7 +22,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "vt_device.cuh"
 #include "vt_kernels.h"
@@ -62,6 +64,10 @@ struct DeviceSlot {
   unsigned char* scratch = nullptr;  // device address of vt_noalloc_scratch
   int num_sms = 0;
   size_t smem_optin = 0;
+  // launch plans already prepared on this device, by (B, V, dtype): planning
+  // sets kernel attributes and queries occupancy, which a decode loop should
+  // not pay on every step (host memory only)
+  std::map<std::tuple<int, int, int>, vt::LaunchPlan> plans;
 };
 
 std::mutex g_setup_mutex;
@@ -178,14 +184,25 @@ extern "C" int vt_sample_noalloc(int32_t device, const void* logits, int32_t dty
   if (rc != VT_OK) return rc;
 
   const int es = dtype == VT_DTYPE_F32 ? 4 : 2;
-  vt::LaunchPlan plan = vt::plan_sample(B, V, es, false, dtype, slot->num_sms);
-  if (plan.smem > slot->smem_optin)
-    return fail(errbuf, errbuf_len, VT_ERR_CAPACITY, "V=%d needs %zu B of shared memory per CTA",
-                V, plan.smem);
-  cudaError_t e = vt::prepare_sample(plan, dtype);
-  if (e != cudaSuccess)
-    return fail(errbuf, errbuf_len, VT_ERR_CUDA, "cannot prepare a %d-CTA cluster plan: %s",
-                plan.cluster, cudaGetErrorString(e));
+  vt::LaunchPlan plan;
+  cudaError_t e = cudaSuccess;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    const auto key = std::make_tuple(B, V, dtype);
+    auto it = slot->plans.find(key);
+    if (it == slot->plans.end()) {
+      vt::LaunchPlan fresh = vt::plan_sample(B, V, es, false, dtype, slot->num_sms);
+      if (fresh.smem > slot->smem_optin)
+        return fail(errbuf, errbuf_len, VT_ERR_CAPACITY,
+                    "V=%d needs %zu B of shared memory per CTA", V, fresh.smem);
+      e = vt::prepare_sample(fresh, dtype);
+      if (e != cudaSuccess)
+        return fail(errbuf, errbuf_len, VT_ERR_CUDA, "cannot prepare a %d-CTA cluster plan: %s",
+                    fresh.cluster, cudaGetErrorString(e));
+      it = slot->plans.emplace(key, fresh).first;
+    }
+    plan = it->second;
+  }
 
   cudaStream_t st = (cudaStream_t)stream;
   unsigned char* scr = slot->scratch;
@@ -225,7 +242,16 @@ extern "C" int vt_sample_noalloc(int32_t device, const void* logits, int32_t dty
     if (e != cudaSuccess)
       return fail(errbuf, errbuf_len, VT_ERR_CUDA, "parameter upload: %s", cudaGetErrorString(e));
   }
-  e = cudaMemcpyAsync(d_seeds, seed, (size_t)B * sizeof(uint64_t), cudaMemcpyHostToDevice, st);
+  // The seeds go through the same kind of host-stack chunk, so that the call
+  // has read the caller's array before it returns even when that array is
+  // pinned (a copy straight from pinned memory would still be in flight).
+  uint64_t hs[kUploadChunk];
+  for (int r0 = 0; r0 < B && e == cudaSuccess; r0 += kUploadChunk) {
+    const int m = B - r0 < kUploadChunk ? B - r0 : kUploadChunk;
+    for (int i = 0; i < m; ++i) hs[i] = seed[r0 + i];
+    e = cudaMemcpyAsync(d_seeds + r0, hs, (size_t)m * sizeof(uint64_t), cudaMemcpyHostToDevice,
+                        st);
+  }
   // What must start at zero: the rows' count-table lengths (no penalties, so
   // no table), the hand-over counters between the two kernels and the device
   // error word (the last three are contiguous).

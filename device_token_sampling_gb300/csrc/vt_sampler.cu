@@ -13,6 +13,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <algorithm>
 #include <map>
@@ -102,6 +103,21 @@ struct vt_sampler {
 namespace {
 
 constexpr int kRowCandCap = 4096;  // candidate records per row-kernel CTA
+
+// Host-side fault injection for the failure-path tests, read at each call:
+//   VT_FAULT_INJECT=alloc:<n>  the n-th device allocation of vt_sampler_create
+//                              (0-based) fails as if the device were full;
+//   VT_FAULT_INJECT=upload     the parameter upload of vt_reset_params fails.
+// Nothing on the device is made to fault.
+int fault_alloc_index() {
+  const char* e = std::getenv("VT_FAULT_INJECT");
+  if (e && std::strncmp(e, "alloc:", 6) == 0) return std::atoi(e + 6);
+  return -1;
+}
+bool fault_upload() {
+  const char* e = std::getenv("VT_FAULT_INJECT");
+  return e && std::strcmp(e, "upload") == 0;
+}
 
 int set_err(vt_sampler* h, int code, const char* fmt, ...) {
   if (h) {
@@ -240,8 +256,10 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   const size_t H = (size_t)(cfg->max_history > 0 ? cfg->max_history : 1);
   const size_t n = (size_t)cfg->max_logprobs;
   bool ok = true;
+  const int fail_at = fault_alloc_index();
+  int nalloc = 0;
   auto dal = [&](void** p, size_t bytes) {
-    if (ok && cudaMalloc(p, bytes) != cudaSuccess) ok = false;
+    if (ok && (nalloc++ == fail_at || cudaMalloc(p, bytes) != cudaSuccess)) ok = false;
   };
   auto hal = [&](void** p, size_t bytes) {
     if (ok && cudaMallocHost(p, bytes) != cudaSuccess) ok = false;
@@ -451,6 +469,10 @@ int vt_reset_params_ex(vt_sampler* h, int32_t B, const float* temperature, const
   };
   for (int r = 0; r < B; ++r) h->h_order[r] = r;
   std::stable_sort(h->h_order, h->h_order + B, [&](int x, int y) { return cost(x) > cost(y); });
+  // A failed upload leaves the device parameters undefined: the handle then
+  // counts as never reset (vt_sample returns VT_ERR_STATE until the next reset).
+  h->params_B = 0;
+  if (fault_upload()) return set_err(h, VT_ERR_CUDA, "parameter upload failed (injected fault)");
   VT_CK(h, cudaMemcpyAsync(h->d_params, h->h_params, (size_t)B * sizeof(vt::RowParams),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_seeds, h->h_seeds, (size_t)B * sizeof(uint64_t),

@@ -416,15 +416,44 @@ def sample_noalloc(logits, temperature, top_k, top_p, min_p, seed, out_tokens,
             raise ValueError(f"unsupported logits dtype {logits.dtype}")
     B, ld = logits.shape[0], logits.stride(0)
     V = logits.shape[1] if V is None else V
-    arr = lambda x, t: np.ascontiguousarray(np.asarray(x, dtype=t))  # noqa: E731
+    n = int(num_logprobs)
+    arr = lambda x, t: np.ascontiguousarray(np.asarray(x, dtype=t)).reshape(-1)  # noqa: E731
     T, K, Pp, MP = arr(temperature, np.float32), arr(top_k, np.int32), arr(top_p, np.float32), \
         arr(min_p, np.float32)
     S = arr(seed, np.uint64)
+    # the library reads B entries of every host array and writes B rows of
+    # every output: check them here, where a short buffer is still an error
+    for name, a in (("temperature", T), ("top_k", K), ("top_p", Pp), ("min_p", MP),
+                    ("seed", S)):
+        if a.shape[0] < B:
+            raise ValueError(f"{name} has {a.shape[0]} entries, need {B}")
+
+    def check_out(t, name, dt, cols=None, required=False):
+        if t is None:
+            if required:
+                raise ValueError(f"{name} is required")
+            return
+        if not t.is_cuda or t.device != logits.device:
+            raise ValueError(f"{name} must be a CUDA tensor on {logits.device}")
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}, got {t.dtype}")
+        want = (B,) if cols is None else (B, cols)
+        if tuple(t.shape) != want or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor of shape {want}")
+
+    check_out(out_tokens, "out_tokens", torch.int32, required=True)
+    check_out(out_logprobs, "out_logprobs", torch.float32)
+    check_out(row_status, "row_status", torch.int32)
+    if n > 0:
+        check_out(out_topk_ids, "out_topk_ids", torch.int32, n, required=True)
+        check_out(out_topk_logprobs, "out_topk_logprobs", torch.float32, n, required=True)
     tp = lambda t: None if t is None else P(t.data_ptr())  # noqa: E731
     err = C.create_string_buffer(256)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
     rc = lib.vt_sample_noalloc(logits.device.index,
                                P(logits.data_ptr()), dtype, B, V, ld, _np_ptr(T), _np_ptr(K),
-                               _np_ptr(Pp), _np_ptr(MP), _np_ptr(S), num_logprobs,
+                               _np_ptr(Pp), _np_ptr(MP), _np_ptr(S), n,
                                tp(out_tokens), tp(out_logprobs), tp(out_topk_ids),
                                tp(out_topk_logprobs), tp(row_status), 1 if synchronize else 0,
                                _stream_ptr(stream), err, len(err))

@@ -107,7 +107,12 @@ void vt_sampler_destroy(vt_sampler* handle);
  *   presence, frequency  finite (0 disables).
  *   repetition   finite and > 0 (1 disables).
  * Errors: VT_ERR_INVALID_ARG (any value out of range; nothing uploaded),
- * VT_ERR_CAPACITY (B > max_batch), VT_ERR_CUDA. */
+ * VT_ERR_CAPACITY (B > max_batch), VT_ERR_CUDA (the upload failed: the handle
+ * then holds no parameters, and vt_sample returns VT_ERR_STATE until the next
+ * successful reset).  For tests of these failure paths, the environment
+ * variable VT_FAULT_INJECT=upload makes the upload fail, and
+ * VT_FAULT_INJECT=alloc:<n> makes the n-th (0-based) device allocation of
+ * vt_sampler_create fail; nothing on the device is made to fault. */
 int vt_reset_params(vt_sampler* handle, int32_t B, const float* temperature,
                     const int32_t* top_k, const float* top_p, const float* min_p,
                     const float* presence, const float* frequency,
