@@ -59,8 +59,8 @@ def make_workload(name: str, rank: int) -> W.Workload:
         return W.b64(seed=2 + 1000 * rank)
     if name == "tiny":
         return W.tiny(seed=1000 * rank)
-    if name == "large":
-        return W.large(seed=4 + 1000 * rank)
+    if name == "large":  # the step logits are made on the device (large_step_device)
+        return W.large(seed=4 + 1000 * rank, with_logits=False)
     raise ValueError(name)
 
 
@@ -237,11 +237,16 @@ def run_reference(args, w: W.Workload):
     import oracle
     oracle.build()
     order = np.arange(w.B)
+    if w.logits.shape[0] == 0:  # Large: its step logits are made on the device; here 64
+        rows = 64              # host rows of the same distribution stand in
+        w.logits = W.pad_rows(W.peaked_rows(np.random.default_rng(1000), rows, w.V), w.V,
+                              w.dtype)
+        order = np.arange(rows)
     for i in range(args.warmup):
-        oracle.sample_workload(w, rows=[int(order[i % w.B])])
+        oracle.sample_workload(w, rows=[int(order[i % len(order)])])
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.sample_workload(w, rows=[int(order[(args.warmup + i) % w.B])])
+        oracle.sample_workload(w, rows=[int(order[(args.warmup + i) % len(order)])])
     dt = time.perf_counter() - t0
     value = args.steps / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
@@ -269,6 +274,122 @@ def workload_config(w: W.Workload):
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
+
+def large_step_device(step: int, B: int, V: int, dev, rank: int = 0):
+    """The Large workload's step logits, made on the device: N(0, 1.5) plus 8
+    positions per row raised by U(8, 12), from seed 1000 + step (per rank)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + step + 1_000_000 * rank)
+    x = torch.randn(B, V, device=dev, generator=g) * 1.5
+    pos = torch.randint(0, V, (B, 8), device=dev, generator=g)
+    add = torch.rand(B, 8, device=dev, generator=g) * 4.0 + 8.0
+    x.scatter_add_(1, pos, add)
+    return x
+
+
+def run_gpu_decode(args, w: W.Workload):
+    """Large: consecutive decode steps, each on its own logits made on the device
+    outside the timed region; every step is timed with events on the launching
+    stream and the counts grow by the drawn tokens."""
+    import torch
+    import torch.distributed as dist
+
+    from device_token_sampling_gb300 import sampler as S
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    B, V, n = w.B, w.V, w.num_logprobs
+    hist = int(np.max(np.diff(w.prompt_offsets) + np.diff(w.output_offsets)))
+    s = S.Sampler(max_batch=B, max_vocab=V, max_logprobs=n,
+                  max_history=hist + args.steps + args.warmup + 64, device=local, host_io=True)
+    s.reset_workload(w)
+    stream = torch.cuda.Stream(device=dev)
+    out = (torch.empty(B, dtype=torch.int32, device=dev),
+           torch.empty(B, dtype=torch.float32, device=dev),
+           torch.empty((B, n), dtype=torch.int32, device=dev),
+           torch.empty((B, n), dtype=torch.float32, device=dev))
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            x = large_step_device(10_000 + i, B, V, dev, rank)
+            s.sample(x, V=V, num_logprobs=n, update_counts=True, out=out, stream=stream)
+    stream.synchronize()
+    s.check_device_errors()
+    s.reset_workload(w)  # the timed decode starts from the workload's state
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for t in range(args.steps):
+            x = large_step_device(t, B, V, dev, rank)  # outside the timed region
+            e0, e1 = evs[t]
+            e0.record(stream)
+            s.sample(x, V=V, num_logprobs=n, update_counts=True, out=out, stream=stream)
+            e1.record(stream)
+    stream.synchronize()
+    clocks.stop()
+    s.check_device_errors()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = sum(step_ms) / 1e3
+    max_s, value = whole_job_rate(total_s, B * args.steps, world, dev)
+    ms_per_step = max_s * 1e3 / args.steps
+    launches = s.last_launches()
+    handed = s.last_handover()
+    # end to end: the step-0 logits from pinned host memory every step
+    host = large_step_device(0, B, V, dev, rank).cpu().pin_memory().numpy()
+    ho = (np.empty(B, np.int32), np.empty(B, np.float32), np.empty((B, n), np.int32),
+          np.empty((B, n), np.float32))
+    e2e_steps = max(3, min(args.steps, 20))
+    s.sample_host(host, V, W.DTYPE_F32, n, True, stream=stream, out=ho)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        s.sample_host(host, V, W.DTYPE_F32, n, True, stream=stream, out=ho)
+    e2e_s = time.perf_counter() - t0
+    _, e2e_value = whole_job_rate(e2e_s, B * e2e_steps, world, dev)
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        alg = int(algorithmic_bytes_per_row(w).sum())
+        achieved = alg / (ms_per_step * 1e-3) / 1e9
+        cfg = workload_config(w)
+        cfg["l2"] = "one fresh 1.02 GB batch per step (> 129 MB L2), made on the device"
+        cfg["decode_steps"] = args.steps
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                         "peak_source": f"{peak_kind} (hbm_gbs)",
+                         "algorithmic_bytes_per_step": alg,
+                         "kernel": "vt_sample step (sample_kernel + select_kernel)",
+                         "kernel_ms": ms_per_step},
+            "step_ms": {"median": float(np.median(step_ms)), "max": float(np.max(step_ms)),
+                        "first": float(step_ms[0]), "last": float(step_ms[-1])},
+            "rows_handed_to_select_kernel_last_step": handed,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(host.nbytes),
+                    "d2h_bytes_per_step": int(sum(a.nbytes for a in ho)), "steps": e2e_steps,
+                    "api": "vt_sample_host (pinned host logits in, host outputs back)"},
+            "gpu_launches": launches * args.steps,
+            "clocks": clocks.summary(),
+            "ns_per_row": 1e6 * ms_per_step / B,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            hw = W.large(seed=4, with_logits=False)
+            hw.logits = host  # the oracle times rows of a real step
+            line["cpu_baseline"] = cpu_baseline(hw, budget_rows=args.cpu_rows or 256)
+        print(json.dumps(line), flush=True)
+    s.close()
+    if world > 1:
+        dist.destroy_process_group()
+
 
 def run_gpu(args, w: W.Workload):
     import torch
@@ -435,13 +556,16 @@ def run_gpu(args, w: W.Workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 2000; Large: 100 decode steps)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="b256", choices=W.NAMES)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 100 if args.workload == "large" else 2000
     rank, world, _ = dist_env()
     w = make_workload(args.workload, rank)
     if args.impl == "reference":
@@ -449,7 +573,10 @@ def main():
     else:
         from device_token_sampling_gb300 import _build
         _build.build()
-        run_gpu(args, w)
+        if args.workload == "large":
+            run_gpu_decode(args, w)
+        else:
+            run_gpu(args, w)
 
 
 if __name__ == "__main__":
