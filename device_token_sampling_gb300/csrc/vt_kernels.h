@@ -226,6 +226,32 @@ cudaError_t launch_rows(const RowArgs& args, const RowPlan& plan, int draw_rows,
 cudaError_t launch_select_handed(const SampleArgs& args, const LaunchPlan& plan, int dtype,
                                  cudaStream_t stream);
 
+// ---- the vocabulary-sharded sampler (vt_shard.cu) ---------------------------
+struct ShardArgs {
+  const void* logits;        // partials: the shard's columns [B][ld]
+  int64_t ld;
+  int32_t B, Vs, v0, V;      // rows, shard width, its first global column, the row width
+  int32_t K;                 // records per row and shard (<= 256)
+  int32_t S;                 // merge: shards
+  int32_t n_logprobs;
+  const RowParams* params;   // [B]
+  uint64_t* seeds;           // [B], advanced by the merge
+  void* part;                // partials: [B] records; merge: [S][B] records
+  int64_t part_bytes;        // bytes of one row's record
+  int32_t* out_tokens;
+  float* out_logprobs;
+  int32_t* out_topk_ids;
+  float* out_topk_logprobs;
+  int32_t* row_status;
+  float* dbg_kth_value;
+  int32_t* dbg_kth_index;
+  int32_t* dbg_kept;
+  int32_t* err_word;
+};
+int64_t shard_part_bytes(int K);
+cudaError_t launch_shard_partials(const ShardArgs& a, int dtype, cudaStream_t stream);
+cudaError_t launch_shard_merge(const ShardArgs& a, cudaStream_t stream);
+
 // ---- the filtered distribution on request (vt_probs.cu) ---------------------
 constexpr int kProbsMaxRange = 65536;  // elements per CTA at most
 constexpr int kProbsMaxSplits = 64;    // CTAs per row at most (unless V needs more)

@@ -957,6 +957,111 @@ int vt_debug_last_handover(vt_sampler* h, int32_t* rows) {
   return VT_OK;
 }
 
+// ---- the vocabulary-sharded sampler ------------------------------------------
+int64_t vt_shard_part_bytes(int32_t K) {
+  if (K < 1 || K > VT_SHARD_MAX_K) return -1;
+  return vt::shard_part_bytes(K);
+}
+
+// Rows the sharded path settles exactly: no penalties, no top-p decay, and a
+// sampled row's kept set inside a top-k of at most K.
+static int shard_rows_ok(vt_sampler* h, int32_t B, int32_t V, int32_t K) {
+  if (h->params_B == 0) return set_err(h, VT_ERR_STATE, "sharded call before vt_reset_params");
+  if (B < 1 || B > h->params_B)
+    return set_err(h, B < 1 ? VT_ERR_INVALID_ARG : VT_ERR_STATE,
+                   "B=%d but parameters were reset for %d rows", B, h->params_B);
+  if (V < 1 || V > (1 << 20)) return set_err(h, VT_ERR_INVALID_ARG, "V=%d out of range", V);
+  if (K < 1 || K > VT_SHARD_MAX_K) return set_err(h, VT_ERR_INVALID_ARG, "K=%d out of range", K);
+  for (int r = 0; r < B; ++r) {
+    const uint32_t f = h->row_flags[r];
+    if (f & (vt::kRowPenalty | vt::kRowDecay))
+      return set_err(h, VT_ERR_INVALID_ARG, "row %d: penalties or top-p decay are not sharded", r);
+    if (f & vt::kRowGreedy) continue;
+    const int k = h->h_params[r].top_k;
+    if (!(k > 1 && k < V && k <= K))
+      return set_err(h, VT_ERR_INVALID_ARG,
+                     "row %d: a sampled row needs 1 < top_k <= K (%d) and top_k < V (top_k=%d)", r,
+                     K, k);
+  }
+  return VT_OK;
+}
+
+int vt_shard_partials(vt_sampler* h, const void* logits, int32_t dtype, int32_t B, int32_t Vs,
+                      int64_t ld, int32_t v0, int32_t V, int32_t K, void* part, void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  const int rc = shard_rows_ok(h, B, V, K);
+  if (rc != VT_OK) return rc;
+  if (dtype != VT_DTYPE_F32 && dtype != VT_DTYPE_BF16)
+    return set_err(h, VT_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (!logits || !part) return set_err(h, VT_ERR_INVALID_ARG, "null logits or partials");
+  if (Vs < 1 || ld < Vs || v0 < 0 || (int64_t)v0 + Vs > V)
+    return set_err(h, VT_ERR_INVALID_ARG, "need 1 <= Vs <= ld and 0 <= v0, v0 + Vs <= V");
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
+  vt::ShardArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.logits = logits;
+  a.ld = ld;
+  a.B = B;
+  a.Vs = Vs;
+  a.v0 = v0;
+  a.V = V;
+  a.K = K;
+  a.params = h->d_params;
+  a.part = part;
+  a.part_bytes = vt::shard_part_bytes(K);
+  cudaStream_t st = (cudaStream_t)stream;
+  VT_CK(h, vt::launch_shard_partials(a, dtype, st));
+  h->last_stream = st;
+  h->err.clear();
+  return VT_OK;
+}
+
+int vt_shard_merge(vt_sampler* h, const void* parts, int32_t S, int32_t B, int32_t V, int32_t K,
+                   int32_t num_logprobs, int32_t* out_tokens, float* out_logprobs,
+                   int32_t* out_topk_ids, float* out_topk_logprobs, void* stream) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  const int rc = shard_rows_ok(h, B, V, K);
+  if (rc != VT_OK) return rc;
+  if (S < 1 || S > 64 || S * K > VT_SHARD_MAX_RECORDS)
+    return set_err(h, VT_ERR_INVALID_ARG, "S=%d: need 1 <= S <= 64 and S * K <= %d", S,
+                   VT_SHARD_MAX_RECORDS);
+  if (num_logprobs < 0 || num_logprobs > h->cfg.max_logprobs || num_logprobs > K)
+    return set_err(h, VT_ERR_INVALID_ARG, "num_logprobs=%d outside [0, min(max_logprobs, K)]",
+                   num_logprobs);
+  if (!parts || !out_tokens) return set_err(h, VT_ERR_INVALID_ARG, "null partials or tokens");
+  if (num_logprobs > 0 && (!out_topk_ids || !out_topk_logprobs))
+    return set_err(h, VT_ERR_INVALID_ARG, "top-n log-prob outputs are null");
+  DeviceGuard guard(h->cfg.device);
+  if (!guard.ok) return set_err(h, VT_ERR_CUDA, "cannot select device %d", h->cfg.device);
+  vt::ShardArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.B = B;
+  a.V = V;
+  a.K = K;
+  a.S = S;
+  a.n_logprobs = num_logprobs;
+  a.params = h->d_params;
+  a.seeds = h->d_seeds;
+  a.part = const_cast<void*>(parts);
+  a.part_bytes = vt::shard_part_bytes(K);
+  a.out_tokens = out_tokens;
+  a.out_logprobs = out_logprobs;
+  a.out_topk_ids = out_topk_ids;
+  a.out_topk_logprobs = out_topk_logprobs;
+  a.row_status = h->d_status;
+  a.dbg_kth_value = h->d_kth_v;
+  a.dbg_kth_index = h->d_kth_i;
+  a.dbg_kept = h->d_kept;
+  a.err_word = h->d_err;
+  cudaStream_t st = (cudaStream_t)stream;
+  VT_CK(h, vt::launch_shard_merge(a, st));
+  h->last_B = B;
+  h->last_stream = st;
+  h->err.clear();
+  return VT_OK;
+}
+
 int vt_debug_row_plan(vt_sampler* h, int32_t B, int32_t V, int32_t* cluster,
                       int32_t* clusters, int32_t* slice, int64_t* smem_bytes) {
   if (!h || !cluster || !clusters || !slice || !smem_bytes || B < 1 || V < 1)

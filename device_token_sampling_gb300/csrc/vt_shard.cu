@@ -1,0 +1,501 @@
+// vt_shard.cu -- the vocabulary-sharded sampler: per-shard partials and their merge.
+//
+// When the vocabulary of a row is split over several devices (the Tenstorrent
+// sampling README: each device takes the top-k of its own slice of the logits,
+// the candidates are all-gathered, and the log-probs combine the devices'
+// maxima and sums of exponentials -- TTSampling and LogProbsCalculator), the
+// draw composes exactly because the noise of column j is keyed by the global
+// row and the global column (vllm.cpp pull request: ArgReduce over true global
+// indices).  Two launches and one small exchange:
+//
+//   partials (one per shard): for each row of the shard's columns
+//     [v0, v0 + Vs), the shard's tempered maximum m_s, its sum of
+//     exp(z_t - m_s), its lowest-index argmax (global index), and its K
+//     largest elements as records (z_t, global index) in the order
+//     (z_t descending, index ascending);
+//   the caller all-gathers the shards' partial buffers (S x B records);
+//   merge (any shard, or every shard): the row's maximum and sum of
+//     exponentials (hence its log-probs), then min-p, top-k and top-p over the
+//     union of the shards' records -- which holds the row's K largest
+//     elements -- with masses in exact fixed point, the Gumbel-max draw over
+//     the kept records, and the top-n.
+//
+// The union covers the kept set of every row whose kept set lies inside a
+// top-k of at most K (and greedy rows); the host rejects other rows, and any
+// S * K above kShardCand (the records one merge CTA sorts).
+#include "vt_device.cuh"
+#include "vt_kernels.h"
+
+#include <climits>
+
+namespace vt {
+namespace {
+
+constexpr int kST = 256;                 // threads per CTA
+constexpr int kSW = kST / 32;
+constexpr int kShardCand = 4096;         // records a CTA collects or merges at most
+
+struct __align__(16) ShardHead {
+  float m_t;        // the shard's tempered maximum (-inf: no finite element)
+  float s;          // sum of exp(z_t - m_t) over the shard
+  int32_t argj;     // lowest global index of m_t (INT_MAX: none)
+  uint32_t info;    // records written (bits 0..15), NaN or +inf seen (bit 30)
+};
+
+// Descending bitonic sort of keys[0, N) in shared memory, N a power of two.
+__device__ void smem_sort_desc(uint64_t* keys, int N) {
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < N; i += kST) {
+        const int p = i ^ j;
+        if (p > i) {
+          const bool desc = (i & k) == 0;
+          const uint64_t a = keys[i], b = keys[p];
+          if (desc ? (a < b) : (a > b)) {
+            keys[i] = b;
+            keys[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+struct ShardSmem {
+  uint64_t keys[kShardCand];
+  float tm[kST];
+  float rf[2 * kSW];
+  int ri[2 * kSW];
+  unsigned long long ru[2 * kSW];
+  int hist[256];
+  int wt[kSW];
+  int count, ties;
+  float bf[4];
+  int bi[4];
+};
+
+// Block argmax (larger value, then lower index).
+__device__ void sblock_argmax(float& v, int& i, float& z, ShardSmem& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+    if (pair_better(v2, i2, v, i)) {
+      v = v2;
+      i = i2;
+      z = z2;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    s.rf[warp] = v;
+    s.ri[warp] = i;
+    s.rf[kSW + warp] = z;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float tv = lane < kSW ? s.rf[lane] : -INFINITY;
+    int ti = lane < kSW ? s.ri[lane] : INT_MAX;
+    float tz = lane < kSW ? s.rf[kSW + lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, tv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, ti, o);
+      const float z2 = __shfl_xor_sync(0xffffffffu, tz, o);
+      if (pair_better(v2, i2, tv, ti)) {
+        tv = v2;
+        ti = i2;
+        tz = z2;
+      }
+    }
+    if (lane == 0) {
+      s.bf[0] = tv;
+      s.bi[0] = ti;
+      s.bf[1] = tz;
+    }
+  }
+  __syncthreads();
+  v = s.bf[0];
+  i = s.bi[0];
+  z = s.bf[1];
+  __syncthreads();
+}
+
+__device__ float sblock_sum(float v, ShardSmem& s) {
+  v = warp_sum_f(v);
+  if ((threadIdx.x & 31) == 0) s.rf[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < kSW ? s.rf[threadIdx.x] : 0.f;
+    t = warp_sum_f(t);
+    if (threadIdx.x == 0) s.bf[2] = t;
+  }
+  __syncthreads();
+  const float r = s.bf[2];
+  __syncthreads();
+  return r;
+}
+
+__device__ unsigned long long sblock_sum_u64(unsigned long long v, ShardSmem& s) {
+  v = warp_sum_u64(v);
+  if ((threadIdx.x & 31) == 0) s.ru[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    unsigned long long t = threadIdx.x < kSW ? s.ru[threadIdx.x] : 0ull;
+    t = warp_sum_u64(t);
+    if (threadIdx.x == 0) s.ru[kSW] = t;
+  }
+  __syncthreads();
+  const unsigned long long r = s.ru[kSW];
+  __syncthreads();
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ float load_x(const T* p, int j);
+template <>
+__device__ __forceinline__ float load_x<float>(const float* p, int j) {
+  return __ldg(p + j);
+}
+template <>
+__device__ __forceinline__ float load_x<uint16_t>(const uint16_t* p, int j) {
+  return __uint_as_float((uint32_t)__ldg(p + j) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// partials: one CTA per row of the shard
+// ---------------------------------------------------------------------------
+// The shard's K largest elements, exactly, when the quick threshold let more
+// than kShardCand elements through (a flat row, heavy ties, masked columns):
+// a most-significant-digit radix select over the order-preserving bits of z_t,
+// eight bits a pass, gives the K-th largest value; then one pass collects the
+// elements above it and, in index order, the lowest-index elements equal to
+// it.  Leaves the K records unsorted in s.keys[0, K).
+template <typename T>
+__device__ void shard_exact_top(const ShardArgs& a, const T* x, float inv_t, ShardSmem& s) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0u, mask = 0u;
+  int r = a.K;  // rank of the wanted value among the elements matching the prefix
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kST) s.hist[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < a.Vs; j += kST) {
+      const uint32_t o = ord_key(__fmul_rn(load_x<T>(x, j), inv_t));
+      if ((o & mask) == prefix) atomicAdd(&s.hist[(o >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int above = 0, b = 255;
+      for (; b > 0 && above + s.hist[b] < r; --b) above += s.hist[b];
+      s.bi[0] = b;
+      s.bi[1] = r - above;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)s.bi[0] << shift;
+    mask |= 255u << shift;
+    r = s.bi[1];
+    __syncthreads();
+  }
+  // K - r elements lie strictly above the K-th largest value; r ties are taken
+  const int g = a.K - r;
+  if (tid == 0) {
+    s.count = 0;
+    s.ties = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < a.Vs; base += kST) {
+    const int j = base + tid;
+    bool tie = false;
+    if (j < a.Vs) {
+      const float z = __fmul_rn(load_x<T>(x, j), inv_t);
+      const uint32_t o = ord_key(z);
+      if (o > prefix) s.keys[atomicAdd(&s.count, 1)] = elem_key(z, (uint32_t)(a.v0 + j));
+      tie = o == prefix;
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, tie);
+    if (lane == 0) s.wt[warp] = __popc(bal);
+    __syncthreads();
+    int rank = s.ties + __popc(bal & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) rank += s.wt[w];
+    if (tie && rank < r) s.keys[g + rank] = elem_key(key_value(prefix), (uint32_t)(a.v0 + j));
+    __syncthreads();
+    if (tid == 0)
+      for (int w = 0; w < kSW; ++w) s.ties += s.wt[w];
+    __syncthreads();
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) {
+  __shared__ ShardSmem s;
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const T* x = reinterpret_cast<const T*>(a.logits) + (int64_t)row * a.ld;
+  const float inv_t = a.params[row].inv_t;
+  // the shard's maximum, its lowest global index, and each thread's maximum
+  float tmax = -INFINITY;
+  int tj = INT_MAX;
+  bool bad = false;
+  for (int j = tid; j < a.Vs; j += kST) {
+    const float z = __fmul_rn(load_x<T>(x, j), inv_t);
+    bad |= (z != z) || z == INFINITY;
+    if (z > tmax) {
+      tmax = z;
+      tj = a.v0 + j;
+    }
+  }
+  s.tm[tid] = tmax;
+  float m = tmax, zz = 0.f;
+  int mj = tj;
+  sblock_argmax(m, mj, zz, s);
+  const int anybad = __syncthreads_or(bad);
+  uint8_t* out = reinterpret_cast<uint8_t*>(a.part) + (size_t)row * a.part_bytes;
+  if (anybad) {  // NaN or +inf: the merge reports the row as non-finite
+    if (tid == 0) {
+      ShardHead h;
+      h.m_t = m;
+      h.s = 0.f;
+      h.argj = mj;
+      h.info = 1u << 30;
+      *reinterpret_cast<ShardHead*>(out) = h;
+    }
+    return;
+  }
+  // a lower bound of the shard's K-th largest: the K-th largest thread maximum
+  // (at least K elements are >= it); -inf when fewer than K threads hold one
+  if (tid == 0) {
+    s.bf[3] = -INFINITY;
+    s.count = 0;
+  }
+  __syncthreads();
+  {
+    const float v = s.tm[tid];
+    int rank = 0;
+    for (int u = 0; u < kST; ++u) {
+      const float w = s.tm[u];
+      rank += (w > v) || (w == v && u < tid);
+    }
+    if (rank == a.K - 1 && v > -INFINITY) s.bf[3] = v;
+  }
+  __syncthreads();
+  const float tau = s.bf[3];
+  // the sum of exponentials against m, and the elements at or above tau
+  float sum = 0.f;
+  const bool finite_max = m > -INFINITY;
+  const float nh = __fmul_rn(-m, kLog2e);
+  const float nl = finite_max ? __fmaf_rn(-m, kLog2e, -nh) : 0.f;
+  for (int j = tid; j < a.Vs; j += kST) {
+    const float z = __fmul_rn(load_x<T>(x, j), inv_t);
+    if (finite_max) sum += ex2_approx(__fadd_rn(__fmaf_rn(z, kLog2e, nh), nl));
+    if (z >= tau) {
+      const int pos = atomicAdd(&s.count, 1);
+      if (pos < kShardCand) s.keys[pos] = elem_key(z, (uint32_t)(a.v0 + j));
+    }
+  }
+  sum = sblock_sum(sum, s);
+  int n = s.count;
+  __syncthreads();
+  if (n > kShardCand) {
+    shard_exact_top<T>(a, x, inv_t, s);
+    n = a.K;
+  }
+  int P2 = kST;
+  while (P2 < n) P2 <<= 1;
+  for (int i = n + tid; i < P2; i += kST) s.keys[i] = 0ull;
+  __syncthreads();
+  smem_sort_desc(s.keys, P2);
+  const int w = min(n, a.K);
+  uint64_t* rec = reinterpret_cast<uint64_t*>(out + sizeof(ShardHead));
+  for (int i = tid; i < w; i += kST) rec[i] = s.keys[i];
+  if (tid == 0) {
+    ShardHead h;
+    h.m_t = m;
+    h.s = sum;
+    h.argj = mj;
+    h.info = (uint32_t)w;
+    *reinterpret_cast<ShardHead*>(out) = h;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// merge: one CTA per row, over the S shards' partials
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
+  __shared__ ShardSmem s;
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const RowParams P = a.params[row];
+  const int n = a.n_logprobs;
+  // the row's statistics
+  if (tid == 0) {
+    float mt = -INFINITY, sm = 0.f;
+    int argj = INT_MAX, bad = 0, total = 0;
+    for (int sh = 0; sh < a.S; ++sh) {
+      const uint8_t* in = reinterpret_cast<const uint8_t*>(a.part) +
+                          ((size_t)sh * a.B + row) * a.part_bytes;
+      const ShardHead h = *reinterpret_cast<const ShardHead*>(in);
+      if (pair_better(h.m_t, h.argj, mt, argj) && h.m_t > -INFINITY) argj = h.argj;
+      lse_combine(mt, sm, h.m_t, h.s, kLog2e);
+      bad |= (h.info >> 30) & 1u;
+      total += (int)(h.info & 0xFFFFu);
+    }
+    s.bf[0] = mt;
+    s.bf[1] = sm;
+    s.bi[0] = argj;
+    s.bi[1] = bad || mt == INFINITY;
+    s.bi[2] = total;
+    s.bi[3] = total > kShardCand;  // the host keeps S * K within kShardCand
+  }
+  __syncthreads();
+  const float m_t = s.bf[0], S = s.bf[1];
+  const int argj = s.bi[0], bad = s.bi[1], ovf = s.bi[3];
+  const int total = min(s.bi[2], kShardCand);
+  const float lnS = logf(S);
+  __syncthreads();
+  const int status = bad ? kRowNonfinite : (m_t == -INFINITY ? kRowEmpty : kRowOk);
+  if (status != kRowOk || ovf) {
+    if (tid < n) {
+      a.out_topk_ids[(int64_t)row * n + tid] = -1;
+      a.out_topk_logprobs[(int64_t)row * n + tid] = __int_as_float(0x7fc00000);
+    }
+    if (tid == 0) {
+      a.out_tokens[row] = -1;
+      if (a.out_logprobs) a.out_logprobs[row] = __int_as_float(0x7fc00000);
+      a.row_status[row] = status;
+      a.dbg_kth_value[row] = __int_as_float(0x7fc00000);
+      a.dbg_kth_index[row] = -1;
+      a.dbg_kept[row] = 0;
+      a.seeds[row] += kSeedStep;
+      if (ovf) atomicOr(a.err_word, kErrInternal);
+    }
+    return;
+  }
+  // the union of the shards' records, in the order (z_t desc, index asc)
+  {
+    int off = 0;
+    for (int sh = 0; sh < a.S; ++sh) {
+      const uint8_t* in = reinterpret_cast<const uint8_t*>(a.part) +
+                          ((size_t)sh * a.B + row) * a.part_bytes;
+      const int w = (int)(reinterpret_cast<const ShardHead*>(in)->info & 0xFFFFu);
+      const uint64_t* rec = reinterpret_cast<const uint64_t*>(in + sizeof(ShardHead));
+      for (int i = tid; i < w && off + i < kShardCand; i += kST) s.keys[off + i] = rec[i];
+      off += w;
+    }
+  }
+  int P2 = kST;
+  while (P2 < total) P2 <<= 1;
+  for (int i = total + tid; i < P2; i += kST) s.keys[i] = 0ull;
+  __syncthreads();
+  smem_sort_desc(s.keys, P2);
+  // finite records (the -inf ones sort last)
+  int fin = 0;
+  for (int i = tid; i < total; i += kST) fin += key_z(s.keys[i]) > -INFINITY;
+  fin = (int)sblock_sum_u64((unsigned long long)fin, s);
+  // top-n: the first n records
+  for (int t = tid; t < n; t += kST) {
+    if (t < total) {
+      const uint64_t k = s.keys[t];
+      a.out_topk_ids[(int64_t)row * n + t] = (int)key_idx(k);
+      a.out_topk_logprobs[(int64_t)row * n + t] = (key_z(k) - m_t) - lnS;
+    } else {
+      a.out_topk_ids[(int64_t)row * n + t] = -1;
+      a.out_topk_logprobs[(int64_t)row * n + t] = -INFINITY;
+    }
+  }
+  const bool greedy = (P.flags & kRowGreedy) != 0;
+  int tok = argj, L3 = 1;
+  float ztok = m_t;
+  if (!greedy) {
+    // min-p, then top-k, then top-p over the top-k survivors renormalised
+    int L1 = fin;
+    if (P.flags & kRowMinP) {
+      int pass = 0;
+      for (int i = tid; i < fin; i += kST) pass += minp_pass(key_z(s.keys[i]), m_t, P.log_min_p);
+      L1 = (int)sblock_sum_u64((unsigned long long)pass, s);
+    }
+    const int L2 = min(P.top_k, L1);
+    L3 = L2;
+    if (P.flags & kRowTopP) {
+      // exclusive prefix masses in 2^-43 fixed point; kept while <= p * W
+      unsigned long long mine = 0ull;
+      const int per = (L2 + kST - 1) / kST;
+      const int i0 = min(L2, tid * per), i1 = min(L2, i0 + per);
+      for (int i = i0; i < i1; ++i) mine += mass_fixed(key_z(s.keys[i]), m_t);
+      // exclusive scan over the threads (serial in warp 0: at most 256 terms)
+      s.ru[0] = 0ull;
+      __syncthreads();
+      __shared__ unsigned long long part[kST];
+      part[tid] = mine;
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long run = 0ull;
+        for (int t = 0; t < kST; ++t) {
+          const unsigned long long v = part[t];
+          part[t] = run;
+          run += v;
+        }
+        s.ru[1] = run;
+      }
+      __syncthreads();
+      const unsigned long long W = s.ru[1];
+      const unsigned long long Tm = (unsigned long long)((double)W * (double)P.top_p);
+      unsigned long long run = part[tid];
+      int kept = 0;
+      for (int i = i0; i < i1; ++i) {
+        if (run <= Tm) ++kept;
+        run += mass_fixed(key_z(s.keys[i]), m_t);
+      }
+      L3 = max(1, (int)sblock_sum_u64((unsigned long long)kept, s));
+    }
+    // the Gumbel-max draw over the kept records, noise keyed by the global row
+    // and column
+    const uint64_t key = row_key(a.seeds[row], row);
+    float bs = -INFINITY, bz = 0.f;
+    int bj = INT_MAX;
+    for (int i = tid; i < L3; i += kST) {
+      const uint64_t k = s.keys[i];
+      const int j = (int)key_idx(k);
+      const float z = key_z(k);
+      const float sc = gumbel_score_inl(z, noise_bits(key, j));
+      if (pair_better(sc, j, bs, bj)) {
+        bs = sc;
+        bj = j;
+        bz = z;
+      }
+    }
+    sblock_argmax(bs, bj, bz, s);
+    tok = bj;
+    ztok = bz;
+  }
+  if (tid == 0) {
+    a.out_tokens[row] = tok;
+    if (a.out_logprobs) a.out_logprobs[row] = (ztok - m_t) - lnS;
+    a.row_status[row] = kRowOk;
+    const uint64_t kk = greedy ? 0ull : s.keys[L3 - 1];
+    a.dbg_kth_value[row] = greedy ? m_t : key_z(kk);
+    a.dbg_kth_index[row] = greedy ? tok : (int)key_idx(kk);
+    a.dbg_kept[row] = L3;
+    a.seeds[row] += kSeedStep;
+  }
+}
+
+}  // namespace
+
+int64_t shard_part_bytes(int K) { return (int64_t)sizeof(ShardHead) + 8 * (int64_t)K; }
+
+cudaError_t launch_shard_partials(const ShardArgs& a, int dtype, cudaStream_t stream) {
+  if (a.B < 1) return cudaSuccess;
+  if (dtype == 0)
+    shard_partials_kernel<float><<<a.B, kST, 0, stream>>>(a);
+  else
+    shard_partials_kernel<uint16_t><<<a.B, kST, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_merge(const ShardArgs& a, cudaStream_t stream) {
+  if (a.B < 1) return cudaSuccess;
+  shard_merge_kernel<<<a.B, kST, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace vt

@@ -77,6 +77,9 @@ SIGNATURES = {
     "vt_debug_last_handover": (C.c_int, [P, P]),
     "vt_debug_last_launches": (C.c_int, [P, P]),
     "vt_debug_set_path": (C.c_int, [P, I32]),
+    "vt_shard_part_bytes": (I64, [I32]),
+    "vt_shard_partials": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, I32, P, P]),
+    "vt_shard_merge": (C.c_int, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P]),
     "vt_debug_row_plan": (C.c_int, [P, I32, I32, P, P, P, P]),
     "vt_sample_noalloc": (C.c_int, [I32, P, I32, I32, I32, I64, P, P, P, P, P, I32, P, P, P, P,
                                     P, I32, P, C.c_char_p, I32]),
@@ -369,6 +372,52 @@ class Sampler:
                                                 C.byref(sl), C.byref(sm)), "vt_debug_row_plan")
         return int(c.value), int(n.value), int(sl.value), int(sm.value)
 
+    # -- the vocabulary split over several devices ----------------------------
+    def shard_partials(self, logits, v0: int, V: int, K: int, out=None, stream=None,
+                       dtype: int | None = None):
+        """vt_shard_partials: this shard's records for the columns [v0, v0 + Vs)
+        held in ``logits`` [B, ld]; returns a uint8 CUDA tensor [B, part_bytes]."""
+        import torch
+        if logits.dim() != 2 or not logits.is_cuda or logits.stride(1) != 1:
+            raise ValueError("logits must be a 2-D CUDA tensor with contiguous rows")
+        if dtype is None:
+            dtype = DTYPE_F32 if logits.dtype == torch.float32 else DTYPE_BF16
+        B, Vs, ld = logits.shape[0], logits.shape[1], logits.stride(0)
+        pb = int(self._lib.vt_shard_part_bytes(K))
+        if pb < 0:
+            raise ValueError(f"K={K} outside 1..256")
+        if out is None:
+            out = torch.empty((B, pb), dtype=torch.uint8, device=logits.device)
+        elif out.dtype != torch.uint8 or tuple(out.shape) != (B, pb) or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous uint8 tensor of shape {(B, pb)}")
+        rc = self._lib.vt_shard_partials(self._h, P(logits.data_ptr()), dtype, B, Vs, ld, v0, V,
+                                         K, P(out.data_ptr()), _stream_ptr(stream))
+        self._check(rc, "vt_shard_partials")
+        return out
+
+    def shard_merge(self, parts, V: int, K: int, num_logprobs: int = 0, stream=None):
+        """vt_shard_merge over ``parts`` (uint8 CUDA [S, B, part_bytes], the
+        shards' records gathered shard-major); returns (tokens, logprobs,
+        topk_ids, topk_logprobs) CUDA tensors."""
+        import torch
+        if parts.dim() != 3 or parts.dtype != torch.uint8 or not parts.is_contiguous():
+            raise ValueError("parts must be a contiguous uint8 tensor [S, B, part_bytes]")
+        S_, B = parts.shape[0], parts.shape[1]
+        if parts.shape[2] != int(self._lib.vt_shard_part_bytes(K)):
+            raise ValueError("parts do not hold records of K elements")
+        n = int(num_logprobs)
+        dev = parts.device
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        lp = torch.empty(B, dtype=torch.float32, device=dev)
+        tid = torch.empty((B, n), dtype=torch.int32, device=dev)
+        tlp = torch.empty((B, n), dtype=torch.float32, device=dev)
+        rc = self._lib.vt_shard_merge(self._h, P(parts.data_ptr()), S_, B, V, K, n,
+                                      P(tok.data_ptr()), P(lp.data_ptr()),
+                                      P(tid.data_ptr()) if n else None,
+                                      P(tlp.data_ptr()) if n else None, _stream_ptr(stream))
+        self._check(rc, "vt_shard_merge")
+        return tok, lp, tid, tlp
+
     def set_path(self, path: int):
         """0: the row kernel for bf16 calls without penalties; 1 (the default):
         the streaming kernel for every call."""
@@ -459,3 +508,26 @@ def sample_noalloc(logits, temperature, top_k, top_p, min_p, seed, out_tokens,
                                _stream_ptr(stream), err, len(err))
     if rc != VT_OK:
         raise VtError(rc, err.value.decode(errors="replace"))
+
+
+def gather_partials(part, group=None):
+    """The exchange of the vocabulary-sharded sampler: every rank's records
+    ``part`` [B, part_bytes] (uint8) all-gathered over ``group`` into one
+    [world, B, part_bytes] tensor, rank-major, as ``vt_shard_merge`` reads them
+    (torch.distributed: NCCL for CUDA tensors, gloo for host tensors)."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = torch.empty((world,) + tuple(part.shape), dtype=part.dtype, device=part.device)
+    dist.all_gather(list(out.unbind(0)), part.contiguous(), group=group)
+    return out
+
+
+def sharded_sample(sampler: Sampler, logits_shard, v0: int, V: int, K: int,
+                   num_logprobs: int = 0, group=None):
+    """One step of the vocabulary-sharded sampler on this rank: this rank's
+    records (``vt_shard_partials``) for its columns [v0, v0 + Vs), the
+    all-gather of every rank's records, then the merge (``vt_shard_merge``).
+    Every rank returns the same outputs and advances the same seeds."""
+    part = sampler.shard_partials(logits_shard, v0, V, K)
+    return sampler.shard_merge(gather_partials(part, group), V, K, num_logprobs)

@@ -362,6 +362,62 @@ int vt_sample_noalloc(int32_t device, const void* logits, int32_t dtype, int32_t
                       int32_t* out_topk_ids, float* out_topk_logprobs, int32_t* row_status,
                       int32_t synchronize, void* stream, char* errbuf, int32_t errbuf_len);
 
+/* ---- the vocabulary split over several devices ---------------------------
+ * The Tenstorrent sampling README splits a row's logits over devices: each
+ * device takes the top-k of its own slice (TTSampling), the candidates are
+ * all-gathered, and the log-probs combine the devices' global maxima and sums
+ * of exponentials (LogProbsCalculator).  The draw composes exactly because the
+ * noise of column j is keyed by the global row and the global column (vllm.cpp
+ * pull request "the Gumbel draw that scanned 248,320 tokens on one thread":
+ * ArgReduce over true global indices).  Protocol, per step:
+ *   1. every shard calls vt_shard_partials on its columns [v0, v0 + Vs) of the
+ *      rows, writing one record of vt_shard_part_bytes(K) bytes per row;
+ *   2. the caller all-gathers the S shards' records into one device buffer
+ *      [S][B] records, shard s at s * B records (e.g. an NCCL all-gather);
+ *   3. vt_shard_merge on that buffer writes the rows' tokens, log-probs and
+ *      top-n exactly as vt_sample on the whole rows would (tokens and kept sets
+ *      identical; log-probs equal within rounding), and advances the seeds.
+ * Every shard's handle must hold the same parameters and seeds (the same
+ * vt_reset_params).  Rows it takes: no penalties, no top-p decay, and each
+ * sampled row bounded by 1 < top_k <= K (top_k < V), after which min-p and
+ * top-p apply over the gathered records; greedy rows always.  Other rows:
+ * VT_ERR_INVALID_ARG.  The union of the shards' K largest elements holds the
+ * row's K largest, hence its kept set and its top-n. */
+#define VT_SHARD_MAX_K 256
+/* Records one merge gathers per row at most: S * K <= VT_SHARD_MAX_RECORDS. */
+#define VT_SHARD_MAX_RECORDS 4096
+
+/* Bytes of one row's record in a shard buffer for 1 <= K <= VT_SHARD_MAX_K
+ * (-1 otherwise): a 16-byte header -- float the shard's tempered maximum m_s
+ * (-inf: no finite element), float the sum of exp(z_t - m_s) over its columns,
+ * int32 its lowest global index holding m_s, uint32 the count w of elements
+ * written (bits 0..15; w = min(K, Vs)) with bit 30 set when a NaN or +inf was
+ * seen -- then K uint64 elements, the first w valid: the shard's w largest in
+ * the order (z_t descending, global index ascending), each with the
+ * order-preserving code of z_t in bits 63..32 (sign bit flipped for z_t >= 0,
+ * all bits flipped below; -0 as +0) and the complement of the global index in
+ * bits 31..0, so that a larger integer is an earlier element. */
+int64_t vt_shard_part_bytes(int32_t K);
+
+/* Step 1 on one shard: logits is device [B][ld] of dtype holding global
+ * columns v0 .. v0 + Vs - 1 of rows 0..B-1 (V: the rows' full width); part is
+ * device memory of B * vt_shard_part_bytes(K) bytes, owned by the caller.
+ * Stream-ordered, no synchronisation, no allocation.  Errors: VT_ERR_STATE (no
+ * parameters yet, or B larger than the last reset), VT_ERR_INVALID_ARG (a row
+ * the sharded path does not take, bad sizes, null pointers), VT_ERR_CUDA. */
+int vt_shard_partials(vt_sampler* handle, const void* logits, int32_t dtype, int32_t B,
+                      int32_t Vs, int64_t ld, int32_t v0, int32_t V, int32_t K, void* part,
+                      void* stream);
+
+/* Step 3: parts is device memory holding S * B records (shard-major, as step
+ * 2 gathers them); outputs as in vt_sample (num_logprobs <= min(max_logprobs,
+ * K)).  Row status, the filter boundary and the seeds are updated as by
+ * vt_sample.  Errors as vt_shard_partials, plus VT_ERR_INVALID_ARG for S
+ * outside 1..64 or S * K above VT_SHARD_MAX_RECORDS. */
+int vt_shard_merge(vt_sampler* handle, const void* parts, int32_t S, int32_t B, int32_t V,
+                   int32_t K, int32_t num_logprobs, int32_t* out_tokens, float* out_logprobs,
+                   int32_t* out_topk_ids, float* out_topk_logprobs, void* stream);
+
 /* Message for the last failing call on `handle` ("" if none); static storage
  * owned by the handle, valid until the next call on it. */
 const char* vt_last_error(const vt_sampler* handle);
