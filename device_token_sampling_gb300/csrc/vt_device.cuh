@@ -225,6 +225,25 @@ __device__ __forceinline__ bool minp_pass(float zt, float m_t, double lmp) {
   return (double)zt - (double)m_t >= lmp;
 }
 
+// bf16 code bins.  Every element whose bf16 pattern is the same has the same
+// tempered value and mass, so a bin per bf16 value below the row maximum
+// gives exact masses as count x mass.  code16 is a signed code, monotone in the
+// value, that merges the magnitudes below 2^-12 (and both zeros) into code 0;
+// slot = code(max) - code(x), slots from kCodeSlots - 1 on are one catch-all.
+// The code-0 slot and the catch-all hold several values: their masses are
+// summed per element.
+constexpr int kCodeSlots = 4096;
+constexpr int kCodeEmin = 115;  // bf16 exponent field of 2^-12
+__device__ __forceinline__ int code16(uint32_t u) {
+  const int m = (int)(u & 0x7FFFu) - (kCodeEmin << 7) + 1;
+  const int v = m > 0 ? m : 0;
+  return (u & 0x8000u) ? -v : v;
+}
+__device__ __forceinline__ float code_value(int code) {  // code != 0
+  const uint32_t mag = (uint32_t)((code < 0 ? -code : code) - 1 + (kCodeEmin << 7));
+  return __uint_as_float(((code < 0 ? 0x8000u : 0u) | mag) << 16);
+}
+
 // ---- order-preserving keys -------------------------------------------------
 // Monotone map of a non-NaN float to uint32 (-0 and +0 map together).
 __device__ __forceinline__ uint32_t ord_key(float f) {
@@ -325,6 +344,28 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
   const float t2 = (m2 == -INFINITY) ? 0.f : s2 * ex2_approx((m2 - mn) * a);
   m = mn;
   s = s1 + t2;
+}
+
+// Descending bitonic sort of keys[0, N) in shared memory by the NT threads of
+// the CTA, N a power of two (every thread calls it).
+template <int NT>
+__device__ void smem_sort_desc(uint64_t* keys, int N) {
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < N; i += NT) {
+        const int p = i ^ j;
+        if (p > i) {
+          const bool desc = (i & k) == 0;
+          const uint64_t a = keys[i], b = keys[p];
+          if (desc ? (a < b) : (a > b)) {
+            keys[i] = b;
+            keys[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
 }
 
 }  // namespace vt

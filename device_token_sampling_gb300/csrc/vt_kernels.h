@@ -124,63 +124,35 @@ cudaError_t launch_build_counts(const int32_t* raw, const int64_t* offs, int max
 cudaError_t launch_append(int2* hist, int32_t* hist_len, int32_t hist_cap, const int32_t* tokens,
                           int32_t* row_status, int B, cudaStream_t stream);
 
-// ---- the row kernels (vt_rows.cu) --------------------------------------------
-// bf16 rows without penalties.  The pass kernel runs one CTA per (row, slice):
-// the slice is copied into shared memory once and every pass reads it there;
-// each CTA leaves its partial results in global memory, and the last CTA of a
-// row to finish (an atomic count per row) completes the row.  Rows whose kept
-// set needs every element (top-p or min-p without a bounding top-k) also get
-// the draw kernel, which reads those rows once more and draws over the kept
-// set; again the last CTA of each row writes it.  Rows neither settles
-// exactly are handed to the selection kernel through the SlowRow records.
-constexpr int kRowMaxC = 16;      // CTAs per row at most
-constexpr int kRowSlots = 4096;   // code slots of the count histogram
+// ---- the flat kernels (vt_flat.cu) -------------------------------------------
+// bf16 batches without penalties or top-p decay, rows 16-byte aligned.  Six
+// launches, none of whose CTAs waits on another: per-slice statistics (one
+// read of the logits from HBM), per-row statistics and thresholds, per-slice
+// collection (candidates, code-slot mass histograms, draw contenders; a second
+// read, from L2), per-row completion of the rows the candidates settle, and for
+// top-p rows a fine count inside the boundary bin and the row's completion.
+// Rows none of them settles exactly go to the selection kernel through the
+// SlowRow records.
+constexpr int kFlatMaxC = 32;        // slices per row at most
+constexpr int kFlatMaxNV = 12;       // 16-byte vectors per thread of a slice
+constexpr int kFlatCandCap = 4096;   // candidate keys per row
+constexpr int kFlatContCap = 512;    // draw contenders per row
+constexpr int kFlatKMax = 1024;      // largest top_k the candidates settle
+constexpr int kFlatBins = 64;        // coarse bins of 64 code slots
 
-struct __align__(16) RowPartG {   // one CTA's partial results for its row
-  float xmax;                     // maximum before temperature (-inf: none)
-  float s;                        // sum of exp(z_t - fl(xmax / T))
-  int arg;                        // lowest index of xmax (INT_MAX: none)
-  int bad;                        // a NaN or +inf
-  int cmax;                       // code of xmax
-  int thr;                        // candidates / counts cover codes >= thr
-  int thr_n;                      // the top-n candidates cover codes >= thr_n
-  unsigned int catch_cnt;         // counted elements below the slot window
-  int ncand;                      // candidates written (> capacity: overflow)
-  int err;
-  float best_s, best_z;           // draw partial: best Gumbel score, its z_t
-  int best_j;                     //   and index
-  int kth_j;                      // the last kept index when held here (-1)
-  unsigned long long last_key;    // rows keeping everything: last of the order here
-  int fin;                        //   and the finite elements here
-  int pad0, pad1, pad2;
+struct FlatPlan {
+  int C;   // slices per row (0: the flat kernels do not take this width)
+  int L;   // elements per slice, a multiple of 8
+  int NV;  // 16-byte vectors per thread
 };
 
-struct __align__(16) RowWalk {    // a full-histogram row's walk, for the draw kernel
-  int action;                     // 0: draw; 1: nothing to draw (written or handed over)
-  int beta;                       // kept boundary slot (-1: every finite element kept)
-  int L3;                         // kept count
-  float kth_z;                    // tempered value of the last kept element
-  float m_t, lnS;                 // row statistics
-  int cmax;                       // code of the row maximum
-  int last_rank;                  // CTA holding the last kept element
-  int cb[kRowMaxC];               // kept elements of slot beta per CTA
-  int nb[kRowMaxC];               // elements of slot beta per CTA
-};
-
-struct RowArgs {
-  const void* logits;        // [rows][ld] bf16
+struct FlatArgs {
+  const void* logits;  // [B][ld] bf16
   int64_t ld;
-  int32_t B, V;
-  const int32_t* order;      // [norder] rows in processing order; rows >= B are skipped
-  int32_t norder;
-  int32_t C;                 // CTAs per row
+  int32_t B, V, C, L, NV;
   int32_t n_logprobs;
-  int32_t slice;             // elements per CTA (a multiple of 8)
-  int32_t aligned;           // rows 16-byte aligned: slices arrive by bulk copy
-  uint32_t buf_bytes;        // bytes of the slice buffer (a multiple of 128)
-  const RowParams* params;   // [B]
-  uint64_t* seeds;           // [B], advanced once per row
-  DecayState* decay;         // [B]
+  const RowParams* params;
+  uint64_t* seeds;
   int32_t* out_tokens;
   float* out_logprobs;       // may be null
   int32_t* out_topk_ids;     // [B][n]
@@ -189,42 +161,23 @@ struct RowArgs {
   float* dbg_kth_value;
   int32_t* dbg_kth_index;
   int32_t* dbg_kept;
-  int32_t* err_word;
-  SlowRow* slow;             // hand-over records and list, as in SampleArgs
+  SlowRow* slow;             // hand-over records and list, as SampleArgs
   int32_t* slow_list;
   uint32_t* slow_ctl;
-  // scratch (handle-owned)
-  RowPartG* part;            // [rows][C]
-  uint64_t* cand;            // [rows][C][cand_cap] candidate records
-  int32_t cand_cap;
-  uint32_t* ghist;           // [rows][C][kRowSlots] count histograms
-  uint32_t* ctl;             // [rows] CTAs arrived (reset by the row's last CTA)
-  int32_t* flist;            // [rows] rows for the draw kernel
-  uint32_t* fctl;            // [4] rows in flist, draw CTAs done (zero between calls)
-  RowWalk* walk;             // [rows]
-  unsigned long long* trace; // optional [rows][C][kTraceSlots] phase stamps (ns)
+  void* scratch;             // flat_scratch_bytes(B, C) bytes
 };
 
-struct RowPlan {
-  int cluster;        // CTAs per row (0: the row kernels do not take this call)
-  int slice;          // elements per CTA
-  uint32_t buf_bytes; // slice buffer
-  size_t smem;        // dynamic shared memory per CTA
-  int clusters;       // unused (kept for the debug view): CTAs resident per SM
-};
+FlatPlan plan_flat(int V);
+size_t flat_scratch_bytes(int B, int C);
+// The six launches on `stream`; the caller then launches the selection kernel
+// for the rows handed over (launch_select_handed).
+cudaError_t launch_flat(const FlatArgs& a, cudaStream_t stream);
 
-// Plan the row kernels for V bf16 elements per row: CTAs per row such that a
-// slice is at most 76 KB.  cluster = 0 when V needs more than kRowMaxC CTAs.
-RowPlan plan_rows(int B, int V);
-
-// The pass kernel over B rows (grid B * C), then, when `draw_rows` > 0, the
-// draw kernel over at most that many rows (grid draw_rows * C).
-cudaError_t launch_rows(const RowArgs& args, const RowPlan& plan, int draw_rows,
-                        cudaStream_t stream);
-
-// The selection kernel alone over the rows the row kernels handed over.
+// The selection kernel alone over the rows another launch handed over
+// (max_clusters > 0: at most that many of its clusters).
 cudaError_t launch_select_handed(const SampleArgs& args, const LaunchPlan& plan, int dtype,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream,
+                                 int max_clusters = 0);
 
 // ---- the vocabulary-sharded sampler (vt_shard.cu) ---------------------------
 struct ShardArgs {

@@ -701,24 +701,6 @@ enum Pred { kPredAll = 0, kPredSurv = 1 };
 constexpr float kDScale = 64.0f;
 constexpr unsigned long long kNegInfKey = 0x007FFFFF00000000ull;  // elem_key(-inf, ~0)
 
-// bf16 code bins.  Every element whose bf16 pattern is the same has the same
-// tempered value and mass, so a bin per bf16 value below the row maximum
-// gives exact masses as count x mass.  code16 is a signed code, monotone in the
-// value, that merges the magnitudes below 2^-12 (and both zeros) into code 0;
-// slot = code(max) - code(x), slots from kCodeSlots - 1 on are one catch-all.
-// The code-0 slot and the catch-all hold several values: their masses are
-// summed per element.
-constexpr int kCodeSlots = 4096;
-constexpr int kCodeEmin = 115;  // bf16 exponent field of 2^-12
-__device__ __forceinline__ int code16(uint32_t u) {
-  const int m = (int)(u & 0x7FFFu) - (kCodeEmin << 7) + 1;
-  const int v = m > 0 ? m : 0;
-  return (u & 0x8000u) ? -v : v;
-}
-__device__ __forceinline__ float code_value(int code) {  // code != 0
-  const uint32_t mag = (uint32_t)((code < 0 ? -code : code) - 1 + (kCodeEmin << 7));
-  return __uint_as_float(((code < 0 ? 0x8000u : 0u) | mag) << 16);
-}
 // tempered value of regular slot sl below the maximum code cmax
 __device__ __forceinline__ float zq_value(int cmax, int sl, float inv_t) {
   return __fmul_rn(code_value(cmax - sl), inv_t);
@@ -3485,17 +3467,19 @@ cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dt
 }
 
 cudaError_t launch_select_handed(const SampleArgs& args, const LaunchPlan& plan, int dtype,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int max_clusters) {
   if (plan.sel.clusters < 1) return cudaErrorInvalidConfiguration;
+  const int G = (max_clusters > 0 && max_clusters < plan.sel.clusters) ? max_clusters
+                                                                      : plan.sel.clusters;
   cudaLaunchAttribute attr[1];
   if (dtype == 0) {
     cudaLaunchConfig_t cfg = select_config<float>(plan.sel, attr);
-    cfg.gridDim = dim3((unsigned)(plan.sel.clusters * plan.sel.cluster), 1, 1);
+    cfg.gridDim = dim3((unsigned)(G * plan.sel.cluster), 1, 1);
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, select_kernel<float>, args, plan.sel);
   }
   cudaLaunchConfig_t cfg = select_config<uint16_t>(plan.sel, attr);
-  cfg.gridDim = dim3((unsigned)(plan.sel.clusters * plan.sel.cluster), 1, 1);
+  cfg.gridDim = dim3((unsigned)(G * plan.sel.cluster), 1, 1);
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, select_kernel<uint16_t>, args, plan.sel);
 }

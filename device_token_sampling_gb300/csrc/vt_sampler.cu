@@ -46,16 +46,8 @@ struct vt_sampler {
   int32_t* d_slow_list = nullptr;  // [2][max_batch]: one list per launch pair
   uint32_t* d_slow_ctl = nullptr;  // [2][4]
   int32_t* d_rows = nullptr;       // [max_batch]: main rows, then side rows
-  int32_t* d_order = nullptr;      // [max_batch]: rows in the row kernels' order
-  // scratch of the row kernels
-  vt::RowPartG* d_rpart = nullptr;  // [max_batch][row_cmax]
-  uint64_t* d_rcand = nullptr;      // [max_batch][row_cmax][kRowCandCap]
-  uint32_t* d_rhist = nullptr;      // [max_batch][row_cmax][kRowSlots]
-  uint32_t* d_rctl = nullptr;       // [max_batch]
-  int32_t* d_rflist = nullptr;      // [max_batch]
-  uint32_t* d_rfctl = nullptr;      // [4]
-  vt::RowWalk* d_rwalk = nullptr;   // [max_batch]
-  int row_cmax = 0;
+  void* d_flat = nullptr;           // scratch of the flat kernels (bf16 rows up to max_vocab)
+  size_t flat_bytes = 0;
   float2* d_probs_part = nullptr;  // (max, exp-sum) partials of the filtered distribution
   size_t probs_part_cap = 0;
   // the side stream: rows routed straight to the selection kernel run there,
@@ -67,8 +59,7 @@ struct vt_sampler {
   int n_main = 0, n_side = 0;
   int last_launches = 0;  // kernels the last vt_sample launched
   int last_pairs = 1;     // hand-over lists the last vt_sample used
-  int path = 1;           // 0: the row kernel where it applies; 1: always the streaming kernel
-  std::map<std::pair<int, int>, vt::RowPlan> row_plans;
+  int path = 1;  // 1: the streaming kernel; 2: the flat kernels where they apply
   // pinned host staging
   vt::RowParams* h_params = nullptr;
   uint64_t* h_seeds = nullptr;
@@ -77,7 +68,6 @@ struct vt_sampler {
   int64_t* h_raw_offs = nullptr;
   int32_t* h_err = nullptr;
   int32_t* h_rows = nullptr;
-  int32_t* h_order = nullptr;
   cudaEvent_t ev_params = nullptr, ev_counts = nullptr;
   bool params_pending = false, counts_pending = false;
   // staging for vt_sample_host
@@ -102,7 +92,6 @@ struct vt_sampler {
 
 namespace {
 
-constexpr int kRowCandCap = 4096;  // candidate records per row-kernel CTA
 
 // Host-side fault injection for the failure-path tests, read at each call:
 //   VT_FAULT_INJECT=alloc:<n>  the n-th device allocation of vt_sampler_create
@@ -176,17 +165,9 @@ void free_all(vt_sampler* h) {
   dfree(h->d_slow_list);
   dfree(h->d_slow_ctl);
   dfree(h->d_rows);
-  dfree(h->d_order);
-  dfree(h->d_rpart);
-  dfree(h->d_rcand);
-  dfree(h->d_rhist);
-  dfree(h->d_rctl);
-  dfree(h->d_rflist);
-  dfree(h->d_rfctl);
-  dfree(h->d_rwalk);
+  dfree(h->d_flat);
   dfree(h->d_probs_part);
   if (h->h_rows) cudaFreeHost(h->h_rows);
-  if (h->h_order) cudaFreeHost(h->h_order);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_launched) cudaEventDestroy(h->ev_launched);
@@ -281,18 +262,13 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   dal((void**)&h->d_slow_list, 2 * B * sizeof(int32_t));
   dal((void**)&h->d_slow_ctl, 8 * sizeof(uint32_t));
   dal((void**)&h->d_rows, B * sizeof(int32_t));
-  dal((void**)&h->d_order, B * sizeof(int32_t));
-  // the row kernels: CTAs per row of the largest bf16 row (76 KB slices)
-  h->row_cmax = std::min(vt::kRowMaxC, (cfg->max_vocab + 38911) / 38912);
+  // the flat kernels: slices of the widest row the handle takes
   {
-    const size_t RC = B * (size_t)h->row_cmax;
-    dal((void**)&h->d_rpart, RC * sizeof(vt::RowPartG));
-    dal((void**)&h->d_rcand, RC * (size_t)kRowCandCap * sizeof(uint64_t));
-    dal((void**)&h->d_rhist, RC * (size_t)vt::kRowSlots * sizeof(uint32_t));
-    dal((void**)&h->d_rctl, B * sizeof(uint32_t));
-    dal((void**)&h->d_rflist, B * sizeof(int32_t));
-    dal((void**)&h->d_rfctl, 4 * sizeof(uint32_t));
-    dal((void**)&h->d_rwalk, B * sizeof(vt::RowWalk));
+    const vt::FlatPlan fp = vt::plan_flat(cfg->max_vocab);
+    if (fp.C > 0) {
+      h->flat_bytes = vt::flat_scratch_bytes((int)B, fp.C);
+      dal(&h->d_flat, h->flat_bytes);
+    }
   }
   // B rows of ceil(V / max range) + 1 splits, plus the splits that small
   // batches add to fill the GPU (plan_probs never asks for more)
@@ -301,7 +277,6 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
                       (size_t)vt::kProbsCtasPerSm * h->num_sms;
   dal((void**)&h->d_probs_part, h->probs_part_cap * sizeof(float2));
   hal((void**)&h->h_rows, B * sizeof(int32_t));
-  hal((void**)&h->h_order, B * sizeof(int32_t));
   hal((void**)&h->h_params, B * sizeof(vt::RowParams));
   hal((void**)&h->h_seeds, B * sizeof(uint64_t));
   hal((void**)&h->h_decay, B * sizeof(vt::DecayState));
@@ -327,8 +302,6 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   if (cudaMemset(h->d_hist_len, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_err, 0, sizeof(int32_t)) != cudaSuccess ||
       cudaMemset(h->d_slow_ctl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
-      cudaMemset(h->d_rctl, 0, B * sizeof(uint32_t)) != cudaSuccess ||
-      cudaMemset(h->d_rfctl, 0, 4 * sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(h->d_seeds, 0, B * sizeof(uint64_t)) != cudaSuccess ||
       cudaMemset(h->d_status, 0, B * sizeof(int32_t)) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess)
@@ -453,22 +426,6 @@ int vt_reset_params_ex(vt_sampler* h, int32_t B, const float* temperature, const
   std::stable_sort(h->h_rows, h->h_rows + nm, [&](int x, int y) { return weight(x) > weight(y); });
   h->n_main = nm;
   h->n_side = ns;
-  // The row kernel's order: its clusters take rows round-robin from this
-  // list, so the costliest rows go first -- top-p rows whose kept set can
-  // reach far (every element counted and many drawn), then rows that draw
-  // over many elements (large top-k, min-p alone, no filter), then top-k rows
-  // by k, greedy rows last.
-  auto cost = [&](int r) -> long long {
-    const uint32_t f = h->row_flags[r];
-    if (f & vt::kRowGreedy) return 0;
-    const int k = top_k[r];
-    const bool kcut = k > 1;
-    if ((f & (vt::kRowTopP | vt::kRowDecay)) && !kcut) return 3LL << 40;
-    if (!kcut || k > 2048) return 2LL << 40;
-    return (1LL << 40) + k;
-  };
-  for (int r = 0; r < B; ++r) h->h_order[r] = r;
-  std::stable_sort(h->h_order, h->h_order + B, [&](int x, int y) { return cost(x) > cost(y); });
   // A failed upload leaves the device parameters undefined: the handle then
   // counts as never reset (vt_sample returns VT_ERR_STATE until the next reset).
   h->params_B = 0;
@@ -480,8 +437,6 @@ int vt_reset_params_ex(vt_sampler* h, int32_t B, const float* temperature, const
   VT_CK(h, cudaMemcpyAsync(h->d_decay, h->h_decay, (size_t)B * sizeof(vt::DecayState),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaMemcpyAsync(h->d_rows, h->h_rows, (size_t)B * sizeof(int32_t),
-                           cudaMemcpyHostToDevice, st));
-  VT_CK(h, cudaMemcpyAsync(h->d_order, h->h_order, (size_t)B * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st));
   VT_CK(h, cudaEventRecord(h->ev_params, st));
   h->params_pending = true;
@@ -653,20 +608,18 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     a.trace_ctas = a.trace ? h->trace_ctas : 0;
     return a;
   };
-  // bf16 rows without penalties: the row kernels, then the selection kernel for
-  // the rows they hand over (counts appended by one more launch)
-  const vt::RowPlan* rplan = nullptr;
-  if (dtype == VT_DTYPE_BF16 && !any_pen && h->path == 0) {
-    auto key = std::make_pair(B, V);
-    auto it = h->row_plans.find(key);
-    if (it == h->row_plans.end()) it = h->row_plans.emplace(key, vt::plan_rows(B, V)).first;
-    if (it->second.cluster > 0 && it->second.cluster <= h->row_cmax) rplan = &it->second;
+  // bf16 calls without penalties or top-p decay on 16-byte aligned rows: the
+  // flat kernels, then the selection kernel for the rows they hand over
+  bool flat = false;
+  vt::FlatPlan fplan{0, 0, 0};
+  if (dtype == VT_DTYPE_BF16 && !any_pen && !out_probs && h->path == 2 && h->d_flat &&
+      (uintptr_t)logits % 16 == 0 && ((uint64_t)ld * 2) % 16 == 0) {
+    fplan = vt::plan_flat(V);
+    bool decay = false;
+    for (int r = 0; r < B && !decay; ++r) decay = (h->row_flags[r] & vt::kRowDecay) != 0;
+    flat = fplan.C > 0 && !decay && vt::flat_scratch_bytes(B, fplan.C) <= h->flat_bytes;
   }
-  // other bf16 calls over every row split the rows between the two streams
-  const bool split = !rplan && dtype == VT_DTYPE_BF16 && B == h->params_B && h->n_side > 0 &&
-                     h->n_main > 0;
-  h->last_pairs = split ? 2 : 1;
-  if (rplan) {
+  if (flat) {
     const vt::LaunchPlan* plan = nullptr;
     const int rc = get_plan(B, &plan);
     if (rc != VT_OK) return rc;
@@ -674,66 +627,57 @@ static int sample_impl(vt_sampler* h, const void* logits, int32_t dtype, int32_t
     sa.update_counts = 0;
     sa.trace = nullptr;
     sa.trace_ctas = 0;
-    // rows whose kept set may need every element go through the draw kernel:
-    // sampled rows with a filter (top-k, top-p, min-p, top-p decay) other than
-    // a top-k of at most 1024 (a superset of the rows the pass kernel lists)
-    int draw_rows = 0;
-    for (int r = 0; r < B; ++r) {
-      const uint32_t f = h->row_flags[r];
-      const int k = h->h_params[r].top_k;
-      const bool topk = k > 1 && k < V;
-      const bool filtered = topk || (f & (vt::kRowTopP | vt::kRowMinP | vt::kRowDecay));
-      if (!(f & vt::kRowGreedy) && filtered && !(topk && k <= 1024)) ++draw_rows;
-    }
-    vt::RowArgs ra;
-    std::memset(&ra, 0, sizeof ra);
-    ra.logits = logits;
-    ra.ld = ld;
-    ra.B = B;
-    ra.V = V;
-    ra.order = h->d_order;
-    ra.norder = h->params_B;
-    ra.C = rplan->cluster;
-    ra.n_logprobs = n;
-    ra.slice = rplan->slice;
-    ra.aligned = sa.aligned;
-    ra.buf_bytes = rplan->buf_bytes;
-    ra.params = h->d_params;
-    ra.seeds = h->d_seeds;
-    ra.decay = h->d_decay;
-    ra.out_tokens = out_tokens;
-    ra.out_logprobs = out_logprobs;
-    ra.out_topk_ids = out_topk_ids;
-    ra.out_topk_logprobs = out_topk_logprobs;
-    ra.row_status = h->d_status;
-    ra.dbg_kth_value = h->d_kth_v;
-    ra.dbg_kth_index = h->d_kth_i;
-    ra.dbg_kept = h->d_kept;
-    ra.err_word = h->d_err;
-    ra.slow = h->d_slow;
-    ra.slow_list = sa.slow_list;
-    ra.slow_ctl = sa.slow_ctl;
-    ra.part = h->d_rpart;
-    ra.cand = h->d_rcand;
-    ra.cand_cap = kRowCandCap;
-    ra.ghist = h->d_rhist;
-    ra.ctl = h->d_rctl;
-    ra.flist = h->d_rflist;
-    ra.fctl = h->d_rfctl;
-    ra.walk = h->d_rwalk;
-    // the phase trace is laid out by row (params_B rows of C CTAs)
-    ra.trace = (h->trace && (int64_t)h->params_B * rplan->cluster <= h->trace_ctas) ? h->trace
-                                                                                     : nullptr;
-    VT_CK(h, vt::launch_rows(ra, *rplan, draw_rows, st));
+    vt::FlatArgs fa;
+    std::memset(&fa, 0, sizeof fa);
+    fa.logits = logits;
+    fa.ld = ld;
+    fa.B = B;
+    fa.V = V;
+    fa.C = fplan.C;
+    fa.L = fplan.L;
+    fa.NV = fplan.NV;
+    fa.n_logprobs = n;
+    fa.params = h->d_params;
+    fa.seeds = h->d_seeds;
+    fa.out_tokens = out_tokens;
+    fa.out_logprobs = out_logprobs;
+    fa.out_topk_ids = out_topk_ids;
+    fa.out_topk_logprobs = out_topk_logprobs;
+    fa.row_status = h->d_status;
+    fa.dbg_kth_value = h->d_kth_v;
+    fa.dbg_kth_index = h->d_kth_i;
+    fa.dbg_kept = h->d_kept;
+    fa.slow = h->d_slow;
+    fa.slow_list = sa.slow_list;
+    fa.slow_ctl = sa.slow_ctl;
+    fa.scratch = h->d_flat;
+    VT_CK(h, vt::launch_flat(fa, st));
     if (h->phase_event) VT_CK(h, cudaEventRecord(h->phase_event, st));
-    VT_CK(h, vt::launch_select_handed(sa, *plan, dtype, st));
-    h->last_launches = draw_rows > 0 ? 3 : 2;
-    if (update_counts && !out_probs) {
+    // rows the flat kernels hand over are rare (a top_k above their limit,
+    // overflowing buffers): a few selection clusters, more for the former
+    int certain = 0;
+    for (int r = 0; r < B; ++r) {
+      const int k = h->h_params[r].top_k;
+      if (!(h->row_flags[r] & vt::kRowGreedy) && k > vt::kFlatKMax && k < V) ++certain;
+    }
+    VT_CK(h, vt::launch_select_handed(sa, *plan, dtype, st, certain + 4));
+    h->last_launches = 7;
+    h->last_pairs = 1;
+    if (update_counts) {
       VT_CK(h, vt::launch_append(h->d_hist, h->d_hist_len, sa.hist_cap, out_tokens, h->d_status,
                                  B, st));
       h->last_launches += 1;
     }
-  } else if (!split) {
+    h->last_B = B;
+    h->last_stream = st;
+    h->err.clear();
+    return VT_OK;
+  }
+  // other bf16 calls over every row split the rows between the two streams
+  const bool split = dtype == VT_DTYPE_BF16 && B == h->params_B && h->n_side > 0 &&
+                     h->n_main > 0;
+  h->last_pairs = split ? 2 : 1;
+  if (!split) {
     const vt::LaunchPlan* plan = nullptr;
     const int rc = get_plan(B, &plan);
     if (rc != VT_OK) return rc;
@@ -1062,21 +1006,8 @@ int vt_shard_merge(vt_sampler* h, const void* parts, int32_t S, int32_t B, int32
   return VT_OK;
 }
 
-int vt_debug_row_plan(vt_sampler* h, int32_t B, int32_t V, int32_t* cluster,
-                      int32_t* clusters, int32_t* slice, int64_t* smem_bytes) {
-  if (!h || !cluster || !clusters || !slice || !smem_bytes || B < 1 || V < 1)
-    return VT_ERR_INVALID_ARG;
-  DeviceGuard guard(h->cfg.device);
-  const vt::RowPlan p = vt::plan_rows(B, V);
-  *cluster = p.cluster;
-  *clusters = p.clusters;
-  *slice = p.slice;
-  *smem_bytes = (int64_t)p.smem;
-  return VT_OK;
-}
-
 int vt_debug_set_path(vt_sampler* h, int32_t path) {
-  if (!h || path < 0 || path > 1) return VT_ERR_INVALID_ARG;
+  if (!h || path < 1 || path > 2) return VT_ERR_INVALID_ARG;
   h->path = path;
   return VT_OK;
 }

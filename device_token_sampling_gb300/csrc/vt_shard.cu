@@ -42,26 +42,6 @@ struct __align__(16) ShardHead {
   uint32_t info;    // records written (bits 0..15), NaN or +inf seen (bit 30)
 };
 
-// Descending bitonic sort of keys[0, N) in shared memory, N a power of two.
-__device__ void smem_sort_desc(uint64_t* keys, int N) {
-  for (int k = 2; k <= N; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < N; i += kST) {
-        const int p = i ^ j;
-        if (p > i) {
-          const bool desc = (i & k) == 0;
-          const uint64_t a = keys[i], b = keys[p];
-          if (desc ? (a < b) : (a > b)) {
-            keys[i] = b;
-            keys[p] = a;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
 struct ShardSmem {
   uint64_t keys[kShardCand];
   float tm[kST];
@@ -304,7 +284,7 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
   while (P2 < n) P2 <<= 1;
   for (int i = n + tid; i < P2; i += kST) s.keys[i] = 0ull;
   __syncthreads();
-  smem_sort_desc(s.keys, P2);
+  smem_sort_desc<kST>(s.keys, P2);
   const int w = min(n, a.K);
   uint64_t* rec = reinterpret_cast<uint64_t*>(out + sizeof(ShardHead));
   for (int i = tid; i < w; i += kST) rec[i] = s.keys[i];
@@ -386,7 +366,7 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
   while (P2 < total) P2 <<= 1;
   for (int i = total + tid; i < P2; i += kST) s.keys[i] = 0ull;
   __syncthreads();
-  smem_sort_desc(s.keys, P2);
+  smem_sort_desc<kST>(s.keys, P2);
   // finite records (the -inf ones sort last)
   int fin = 0;
   for (int i = tid; i < total; i += kST) fin += key_z(s.keys[i]) > -INFINITY;

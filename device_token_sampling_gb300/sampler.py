@@ -80,7 +80,6 @@ SIGNATURES = {
     "vt_shard_part_bytes": (I64, [I32]),
     "vt_shard_partials": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, I32, P, P]),
     "vt_shard_merge": (C.c_int, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P]),
-    "vt_debug_row_plan": (C.c_int, [P, I32, I32, P, P, P, P]),
     "vt_sample_noalloc": (C.c_int, [I32, P, I32, I32, I32, I64, P, P, P, P, P, I32, P, P, P, P,
                                     P, I32, P, C.c_char_p, I32]),
     "vt_last_error": (C.c_char_p, [P]),
@@ -364,15 +363,6 @@ class Sampler:
         self._check(self._lib.vt_debug_last_handover(self._h, C.byref(v)), "vt_debug_last_handover")
         return int(v.value)
 
-    def row_plan(self, B: int, V: int):
-        """The row kernel's plan for B rows of V bf16 logits: (CTAs per row,
-        resident clusters, elements per CTA, dynamic shared memory bytes)."""
-        c, n, sl, sm = C.c_int32(), C.c_int32(), C.c_int32(), C.c_int64()
-        self._check(self._lib.vt_debug_row_plan(self._h, B, V, C.byref(c), C.byref(n),
-                                                C.byref(sl), C.byref(sm)), "vt_debug_row_plan")
-        return int(c.value), int(n.value), int(sl.value), int(sm.value)
-
-    # -- the vocabulary split over several devices ----------------------------
     def shard_partials(self, logits, v0: int, V: int, K: int, out=None, stream=None,
                        dtype: int | None = None):
         """vt_shard_partials: this shard's records for the columns [v0, v0 + Vs)
@@ -419,8 +409,8 @@ class Sampler:
         return tok, lp, tid, tlp
 
     def set_path(self, path: int):
-        """0: the row kernel for bf16 calls without penalties; 1 (the default):
-        the streaming kernel for every call."""
+        """1 (the default): the streaming kernel for every call; 2: the flat
+        kernels for bf16 calls without penalties or top-p decay."""
         self._check(self._lib.vt_debug_set_path(self._h, int(path)), "vt_debug_set_path")
 
     def last_launches(self) -> int:

@@ -274,8 +274,9 @@ int vt_debug_probs_plan(int32_t B, int32_t V, int32_t num_sms, int32_t* splits, 
 /* Debug: phase trace.  With a device buffer of capacity_ctas * slots_per_cta
  * uint64 entries set, each later vt_sample whose grid fits writes, per CTA,
  * the GPU global timer (ns) at each phase boundary (slots not reached keep
- * their old value).  The row kernel writes entry (row * CTAs per row + rank)
- * per row it processes.  *slots_per_cta receives the slot count.  NULL turns it
+ * their old value): the streaming kernel's CTA (row * CTAs per row + rank)
+ * writes entry row * CTAs per row + rank.  *slots_per_cta receives the slot
+ * count.  NULL turns it
  * off.  The buffer stays owned by the caller and must outlive its use. */
 int vt_debug_set_trace(vt_sampler* handle, uint64_t* dev_trace, int64_t capacity_ctas,
                        int32_t* slots_per_cta);
@@ -291,24 +292,20 @@ int vt_debug_set_phase_event(vt_sampler* handle, void* event);
  * in one pass could not settle).  Synchronises the handle's last stream. */
 int vt_debug_last_handover(vt_sampler* handle, int32_t* rows);
 
-/* Debug: which sampling path later vt_sample calls take.  0: bf16 calls
- * without penalties run the persistent row kernel (each row's slice resident
- * in shared memory, rows it cannot settle handed to the selection kernel);
- * other calls run the streaming kernel.  1 (the default): every call runs the
- * streaming kernel (and its hand-over to the selection kernel).
- * Both give the same tokens and kept sets.  Errors: VT_ERR_INVALID_ARG. */
+/* Debug: which sampling path later vt_sample calls take.  1 (the default):
+ * every call runs the streaming kernel (and its hand-over to the selection
+ * kernel).  2: bf16 calls without penalties, top-p decay or the exported
+ * distribution, on 16-byte aligned rows, run the six flat kernels (per-slice
+ * statistics, per-row thresholds, per-slice candidates and code-slot counts,
+ * per-row completion, and for top-p rows a fine count and the boundary), the
+ * rows they cannot settle handed to the selection kernel; other calls run the
+ * streaming kernel.  Both give the same tokens and kept sets.
+ * Errors: VT_ERR_INVALID_ARG. */
 int vt_debug_set_path(vt_sampler* handle, int32_t path);
 
-/* Debug: the row kernel's plan for B rows of V bf16 elements: CTAs per row
- * (0: the row kernel does not take such calls), clusters resident at once
- * (the persistent grid), elements per CTA and dynamic shared memory per CTA.
- * Errors: VT_ERR_INVALID_ARG. */
-int vt_debug_row_plan(vt_sampler* handle, int32_t B, int32_t V, int32_t* cluster,
-                      int32_t* clusters, int32_t* slice, int64_t* smem_bytes);
-
 /* Debug: how many kernels the last vt_sample launched: 2 on one stream (the
- * streaming or row kernel, then the selection kernel; one more when a row
- * kernel call appends the tokens to the counts), or 3 when the call split its
+ * streaming kernel, then the selection kernel), 7 on the flat path (one more
+ * when it appends the tokens to the counts), or 3 when the call split its
  * rows between the handle's two streams (the selection kernel alone, taking
  * its rows' statistics itself, on the second stream; the pair on the first).
  * 0 before the first call.  Does not synchronise. */

@@ -35,10 +35,10 @@ def _built():
 def check(w, expect_handover=True):
     """Both sampling paths against the oracle: the streaming kernel (which must
     hand rows to the selection kernel here) and, for bf16 rows without
-    penalties, the row kernel (which settles most rows itself)."""
+    penalties, the flat kernels (which settle most rows themselves)."""
     o = O.sample_workload(w, want_zt=True)
     g = None
-    for path in (1, 0):
+    for path in (1, 2):
         s = make_sampler(w)
         try:
             s.set_path(path)
