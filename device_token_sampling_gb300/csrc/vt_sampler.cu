@@ -71,12 +71,22 @@ struct vt_sampler {
   cudaEvent_t ev_params = nullptr, ev_counts = nullptr;
   bool params_pending = false, counts_pending = false;
   // staging for vt_sample_host
-  void* d_io_logits = nullptr;
+  // host-memory calls: two staging slots; a step's logits are copied in on
+  // io_copy while the previous step samples on the caller's stream
+  struct IoSlot {
+    void* logits = nullptr;
+    int32_t* tokens = nullptr;
+    float* lp = nullptr;
+    int32_t* tid = nullptr;
+    float* tlp = nullptr;
+    cudaEvent_t copied = nullptr;  // its logits are on the device
+    cudaEvent_t done = nullptr;    // its step and output copies are complete
+    bool busy = false;
+  };
+  IoSlot io[2];
   size_t io_bytes = 0;
-  int32_t* d_io_tokens = nullptr;
-  float* d_io_lp = nullptr;
-  int32_t* d_io_tid = nullptr;
-  float* d_io_tlp = nullptr;
+  cudaStream_t io_copy = nullptr;
+  int io_next = 0;
   // host mirror of the state machine
   int params_B = 0;
   std::vector<uint32_t> row_flags;
@@ -172,11 +182,16 @@ void free_all(vt_sampler* h) {
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_launched) cudaEventDestroy(h->ev_launched);
   if (h->side) cudaStreamDestroy(h->side);
-  dfree(h->d_io_logits);
-  dfree(h->d_io_tokens);
-  dfree(h->d_io_lp);
-  dfree(h->d_io_tid);
-  dfree(h->d_io_tlp);
+  for (auto& slot : h->io) {
+    dfree(slot.logits);
+    dfree(slot.tokens);
+    dfree(slot.lp);
+    dfree(slot.tid);
+    dfree(slot.tlp);
+    if (slot.copied) cudaEventDestroy(slot.copied);
+    if (slot.done) cudaEventDestroy(slot.done);
+  }
+  if (h->io_copy) cudaStreamDestroy(h->io_copy);
   hfree(h->h_params);
   hfree(h->h_seeds);
   hfree(h->h_decay);
@@ -285,11 +300,18 @@ int vt_sampler_create(const vt_sampler_config* cfg, vt_sampler** out) {
   hal((void**)&h->h_err, sizeof(int32_t));
   if (cfg->host_io) {
     h->io_bytes = B * (size_t)cfg->max_vocab * 4;
-    dal(&h->d_io_logits, h->io_bytes);
-    dal((void**)&h->d_io_tokens, B * sizeof(int32_t));
-    dal((void**)&h->d_io_lp, B * sizeof(float));
-    dal((void**)&h->d_io_tid, B * (n ? n : 1) * sizeof(int32_t));
-    dal((void**)&h->d_io_tlp, B * (n ? n : 1) * sizeof(float));
+    for (auto& slot : h->io) {
+      dal(&slot.logits, h->io_bytes);
+      dal((void**)&slot.tokens, B * sizeof(int32_t));
+      dal((void**)&slot.lp, B * sizeof(float));
+      dal((void**)&slot.tid, B * (n ? n : 1) * sizeof(int32_t));
+      dal((void**)&slot.tlp, B * (n ? n : 1) * sizeof(float));
+      if (ok && (cudaEventCreateWithFlags(&slot.copied, cudaEventDisableTiming) != cudaSuccess ||
+                 cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming) != cudaSuccess))
+        ok = false;
+    }
+    if (ok && cudaStreamCreateWithFlags(&h->io_copy, cudaStreamNonBlocking) != cudaSuccess)
+      ok = false;
   }
   if (!ok) return bail(VT_ERR_CUDA);
   if (cudaEventCreateWithFlags(&h->ev_params, cudaEventDisableTiming) != cudaSuccess ||
@@ -803,37 +825,69 @@ int vt_check_device_errors(vt_sampler* h) {
   return VT_OK;
 }
 
-int vt_sample_host(vt_sampler* h, const void* host_logits, int32_t dtype, int32_t B, int32_t V,
-                   int64_t ld, int32_t n, int32_t update_counts, int32_t* host_tokens,
-                   float* host_logprobs, int32_t* host_topk_ids, float* host_topk_logprobs,
-                   void* stream) {
+int vt_sample_host_async(vt_sampler* h, const void* host_logits, int32_t dtype, int32_t B,
+                         int32_t V, int64_t ld, int32_t n, int32_t update_counts,
+                         int32_t* host_tokens, float* host_logprobs, int32_t* host_topk_ids,
+                         float* host_topk_logprobs, void* stream) {
   if (!h) return VT_ERR_INVALID_ARG;
-  if (!h->d_io_logits) return set_err(h, VT_ERR_STATE, "handle created without host_io");
+  if (!h->io_copy) return set_err(h, VT_ERR_STATE, "handle created without host_io");
   if (!host_logits || !host_tokens) return set_err(h, VT_ERR_INVALID_ARG, "null host buffer");
   if (n > 0 && (!host_topk_ids || !host_topk_logprobs))
     return set_err(h, VT_ERR_INVALID_ARG, "top-k log-prob outputs are null");
+  if (dtype != VT_DTYPE_F32 && dtype != VT_DTYPE_BF16)
+    return set_err(h, VT_ERR_INVALID_ARG, "unknown dtype %d", dtype);
   const int es = dtype == VT_DTYPE_F32 ? 4 : 2;
   if (B < 1 || ld < 1) return set_err(h, VT_ERR_INVALID_ARG, "bad shape");
   const size_t bytes = (size_t)B * (size_t)ld * es;
   if (bytes > h->io_bytes) return set_err(h, VT_ERR_CAPACITY, "logits exceed host_io staging");
   DeviceGuard guard(h->cfg.device);
   cudaStream_t st = (cudaStream_t)stream;
-  VT_CK(h, cudaMemcpyAsync(h->d_io_logits, host_logits, bytes, cudaMemcpyHostToDevice, st));
-  const int rc = sample_impl(h, h->d_io_logits, dtype, B, V, ld, n, update_counts, h->d_io_tokens,
-                             h->d_io_lp, n ? h->d_io_tid : nullptr, n ? h->d_io_tlp : nullptr,
-                             nullptr, 0, st);
+  vt_sampler::IoSlot& slot = h->io[h->io_next];
+  // the copy-in waits, on the device, for the slot's previous step to finish
+  // with its buffers; the step waits for its copy-in
+  if (slot.busy) VT_CK(h, cudaStreamWaitEvent(h->io_copy, slot.done, 0));
+  VT_CK(h, cudaMemcpyAsync(slot.logits, host_logits, bytes, cudaMemcpyHostToDevice, h->io_copy));
+  VT_CK(h, cudaEventRecord(slot.copied, h->io_copy));
+  VT_CK(h, cudaStreamWaitEvent(st, slot.copied, 0));
+  const int rc = sample_impl(h, slot.logits, dtype, B, V, ld, n, update_counts, slot.tokens,
+                             slot.lp, n ? slot.tid : nullptr, n ? slot.tlp : nullptr, nullptr, 0,
+                             st);
   if (rc != VT_OK) return rc;
-  VT_CK(h, cudaMemcpyAsync(host_tokens, h->d_io_tokens, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
+  VT_CK(h, cudaMemcpyAsync(host_tokens, slot.tokens, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
   if (host_logprobs)
-    VT_CK(h, cudaMemcpyAsync(host_logprobs, h->d_io_lp, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
+    VT_CK(h, cudaMemcpyAsync(host_logprobs, slot.lp, (size_t)B * 4, cudaMemcpyDeviceToHost, st));
   if (n > 0) {
-    VT_CK(h, cudaMemcpyAsync(host_topk_ids, h->d_io_tid, (size_t)B * n * 4,
-                             cudaMemcpyDeviceToHost, st));
-    VT_CK(h, cudaMemcpyAsync(host_topk_logprobs, h->d_io_tlp, (size_t)B * n * 4,
+    VT_CK(h, cudaMemcpyAsync(host_topk_ids, slot.tid, (size_t)B * n * 4, cudaMemcpyDeviceToHost,
+                             st));
+    VT_CK(h, cudaMemcpyAsync(host_topk_logprobs, slot.tlp, (size_t)B * n * 4,
                              cudaMemcpyDeviceToHost, st));
   }
-  VT_CK(h, cudaStreamSynchronize(st));
+  VT_CK(h, cudaEventRecord(slot.done, st));
+  slot.busy = true;
+  h->io_next ^= 1;
+  return VT_OK;
+}
+
+int vt_sample_host_wait(vt_sampler* h) {
+  if (!h) return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  for (auto& slot : h->io) {
+    if (!slot.busy) continue;
+    slot.busy = false;
+    VT_CK(h, cudaEventSynchronize(slot.done));
+  }
   return vt_check_device_errors(h);
+}
+
+int vt_sample_host(vt_sampler* h, const void* host_logits, int32_t dtype, int32_t B, int32_t V,
+                   int64_t ld, int32_t n, int32_t update_counts, int32_t* host_tokens,
+                   float* host_logprobs, int32_t* host_topk_ids, float* host_topk_logprobs,
+                   void* stream) {
+  const int rc = vt_sample_host_async(h, host_logits, dtype, B, V, ld, n, update_counts,
+                                      host_tokens, host_logprobs, host_topk_ids,
+                                      host_topk_logprobs, stream);
+  if (rc != VT_OK) return rc;
+  return vt_sample_host_wait(h);
 }
 
 int vt_get_row_status(vt_sampler* h, int32_t* dev_status, void* stream) {

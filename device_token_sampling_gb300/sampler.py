@@ -77,6 +77,8 @@ SIGNATURES = {
     "vt_debug_last_handover": (C.c_int, [P, P]),
     "vt_debug_last_launches": (C.c_int, [P, P]),
     "vt_debug_set_path": (C.c_int, [P, I32]),
+    "vt_sample_host_async": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
+    "vt_sample_host_wait": (C.c_int, [P]),
     "vt_shard_part_bytes": (I64, [I32]),
     "vt_shard_partials": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, I32, P, P]),
     "vt_shard_merge": (C.c_int, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P]),
@@ -301,6 +303,29 @@ class Sampler:
                                       _stream_ptr(stream))
         self._check(rc, "vt_sample_host")
         return out
+
+    def sample_host_async(self, logits: np.ndarray, V: int, dtype: int, num_logprobs: int = 0,
+                          update_counts: bool = False, stream=None, out=None):
+        """vt_sample_host_async: enqueue one step from host logits [B, ld]
+        (pinned for an asynchronous copy); ``out`` is filled once
+        ``sample_host_wait`` returns, and both must stay alive until then."""
+        x = logits if logits.flags["C_CONTIGUOUS"] else np.ascontiguousarray(logits)
+        B, ld = x.shape
+        n = int(num_logprobs)
+        if out is None:
+            out = (np.empty(B, np.int32), np.empty(B, np.float32), np.empty((B, n), np.int32),
+                   np.empty((B, n), np.float32))
+        tok, lp, tid, tlp = out
+        rc = self._lib.vt_sample_host_async(self._h, _np_ptr(x), dtype, B, V, ld, n,
+                                            1 if update_counts else 0, _np_ptr(tok), _np_ptr(lp),
+                                            _np_ptr(tid) if n else None,
+                                            _np_ptr(tlp) if n else None, _stream_ptr(stream))
+        self._check(rc, "vt_sample_host_async")
+        return out
+
+    def sample_host_wait(self):
+        """vt_sample_host_wait: every enqueued host step complete."""
+        self._check(self._lib.vt_sample_host_wait(self._h), "vt_sample_host_wait")
 
     # -- views -----------------------------------------------------------------
     def check_device_errors(self):

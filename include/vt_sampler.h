@@ -223,15 +223,33 @@ int vt_sample_ex(vt_sampler* handle, const void* logits, int32_t dtype, int32_t 
                  float* out_logprobs, int32_t* out_topk_ids, float* out_topk_logprobs,
                  float* out_probs, int64_t ld_probs, void* stream);
 
-/* vt_sample from host memory: copies host logits [B][ld] into the handle's
- * device staging (created with host_io = 1), samples, copies the outputs back
- * into the host arrays (same shapes as vt_sample's), and synchronises
- * `stream` before returning.  Errors as vt_sample, plus VT_ERR_STATE when the
- * handle has no host staging. */
+/* vt_sample from host memory: vt_sample_host_async, then vt_sample_host_wait
+ * (the outputs are in the host arrays when it returns).  Errors as vt_sample,
+ * plus VT_ERR_STATE when the handle has no host staging (host_io = 0). */
 int vt_sample_host(vt_sampler* handle, const void* host_logits, int32_t dtype, int32_t B,
                    int32_t V, int64_t ld, int32_t num_logprobs, int32_t update_counts,
                    int32_t* host_tokens, float* host_logprobs, int32_t* host_topk_ids,
                    float* host_topk_logprobs, void* stream);
+
+/* One step from host memory without waiting: host logits [B][ld] (pinned
+ * memory for an asynchronous copy) are copied into the next of the handle's
+ * two device staging slots on the handle's own copy stream, the step samples
+ * on `stream` once they are there, and the outputs (vt_sample's shapes) are
+ * copied back into the host arrays on `stream`.  So the copy-in of one step
+ * runs while the previous step samples; a slot is reused only after its
+ * previous step's output copies are done (the copy stream waits for it on the
+ * device).  Steps keep their call order: seeds and counts advance as with
+ * vt_sample.  The host buffers must stay valid, and the outputs are not to be
+ * read, until vt_sample_host_wait returns.  Errors as vt_sample_host (raised
+ * before anything is enqueued). */
+int vt_sample_host_async(vt_sampler* handle, const void* host_logits, int32_t dtype, int32_t B,
+                         int32_t V, int64_t ld, int32_t num_logprobs, int32_t update_counts,
+                         int32_t* host_tokens, float* host_logprobs, int32_t* host_topk_ids,
+                         float* host_topk_logprobs, void* stream);
+
+/* Wait until every step enqueued by vt_sample_host_async is complete (its
+ * outputs in the host arrays), then vt_check_device_errors. */
+int vt_sample_host_wait(vt_sampler* handle);
 
 /* Synchronise the handle's last stream and report device-side faults raised
  * since the previous check: VT_ERR_TIMEOUT when a bounded wait inside a kernel

@@ -83,6 +83,36 @@ def test_sample_host(name):
         s.close()
 
 
+@pytest.mark.parametrize("path", [1, 2])
+def test_sample_host_async_steps(path):
+    """Four host steps enqueued back to back (each step's copy-in overlaps the
+    previous step's sampling through the two staging slots), waited for once:
+    every step equals the oracle on its own logits and advanced seeds."""
+    import copy
+    w = W.b256()
+    rng = np.random.default_rng(5)
+    steps = [w.logits] + [w.logits[rng.permutation(w.B)] for _ in range(3)]
+    pinned = []
+    for x in steps:
+        t = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+        pinned.append(t.numpy())
+    s = make_sampler(w, host_io=True)
+    try:
+        s.set_path(path)
+        s.reset_workload(w)
+        outs = [s.sample_host_async(x, w.V, W.DTYPE_BF16, num_logprobs=w.num_logprobs)
+                for x in pinned]
+        s.sample_host_wait()
+        for k, (x, (tok, lp, tid, tlp)) in enumerate(zip(steps, outs)):
+            wk = copy.copy(w)
+            wk.logits = x
+            o = O.sample_workload(wk, seed=advanced(w.seed, k))
+            compare_tokens(tok, lp, tid, tlp, o, where=f"async step {k} path {path}")
+        np.testing.assert_array_equal(s.seeds(w.B), advanced(w.seed, len(steps)))
+    finally:
+        s.close()
+
+
 # --------------------------------------------------------------------------
 # graph-captured steps on two streams, replayed as the benchmark replays them
 # --------------------------------------------------------------------------
