@@ -577,6 +577,150 @@ def run_gpu(args, w: W.Workload):
         dist.destroy_process_group()
 
 
+SHARD_K = 256  # the records each shard keeps per row
+
+
+def shard_bounded(w: W.Workload) -> W.Workload:
+    """The workload with every sampled row bounded by a top-k of at most
+    SHARD_K, the rows the vocabulary-split path takes: top-k rows keep
+    min(k, SHARD_K); rows without top-k get top_k = SHARD_K."""
+    import copy
+    v = copy.copy(w)
+    v.top_k = w.top_k.copy()
+    greedy = (w.temperature == 0) | (w.top_k == 1) | (w.top_p == 0) | (w.min_p == 1)
+    k = v.top_k
+    k[~greedy & ((k <= 1) | (k > SHARD_K))] = SHARD_K
+    v.name = f"{w.name} bounded to top_k <= {SHARD_K}"
+    return v
+
+
+def run_gpu_sharded(args, w: W.Workload):
+    """The vocabulary split over args.shards devices, run one shard after
+    another on one GPU: per step, vt_shard_partials over each shard's columns
+    (the work one device of a tensor-parallel group does), then vt_shard_merge
+    over the stacked records (what every device does after the all-gather)."""
+    import torch
+
+    from device_token_sampling_gb300 import sampler as S
+
+    rank, world, local = dist_env()
+    if world > 1:
+        raise SystemExit("--shards runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    w = shard_bounded(w)
+    B, V, n, Sh = w.B, w.V, w.num_logprobs, args.shards
+    s = S.Sampler(max_batch=B, max_vocab=V, max_logprobs=n, max_history=0, device=local)
+    s.reset_workload(w)
+    base = torch.from_numpy(np.ascontiguousarray(w.logits))
+    if w.dtype == W.DTYPE_BF16:
+        base = base.view(torch.int16)
+    bufs = [base.to(dev)]
+    gen = torch.Generator(device=dev)
+    for i in range(1, N_ROTATE):
+        gen.manual_seed(1000 + i)
+        bufs.append(bufs[0][torch.randperm(B, device=dev, generator=gen)].contiguous())
+    edges = np.linspace(0, V, Sh + 1).astype(int)
+    pb = int(s._lib.vt_shard_part_bytes(SHARD_K))
+    parts = torch.empty((Sh, B, pb), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, mid=None):
+        x = bufs[i % N_ROTATE]
+        for sh in range(Sh):
+            s.shard_partials(x[:, edges[sh]:edges[sh + 1]], int(edges[sh]), V, SHARD_K,
+                             out=parts[sh], stream=stream)
+        if mid is not None:
+            mid.record(stream)
+        return s.shard_merge(parts, V, SHARD_K, n, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    stream.synchronize()
+    s.check_device_errors()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(N_ROTATE):
+            step(i)
+    graph.replay()
+    stream.synchronize()
+    reps = max(1, args.steps // N_ROTATE)
+    clocks = ClockSampler(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    clocks.stop()
+    s.check_device_errors()
+    steps = reps * N_ROTATE
+    ms_per_step = ev0.elapsed_time(ev1) / steps
+    # the partials and the merge timed apart (eager steps, events on the stream)
+    split = []
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            a, m, b = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            step(i, mid=m)
+            b.record(stream)
+            split.append((a, m, b))
+    stream.synchronize()
+    part_ms = float(np.mean([a.elapsed_time(m) for a, m, _ in split[3:]]))
+    merge_ms = float(np.mean([m.elapsed_time(b) for _, m, b in split[3:]]))
+    # end to end: the step's logits from pinned host memory, the step, the
+    # outputs back to pinned host memory, every step
+    host = torch.from_numpy(np.ascontiguousarray(w.logits)).pin_memory()
+    if w.dtype == W.DTYPE_BF16:
+        host = host.view(torch.int16)
+    stage = torch.empty_like(bufs[0])
+    ho = pinned_outputs(B, n)
+    e2e_steps = 50
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            stage.copy_(host, non_blocking=True)
+            for sh in range(Sh):
+                s.shard_partials(stage[:, edges[sh]:edges[sh + 1]], int(edges[sh]), V, SHARD_K,
+                                 out=parts[sh], stream=stream)
+            tok, lp, tid, tlp = s.shard_merge(parts, V, SHARD_K, n, stream=stream)
+            for dst, src in zip(ho, (tok, lp, tid, tlp)):
+                torch.from_numpy(dst).copy_(src, non_blocking=True)
+    stream.synchronize()
+    e2e_value = B * e2e_steps / (time.perf_counter() - t0)
+    peak, peak_kind = load_peaks()
+    alg = int(w.V * w.elem_size * B + 2 * Sh * B * pb + B * (16 + 8 * n))
+    achieved = alg / (ms_per_step * 1e-3) / 1e9
+    cfg = workload_config(w)
+    cfg["workload"] = f"b256 (top_k <= {SHARD_K}) with the vocabulary split in {Sh} shards"
+    cfg["shards"] = Sh
+    cfg["parallelism"] = f"{Sh} vocabulary shards run one after another on one GPU"
+    line = {
+        "metric": METRIC, "value": B / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} (hbm_gbs)", "algorithmic_bytes_per_step": alg,
+                     "kernel": "vt_shard_partials x shards + vt_shard_merge",
+                     "kernel_ms": ms_per_step},
+        "split_ms": {"partials_all_shards": part_ms, "merge": merge_ms},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(host.numel() * host.element_size()),
+                "d2h_bytes_per_step": int(sum(a.nbytes for a in ho)), "steps": e2e_steps,
+                "api": "pinned host logits copied in, vt_shard_partials per shard, vt_shard_merge, "
+                       "outputs copied to pinned host memory, every step"},
+        "gpu_launches": (Sh + 1) * steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    s.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,6 +731,8 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shards", type=int, default=0,
+                    help="time the vocabulary-split variant with this many shards (one GPU)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 100 if args.workload == "large" else 2000
@@ -597,7 +743,9 @@ def main():
     else:
         from device_token_sampling_gb300 import _build
         _build.build()
-        if args.workload == "large":
+        if args.shards > 0:
+            run_gpu_sharded(args, w)
+        elif args.workload == "large":
             run_gpu_decode(args, w)
         else:
             run_gpu(args, w)
