@@ -108,13 +108,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
-// Wait for phase `phase` of an mbarrier, at most kWaitLimitNs.  Returns false
-// on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase) {
+// Wait for phase `phase` of an mbarrier, at most `limit_ns` of the global
+// timer (and at most 2^28 polls, should the timer not advance).  Returns
+// false when the wait ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, phase)) return true;
   const unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, phase)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  for (uint32_t polls = 0; !mbar_try_wait(bar, phase); ++polls) {
+    if (global_timer_ns() - t0 > limit_ns || polls >= (1u << 28)) return false;
   }
   return true;
 }

@@ -110,6 +110,12 @@ cudaError_t launch_sample(const SampleArgs& args, const LaunchPlan& plan, int dt
 cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, int dtype,
                               cudaStream_t stream, cudaEvent_t launched = nullptr);
 
+// One CTA of one thread waits, at most limit_ns, on a barrier nothing
+// completes, then sets kErrTimeout in *err_word (the bounded-wait path of the
+// sampling kernels, made to run out).
+cudaError_t launch_wait_probe(int32_t* err_word, unsigned long long limit_ns,
+                              cudaStream_t stream);
+
 // Build the per-row sorted (id, count) tables from raw ids.
 //   raw, offs  CSR: row r owns raw[offs[r] .. offs[r+1]) (prompt then output)
 //   max_len    the longest row (sizes the shared-memory sort)

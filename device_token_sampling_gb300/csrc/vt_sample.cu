@@ -3501,6 +3501,24 @@ cudaError_t launch_select_own(const SampleArgs& args, const LaunchPlan& plan, in
   return cudaLaunchKernelEx(&cfg, select_kernel<uint16_t>, args, plan.own);
 }
 
+namespace {
+// A wait that nothing completes (an mbarrier expecting one arrival that never
+// comes), bounded by `limit_ns`: the kernel records kErrTimeout and returns,
+// as every bounded wait of the sampling kernels does when it runs out.
+__global__ void wait_probe_kernel(int32_t* err_word, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait_bounded(&bar, 0u, limit_ns)) atomicOr(err_word, kErrTimeout);
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(int32_t* err_word, unsigned long long limit_ns,
+                              cudaStream_t stream) {
+  wait_probe_kernel<<<1, 1, 0, stream>>>(err_word, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(int2* hist, int32_t* hist_len, int32_t hist_cap, const int32_t* tokens,
                           int32_t* row_status, int B, cudaStream_t stream) {
   if (B < 1) return cudaSuccess;

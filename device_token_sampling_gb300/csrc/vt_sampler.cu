@@ -1060,6 +1060,15 @@ int vt_shard_merge(vt_sampler* h, const void* parts, int32_t S, int32_t B, int32
   return VT_OK;
 }
 
+int vt_debug_wait_probe(vt_sampler* h, int64_t limit_ns, void* stream) {
+  if (!h || limit_ns < 1 || limit_ns > 1000000000LL) return VT_ERR_INVALID_ARG;
+  DeviceGuard guard(h->cfg.device);
+  cudaStream_t st = (cudaStream_t)stream;
+  VT_CK(h, vt::launch_wait_probe(h->d_err, (unsigned long long)limit_ns, st));
+  h->last_stream = st;
+  return VT_OK;
+}
+
 int vt_debug_set_path(vt_sampler* h, int32_t path) {
   if (!h || path < 1 || path > 2) return VT_ERR_INVALID_ARG;
   h->path = path;

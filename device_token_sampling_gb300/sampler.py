@@ -79,6 +79,7 @@ SIGNATURES = {
     "vt_debug_set_path": (C.c_int, [P, I32]),
     "vt_sample_host_async": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, P, P, P, P, P]),
     "vt_sample_host_wait": (C.c_int, [P]),
+    "vt_debug_wait_probe": (C.c_int, [P, I64, P]),
     "vt_shard_part_bytes": (I64, [I32]),
     "vt_shard_partials": (C.c_int, [P, P, I32, I32, I32, I64, I32, I32, I32, P, P]),
     "vt_shard_merge": (C.c_int, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P]),

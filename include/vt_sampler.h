@@ -310,6 +310,14 @@ int vt_debug_set_phase_event(vt_sampler* handle, void* event);
  * in one pass could not settle).  Synchronises the handle's last stream. */
 int vt_debug_last_handover(vt_sampler* handle, int32_t* rows);
 
+/* Debug: run the bounded-wait path to its end.  One thread waits on a barrier
+ * that nothing completes for limit_ns (1 ns .. 1 s) of the GPU timer, as the
+ * sampling kernels' bounded waits do, then records a timeout in the handle's
+ * error word and returns, leaving the context usable; the next
+ * vt_check_device_errors returns VT_ERR_TIMEOUT.  Stream-ordered on `stream`.
+ * Errors: VT_ERR_INVALID_ARG, VT_ERR_CUDA. */
+int vt_debug_wait_probe(vt_sampler* handle, int64_t limit_ns, void* stream);
+
 /* Debug: which sampling path later vt_sample calls take.  1 (the default):
  * every call runs the streaming kernel (and its hand-over to the selection
  * kernel).  2: bf16 calls without penalties, top-p decay or the exported

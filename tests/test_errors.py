@@ -245,3 +245,21 @@ def test_injected_upload_failure_invalidates_the_parameters(monkeypatch):
         assert raw_sample(s, xd, 4, 3000) == S.VT_ERR_STATE
         monkeypatch.delenv("VT_FAULT_INJECT")
         check_workload(w, s=s)  # a clean reset makes the handle sample exactly again
+
+
+# --------------------------------------------------------------------------
+# a device wait that runs out (bounded; nothing faults)
+# --------------------------------------------------------------------------
+
+def test_bounded_wait_reports_timeout_and_the_handle_still_samples():
+    w = custom_workload(np.random.default_rng(3).normal(0, 2, size=(4, 3000)).astype(np.float32),
+                        T=[0.0, 0.8, 1.0, 1.2], k=[0, 5, 0, 40], p=[1.0, 1.0, 0.7, 0.9], n=2,
+                        name="after a timeout")
+    with S.Sampler(4, 3000, 2, 64) as s:
+        assert s._lib.vt_debug_wait_probe(s.handle, 1_000_000, None) == S.VT_OK  # 1 ms
+        with pytest.raises(S.VtError) as e:
+            s.check_device_errors()
+        assert code(e) == S.VT_ERR_TIMEOUT
+        assert b"wait" in s._lib.vt_last_error(s.handle)
+        s.check_device_errors()  # the error word was cleared
+        check_workload(w, s=s)
