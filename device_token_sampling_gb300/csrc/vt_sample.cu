@@ -1625,6 +1625,17 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
         consume(x, g);
       }
       __syncthreads();  // slot free
+      if (s.part.err & kErrTimeout) {
+        // a wait ran out: issue nothing more, and wait once more (bounded) for
+        // the copies still in flight (stages k .. k + kStages - 1) before the
+        // ring is left; the row's results are void and the error word says so
+        if (c.tid == 0) {
+          for (int q = k; q < min(nstage, k + kStages); ++q)
+            if (stage_bytes(q)) (void)mbar_wait_bounded(&s.full[q % kStages], (uint32_t)((q / kStages) & 1));
+        }
+        __syncthreads();
+        break;
+      }
       if (c.tid == 0 && k + kStages < nstage) {
         const uint32_t nb = stage_bytes(k + kStages);
         if (nb) {
