@@ -370,4 +370,45 @@ __device__ void smem_sort_desc(uint64_t* keys, int N) {
   }
 }
 
+// Warp 0: of the 256-bin histogram h, the bin holding the r-th largest value
+// counting from bin 255 down (*bin = -1 when the bins hold fewer than r), and
+// that value's rank inside it.
+__device__ inline void find_bin_desc(const unsigned int* h, int r, int* bin, int* rank) {
+  const int lane = threadIdx.x & 31;
+  // lane l owns bins 255 - 8l .. 248 - 8l
+  int c[8], tot = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    c[q] = (int)h[255 - 8 * lane - q];
+    tot += c[q];
+  }
+  int inc = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, inc >= r);
+  if (hit == 0u) {
+    if (lane == 0) {
+      *bin = -1;
+      *rank = 0;
+    }
+    return;
+  }
+  const int owner = __ffs(hit) - 1;
+  if (lane == owner) {
+    int above = inc - tot;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (above + c[q] >= r) {
+        *bin = 255 - 8 * lane - q;
+        *rank = r - above;
+        break;
+      }
+      above += c[q];
+    }
+  }
+}
+
 }  // namespace vt

@@ -25,6 +25,7 @@
 // S * K above kShardCand (the records one merge CTA sorts).
 #include "vt_device.cuh"
 #include "vt_kernels.h"
+#include "vt_sampler.h"
 
 #include <climits>
 
@@ -44,11 +45,14 @@ struct __align__(16) ShardHead {
 
 struct ShardSmem {
   uint64_t keys[kShardCand];
+  uint64_t sel[VT_SHARD_MAX_K];   // the leading records, sorted
+  uint64_t found;
+  int nsel;
   float tm[kST];
   float rf[2 * kSW];
   int ri[2 * kSW];
   unsigned long long ru[2 * kSW];
-  int hist[256];
+  unsigned int hist[256];
   int wt[kSW];
   int count, ties;
   float bf[4];
@@ -144,6 +148,94 @@ __device__ __forceinline__ float load_x<uint16_t>(const uint16_t* p, int j) {
   return __uint_as_float((uint32_t)__ldg(p + j) << 16);
 }
 
+// Visit every element j of x[0, n) once, fn(j, value): 16-byte vector loads
+// between a scalar head (up to the first 16-byte boundary) and a scalar tail.
+// Each thread sees its elements in increasing j.
+template <typename T>
+__device__ __forceinline__ float vec_elem(const uint4& q, int e);
+template <>
+__device__ __forceinline__ float vec_elem<float>(const uint4& q, int e) {
+  return __uint_as_float(e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w);
+}
+template <>
+__device__ __forceinline__ float vec_elem<uint16_t>(const uint4& q, int e) {
+  const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
+  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+template <typename T, typename F>
+__device__ __forceinline__ void scan_elems(const T* x, int n, F&& fn) {
+  constexpr int E = 16 / (int)sizeof(T);
+  const int mis = (int)(((uintptr_t)x / sizeof(T)) % E);
+  const int head = mis ? min(n, E - mis) : 0;
+  for (int j = threadIdx.x; j < head; j += kST) fn(j, load_x<T>(x, j));
+  const int nv = (n - head) / E;
+  const uint4* vp = reinterpret_cast<const uint4*>(x + head);
+  int v = threadIdx.x;
+  for (; v + kST < nv; v += 2 * kST) {  // two vectors in flight a thread
+    const uint4 q0 = __ldg(vp + v), q1 = __ldg(vp + v + kST);
+#pragma unroll
+    for (int e = 0; e < E; ++e) fn(head + v * E + e, vec_elem<T>(q0, e));
+#pragma unroll
+    for (int e = 0; e < E; ++e) fn(head + (v + kST) * E + e, vec_elem<T>(q1, e));
+  }
+  if (v < nv) {
+    const uint4 q = __ldg(vp + v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) fn(head + v * E + e, vec_elem<T>(q, e));
+  }
+  for (int j = head + nv * E + threadIdx.x; j < n; j += kST) fn(j, load_x<T>(x, j));
+}
+
+// The r-th largest of the distinct keys keys[0, n) (1 <= r <= n): byte-wise
+// radix selection, most significant byte first, stopping once one key is left.
+__device__ uint64_t select_kth_desc(const uint64_t* keys, int n, int r, ShardSmem& s) {
+  uint64_t prefix = 0ull, mask = 0ull;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += kST) s.hist[b] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kST) {
+      const uint64_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&s.hist[(k >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) find_bin_desc(s.hist, r, &s.bi[0], &s.bi[1]);
+    __syncthreads();
+    const int b = max(s.bi[0], 0);  // (r never exceeds the keys matching the prefix)
+    const unsigned int in_bin = s.hist[b];
+    prefix |= (uint64_t)b << shift;
+    mask |= 0xFFull << shift;
+    r = s.bi[1];
+    if (in_bin == 1u) {
+      for (int i = threadIdx.x; i < n; i += kST)
+        if ((keys[i] & mask) == prefix) s.found = keys[i];
+      __syncthreads();
+      return s.found;
+    }
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// The m largest of the distinct keys keys[0, n) (m <= VT_SHARD_MAX_K), sorted
+// descending into s.sel[0, m): a selection of the m-th, a gather, a small sort.
+__device__ void sorted_top(const uint64_t* keys, int n, int m, ShardSmem& s) {
+  m = min(m, n);
+  const uint64_t kmin = (m > 0 && n > m) ? select_kth_desc(keys, n, m, s) : 0ull;
+  int P2 = 64;
+  while (P2 < m) P2 <<= 1;
+  if (threadIdx.x == 0) s.nsel = 0;
+  for (int i = threadIdx.x; i < P2; i += kST) s.sel[i] = 0ull;
+  __syncthreads();
+  if (m > 0)
+    for (int i = threadIdx.x; i < n; i += kST) {
+      const uint64_t k = keys[i];
+      if (k >= kmin) s.sel[atomicAdd(&s.nsel, 1)] = k;
+    }
+  __syncthreads();
+  smem_sort_desc<kST>(s.sel, P2);
+}
+
 // ---------------------------------------------------------------------------
 // partials: one CTA per row of the shard
 // ---------------------------------------------------------------------------
@@ -161,14 +253,14 @@ __device__ void shard_exact_top(const ShardArgs& a, const T* x, float inv_t, Sha
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kST) s.hist[i] = 0;
     __syncthreads();
-    for (int j = tid; j < a.Vs; j += kST) {
-      const uint32_t o = ord_key(__fmul_rn(load_x<T>(x, j), inv_t));
-      if ((o & mask) == prefix) atomicAdd(&s.hist[(o >> shift) & 255u], 1);
-    }
+    scan_elems<T>(x, a.Vs, [&](int, float xv) {
+      const uint32_t o = ord_key(__fmul_rn(xv, inv_t));
+      if ((o & mask) == prefix) atomicAdd(&s.hist[(o >> shift) & 255u], 1u);
+    });
     __syncthreads();
     if (tid == 0) {
       int above = 0, b = 255;
-      for (; b > 0 && above + s.hist[b] < r; --b) above += s.hist[b];
+      for (; b > 0 && above + (int)s.hist[b] < r; --b) above += (int)s.hist[b];
       s.bi[0] = b;
       s.bi[1] = r - above;
     }
@@ -217,14 +309,14 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
   float tmax = -INFINITY;
   int tj = INT_MAX;
   bool bad = false;
-  for (int j = tid; j < a.Vs; j += kST) {
-    const float z = __fmul_rn(load_x<T>(x, j), inv_t);
+  scan_elems<T>(x, a.Vs, [&](int j, float xv) {
+    const float z = __fmul_rn(xv, inv_t);
     bad |= (z != z) || z == INFINITY;
     if (z > tmax) {
       tmax = z;
       tj = a.v0 + j;
     }
-  }
+  });
   s.tm[tid] = tmax;
   float m = tmax, zz = 0.f;
   int mj = tj;
@@ -265,14 +357,14 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
   const bool finite_max = m > -INFINITY;
   const float nh = __fmul_rn(-m, kLog2e);
   const float nl = finite_max ? __fmaf_rn(-m, kLog2e, -nh) : 0.f;
-  for (int j = tid; j < a.Vs; j += kST) {
-    const float z = __fmul_rn(load_x<T>(x, j), inv_t);
+  scan_elems<T>(x, a.Vs, [&](int j, float xv) {
+    const float z = __fmul_rn(xv, inv_t);
     if (finite_max) sum += ex2_approx(__fadd_rn(__fmaf_rn(z, kLog2e, nh), nl));
     if (z >= tau) {
       const int pos = atomicAdd(&s.count, 1);
       if (pos < kShardCand) s.keys[pos] = elem_key(z, (uint32_t)(a.v0 + j));
     }
-  }
+  });
   sum = sblock_sum(sum, s);
   int n = s.count;
   __syncthreads();
@@ -280,14 +372,10 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
     shard_exact_top<T>(a, x, inv_t, s);
     n = a.K;
   }
-  int P2 = kST;
-  while (P2 < n) P2 <<= 1;
-  for (int i = n + tid; i < P2; i += kST) s.keys[i] = 0ull;
-  __syncthreads();
-  smem_sort_desc<kST>(s.keys, P2);
   const int w = min(n, a.K);
+  sorted_top(s.keys, n, w, s);
   uint64_t* rec = reinterpret_cast<uint64_t*>(out + sizeof(ShardHead));
-  for (int i = tid; i < w; i += kST) rec[i] = s.keys[i];
+  for (int i = tid; i < w; i += kST) rec[i] = s.sel[i];
   if (tid == 0) {
     ShardHead h;
     h.m_t = m;
@@ -362,19 +450,26 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
       off += w;
     }
   }
-  int P2 = kST;
-  while (P2 < total) P2 <<= 1;
-  for (int i = total + tid; i < P2; i += kST) s.keys[i] = 0ull;
   __syncthreads();
-  smem_sort_desc<kST>(s.keys, P2);
-  // finite records (the -inf ones sort last)
-  int fin = 0;
-  for (int i = tid; i < total; i += kST) fin += key_z(s.keys[i]) > -INFINITY;
+  // finite records, and min-p survivors (order-independent counts)
+  const bool greedy = (P.flags & kRowGreedy) != 0;
+  const bool minp = (P.flags & kRowMinP) != 0;
+  int fin = 0, pass = 0;
+  for (int i = tid; i < total; i += kST) {
+    const float z = key_z(s.keys[i]);
+    fin += z > -INFINITY;
+    pass += minp && z > -INFINITY && minp_pass(z, m_t, P.log_min_p);
+  }
   fin = (int)sblock_sum_u64((unsigned long long)fin, s);
+  const int L1 = minp ? (int)sblock_sum_u64((unsigned long long)pass, s) : fin;
+  // the leading records in the order (z_t desc, index asc): the top-n and the
+  // top-k survivors
+  const int L2 = greedy ? 0 : min(P.top_k, L1);
+  sorted_top(s.keys, total, max(n, L2), s);
   // top-n: the first n records
   for (int t = tid; t < n; t += kST) {
     if (t < total) {
-      const uint64_t k = s.keys[t];
+      const uint64_t k = s.sel[t];
       a.out_topk_ids[(int64_t)row * n + t] = (int)key_idx(k);
       a.out_topk_logprobs[(int64_t)row * n + t] = (key_z(k) - m_t) - lnS;
     } else {
@@ -382,25 +477,17 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
       a.out_topk_logprobs[(int64_t)row * n + t] = -INFINITY;
     }
   }
-  const bool greedy = (P.flags & kRowGreedy) != 0;
   int tok = argj, L3 = 1;
   float ztok = m_t;
   if (!greedy) {
     // min-p, then top-k, then top-p over the top-k survivors renormalised
-    int L1 = fin;
-    if (P.flags & kRowMinP) {
-      int pass = 0;
-      for (int i = tid; i < fin; i += kST) pass += minp_pass(key_z(s.keys[i]), m_t, P.log_min_p);
-      L1 = (int)sblock_sum_u64((unsigned long long)pass, s);
-    }
-    const int L2 = min(P.top_k, L1);
     L3 = L2;
     if (P.flags & kRowTopP) {
       // exclusive prefix masses in 2^-43 fixed point; kept while <= p * W
       unsigned long long mine = 0ull;
       const int per = (L2 + kST - 1) / kST;
       const int i0 = min(L2, tid * per), i1 = min(L2, i0 + per);
-      for (int i = i0; i < i1; ++i) mine += mass_fixed(key_z(s.keys[i]), m_t);
+      for (int i = i0; i < i1; ++i) mine += mass_fixed(key_z(s.sel[i]), m_t);
       // exclusive scan over the threads (serial in warp 0: at most 256 terms)
       s.ru[0] = 0ull;
       __syncthreads();
@@ -423,7 +510,7 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
       int kept = 0;
       for (int i = i0; i < i1; ++i) {
         if (run <= Tm) ++kept;
-        run += mass_fixed(key_z(s.keys[i]), m_t);
+        run += mass_fixed(key_z(s.sel[i]), m_t);
       }
       L3 = max(1, (int)sblock_sum_u64((unsigned long long)kept, s));
     }
@@ -433,7 +520,7 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
     float bs = -INFINITY, bz = 0.f;
     int bj = INT_MAX;
     for (int i = tid; i < L3; i += kST) {
-      const uint64_t k = s.keys[i];
+      const uint64_t k = s.sel[i];
       const int j = (int)key_idx(k);
       const float z = key_z(k);
       const float sc = gumbel_score_inl(z, noise_bits(key, j));
@@ -451,7 +538,7 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
     a.out_tokens[row] = tok;
     if (a.out_logprobs) a.out_logprobs[row] = (ztok - m_t) - lnS;
     a.row_status[row] = kRowOk;
-    const uint64_t kk = greedy ? 0ull : s.keys[L3 - 1];
+    const uint64_t kk = greedy ? 0ull : s.sel[L3 - 1];
     a.dbg_kth_value[row] = greedy ? m_t : key_z(kk);
     a.dbg_kth_index[row] = greedy ? tok : (int)key_idx(kk);
     a.dbg_kept[row] = L3;
