@@ -12,8 +12,10 @@
 //   P2 row      (row): the row's statistics; its route; the candidate
 //               threshold tau, the K-th largest of the C x 256 thread maxima
 //               (at least K elements are >= tau, K = max(top_k, n)); for rows
-//               without top-k the Gumbel score of the row's maximum and the
-//               first code slot that holds no survivor.
+//               without top-k the Gumbel score of the row's maximum; for
+//               top-p rows, per code slot, its mass and the noise bits from
+//               which one of its elements may out-score the maximum, and the
+//               first slot that holds no survivor.
 //   P2 -> P3 the slices are read again (from L2):
 //   P3 collect  (row, slice): the elements >= tau as candidate keys; for rows
 //               without top-k the survivors' count and last key, the draw
@@ -21,7 +23,8 @@
 //               the winner is one of them or the maximum itself), and for
 //               top-p rows a count per bf16 code slot, summed into 64 coarse
 //               bins of exact 2^-43 fixed-point masses.
-//   P4 finish   (row): top-n from the sorted candidates; rows with top-k (or
+//   P4 finish   (row): top-n from the candidates (sorted when few, else
+//               selected then sorted); rows with top-k (or
 //               greedy) settle on the candidates exactly as on the whole row;
 //               rows without top-p settle on the survivors and contenders;
 //               top-p rows find the coarse bin holding the nucleus boundary.
@@ -508,10 +511,9 @@ __global__ void __launch_bounds__(kFT) flat_stats_kernel(const FlatArgs a) {
 // P2: per-row statistics, route and thresholds
 // ---------------------------------------------------------------------------
 struct RowSmem {
-  RedSmem red;
   uint16_t tm[kFlatMaxC * kFT];  // the row's thread maxima
   unsigned int hist[256];
-  int bin, rank, total;
+  int bin, rank;
   int dmin;
 };
 
