@@ -439,6 +439,7 @@ def run_gpu(args, w: W.Workload):
     max_hist = hist + args.steps + args.warmup + 512 if penalised else 0
     s = S.Sampler(max_batch=B, max_vocab=V, max_logprobs=n, max_history=max_hist, device=local,
                   host_io=True)
+    s.set_path(args.path)
     s.reset_workload(w)
     update = penalised
     # device inputs: N_ROTATE distinct batches (inputs larger than L2)
@@ -546,14 +547,18 @@ def run_gpu(args, w: W.Workload):
         # (bf16 batches with top-p-only rows) a second stream beside it.  The
         # launches overlap, so the roofline is taken over the whole step: the
         # step's algorithmic bytes over its device time.
-        kernel, kernel_ms, kbytes = "vt_sample step (sample_kernel + select_kernel)", ms_per_step, alg
-        traffic = profiled_traffic(w.name)
+        kernel = ("vt_sample step (sample_kernel + select_kernel)" if args.path == 1 else
+                  "vt_sample step (the six flat kernels + select_kernel)")
+        kernel_ms, kbytes = ms_per_step, alg
+        traffic = profiled_traffic(w.name) if args.path == 1 else None
         achieved = kbytes / (kernel_ms * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": workload_config(w),
+            "data": "synthetic",
+            "config": dict(workload_config(w),
+                           sampling_path="streaming" if args.path == 1 else "flat"),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} (hbm_gbs)",
@@ -731,6 +736,8 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", type=int, default=1, choices=[1, 2],
+                    help="1: the streaming kernel; 2: the flat kernels where they apply")
     ap.add_argument("--shards", type=int, default=0,
                     help="time the vocabulary-split variant with this many shards (one GPU)")
     args = ap.parse_args()
