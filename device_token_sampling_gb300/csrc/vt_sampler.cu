@@ -976,10 +976,12 @@ static int shard_rows_ok(vt_sampler* h, int32_t B, int32_t V, int32_t K) {
       return set_err(h, VT_ERR_INVALID_ARG, "row %d: penalties or top-p decay are not sharded", r);
     if (f & vt::kRowGreedy) continue;
     const int k = h->h_params[r].top_k;
-    if (!(k > 1 && k < V && k <= K))
+    const bool topk = k > 1 && k < V;
+    if (!topk && !(f & (vt::kRowTopP | vt::kRowMinP))) continue;  // no filter: every element kept
+    if (!(topk && k <= K))
       return set_err(h, VT_ERR_INVALID_ARG,
-                     "row %d: a sampled row needs 1 < top_k <= K (%d) and top_k < V (top_k=%d)", r,
-                     K, k);
+                     "row %d: a filtered row needs 1 < top_k <= K (%d) and top_k < V (top_k=%d)",
+                     r, K, k);
   }
   return VT_OK;
 }
@@ -1006,6 +1008,7 @@ int vt_shard_partials(vt_sampler* h, const void* logits, int32_t dtype, int32_t 
   a.V = V;
   a.K = K;
   a.params = h->d_params;
+  a.seeds = h->d_seeds;
   a.part = part;
   a.part_bytes = vt::shard_part_bytes(K);
   cudaStream_t st = (cudaStream_t)stream;

@@ -41,10 +41,31 @@ struct __align__(16) ShardHead {
   float s;          // sum of exp(z_t - m_t) over the shard
   int32_t argj;     // lowest global index of m_t (INT_MAX: none)
   uint32_t info;    // records written (bits 0..15), NaN or +inf seen (bit 30)
+  // rows without a filter (every finite element kept): the shard's Gumbel
+  // winner, its finite count and its last finite element in the order
+  float wscore;     // the best score z_t - ln(-ln u) (-inf: none)
+  int32_t wj;       // its global index (INT_MAX: none)
+  float wz;         // its tempered value
+  uint32_t nfin;    // finite elements
+  unsigned long long last;  // ~key of the last finite element (0: none)
+  unsigned long long pad;
 };
+static_assert(sizeof(ShardHead) == 48, "the documented record header is 48 bytes");
+
+// A row every finite element of which is kept: sampled, without top-k, top-p
+// or min-p.
+__device__ __forceinline__ bool unfiltered_row(const RowParams& P, int V) {
+  const bool greedy = (P.flags & kRowGreedy) != 0;
+  const bool topk = P.top_k > 1 && P.top_k < V;
+  return !greedy && !topk && !(P.flags & (kRowTopP | kRowMinP));
+}
 
 struct ShardSmem {
   uint64_t keys[kShardCand];
+  float w_score, w_z;   // merge: the shards' best Gumbel winner (rows without a filter)
+  int w_j;
+  unsigned int nfin_all;
+  unsigned long long last_all;
   uint64_t sel[VT_SHARD_MAX_K];   // the leading records, sorted
   uint64_t found;
   int nsel;
@@ -129,6 +150,29 @@ __device__ unsigned long long sblock_sum_u64(unsigned long long v, ShardSmem& s)
   if (threadIdx.x < 32) {
     unsigned long long t = threadIdx.x < kSW ? s.ru[threadIdx.x] : 0ull;
     t = warp_sum_u64(t);
+    if (threadIdx.x == 0) s.ru[kSW] = t;
+  }
+  __syncthreads();
+  const unsigned long long r = s.ru[kSW];
+  __syncthreads();
+  return r;
+}
+
+__device__ unsigned long long sblock_max_u64(unsigned long long v, ShardSmem& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(0xffffffffu, v, o);
+    v = t > v ? t : v;
+  }
+  if ((threadIdx.x & 31) == 0) s.ru[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    unsigned long long t = threadIdx.x < kSW ? s.ru[threadIdx.x] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long q = __shfl_xor_sync(0xffffffffu, t, o);
+      t = q > t ? q : t;
+    }
     if (threadIdx.x == 0) s.ru[kSW] = t;
   }
   __syncthreads();
@@ -325,11 +369,13 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
   uint8_t* out = reinterpret_cast<uint8_t*>(a.part) + (size_t)row * a.part_bytes;
   if (anybad) {  // NaN or +inf: the merge reports the row as non-finite
     if (tid == 0) {
-      ShardHead h;
+      ShardHead h{};
       h.m_t = m;
       h.s = 0.f;
       h.argj = mj;
       h.info = 1u << 30;
+      h.wscore = -INFINITY;
+      h.wj = INT_MAX;
       *reinterpret_cast<ShardHead*>(out) = h;
     }
     return;
@@ -357,6 +403,15 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
   const bool finite_max = m > -INFINITY;
   const float nh = __fmul_rn(-m, kLog2e);
   const float nl = finite_max ? __fmaf_rn(-m, kLog2e, -nh) : 0.f;
+  // rows without a filter: the shard's Gumbel winner over its finite elements,
+  // with the noise of the global (row, column) [the draw composes across
+  // shards as an argmax], its finite count and its last finite element
+  const bool unf = unfiltered_row(a.params[row], a.V);
+  const uint64_t key = unf ? row_key(a.seeds[row], row) : 0ull;
+  float ws = -INFINITY, wz = 0.f;
+  int wj = INT_MAX;
+  uint32_t nfin = 0u;
+  unsigned long long last = 0ull;
   scan_elems<T>(x, a.Vs, [&](int j, float xv) {
     const float z = __fmul_rn(xv, inv_t);
     if (finite_max) sum += ex2_approx(__fadd_rn(__fmaf_rn(z, kLog2e, nh), nl));
@@ -364,8 +419,28 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
       const int pos = atomicAdd(&s.count, 1);
       if (pos < kShardCand) s.keys[pos] = elem_key(z, (uint32_t)(a.v0 + j));
     }
+    if (unf && z > -INFINITY) {
+      const int gj = a.v0 + j;
+      ++nfin;
+      const unsigned long long nk = ~elem_key(z, (uint32_t)gj);
+      last = nk > last ? nk : last;
+      const uint32_t b = noise_bits(key, gj);
+      if (ws == -INFINITY || may_beat(z, ws, b)) {
+        const float sc = gumbel_score(z, b);
+        if (pair_better(sc, gj, ws, wj)) {
+          ws = sc;
+          wj = gj;
+          wz = z;
+        }
+      }
+    }
   });
   sum = sblock_sum(sum, s);
+  if (unf) {
+    sblock_argmax(ws, wj, wz, s);
+    nfin = (uint32_t)sblock_sum_u64((unsigned long long)nfin, s);
+    last = sblock_max_u64(last, s);
+  }
   int n = s.count;
   __syncthreads();
   if (n > kShardCand) {
@@ -377,11 +452,16 @@ __global__ void __launch_bounds__(kST) shard_partials_kernel(const ShardArgs a) 
   uint64_t* rec = reinterpret_cast<uint64_t*>(out + sizeof(ShardHead));
   for (int i = tid; i < w; i += kST) rec[i] = s.sel[i];
   if (tid == 0) {
-    ShardHead h;
+    ShardHead h{};
     h.m_t = m;
     h.s = sum;
     h.argj = mj;
     h.info = (uint32_t)w;
+    h.wscore = ws;
+    h.wj = wj;
+    h.wz = wz;
+    h.nfin = nfin;
+    h.last = last;
     *reinterpret_cast<ShardHead*>(out) = h;
   }
 }
@@ -396,8 +476,10 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
   const int n = a.n_logprobs;
   // the row's statistics
   if (tid == 0) {
-    float mt = -INFINITY, sm = 0.f;
-    int argj = INT_MAX, bad = 0, total = 0;
+    float mt = -INFINITY, sm = 0.f, ws = -INFINITY, wz = 0.f;
+    int argj = INT_MAX, bad = 0, total = 0, wj = INT_MAX;
+    unsigned int nfin = 0u;
+    unsigned long long last = 0ull;
     for (int sh = 0; sh < a.S; ++sh) {
       const uint8_t* in = reinterpret_cast<const uint8_t*>(a.part) +
                           ((size_t)sh * a.B + row) * a.part_bytes;
@@ -406,7 +488,19 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
       lse_combine(mt, sm, h.m_t, h.s, kLog2e);
       bad |= (h.info >> 30) & 1u;
       total += (int)(h.info & 0xFFFFu);
+      if (h.wj != INT_MAX && pair_better(h.wscore, h.wj, ws, wj)) {
+        ws = h.wscore;
+        wj = h.wj;
+        wz = h.wz;
+      }
+      nfin += h.nfin;
+      last = h.last > last ? h.last : last;
     }
+    s.w_score = ws;
+    s.w_j = wj;
+    s.w_z = wz;
+    s.nfin_all = nfin;
+    s.last_all = last;
     s.bf[0] = mt;
     s.bf[1] = sm;
     s.bi[0] = argj;
@@ -464,7 +558,7 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
   const int L1 = minp ? (int)sblock_sum_u64((unsigned long long)pass, s) : fin;
   // the leading records in the order (z_t desc, index asc): the top-n and the
   // top-k survivors
-  const int L2 = greedy ? 0 : min(P.top_k, L1);
+  const int L2 = (greedy || unfiltered_row(P, a.V)) ? 0 : min(P.top_k, L1);
   sorted_top(s.keys, total, max(n, L2), s);
   // top-n: the first n records
   for (int t = tid; t < n; t += kST) {
@@ -476,6 +570,20 @@ __global__ void __launch_bounds__(kST) shard_merge_kernel(const ShardArgs a) {
       a.out_topk_ids[(int64_t)row * n + t] = -1;
       a.out_topk_logprobs[(int64_t)row * n + t] = -INFINITY;
     }
+  }
+  if (unfiltered_row(P, a.V)) {
+    // every finite element kept: the best of the shards' Gumbel winners
+    if (tid == 0) {
+      const uint64_t lk = ~s.last_all;
+      a.out_tokens[row] = s.w_j;
+      if (a.out_logprobs) a.out_logprobs[row] = (s.w_z - m_t) - lnS;
+      a.row_status[row] = kRowOk;
+      a.dbg_kth_value[row] = key_z(lk);
+      a.dbg_kth_index[row] = (int)key_idx(lk);
+      a.dbg_kept[row] = (int)s.nfin_all;
+      a.seeds[row] += kSeedStep;
+    }
+    return;
   }
   int tok = argj, L3 = 1;
   float ztok = m_t;

@@ -401,25 +401,39 @@ int vt_sample_noalloc(int32_t device, const void* logits, int32_t dtype, int32_t
  *      top-n exactly as vt_sample on the whole rows would (tokens and kept sets
  *      identical; log-probs equal within rounding), and advances the seeds.
  * Every shard's handle must hold the same parameters and seeds (the same
- * vt_reset_params).  Rows it takes: no penalties, no top-p decay, and each
- * sampled row bounded by 1 < top_k <= K (top_k < V), after which min-p and
- * top-p apply over the gathered records; greedy rows always.  Other rows:
- * VT_ERR_INVALID_ARG.  The union of the shards' K largest elements holds the
- * row's K largest, hence its kept set and its top-n. */
+ * vt_reset_params).  Rows it takes: no penalties, no top-p decay; greedy
+ * rows; rows without a filter (every finite element kept: the draw is the
+ * best of the shards' Gumbel winners); and filtered rows bounded by
+ * 1 < top_k <= K (top_k < V), after which min-p and top-p apply over the
+ * gathered records.  Other rows: VT_ERR_INVALID_ARG.  The union of the
+ * shards' K largest elements holds the row's K largest, hence a bounded
+ * row's kept set, and every row's top-n. */
 #define VT_SHARD_MAX_K 256
 /* Records one merge gathers per row at most: S * K <= VT_SHARD_MAX_RECORDS. */
 #define VT_SHARD_MAX_RECORDS 4096
 
 /* Bytes of one row's record in a shard buffer for 1 <= K <= VT_SHARD_MAX_K
- * (-1 otherwise): a 16-byte header -- float the shard's tempered maximum m_s
- * (-inf: no finite element), float the sum of exp(z_t - m_s) over its columns,
- * int32 its lowest global index holding m_s, uint32 the count w of elements
- * written (bits 0..15; w = min(K, Vs)) with bit 30 set when a NaN or +inf was
- * seen -- then K uint64 elements, the first w valid: the shard's w largest in
- * the order (z_t descending, global index ascending), each with the
- * order-preserving code of z_t in bits 63..32 (sign bit flipped for z_t >= 0,
- * all bits flipped below; -0 as +0) and the complement of the global index in
- * bits 31..0, so that a larger integer is an earlier element. */
+ * (-1 otherwise): a 48-byte header, then K uint64 elements.  The header:
+ *   float    the shard's tempered maximum m_s (-inf: no finite element);
+ *   float    the sum of exp(z_t - m_s) over its columns;
+ *   int32    its lowest global index holding m_s;
+ *   uint32   the count w of elements written (bits 0..15; w = min(K, Vs)),
+ *            bit 30 set when a NaN or +inf was seen;
+ *   float    rows without a filter (sampled, no top-k, top-p or min-p): the
+ *            best Gumbel score z_t - ln(-ln u) over its finite elements, with
+ *            the noise of the global row and column (-inf: none);
+ *   int32    that element's global index (INT_MAX: none);
+ *   float    its tempered value;
+ *   uint32   the shard's count of finite elements;
+ *   uint64   the bitwise complement of the element code (below) of its last
+ *            finite element in the order (0: none);
+ *   uint64   padding (zero);
+ * (the last five are written for rows without a filter only).  The elements:
+ * the shard's w largest in the order (z_t descending, global index
+ * ascending), each with the order-preserving code of z_t in bits 63..32
+ * (sign bit flipped for z_t >= 0, all bits flipped below; -0 as +0) and the
+ * complement of the global index in bits 31..0, so that a larger integer is
+ * an earlier element. */
 int64_t vt_shard_part_bytes(int32_t K);
 
 /* Step 1 on one shard: logits is device [B][ld] of dtype holding global

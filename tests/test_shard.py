@@ -36,7 +36,7 @@ from device_token_sampling_gb300 import workloads as W
 from paritylib import LP_TOL, compare, custom_workload, device_logits, make_sampler, run_gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEAD_BYTES = 16
+HEAD_BYTES = 48
 
 
 def part_bytes(K: int) -> int:
@@ -62,14 +62,17 @@ def advanced(seeds: np.ndarray, steps: int) -> np.ndarray:
 
 
 def sampled_workload(rng, B, V, K, dtype, n, name, x=None):
-    """Rows the sharded path takes: greedy rows, and sampled rows bounded by a
-    top-k of at most K, some with min-p and some with top-p."""
+    """Rows the sharded path takes: greedy rows, rows without a filter, and
+    sampled rows bounded by a top-k of at most K, some with min-p and some
+    with top-p."""
     if x is None:
         x = W.peaked_rows(rng, B, V)
     T = rng.choice(np.array([0.0, 0.6, 1.0, 1.3], np.float32), B)
     k = rng.integers(2, K + 1, B).astype(np.int32)
     p = np.where(rng.random(B) < 0.5, rng.uniform(0.3, 0.99, B), 1.0).astype(np.float32)
     mp_ = np.where(rng.random(B) < 0.3, rng.uniform(0.001, 0.2, B), 0.0).astype(np.float32)
+    free = rng.random(B) < 0.2  # no filter: every finite element kept
+    k[free], p[free], mp_[free] = 0, 1.0, 0.0
     return custom_workload(x, dtype=dtype, T=T, k=k, p=p, mp=mp_, n=n,
                            seed=int(rng.integers(1 << 30)), name=name)
 
@@ -255,10 +258,10 @@ def test_sharded_rejects_rows_it_cannot_compose(_gpu):
         assert merge(S_=65) == S.VT_ERR_INVALID_ARG
         assert merge(S_=64, K_=65) == S.VT_ERR_INVALID_ARG    # S * K above 4096
         assert merge(n=5) == S.VT_ERR_INVALID_ARG             # n > max_logprobs
-        for bad in (dict(k=[0, 0, 10, 10]),                    # a sampled row without top-k
+        for bad in (dict(k=[0, 0, 10, 10], p=[1.0, 0.9, 1.0, 1.0]),  # top-p without top-k
                     dict(k=[0, 65, 10, 10]),                   # top-k above K
                     dict(k=[0, 10, 10, 10], pres=[0, 0.5, 0, 0])):  # penalties
-            w = custom_workload(x, T=[0.0, 1.0, 1.0, 1.0], **{"p": 1.0, **bad})
+            w = custom_workload(x, T=[0.0, 1.0, 1.0, 1.0], **{"p": 1.0, **bad})  # noqa: PIE800
             s.reset_workload(w)
             assert partials() == S.VT_ERR_INVALID_ARG, bad
             assert b"row 1" in lib.vt_last_error(s.handle)
@@ -284,26 +287,49 @@ def code_value(c: np.ndarray) -> np.ndarray:
     return np.where(c & 0x80000000, c & 0x7FFFFFFF, ~c).astype(np.uint32).view(np.float32)
 
 
-def write_records(zt: np.ndarray, v0: int, K: int) -> np.ndarray:
+def unfiltered(w: W.Workload, r: int) -> bool:
+    """A sampled row without top-k, top-p or min-p: every finite element kept."""
+    greedy = w.temperature[r] == 0 or w.top_k[r] == 1 or w.top_p[r] == 0 or w.min_p[r] == 1
+    topk = 1 < w.top_k[r] < w.V
+    return not greedy and not topk and not (0 < w.top_p[r] < 1) and not (0 < w.min_p[r] < 1)
+
+
+def gumbel_scores(w: W.Workload, r: int, z: np.ndarray, v0: int) -> np.ndarray:
+    """z_t - ln(-ln u) in float64 for global columns v0 .. v0 + len(z) - 1."""
+    b = O.noise_bits(int(w.seed[r]), r, v0, len(z)).astype(np.float64)
+    return z.astype(np.float64) - np.log(-np.log((b + 0.5) * 2.0**-24))
+
+
+def write_records(zt: np.ndarray, v0: int, K: int, w: W.Workload) -> np.ndarray:
     """One shard's records, in the documented layout, from its tempered logits
     zt [B, Vs] (finite or -inf) holding global columns v0 .. v0 + Vs - 1."""
     B, Vs = zt.shape
     out = np.zeros((B, part_bytes(K)), np.uint8)
     j = np.arange(v0, v0 + Vs, dtype=np.int64)
+    f32 = lambda v: np.array([v], np.float32).view(np.uint32)[0]  # noqa: E731
     for r in range(B):
         z = zt[r].astype(np.float32)
         m = np.float32(z.max())
         s = np.float32(np.exp(z.astype(np.float64) - m).sum()) if m > -np.inf else np.float32(0)
         argj = int(j[np.argmax(z)]) if m > -np.inf else 2**31 - 1
         wn = min(K, Vs)
-        order = np.lexsort((j, -z))[:wn]
-        keys = (ord_code(z[order]).astype(np.uint64) << np.uint64(32)) | \
-            (~j[order].astype(np.uint32)).astype(np.uint64)
-        head = np.zeros(4, np.uint32)
-        head[0] = np.array([m], np.float32).view(np.uint32)[0]
-        head[1] = np.array([s], np.float32).view(np.uint32)[0]
-        head[2] = np.uint32(argj)
-        head[3] = np.uint32(wn)
+        order = np.lexsort((j, -z))
+        top = order[:wn]
+        keys = (ord_code(z[top]).astype(np.uint64) << np.uint64(32)) | \
+            (~j[top].astype(np.uint32)).astype(np.uint64)
+        head = np.zeros(12, np.uint32)
+        head[0], head[1], head[2], head[3] = f32(m), f32(s), np.uint32(argj), np.uint32(wn)
+        head[4], head[5] = f32(-np.inf), np.uint32(2**31 - 1)
+        fin = np.isfinite(z)
+        if unfiltered(w, r) and fin.any():
+            sc = np.where(fin, gumbel_scores(w, r, z, v0), -np.inf)
+            best = int(np.lexsort((j, -sc))[0])
+            lastpos = [q for q in order if fin[q]][-1]
+            lastkey = (int(ord_code(z[lastpos:lastpos + 1])[0]) << 32) | (~int(j[lastpos]) & 0xFFFFFFFF)
+            nk = (~lastkey) & 0xFFFFFFFFFFFFFFFF
+            head[4], head[5], head[6] = f32(sc[best]), np.uint32(j[best]), f32(z[best])
+            head[7] = np.uint32(fin.sum())
+            head[8], head[9] = np.uint32(nk & 0xFFFFFFFF), np.uint32(nk >> 32)
         out[r, :HEAD_BYTES] = head.view(np.uint8)
         out[r, HEAD_BYTES:HEAD_BYTES + 8 * wn] = keys.view(np.uint8)
     return out
@@ -329,6 +355,18 @@ def merge_records(parts: np.ndarray, w: W.Workload, K: int):
         j = (~(keys & np.uint64(0xFFFFFFFF)).astype(np.uint32)).astype(np.int64)
         out["topn_ids"].append(j[:n])
         out["topn_lp"].append(z[:n] - lse)
+        if unfiltered(w, r):
+            # the best of the shards' Gumbel winners (score, then lower index)
+            sc = heads[:, 4].view(np.float32).astype(np.float64)
+            wj = heads[:, 5].view(np.int32)
+            live = wj != 2**31 - 1
+            best = min((-sc[q], wj[q], q) for q in np.flatnonzero(live))[2]
+            tok, kept = int(wj[best]), int(heads[:, 7].sum())
+            zt_tok = float(heads[best, 6:7].view(np.float32)[0])
+            out["token"].append(tok)
+            out["kept"].append(kept)
+            out["logprob"].append(zt_tok - lse)
+            continue
         if w.temperature[r] == 0:
             cand = heads[:, 2].view(np.int32)[ms == m]
             tok, kept = int(cand.min()), 1
@@ -363,6 +401,8 @@ def shard_cpu_workload(K: int):
     x[4, 17] = x[4, 4000] = 20.0       # a greedy tie across the ranks
     w = sampled_workload(rng, B, V, K, W.DTYPE_F32, n=5, name="gloo shards", x=x)
     w.temperature[4] = 0.0
+    for r in (5, 9):  # rows without a filter: the shards' Gumbel winners compose
+        w.temperature[r], w.top_k[r], w.top_p[r], w.min_p[r] = 1.1, 0, 1.0, 0.0
     return w, [(0, 2500), (2500, V)]
 
 
@@ -376,7 +416,7 @@ def _rank(rank: int, world: int, port: int, out):
         w, bounds = shard_cpu_workload(K)
         o = O.sample_workload(w, want_zt=True)
         v0, v1 = bounds[rank]
-        mine = torch.from_numpy(write_records(o.zt[:, v0:v1], v0, K))
+        mine = torch.from_numpy(write_records(o.zt[:, v0:v1], v0, K, w))
         gathered = S.gather_partials(mine).numpy()
         assert gathered.shape == (world, w.B, part_bytes(K))
         g = merge_records(gathered, w, K)

@@ -104,8 +104,11 @@ def test_draw_frequencies_match_the_filtered_softmax(path, T, k, p):
     assert not np.all(wrong[tokens] > 0) or binned_chi_square(tokens, wrong)[1] < 1e-6
 
 
-def test_vocabulary_split_draw_frequencies():
-    w, prob, wrong = one_row_case(1.2, 200, 0.9)
+@pytest.mark.parametrize("T,k,p", [(1.2, 200, 0.9), (1.0, 0, 1.0)])
+def test_vocabulary_split_draw_frequencies(T, k, p):
+    """Bounded rows draw over the merged records; a row without a filter is
+    the best of the shards' own Gumbel winners over every column."""
+    w, prob, wrong = one_row_case(T, k, p)
     tokens = draws(w, shards=4)
     stat, pval = binned_chi_square(tokens, prob)
     assert pval > 1e-4, (stat, pval)
