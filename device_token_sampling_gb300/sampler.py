@@ -310,13 +310,21 @@ class Sampler:
         """vt_sample_host_async: enqueue one step from host logits [B, ld]
         (pinned for an asynchronous copy); ``out`` is filled once
         ``sample_host_wait`` returns, and both must stay alive until then."""
-        x = logits if logits.flags["C_CONTIGUOUS"] else np.ascontiguousarray(logits)
+        # the buffers are read and written after the call returns: no hidden
+        # copies, and outputs of the exact dtype and shape
+        if logits.ndim != 2 or not logits.flags["C_CONTIGUOUS"]:
+            raise ValueError("host logits must be a C-contiguous 2-D array")
+        x = logits
         B, ld = x.shape
         n = int(num_logprobs)
         if out is None:
             out = (np.empty(B, np.int32), np.empty(B, np.float32), np.empty((B, n), np.int32),
                    np.empty((B, n), np.float32))
         tok, lp, tid, tlp = out
+        for arr, dt, shape in ((tok, np.int32, (B,)), (lp, np.float32, (B,)),
+                               (tid, np.int32, (B, n)), (tlp, np.float32, (B, n))):
+            if arr.dtype != dt or arr.shape != shape or not arr.flags["C_CONTIGUOUS"]:
+                raise ValueError(f"output arrays must be C-contiguous {dt.__name__} {shape}")
         rc = self._lib.vt_sample_host_async(self._h, _np_ptr(x), dtype, B, V, ld, n,
                                             1 if update_counts else 0, _np_ptr(tok), _np_ptr(lp),
                                             _np_ptr(tid) if n else None,
