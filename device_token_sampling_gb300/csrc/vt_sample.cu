@@ -46,8 +46,9 @@ constexpr int kBins = 1 << kBinBits;
 constexpr int kDefaultCand = 512;   // candidates tried for top-p / min-p rows
 constexpr int kGroupBytes = 32;     // one thread step: two 16-byte vectors
 constexpr int kMaxCluster = 16;
-constexpr int kStageBytes = kThreads * kGroupBytes;  // 8 KB: one group per thread
-constexpr int kStages = 4;                           // bulk-copy ring depth of pass A
+constexpr int kGroupsPerStage = 2;                   // groups a thread consumes per stage
+constexpr int kStageBytes = kThreads * kGroupBytes * kGroupsPerStage;  // 16 KB a stage
+constexpr int kStages = 2;                           // bulk-copy ring depth of pass A
 constexpr int kRingBytes = kStageBytes * kStages;    // aliases the candidate buffer
 constexpr int kSmallK = 32;  // up to this many per CTA, thresholds come from thread maxima
 // the ring region also holds the candidate buffer (kBufCap keys) followed by
@@ -1570,10 +1571,10 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
     }
   };
   if (c.aligned) {
-    // bulk copies through a ring of kStages 8 KB slots: one group per thread
-    // per stage, kStages - 1 stages in flight while one is consumed
+    // bulk copies through a ring of kStages slots of kGroupsPerStage groups a
+    // thread, kStages - 1 stages in flight while one is consumed
     const uint32_t bulk = ((uint32_t)(c.hi > c.lo ? c.hi - c.lo : 0) * (uint32_t)sizeof(T)) & ~15u;
-    const int nstage = (c.ngroups + kThreads - 1) / kThreads;
+    const int nstage = (c.ngroups + kThreads * kGroupsPerStage - 1) / (kThreads * kGroupsPerStage);
     const char* src = reinterpret_cast<const char*>(reinterpret_cast<const T*>(c.rowp) + c.lo);
     auto stage_bytes = [&](int k) -> uint32_t {
       const int64_t b = (int64_t)bulk - (int64_t)k * kStageBytes;
@@ -1598,11 +1599,14 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
       const uint32_t by = stage_bytes(k);
       if (by && !mbar_wait_bounded(&s.full[slot], (uint32_t)((k / kStages) & 1)))
         atomicOr(&s.part.err, kErrTimeout);
-      const int g = k * kThreads + c.tid;
+#pragma unroll
+      for (int gi = 0; gi < kGroupsPerStage; ++gi) {
+      const int gs = gi * kThreads + c.tid;  // the group's place in the stage
+      const int g = k * kThreads * kGroupsPerStage + gs;
       if (g < c.ngroups) {
         float x[E];
-        if ((uint32_t)(c.tid + 1) * kGroupBytes <= by) {
-          const uint4* q = reinterpret_cast<const uint4*>(ring + slot * kStageBytes) + 2 * c.tid;
+        if ((uint32_t)(gs + 1) * kGroupBytes <= by) {
+          const uint4* q = reinterpret_cast<const uint4*>(ring + slot * kStageBytes) + 2 * gs;
           if constexpr (E == 8) {
             const uint4 u0 = q[0], u1 = q[1];
             x[0] = __uint_as_float(u0.x); x[1] = __uint_as_float(u0.y);
@@ -1623,6 +1627,7 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
           load_group<T>(c, g, x);  // the ragged tail, from global memory
         }
         consume(x, g);
+      }
       }
       __syncthreads();  // slot free
       if (s.part.err & kErrTimeout) {
@@ -3281,7 +3286,9 @@ static SelectPlan plan_select_layout(int V, int elem_size, int cluster, bool pen
   p.off_code = 0u;
   if (elem_size == 2) {  // bf16 code slots: counts and best noise bits
     p.off_code = (uint32_t)off;
-    off += (size_t)kCodeSlots * 8;
+    // the code slots' counts and best noise bits; the own-statistics pass runs
+    // its bulk-copy ring in the same region before the selection starts
+    off += (size_t)(kCodeSlots * 8 > kRingBytes ? kCodeSlots * 8 : kRingBytes);
   }
   p.off_stage = (uint32_t)off;
   p.staged = staged ? 1 : 0;
