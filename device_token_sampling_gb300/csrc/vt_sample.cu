@@ -3423,11 +3423,11 @@ static SelectPlan plan_select_own(int V, int elem_size, int dtype, const LaunchP
 }
 
 LaunchPlan plan_sample(int B, int V, int elem_size, bool penalties, int dtype, int num_sms) {
-  // Slices of at most 256 KB (so the per-group structures stay small) and at
+  // Slices of at most 512 KB (so the per-group structures stay small) and at
   // least 8 KB of logits; among those, the largest cluster that still lets
   // all B rows be resident at once, else the smallest one.
   (void)num_sms;
-  const size_t max_slice = 256 * 1024, min_slice = 8 * 1024;
+  const size_t max_slice = 512 * 1024, min_slice = 8 * 1024;
   int cmin = 1;
   while (cmin < kMaxCluster && (size_t)((V + cmin - 1) / cmin) * elem_size > max_slice) cmin <<= 1;
   LaunchPlan best = plan_layout(V, elem_size, cmin, penalties, false);
