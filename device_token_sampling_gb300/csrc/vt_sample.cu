@@ -1771,10 +1771,10 @@ __device__ __forceinline__ void cluster_stats(const Ctx& c, Smem& s, cg::cluster
 }
 
 template <typename T>
-// fp32 rows (penalties and 4-byte logits) run at 3 CTAs an SM with the
+// fp32 rows (penalties and 4-byte logits) run at 2 CTAs an SM with the
 // registers that frees; bf16 rows at 4, which keeps every row of a large batch
 // resident beside the selection kernel's CTAs
-__global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 ? 3 : 4))
+__global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 ? 2 : 4))
     sample_kernel(const SampleArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];
   __shared__ Smem s;
