@@ -1412,7 +1412,7 @@ __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowP
 // kThreads, the Kc-th largest thread maximum (s.tmax); beyond, a two-round
 // radix select over the bf16 lower bounds of the group maxima.  bv is the
 // CTA's maximum.  All threads of the CTA call it.
-__device__ __noinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int Kn, float bv) {
+__device__ __forceinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, int Kn, float bv) {
   if (c.tid == 0) {
     s.part.tau = INFINITY;
     s.part.tau_n = INFINITY;
@@ -2097,7 +2097,7 @@ __device__ __forceinline__ float approx_score(float z, uint32_t b) {
 }
 
 template <typename T>
-__device__ __noinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
+__device__ __forceinline__ bool code_row(Ctx& c, Smem& s, const SampleArgs& a,
                                       cg::cluster_group& cluster, bool topn_done,
                                       uint8_t* code_mem) {
   if constexpr (sizeof(T) != 2) {
