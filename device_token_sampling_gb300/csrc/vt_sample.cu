@@ -1512,13 +1512,26 @@ __device__ __forceinline__ void cta_thresholds(const Ctx& c, Smem& s, int Kc, in
 // ---------------------------------------------------------------------------
 // pass A of a row slice: statistics while streaming it once
 // ---------------------------------------------------------------------------
+// A thread's group with the largest maximum, kept in registers by pass A, and
+// the largest maximum of its other groups: pass B takes its candidates from
+// here instead of reading the slice again whenever no other group of the
+// thread can hold one (fp32 groups of 8).
+struct GroupStash {
+  float v[8];
+  float gm = -INFINITY;      // the kept group's maximum
+  float second = -INFINITY;  // the largest maximum of the thread's other groups
+  int g = -1;                // the kept group (-1: none)
+};
+
 // Streams this CTA's slice (bulk copies through a ring of kStages slots in
 // `ring` for aligned rows, else plain loads) and leaves in s.part its tempered
 // maximum m, sum of exp(z_t - m) s, the lowest-index argmax (bv, bi) and the
 // non-finite flag; s.tmax holds each thread's maximum and c.gmax each group's
-// (a bf16 lower bound).  Returns this CTA's maximum bv.  All threads call it.
+// (a bf16 lower bound).  With a stash (fp32 rows), also this thread's best
+// group.  Returns this CTA's maximum bv.  All threads call it.
 template <typename T>
-__device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
+__device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring,
+                                              GroupStash* stash = nullptr) {
   constexpr int E = Elt<T>::E;
   // rm: this thread's running maximum (pre-temperature); rmt = fl(rm / T),
   // the tempered reference of rsum = sum of exp(z_t - rmt).
@@ -1530,6 +1543,19 @@ __device__ __forceinline__ float stream_stats(Ctx& c, Smem& s, uint8_t* ring) {
 #pragma unroll
     for (int i = 1; i < E; ++i) gm = fmaxf(gm, x[i]);
     c.gmax[g] = bf16_down(gm);
+    if constexpr (E == 8) {
+      if (stash) {
+        if (gm > stash->gm) {
+          stash->second = fmaxf(stash->second, stash->gm);
+          stash->gm = gm;
+          stash->g = g;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) stash->v[i] = x[i];
+        } else {
+          stash->second = fmaxf(stash->second, gm);
+        }
+      }
+    }
     if (gm > bv) {
       int first = 0;
 #pragma unroll
@@ -1808,7 +1834,9 @@ __global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 ? 2 : 4))
     K_main = n;
     topk_beyond = true;
   }
-  const float cta_max = stream_stats<T>(c, s, reinterpret_cast<uint8_t*>(c.buf));
+  GroupStash stash;
+  const float cta_max = stream_stats<T>(c, s, reinterpret_cast<uint8_t*>(c.buf),
+                                        sizeof(T) == 4 ? &stash : nullptr);
   {
     // (rows handed over after their statistics take no thresholds)
     const int Kc = a.early ? 0 : (K_main + c.C - 1) / c.C;
@@ -1865,9 +1893,7 @@ __global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 ? 2 : 4))
     unsigned long long my_mass = 0;
     if (K_need > 0) {
       const float tau_t = __fmul_rn(tau, c.inv_t);
-      for_each_group<T>(
-          c, [&](float gz) { return gz >= tau_t; },
-          [&](float* x, int, int j0) {
+      auto collect = [&](float* x, int, int j0) {
             uint32_t take = 0u;
 #pragma unroll
             for (int i = 0; i < E; ++i) {
@@ -1887,7 +1913,16 @@ __global__ void __launch_bounds__(kThreads, (sizeof(T) == 4 ? 2 : 4))
                 if (c.minp && minp_pass(x[i], c.m_t, c.lmp)) ++my_minp;
               }
             }
-          });
+          };
+      // fp32: the stashed group serves unless another group of this thread
+      // reaches the threshold (fl(max / T) bounds every tempered value of it)
+      bool from_stash = false;
+      if constexpr (E == 8) {
+        from_stash = !(__fmul_rn(stash.second, c.inv_t) >= tau_t);
+        if (from_stash && stash.g >= 0 && __fmul_rn(stash.gm, c.inv_t) >= tau_t)
+          collect(stash.v, stash.g, c.lo + stash.g * E);
+      }
+      if (!from_stash) for_each_group<T>(c, [&](float gz) { return gz >= tau_t; }, collect);
     }
     // one combined CTA reduction of (count, min-p count, mass)
     my_n = warp_sum_i(my_n);
