@@ -51,6 +51,7 @@ constexpr int kStageBytes = kThreads * kGroupBytes * kGroupsPerStage;  // 16 KB 
 constexpr int kStages = 2;                           // bulk-copy ring depth of pass A
 constexpr int kRingBytes = kStageBytes * kStages;    // aliases the candidate buffer
 constexpr int kSmallK = 32;  // up to this many per CTA, thresholds come from thread maxima
+constexpr int kSideSmem = 2048;  // penalised values of a slice held in shared memory
 // the ring region also holds the candidate buffer (kBufCap keys) followed by
 // the level-0 per-bin bests; the histograms alias the buffer
 static_assert(kBufCap * 8 <= kRingBytes, "the candidate buffer lives in the ring region");
@@ -1355,7 +1356,10 @@ __device__ RowParams init_row(Ctx& c, const SampleArgs& a, uint8_t* dsm, int row
 
 // Penalties of the slice's seen tokens: a bitmap of their positions and the
 // side-list index of each bitmap word in shared memory; their penalised values
-// go to the row's side list in global memory (id order).
+// (id order) go to shared memory after the prefixes when they fit (kSideSmem),
+// else to the row's side list in global memory.  Pass A patches every group
+// that holds one, and with the values in global memory each such group would
+// wait on a dependent load before the stage's barrier.
 template <typename T>
 __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowParams& P,
                                 uint8_t* dsm, uint32_t off_bitmap, uint32_t off_prefix,
@@ -1365,6 +1369,8 @@ __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowP
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(dsm + off_bitmap);
   uint16_t* prefix = reinterpret_cast<uint16_t*>(dsm + off_prefix);
   const int nwords = c.slice / 32;
+  float* side_smem =
+      reinterpret_cast<float*>(dsm + ((off_prefix + (uint32_t)nwords * 2u + 15u) & ~15u));
   for (int w = c.tid; w < nwords; w += kThreads) bitmap[w] = 0u;
   int below_lo = 0, below_hi = 0;
   for (int e = c.tid; e < hist_len; e += kThreads) {
@@ -1375,6 +1381,7 @@ __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowP
   const int e_lo = block_sum_int(below_lo, s);
   const int e_hi = block_sum_int(below_hi, s);
   const T* row = reinterpret_cast<const T*>(c.rowp);
+  float* side = e_hi - e_lo <= kSideSmem ? side_smem : zs + e_lo;
   for (int e = e_lo + c.tid; e < e_hi; e += kThreads) {
     const int2 t = tab[e];
     const int local = t.x - c.lo;
@@ -1382,7 +1389,7 @@ __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowP
       atomicOr(&s.part.err, kErrInternal);
       continue;
     }
-    zs[e] = penalize(Elt<T>::load1(row + t.x), t.y, P);
+    side[e - e_lo] = penalize(Elt<T>::load1(row + t.x), t.y, P);
     atomicOr(&bitmap[local >> 5], 1u << (local & 31));
   }
   __syncthreads();
@@ -1399,7 +1406,7 @@ __device__ void setup_penalties(Ctx& c, Smem& s, const SampleArgs& a, const RowP
   }
   c.bitmap = bitmap;
   c.prefix = prefix;
-  c.side_z = zs + e_lo;
+  c.side_z = side;
   c.pen = true;
   __syncthreads();
 }
@@ -3301,6 +3308,7 @@ LaunchPlan plan_layout(int V, int elem_size, int cluster, bool penalties, bool s
     p.off_prefix = (uint32_t)off;
     off += (size_t)(slice / 32) * 2;
     off = (off + 15) & ~(size_t)15;
+    off += (size_t)kSideSmem * 4;  // the slice's penalised values, when they fit
   }
   p.smem = off;
   p.active_clusters = 0;

@@ -194,6 +194,29 @@ def test_penalties(dtype):
     check_workload(w)
 
 
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_BF16])
+def test_dense_penalties(dtype):
+    """Histories that cover most of the row: a slice then holds more penalised
+    values than the kernels keep in shared memory (2048), and they go to the
+    row's side list in global memory instead; beside them, rows whose
+    penalised values fit."""
+    rng = np.random.default_rng(23)
+    B, V = 4, 150_000
+    x = rng_rows(B, V, seed=24)
+    # (at most 32,768 ids a row; contiguous id ranges make whole slices dense)
+    prompt = [rng.permutation(30_000).astype(np.int32),                # ids 0 .. 29,999
+              np.arange(V - 30_000, V, dtype=np.int32),                 # the last 30,000 ids
+              W.zipf_ids(rng, 3000, V),
+              np.repeat(np.arange(60_000, 76_000, dtype=np.int32), 2)]  # 16,000 ids, twice
+    output = [rng.integers(0, V, 50).astype(np.int32) for _ in range(B)]
+    w = custom_workload(x, dtype=dtype, T=[1.0, 0.7, 1.2, 0.0], k=[0, 40, 0, 0],
+                        p=[0.9, 1.0, 0.95, 1.0], mp=[0.0, 0.0, 0.05, 0.0],
+                        pres=[0.4, 0.2, 0.5, 0.3], freq=[0.1, 0.3, 0.2, 0.0],
+                        rep=[1.1, 1.3, 0.9, 1.2], prompt=prompt, output=output, n=4,
+                        name="dense pen")
+    check_workload(w)
+
+
 def test_counts_table_matches_history():
     rng = np.random.default_rng(31)
     B, V = 5, 20_000
